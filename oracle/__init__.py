@@ -1,0 +1,323 @@
+"""Plain CPU oracle for LServe-style decode-phase sparse attention.
+
+TEST INFRASTRUCTURE ONLY: imported by ``tests/``, by the smoke check in
+``__graft_entry__`` and by the CPU-baseline leg of ``bench.py``.  The product
+path (the CUDA library and its binding) never imports it.
+
+Two layers:
+
+* ``liboracle.so`` (``spd_oracle.c``): the arithmetic, written out from the
+  definitions (page min/max, page score, top-k under a budget, attended
+  token sets, two-pass fp64 softmax attention).  Thin ctypes wrappers below.
+* ``OracleLayer``: the per-sequence decode state on logical positions --
+  length, the step counter that drives selection reuse every C steps, the
+  page count at the last selection and the stored selection.  Plain Python
+  control flow around the C arithmetic.
+
+Sources ("LServe long-sequence LLM serving system" write-up unless noted):
+  section 2.1  streaming heads, dynamic query-aware selection with a token
+               budget (default 4096), min-max pooling of key blocks;
+  section 2.2  hierarchical paging: logical pages of 16-64 tokens;
+  section 3.2  reusable page selector (C = 4), dynamic budget
+               min(4096, length/32);
+  "Long-context inference optimization for LLMs" survey, section 2.2
+               (StreamingLLM = attention sink + local window; Quest =
+               query-aware block importance) and section 2.3 (GQA head
+               sharing, 1/sqrt(head_dim) scale).
+
+Readings where the pages are silent (each also listed in the design doc):
+  the group score is the max over the G query heads sharing a kv head; the
+  page holding the newest token is always kept; pages created during a
+  reuse window are attended; the window includes the newest token and sink
+  and window never double-count a position; the output is fp32/fp64.
+
+Pins: tests/test_oracle_pins.py checks every function here against closed
+forms, textbook routines (torch SDPA in fp64), brute force and hand-worked
+fixtures in tests/golden/.
+"""
+import ctypes
+import os
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+
+from . import build as _build
+
+F16, BF16 = 0, 1
+_DTYPES = {"f16": F16, "fp16": F16, "float16": F16,
+           "bf16": BF16, "bfloat16": BF16}
+
+_lib = None
+
+
+def lib():
+    """Load (building first if needed) the oracle's shared library."""
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        L = ctypes.CDLL(path)
+        u16p = np.ctypeslib.ndpointer(np.uint16, flags="C_CONTIGUOUS")
+        f32p = np.ctypeslib.ndpointer(np.float32, flags="C_CONTIGUOUS")
+        f64p = np.ctypeslib.ndpointer(np.float64, flags="C_CONTIGUOUS")
+        i32p = np.ctypeslib.ndpointer(np.int32, flags="C_CONTIGUOUS")
+        ci, cl = ctypes.c_int, ctypes.c_long
+        L.orc_value.argtypes = [ctypes.c_uint16, ci]
+        L.orc_value.restype = ctypes.c_double
+        L.orc_decode.argtypes = [u16p, ci, cl, f64p]
+        L.orc_decode.restype = None
+        L.orc_page_minmax.argtypes = [u16p, ci, ci, ci, ci, ci, ci, u16p, u16p]
+        L.orc_page_minmax.restype = ci
+        L.orc_page_scores_f32.argtypes = [u16p, u16p, u16p, ci, ci, ci, ci, f32p]
+        L.orc_page_scores_f32.restype = None
+        L.orc_page_scores_f64.argtypes = [u16p, u16p, u16p, ci, ci, ci, ci, f64p]
+        L.orc_page_scores_f64.restype = None
+        L.orc_budget_pages.argtypes = [cl, ci, ci]
+        L.orc_budget_pages.restype = ci
+        L.orc_select.argtypes = [f32p, ci, ci, i32p]
+        L.orc_select.restype = ci
+        L.orc_dynamic_tokens.argtypes = [i32p, ci, ci, cl, ci, i32p]
+        L.orc_dynamic_tokens.restype = ci
+        L.orc_streaming_tokens.argtypes = [cl, ci, ci, i32p]
+        L.orc_streaming_tokens.restype = ci
+        L.orc_attention.argtypes = [u16p, u16p, u16p, ci, ci, ci, i32p, ci, f64p]
+        L.orc_attention.restype = ci
+        _lib = L
+    return _lib
+
+
+def dtype_code(dtype):
+    return _DTYPES[dtype] if isinstance(dtype, str) else int(dtype)
+
+
+def _u16(a):
+    return np.ascontiguousarray(a, dtype=np.uint16)
+
+
+# ---- thin wrappers over the C arithmetic -----------------------------------
+
+def decode(bits, dtype):
+    """Exact value (fp64) of fp16/bf16 bit patterns."""
+    b = _u16(bits)
+    out = np.empty(b.shape, np.float64)
+    lib().orc_decode(b.reshape(-1), dtype_code(dtype), b.size, out.reshape(-1))
+    return out
+
+
+def page_minmax(K, dtype, ell, j0=0, j1=None):
+    """Per logical page min/max bit patterns of K [L][d] for pages [j0, j1)."""
+    K = _u16(K)
+    L, d = K.shape
+    nL = -(-L // ell)
+    j1 = nL if j1 is None else j1
+    kmin = np.empty((j1 - j0, d), np.uint16)
+    kmax = np.empty((j1 - j0, d), np.uint16)
+    rc = lib().orc_page_minmax(K, dtype_code(dtype), L, d, ell, j0, j1, kmin, kmax)
+    if rc != 0:
+        raise ValueError("orc_page_minmax: bad arguments")
+    return kmin, kmax
+
+
+def page_scores(q, kmin, kmax, dtype):
+    """fp32 kv-head score S[nL] = max over the G query heads of q [G][d]."""
+    q, kmin, kmax = _u16(q), _u16(kmin), _u16(kmax)
+    G, d = q.shape
+    nL = kmin.shape[0]
+    S = np.empty(nL, np.float32)
+    lib().orc_page_scores_f32(q, kmin, kmax, dtype_code(dtype), nL, G, d, S)
+    return S
+
+
+def page_scores_f64(q, kmin, kmax, dtype):
+    """fp64 per-head score s[G][nL] (not reduced over the group)."""
+    q, kmin, kmax = _u16(q), _u16(kmin), _u16(kmax)
+    G, d = q.shape
+    nL = kmin.shape[0]
+    s = np.empty((G, nL), np.float64)
+    lib().orc_page_scores_f64(q, kmin, kmax, dtype_code(dtype), nL, G, d, s)
+    return s
+
+
+def budget_pages(L, token_budget, ell):
+    return int(lib().orc_budget_pages(int(L), int(token_budget), int(ell)))
+
+
+def select(S, nL, K_sel):
+    """Sorted selection of logical pages (see orc_select)."""
+    S = np.ascontiguousarray(S, dtype=np.float32)
+    if S.shape[0] < nL:
+        S = np.concatenate([S, np.zeros(nL - S.shape[0], np.float32)])
+    sel = np.empty(max(K_sel, 1), np.int32)
+    n = lib().orc_select(S, int(nL), int(K_sel), sel)
+    if n < 0:
+        raise ValueError("orc_select: bad arguments")
+    return sel[:n].copy()
+
+
+def dynamic_tokens(sel, nL0, L, ell):
+    sel = np.ascontiguousarray(sel, dtype=np.int32)
+    out = np.empty(max(int(L), 1), np.int32)
+    n = lib().orc_dynamic_tokens(sel, sel.size, int(nL0), int(L), int(ell), out)
+    if n < 0:
+        raise ValueError("orc_dynamic_tokens: bad arguments")
+    return out[:n].copy()
+
+
+def streaming_tokens(L, sink, window):
+    out = np.empty(max(int(L), 1), np.int32)
+    n = lib().orc_streaming_tokens(int(L), int(sink), int(window), out)
+    return out[:n].copy()
+
+
+def attention(q, K, V, dtype, tokens):
+    """fp64 softmax attention of q [G][d] over rows `tokens` of K/V [L][d]."""
+    q, K, V = _u16(q), _u16(K), _u16(V)
+    tokens = np.ascontiguousarray(tokens, dtype=np.int32)
+    G, d = q.shape
+    out = np.empty((G, d), np.float64)
+    if lib().orc_attention(q, K, V, dtype_code(dtype), G, d, tokens,
+                           tokens.size, out) != 0:
+        raise ValueError("orc_attention: empty token set")
+    return out
+
+
+# ---- decode state on logical positions ------------------------------------
+
+class _Seq:
+    def __init__(self, Hkv, d, cap):
+        self.L = 0
+        self.counter = 0          # decode steps since the sequence started
+        self.nL0 = {}             # kv head -> page count when last selected
+        self.sel = {}             # kv head -> selected pages (ascending)
+        self.K = np.zeros((Hkv, cap, d), np.uint16)
+        self.V = np.zeros((Hkv, cap, d), np.uint16)
+        self.kmin = {}            # kv head -> [nL][d] bit patterns
+        self.kmax = {}
+
+
+class OracleLayer:
+    """One attention layer's KV state and the decode step, on logical positions.
+
+    cfg keys: num_q_heads, num_kv_heads, head_dim, dtype ('f16'/'bf16'),
+    logical_page, streaming (list of bool per kv head), sink, window,
+    token_budget (<=0: min(4096, L/32)), reuse_interval (C), max_context.
+
+    Step order (LServe write-up, section 3.2): append the new token, select
+    when the sequence's step counter is a multiple of C (or when forced),
+    attend, then advance the counter.
+    """
+
+    def __init__(self, cfg):
+        self.cfg = dict(cfg)
+        self.Hq = cfg["num_q_heads"]
+        self.Hkv = cfg["num_kv_heads"]
+        self.G = self.Hq // self.Hkv
+        self.d = cfg["head_dim"]
+        self.dtype = dtype_code(cfg["dtype"])
+        self.ell = cfg["logical_page"]
+        self.streaming = [bool(x) for x in cfg["streaming"]]
+        self.S = cfg.get("sink", 0)
+        self.W = cfg.get("window", 0)
+        self.budget = cfg.get("token_budget", 0)
+        self.C = cfg.get("reuse_interval", 4)
+        self.cap = cfg["max_context"]
+        self.seqs = {}
+        self._next = 0
+
+    def new_seq(self):
+        sid = self._next
+        self._next += 1
+        self.seqs[sid] = _Seq(self.Hkv, self.d, self.cap)
+        return sid
+
+    def free_seq(self, sid):
+        del self.seqs[sid]
+
+    def dyn_heads(self):
+        return [h for h in range(self.Hkv) if not self.streaming[h]]
+
+    # (metadata) ------------------------------------------------------------
+    def append(self, sid, k, v):
+        """Append tokens k, v [n][Hkv][d] (bit patterns) at positions L..L+n-1
+        and recompute the min/max metadata of every logical page they touch."""
+        s = self.seqs[sid]
+        k, v = _u16(k), _u16(v)
+        n = k.shape[0]
+        if s.L + n > self.cap:
+            raise ValueError("append beyond max_context")
+        L0, L1 = s.L, s.L + n
+        s.K[:, L0:L1] = k.transpose(1, 0, 2)
+        s.V[:, L0:L1] = v.transpose(1, 0, 2)
+        s.L = L1
+        j0, j1 = L0 // self.ell, -(-L1 // self.ell)
+        for h in self.dyn_heads():
+            mn, mx = page_minmax(s.K[h, :L1], self.dtype, self.ell, j0, j1)
+            old_min = s.kmin.get(h, np.zeros((0, self.d), np.uint16))[:j0]
+            old_max = s.kmax.get(h, np.zeros((0, self.d), np.uint16))[:j0]
+            s.kmin[h] = np.concatenate([old_min, mn])
+            s.kmax[h] = np.concatenate([old_max, mx])
+
+    # (score, budget, top-k, reuse) ----------------------------------------
+    def selection_due(self, sid):
+        return self.seqs[sid].counter % self.C == 0
+
+    def scores(self, sid, q, h):
+        s = self.seqs[sid]
+        qg = _u16(q)[h * self.G:(h + 1) * self.G]
+        return page_scores(qg, s.kmin[h], s.kmax[h], self.dtype)
+
+    def select(self, sid, q, force=False):
+        """Run the selection if due (counter % C == 0) or forced; returns
+        whether it ran.  Otherwise the stored selection is kept as is."""
+        s = self.seqs[sid]
+        if not (force or self.selection_due(sid)):
+            return False
+        if s.L <= 0:
+            raise ValueError("select on an empty sequence")
+        nL = -(-s.L // self.ell)
+        K_sel = budget_pages(s.L, self.budget, self.ell)
+        for h in self.dyn_heads():
+            S = self.scores(sid, q, h)
+            s.sel[h] = select(S, nL, K_sel)
+            s.nL0[h] = nL
+        return True
+
+    def tokens(self, sid, h):
+        """Attended logical positions of kv head h at the current length."""
+        s = self.seqs[sid]
+        if self.streaming[h]:
+            return streaming_tokens(s.L, self.S, self.W)
+        return dynamic_tokens(s.sel[h], s.nL0[h], s.L, self.ell)
+
+    # (attention) ------------------------------------------------------------
+    def attend(self, sid, q, advance=True, threads=1):
+        """Output [Hq][d] fp64 for query q [Hq][d]; advances the step counter."""
+        s = self.seqs[sid]
+        q = _u16(q)
+        out = np.empty((self.Hq, self.d), np.float64)
+
+        def one(h):
+            T = self.tokens(sid, h)
+            qg = q[h * self.G:(h + 1) * self.G]
+            out[h * self.G:(h + 1) * self.G] = attention(
+                qg, s.K[h, :s.L], s.V[h, :s.L], self.dtype, T)
+
+        if threads > 1:
+            with ThreadPoolExecutor(threads) as ex:
+                list(ex.map(one, range(self.Hkv)))
+        else:
+            for h in range(self.Hkv):
+                one(h)
+        if advance:
+            s.counter += 1
+        return out
+
+    def step(self, sid, q, k, v, threads=1):
+        """One decode step: append one token, select if due, attend."""
+        self.append(sid, np.asarray(k)[None], np.asarray(v)[None])
+        self.select(sid, q)
+        return self.attend(sid, q, threads=threads)
+
+
+def cpu_threads():
+    return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") \
+        else os.cpu_count()

@@ -1,0 +1,448 @@
+"""Pins for the CPU oracle: every function checked against something other
+than itself -- hand-worked fixtures (tests/golden/), closed forms, textbook
+routines (torch SDPA in fp64 on the CPU, numpy reductions), invariants and
+brute force on tiny inputs.  CPU only."""
+import itertools
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _lines(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        for ln in f:
+            ln = ln.strip()
+            if ln and not ln.startswith("#"):
+                yield ln
+
+
+def f16(x):
+    return np.asarray(x, np.float32).astype(np.float16).view(np.uint16)
+
+
+# ---- exact decoding of the storage formats --------------------------------
+
+def test_decode_all_f16_patterns_match_numpy():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)
+    got = oracle.decode(bits, "f16")
+    ok = np.isnan(ref) == np.isnan(got)
+    assert ok.all()
+    m = ~np.isnan(ref)
+    assert np.array_equal(got[m], ref[m])
+    assert np.array_equal(np.signbit(got[m]), np.signbit(ref[m]))
+
+
+def test_decode_all_bf16_patterns_match_float32_view():
+    bits = np.arange(65536, dtype=np.uint32)
+    with np.errstate(invalid="ignore"):
+        ref = (bits << 16).astype(np.uint32).view(np.float32).astype(np.float64)
+    got = oracle.decode(bits.astype(np.uint16), "bf16")
+    m = ~np.isnan(ref)
+    assert (np.isnan(got) == ~m).all()
+    assert np.array_equal(got[m], ref[m])
+    assert np.array_equal(np.signbit(got[m]), np.signbit(ref[m]))
+
+
+def test_bf16_rounding_is_nearest_even():
+    # generator rounding (not oracle arithmetic) must be RNE: torch's cast is
+    # an independent implementation of the same rounding
+    x = np.random.default_rng(1).standard_normal(100000).astype(np.float32)
+    x[:4] = [1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8, -1.0 - 2 ** -8, 3.0e38]
+    ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy()
+    assert np.array_equal(W.to_bits(x, "bf16"), ref.view(np.uint16))
+
+
+# ---- metadata (min/max pooling per logical page) ---------------------------
+
+def test_score_fixture_metadata_and_scores():
+    d = ell = None
+    q, k, kmin, kmax, s, S, maxdot = [], [], {}, {}, {}, {}, {}
+    for ln in _lines("score_example.txt"):
+        t = ln.split()
+        if t[0] == "d":
+            d = int(t[1])
+        elif t[0] == "ell":
+            ell = int(t[1])
+        elif t[0] == "q":
+            q.append([float(x) for x in t[1:]])
+        elif t[0] == "k":
+            k.append([float(x) for x in t[1:]])
+        elif t[0] in ("kmin", "kmax"):
+            (kmin if t[0] == "kmin" else kmax)[int(t[1])] = [float(x) for x in t[2:]]
+        elif t[0] == "s":
+            s[(int(t[1]), int(t[2]))] = float(t[3])
+        elif t[0] == "S":
+            S[int(t[1])] = float(t[2])
+        elif t[0] == "maxdot":
+            maxdot[(int(t[1]), int(t[2]))] = float(t[3])
+    K = f16(k)
+    mn, mx = oracle.page_minmax(K, "f16", ell)
+    assert mn.shape == (2, d)
+    for j in kmin:
+        assert np.array_equal(oracle.decode(mn[j], "f16"), kmin[j])
+        assert np.array_equal(oracle.decode(mx[j], "f16"), kmax[j])
+    s64 = oracle.page_scores_f64(f16(q), mn, mx, "f16")
+    for (h, j), v in s.items():
+        assert s64[h, j] == v
+    S32 = oracle.page_scores(f16(q), mn, mx, "f16")
+    for j, v in S.items():
+        assert S32[j] == np.float32(v)
+    for (h, j), v in maxdot.items():
+        assert v <= s64[h, j]
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("L,ell", [(1, 16), (15, 16), (16, 16), (17, 16),
+                                   (1000, 32), (4096, 64)])
+def test_metadata_equals_numpy_reduction(dtype, L, ell):
+    r = np.random.default_rng(L * 7 + ell)
+    x = r.standard_normal((L, 24)).astype(np.float32)
+    x[r.random(x.shape) < 0.05] = 0.0
+    x[r.random(x.shape) < 0.05] *= -0.0
+    K = W.to_bits(x, dtype)
+    mn, mx = oracle.page_minmax(K, dtype, ell)
+    vals = oracle.decode(K, dtype)
+    nL = -(-L // ell)
+    pad = nL * ell - L
+    lo = np.concatenate([vals, np.full((pad, 24), np.inf)]).reshape(nL, ell, 24).min(1)
+    hi = np.concatenate([vals, np.full((pad, 24), -np.inf)]).reshape(nL, ell, 24).max(1)
+    assert np.array_equal(oracle.decode(mn, dtype), lo)
+    assert np.array_equal(oracle.decode(mx, dtype), hi)
+
+
+def test_metadata_incremental_equals_from_scratch():
+    # the layer model recomputes only the pages touched by each append; that
+    # must equal a from-scratch reduction over the whole key array
+    cfg = dict(num_q_heads=4, num_kv_heads=2, head_dim=16, dtype="f16",
+               logical_page=8, streaming=[False, False], max_context=200)
+    lay = oracle.OracleLayer(cfg)
+    sid = lay.new_seq()
+    r = np.random.default_rng(5)
+    for n in [1, 7, 8, 1, 30, 2, 64, 1, 1]:
+        k = f16(r.standard_normal((n, 2, 16)))
+        lay.append(sid, k, k)
+    s = lay.seqs[sid]
+    for h in (0, 1):
+        mn, mx = oracle.page_minmax(s.K[h, :s.L], "f16", 8)
+        assert np.array_equal(mn, s.kmin[h]) and np.array_equal(mx, s.kmax[h])
+
+
+# ---- page score ------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_score_upper_bounds_every_token_dot(dtype):
+    # closed-form invariant: q_c k_c <= max(q_c kmax_c, q_c kmin_c) for
+    # k_c in [kmin_c, kmax_c], so s_h(j) >= max_{t in page j} q_h . k_t
+    r = np.random.default_rng(11)
+    L, d, ell, G = 1000, 64, 16, 4
+    x = r.standard_normal((L, d)).astype(np.float32)
+    x[:, [3, 40]] *= 50.0
+    K = W.to_bits(x, dtype)
+    q = W.to_bits(r.standard_normal((G, d)).astype(np.float32), dtype)
+    mn, mx = oracle.page_minmax(K, dtype, ell)
+    s = oracle.page_scores_f64(q, mn, mx, dtype)
+    dots = oracle.decode(q, dtype) @ oracle.decode(K, dtype).T  # [G][L] fp64
+    nL = mn.shape[0]
+    for j in range(nL):
+        best = dots[:, j * ell:min((j + 1) * ell, L)].max(axis=1)
+        assert (s[:, j] >= best - 1e-9 * np.abs(best)).all()
+    S = oracle.page_scores(q, mn, mx, dtype)
+    assert np.allclose(S, s.max(0), rtol=1e-5, atol=1e-4)
+
+
+def test_score_single_token_page_equals_dot():
+    # a one-token page has kmin == kmax == k, so the score is exactly q . k
+    r = np.random.default_rng(3)
+    K = f16(r.standard_normal((5, 32)))
+    q = f16(r.standard_normal((3, 32)))
+    mn, mx = oracle.page_minmax(K, "f16", 1)
+    s = oracle.page_scores_f64(q, mn, mx, "f16")
+    ref = oracle.decode(q, "f16") @ oracle.decode(K, "f16").T
+    assert np.allclose(s, ref, rtol=0, atol=1e-12)
+
+
+def test_score_nonnegative_query_reads_kmax():
+    r = np.random.default_rng(4)
+    K = f16(r.standard_normal((64, 16)))
+    q = f16(np.abs(r.standard_normal((2, 16))))
+    mn, mx = oracle.page_minmax(K, "f16", 16)
+    s = oracle.page_scores_f64(q, mn, mx, "f16")
+    ref = oracle.decode(q, "f16") @ oracle.decode(mx, "f16").T
+    assert np.allclose(s, ref, rtol=0, atol=1e-12)
+
+
+def test_score_fp32_matches_numpy_fp64_expression():
+    r = np.random.default_rng(6)
+    K = f16(r.standard_normal((512, 128)))
+    q = f16(r.standard_normal((4, 128)))
+    mn, mx = oracle.page_minmax(K, "f16", 32)
+    qv, lo, hi = (oracle.decode(a, "f16") for a in (q, mn, mx))
+    ref = np.maximum(qv[:, None, :] * hi[None], qv[:, None, :] * lo[None]).sum(-1)
+    S = oracle.page_scores(q, mn, mx, "f16")
+    assert np.allclose(S, ref.max(0), rtol=1e-6, atol=1e-5)
+
+
+def test_pins_catch_planted_score_mistakes():
+    # plant plausible mistakes in the score (on the CPU) and check that a pin
+    # rejects each: reading only kmin or a flipped sign breaks the upper
+    # bound; a dropped channel breaks the single-token-page equality
+    r = np.random.default_rng(12)
+    K = f16(r.standard_normal((256, 32)))
+    q = f16(r.standard_normal((2, 32)))
+    mn, mx = oracle.page_minmax(K, "f16", 16)
+    dots = oracle.decode(q, "f16") @ oracle.decode(K, "f16").T
+
+    def bound_holds(s):
+        return all((s[:, j] >= dots[:, j * 16:(j + 1) * 16].max(1) - 1e-9).all()
+                   for j in range(16))
+
+    assert bound_holds(oracle.page_scores_f64(q, mn, mx, "f16"))
+    assert not bound_holds(oracle.page_scores_f64(q, mn, mn, "f16"))
+    assert not bound_holds(-oracle.page_scores_f64(q, mx, mn, "f16"))
+    m1, x1 = oracle.page_minmax(K, "f16", 1)
+    exact = np.allclose(oracle.page_scores_f64(q, m1, x1, "f16"), dots, atol=1e-12)
+    assert exact
+    dropped = q.copy()
+    dropped[:, -1] = 0
+    assert not np.allclose(oracle.page_scores_f64(dropped, m1, x1, "f16"), dots,
+                           atol=1e-12)
+
+
+# ---- budget and top-k ------------------------------------------------------
+
+def test_budget_fixture():
+    for ln in _lines("budget_rule.txt"):
+        L, tb, ell, pages = (int(x) for x in ln.split())
+        assert oracle.budget_pages(L, tb, ell) == pages, ln
+
+
+def test_selection_fixture():
+    for ln in _lines("selection_example.txt"):
+        a, b, c = ln.split("|")
+        K_sel = int(a)
+        S = np.array([float(x) for x in b.split()], np.float32)
+        exp = [int(x) for x in c.split()]
+        assert oracle.select(S, S.size, K_sel).tolist() == exp, ln
+
+
+def _lexsort_select(S, nL, K_sel):
+    if nL <= K_sel:
+        return list(range(nL))
+    j = np.arange(nL - 1)
+    order = np.lexsort((j, -S[:nL - 1].astype(np.float64)))
+    return sorted(order[:K_sel - 1].tolist() + [nL - 1])
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_selection_equals_lexsort(seed):
+    r = np.random.default_rng(100 + seed)
+    nL = int(r.integers(1, 3000))
+    K_sel = int(r.integers(1, 200))
+    S = r.integers(-20, 20, size=nL).astype(np.float32) * 0.25  # many ties
+    if seed % 2:
+        S = r.standard_normal(nL).astype(np.float32)
+    got = oracle.select(S, nL, K_sel)
+    assert got.tolist() == _lexsort_select(S, nL, K_sel)
+
+
+@pytest.mark.parametrize("seed", range(30))
+def test_selection_brute_force_tiny(seed):
+    # enumerate every K_sel subset that contains the newest page; the chosen
+    # one has the lexicographically best (descending score multiset, then
+    # ascending indices) order
+    r = np.random.default_rng(seed)
+    nL = int(r.integers(2, 10))
+    K_sel = int(r.integers(1, nL))
+    S = r.integers(0, 4, size=nL).astype(np.float32)
+    best = None
+    for sub in itertools.combinations(range(nL - 1), K_sel - 1):
+        key = (sorted((-S[j] for j in sub)), list(sub))
+        if best is None or key < best[0]:
+            best = (key, sorted(list(sub) + [nL - 1]))
+    assert oracle.select(S, nL, K_sel).tolist() == best[1]
+
+
+def test_newest_page_always_kept():
+    S = np.array([5, 4, 3, 2, -100], np.float32)
+    assert oracle.select(S, 5, 2).tolist() == [0, 4]
+
+
+# ---- attended token sets ---------------------------------------------------
+
+def test_token_set_fixture():
+    for ln in _lines("token_sets.txt"):
+        head, rest = ln.split("|", 1)
+        h = head.split()
+        if h[0] == "stream":
+            L, S_, W_ = (int(x) for x in h[1:])
+            exp = [int(x) for x in rest.split()]
+            assert oracle.streaming_tokens(L, S_, W_).tolist() == exp, ln
+        else:
+            ell, L, nL0 = (int(x) for x in h[1:])
+            sel_s, pos_s = rest.split("|")
+            sel = [int(x) for x in sel_s.split()]
+            exp = [int(x) for x in pos_s.split()]
+            assert oracle.dynamic_tokens(sel, nL0, L, ell).tolist() == exp, ln
+
+
+@pytest.mark.parametrize("L,S_,W_", [(5000, 128, 4096), (100, 16, 256),
+                                     (4224, 128, 4096), (4225, 128, 4096)])
+def test_streaming_set_closed_form(L, S_, W_):
+    T = oracle.streaming_tokens(L, S_, W_)
+    assert len(set(T.tolist())) == len(T)
+    exp = min(L, S_ + W_)
+    assert len(T) == exp
+
+
+# ---- attention --------------------------------------------------------------
+
+def _sdpa(q, K, V, dtype, mask=None):
+    qv = torch.from_numpy(oracle.decode(q, dtype))[None, :, None, :]
+    kv = torch.from_numpy(oracle.decode(K, dtype))[None, None]
+    vv = torch.from_numpy(oracle.decode(V, dtype))[None, None]
+    m = None if mask is None else torch.from_numpy(mask)[None, None, None, :]
+    G = q.shape[0]
+    out = torch.nn.functional.scaled_dot_product_attention(
+        qv, kv.expand(1, G, -1, -1), vv.expand(1, G, -1, -1), attn_mask=m)
+    return out[0, :, 0].numpy()
+
+
+def test_attention_fixture_closed_form():
+    q = f16([[2, 0, 0, 0]])
+    K = f16([[0, 0, 0, 0], [1, 0, 0, 0], [-1, 0, 0, 0]])
+    V = f16([[1, 0, 0, 0], [0, 1, 0, 0], [0, 0, 1, 0]])
+    # z = q.k / sqrt(4) = (0, 1, -1); weights proportional to (1, e, 1/e)
+    den = 1 + math.e + 1 / math.e
+    exp = np.array([1 / den, math.e / den, 1 / (math.e * den), 0.0])
+    out = oracle.attention(q, K, V, "f16", [0, 1, 2])
+    assert np.allclose(out[0], exp, rtol=0, atol=1e-15)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_dense_equivalence_with_sdpa(dtype):
+    # budget >= L: every page is selected and the output is full attention
+    r = np.random.default_rng(21)
+    L, d, G = 700, 64, 4
+    K = W.to_bits(r.standard_normal((L, d)).astype(np.float32), dtype)
+    V = W.to_bits(r.standard_normal((L, d)).astype(np.float32), dtype)
+    q = W.to_bits(r.standard_normal((G, d)).astype(np.float32), dtype)
+    ell = 16
+    nL = -(-L // ell)
+    mn, mx = oracle.page_minmax(K, dtype, ell)
+    sel = oracle.select(oracle.page_scores(q, mn, mx, dtype), nL,
+                        oracle.budget_pages(L, L + 5, ell))
+    assert sel.tolist() == list(range(nL))
+    T = oracle.dynamic_tokens(sel, nL, L, ell)
+    out = oracle.attention(q, K, V, dtype, T)
+    assert np.allclose(out, _sdpa(q, K, V, dtype), rtol=0, atol=1e-12)
+
+
+def test_streaming_equals_masked_sdpa():
+    r = np.random.default_rng(22)
+    L, d = 1500, 64
+    K, V = (f16(r.standard_normal((L, d))) for _ in range(2))
+    q = f16(r.standard_normal((2, d)))
+    T = oracle.streaming_tokens(L, 16, 256)
+    mask = np.zeros(L, bool)
+    mask[:16] = True
+    mask[L - 256:] = True
+    out = oracle.attention(q, K, V, "f16", T)
+    assert np.allclose(out, _sdpa(q, K, V, "f16", mask), rtol=0, atol=1e-12)
+
+
+def test_sparse_equals_dense_with_mask():
+    r = np.random.default_rng(23)
+    L, d, ell = 2000, 32, 32
+    K, V = (f16(r.standard_normal((L, d))) for _ in range(2))
+    q = f16(r.standard_normal((4, d)))
+    sel = np.sort(r.choice(-(-L // ell) - 1, size=9, replace=False)).astype(np.int32)
+    sel = np.concatenate([sel, [-(-L // ell) - 1]]).astype(np.int32)
+    T = oracle.dynamic_tokens(sel, -(-L // ell), L, ell)
+    mask = np.zeros(L, bool)
+    mask[T] = True
+    assert mask.sum() == len(T)
+    out = oracle.attention(q, K, V, "f16", T)
+    assert np.allclose(out, _sdpa(q, K, V, "f16", mask), rtol=0, atol=1e-12)
+
+
+def test_special_cases():
+    r = np.random.default_rng(24)
+    d = 64
+    V = f16(r.standard_normal((50, d)))
+    K = f16(r.standard_normal((50, d)))
+    q = f16(r.standard_normal((2, d)))
+    # one token: out = v_0
+    out = oracle.attention(q, K, V, "f16", [0])
+    assert np.array_equal(out, np.repeat(oracle.decode(V[:1], "f16"), 2, 0))
+    # identical keys: uniform weights, out = mean of V over the set
+    Ks = np.repeat(K[:1], 50, 0)
+    T = np.arange(3, 40)
+    out = oracle.attention(q, Ks, V, "f16", T)
+    assert np.allclose(out, oracle.decode(V[T], "f16").mean(0)[None], atol=1e-12)
+    # a needle with a huge logit takes all the weight
+    Kn = K.copy()
+    qd = oracle.decode(q[:1], "f16")[0]
+    Kn[17] = f16(60.0 * qd / np.linalg.norm(qd))
+    out = oracle.attention(q[:1], Kn, V, "f16", np.arange(50))
+    assert np.allclose(out[0], oracle.decode(V[17], "f16"), atol=1e-6)
+
+
+# ---- selection reuse over decode steps --------------------------------------
+
+def _tiny_layer(C=4, budget=64, streaming=(False, True)):
+    cfg = dict(num_q_heads=4, num_kv_heads=2, head_dim=16, dtype="f16",
+               logical_page=8, streaming=list(streaming), sink=4, window=24,
+               token_budget=budget, reuse_interval=C, max_context=2000)
+    return oracle.OracleLayer(cfg)
+
+
+def test_selection_reused_for_C_steps_and_tail_pages_attended():
+    lay = _tiny_layer()
+    sid = lay.new_seq()
+    r = np.random.default_rng(30)
+    ctx = f16(r.standard_normal((301, 2, 16)))
+    lay.append(sid, ctx, ctx)
+    ran, sels = [], []
+    for step in range(13):
+        q = f16(r.standard_normal((4, 16)))
+        kv = f16(r.standard_normal((2, 16)))
+        lay.append(sid, kv[None], kv[None])
+        ran.append(lay.select(sid, q))
+        sels.append(lay.seqs[sid].sel[0].copy())
+        nL = -(-lay.seqs[sid].L // 8)
+        T = set(lay.tokens(sid, 0).tolist())
+        # every page from the selection-time last page to the current last
+        # page is attended, whatever the stored selection holds
+        for j in range(lay.seqs[sid].nL0[0] - 1, nL):
+            assert set(range(j * 8, min((j + 1) * 8, lay.seqs[sid].L))) <= T
+        lay.attend(sid, q)
+    assert ran == [s % 4 == 0 for s in range(13)]
+    for s in range(13):
+        if s % 4:
+            assert np.array_equal(sels[s], sels[s - s % 4])
+    # a page boundary was crossed inside a reuse window (L 302..314, ell 8)
+    assert any(not ran[s] and (302 + s) % 8 == 1 for s in range(13))
+
+
+def test_layer_step_dense_when_budget_covers_context():
+    lay = _tiny_layer(budget=10 ** 6, streaming=(False, False))
+    sid = lay.new_seq()
+    r = np.random.default_rng(31)
+    ctx = f16(r.standard_normal((120, 2, 16)))
+    vv = f16(r.standard_normal((120, 2, 16)))
+    lay.append(sid, ctx, vv)
+    q = f16(r.standard_normal((4, 16)))
+    lay.select(sid, q)
+    out = lay.attend(sid, q)
+    for h in range(2):
+        ref = _sdpa(q[2 * h:2 * h + 2], ctx[:, h], vv[:, h], "f16")
+        assert np.allclose(out[2 * h:2 * h + 2], ref, atol=1e-12)
