@@ -1,0 +1,237 @@
+/*
+ * spd.h -- C ABI of the GB300 sparse paged decode attention library.
+ *
+ * Decode-phase unified sparse attention over a hierarchically paged KV cache,
+ * after "LServe long-sequence LLM serving system" (the LServe write-up):
+ *
+ *   section 2.1  static sparsity: a fixed share of kv heads become streaming
+ *                heads that see only local context; dynamic sparsity: the
+ *                other heads keep a fixed KV token budget (default 4096),
+ *                chosen per query from min-max pooled key features;
+ *   section 2.2  hierarchical paging: large physical pages (256-1024 tokens)
+ *                are the allocation unit, small logical pages (16-64 tokens)
+ *                are the selection unit, a page table maps between them;
+ *   section 3.2  the page selector runs once every C (= 4) decode steps and
+ *                is reused in between; the budget follows
+ *                min(4096, sequence length / 32); streaming heads read recent
+ *                tokens through on-chip memory.
+ *
+ * Everything below the ABI is hand-written CUDA for sm_103a plus a C++ host
+ * runtime (page pool, per-sequence tables, work partitioning).  No type from
+ * PyTorch or any other framework appears here.
+ *
+ * Conventions
+ *   - Every function returns spd_status; nothing throws across the ABI.
+ *   - Pointers documented as "device" must point to memory of the GPU the
+ *     context runs on and be 16-byte aligned; "host" pointers are read
+ *     during the call only.
+ *   - All GPU work is enqueued on the `stream` argument (a cudaStream_t;
+ *     NULL means the legacy default stream).  Host-side state (lengths, step
+ *     counters, page tables) advances when the call returns, before the GPU
+ *     has run the work, so calls on one context must be issued in decode
+ *     order on one stream.  A context is not thread-safe.
+ *   - Argument errors are detected on the host before anything is enqueued
+ *     and leave the context unchanged.
+ */
+#ifndef SPD_H
+#define SPD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct spd_ctx spd_ctx;
+typedef struct CUstream_st *spd_stream; /* same type as cudaStream_t */
+
+typedef enum {
+  SPD_OK = 0,
+  SPD_ERR_INVALID_ARG = 1,  /* bad argument or configuration               */
+  SPD_ERR_NO_PAGES = 2,     /* physical page pool exhausted                 */
+  SPD_ERR_BAD_SEQ = 3,      /* unknown, freed or duplicated sequence id     */
+  SPD_ERR_CAPACITY = 4,     /* beyond max_context / max_seqs / budget room  */
+  SPD_ERR_CUDA = 5,         /* a CUDA runtime call or launch failed         */
+  SPD_ERR_DEVICE_CHECK = 6, /* a kernel's own bounds check tripped          */
+  SPD_ERR_STATE = 7         /* call out of order (e.g. no selection yet)    */
+} spd_status;
+
+typedef enum { SPD_F16 = 0, SPD_BF16 = 1 } spd_dtype;
+
+/*
+ * Configuration of one attention layer's KV cache.  Keys follow the
+ * `sparse_config` block of the LServe write-up, section 5.2
+ * (dynamic_token_budget, reuse_interval, physical_page_size,
+ * logical_page_size; the streaming share becomes an explicit per-head mask).
+ */
+typedef struct {
+  int num_q_heads;   /* Hq; Hq % Hkv == 0 and Hq / Hkv in {1, 2, 4, 8}      */
+  int num_kv_heads;  /* Hkv, 1..128                                          */
+  int head_dim;      /* d in {64, 128}                                       */
+  spd_dtype dtype;   /* storage type of q, K, V and the min/max metadata     */
+  int logical_page;  /* l in {16, 32, 64}: selection unit, tokens           */
+  int physical_page; /* P, a multiple of l, <= 4096: allocation unit       */
+  int num_physical_pages; /* pool size (shared by all sequences)            */
+  int max_seqs;           /* live sequences at once                         */
+  int max_context;        /* tokens per sequence                            */
+  const unsigned char *kv_head_is_streaming; /* host [Hkv], copied; NULL=none */
+  int sink;          /* streaming heads: attention-sink tokens S >= 0        */
+  int window;        /* streaming heads: local window W >= 1 (incl. newest)  */
+  int token_budget;  /* dynamic heads: tokens kept; <= 0: min(4096, L/32)    */
+  int reuse_interval;/* C >= 1: selection runs when step % C == 0            */
+  unsigned long long free_list_seed; /* 0: pages handed out in order;
+                                        else a seeded permutation of the pool */
+} spd_config;
+
+/*
+ * Bytes of every device buffer the caller must provide.  Layouts (elements
+ * of `dtype` unless noted; Hd / Hs = number of dynamic / streaming kv heads,
+ * R = P / l, MP = ceil(max_context / P), KS = pages kept at the largest
+ * budget):
+ *   k_pool, v_pool [num_physical_pages][Hd][P][d]   keys / values of dynamic
+ *                   heads; logical page j of a sequence lives in physical
+ *                   page table[j / R], rows (j % R) * l ... + l - 1.
+ *   meta           [num_physical_pages][Hd][R][2][d]  per logical page the
+ *                   channel-wise key minimum ([..][0][:]) and maximum.
+ *   stream_k, stream_v [max_seqs][Hs][S + W][d]  streaming heads: slots
+ *                   0..S-1 hold positions 0..S-1, slot S + ((t - S) mod W)
+ *                   holds position t >= S (a ring, never shifted).
+ *   page_table     int32 [max_seqs][MP]   physical page of each sequence's
+ *                   i-th P-token block (mirrors the host table).
+ *   selection      int32 [max_seqs][Hd][KS]  kept logical pages, ascending.
+ *   scratch        split partials, tickets, page scores and the device error
+ *                   word; contents need no initialisation.
+ * Every buffer must be 256-byte aligned.  Sizes of 0 mean "not used".
+ */
+typedef struct {
+  size_t k_pool, v_pool, meta, stream_k, stream_v, page_table, selection,
+      scratch;
+} spd_sizes;
+
+typedef struct {
+  void *k_pool, *v_pool, *meta, *stream_k, *stream_v, *page_table, *selection,
+      *scratch;
+} spd_buffers;
+
+/* Validate a configuration and report the buffer sizes it needs.  Host only.
+ * SPD_ERR_INVALID_ARG on a bad configuration. */
+spd_status spd_query_sizes(const spd_config *cfg, spd_sizes *out);
+
+/*
+ * Create a context over caller-owned device buffers (sizes from
+ * spd_query_sizes).  The library never allocates or frees device memory for
+ * the caller's data; it owns only host tables.  Host only: no GPU work is
+ * enqueued and the buffers are not touched until the first append.
+ */
+spd_status spd_create(const spd_config *cfg, const spd_buffers *bufs,
+                      spd_ctx **out);
+void spd_destroy(spd_ctx *ctx);
+
+/*
+ * Page-table allocation and release (LServe write-up, section 2.2: the page
+ * table maps logical pages onto larger physical pages; survey "Long-context
+ * inference optimization for LLMs", section 3.4: a fixed pool with a free
+ * list that reports exhaustion).  Host only.
+ *   spd_seq_create  picks a free sequence slot; id in [0, max_seqs).
+ *                   SPD_ERR_CAPACITY when max_seqs are live.
+ *   spd_seq_free    returns the sequence's physical pages to the free list
+ *                   and clears its length, step counter and selection.
+ *   spd_seq_reserve makes sure physical pages exist for the next n_tokens
+ *                   positions.  All or nothing: SPD_ERR_NO_PAGES (pool
+ *                   exhausted) or SPD_ERR_CAPACITY (beyond max_context)
+ *                   leave the pool and the sequence unchanged.  The device
+ *                   page table is updated by the next spd_kv_append.
+ *   spd_seq_info    length L, decode-step counter, page count at the last
+ *                   selection (0 if none) and pages kept at it.
+ *   spd_get_page_table copies the sequence's physical page ids (host table)
+ *                   to phys_host (capacity cap entries), count to *n_host.
+ */
+spd_status spd_seq_create(spd_ctx *ctx, int *seq_id_out);
+spd_status spd_seq_free(spd_ctx *ctx, int seq_id);
+spd_status spd_seq_reserve(spd_ctx *ctx, int seq_id, int n_tokens);
+spd_status spd_seq_info(spd_ctx *ctx, int seq_id, long long *length,
+                        long long *step_counter, int *pages_at_selection,
+                        int *pages_kept);
+spd_status spd_get_page_table(spd_ctx *ctx, int seq_id, int *phys_host,
+                              int cap, int *n_host);
+/* Free physical pages left in the pool. */
+spd_status spd_free_pages(spd_ctx *ctx, int *n_free);
+
+/*
+ * Append n_tokens key/value rows to each listed sequence and update the
+ * min/max metadata of every logical page they touch (LServe write-up,
+ * section 2.1: min-max pooling of each block's keys).
+ *   seq_ids  host [n_seqs], distinct live sequences.
+ *   k, v     device [n_seqs][n_tokens][Hkv][d] of dtype.
+ * Dynamic heads go to the paged pool (pages allocated as needed, all or
+ * nothing across the call: SPD_ERR_NO_PAGES / SPD_ERR_CAPACITY change
+ * nothing); streaming heads go to their sink slots and ring window.
+ * Metadata is exact (a min/max of stored values, no rounding).
+ */
+spd_status spd_kv_append(spd_ctx *ctx, const int *seq_ids, int n_seqs,
+                         int n_tokens, const void *k, const void *v,
+                         spd_stream stream);
+
+/*
+ * Query-aware page selection for the dynamic heads (LServe write-up,
+ * section 2.1 dynamic sparsity; section 3.2 reusable selector and dynamic
+ * budget).  For each listed sequence whose step counter is a multiple of C
+ * (or every listed sequence if `force`):
+ *   score  S(j) = max over the G query heads h of the kv head of
+ *          sum_c max(q_h[c] * kmax_j[c], q_h[c] * kmin_j[c])   (fp32),
+ *   keep   K_sel = max(1, budget / l) pages: the page holding the newest
+ *          token plus the K_sel - 1 best other pages, ties to the lower
+ *          page index; every page if there are at most K_sel.
+ * Other sequences keep their stored selection untouched.
+ *   q  device [n_seqs][Hq][d] of dtype.
+ * SPD_ERR_STATE for a sequence with no tokens.
+ */
+spd_status spd_select_pages(spd_ctx *ctx, const void *q, const int *seq_ids,
+                            int n_seqs, int force, spd_stream stream);
+
+/*
+ * Sparse decode attention (LServe write-up, section 2.1 unified sparse
+ * kernel; split-K with exported row max and sum, Novita KV-sparsity article,
+ * "attention mechanism modifications").  For query head h of kv head
+ * g = h / G and the attended positions T of g:
+ *   dynamic   T = tokens of (stored selection U pages created since it)
+ *   streaming T = {t < S} U {t >= L - W}
+ *   out[h] = sum_{t in T} softmax_t(q_h . k_t / sqrt(d)) v_t      (fp32).
+ * Advances every listed sequence's decode-step counter by one.
+ *   q    device [n_seqs][Hq][d] of dtype;  out device [n_seqs][Hq][d] fp32.
+ * SPD_ERR_STATE if a sequence with dynamic heads has never been selected
+ * or has no tokens.
+ */
+spd_status spd_sparse_decode_attention(spd_ctx *ctx, const void *q,
+                                       const int *seq_ids, int n_seqs,
+                                       float *out, spd_stream stream);
+
+/*
+ * One decode step for each listed sequence: append one token (k, v device
+ * [n_seqs][Hkv][d]), select if due, attend.  Same results as calling the
+ * three entry points above in that order; enqueues fewer launches.
+ */
+spd_status spd_decode_step(spd_ctx *ctx, const void *q, const void *k,
+                           const void *v, const int *seq_ids, int n_seqs,
+                           float *out, spd_stream stream);
+
+/* Introspection for tests.  spd_get_selection synchronises `stream` and
+ * copies the kept pages of (seq, kv head) to idx_host (capacity cap). */
+spd_status spd_get_selection(spd_ctx *ctx, int seq_id, int kv_head,
+                             int *idx_host, int cap, int *count_host,
+                             spd_stream stream);
+
+/* Synchronise `stream` and read the device error word: SPD_OK, or
+ * SPD_ERR_DEVICE_CHECK if a kernel's bounds check tripped (the word is then
+ * cleared), or SPD_ERR_CUDA. */
+spd_status spd_check_status(spd_ctx *ctx, spd_stream stream);
+
+const char *spd_status_string(spd_status s);
+/* Human-readable detail of the last error on this context ("" if none). */
+const char *spd_last_error(spd_ctx *ctx);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SPD_H */

@@ -1,0 +1,128 @@
+// Internal interface between the host runtime (spd_runtime.cpp) and the CUDA
+// kernels.  Every per-call quantity travels in a parameter block passed by
+// value, so a launch needs no host staging buffer and can be captured into a
+// CUDA graph as is.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace spd {
+
+constexpr int kSeqsPerLaunch = 64;    // sequences described per parameter block
+constexpr int kMaxItems = 4096;       // split-K work items per decode launch
+constexpr int kMaxKvHeads = 128;
+constexpr int kPtUpdPerLaunch = 240;  // page-table entries per pt_write launch
+constexpr int kScratchHeader = 256;   // bytes: device error word and info
+
+// Device error word layout (int32 at scratch + 0): 0 = ok, else a code below;
+// scratch + 4 .. + 16 hold details of the first violation.
+enum DevErr : int {
+  kDevOk = 0,
+  kDevBadPhys = 1,      // page table entry outside the pool
+  kDevBadPage = 2,      // logical page beyond the page table row
+  kDevBadSelection = 3, // selection entry out of range
+  kDevTopkCount = 4,    // top-k produced a count different from K_sel
+};
+
+struct ScratchLayout {
+  size_t tickets_dec;  // int [kSeqsPerLaunch * Hkv]
+  size_t tickets_sel;  // int [kSeqsPerLaunch * Hd]
+  size_t part_ml;      // float2 [kMaxItems * G]   (row max in log2 units, sum)
+  size_t part_o;       // float  [kMaxItems * G * d]
+  size_t scores;       // float  [kSeqsPerLaunch * Hd * max_nL]
+  size_t total;
+};
+
+// ---- kv append + metadata ------------------------------------------------
+struct AppendSeq {
+  int slot;      // sequence slot (row of the page table / stream buffers)
+  int L_old;     // length before this append
+  int cta_off;   // first dynamic CTA of this sequence
+};
+
+struct AppendParams {
+  const void *k, *v;           // [n_seqs][n_tokens][Hkv][d]
+  void *k_pool, *v_pool, *meta, *stream_k, *stream_v;
+  const int *page_table;
+  int *err;
+  int n_seqs, n_tokens, Hkv, Hd, Hs, ell, P, R, max_pp, S, W, num_phys;
+  int dyn_ctas;                // sum over seqs of touched logical pages * Hd
+  unsigned char dyn_kv[kMaxKvHeads];  // dynamic index -> kv head
+  unsigned char str_kv[kMaxKvHeads];  // streaming index -> kv head
+  AppendSeq seqs[kSeqsPerLaunch];
+};
+
+struct PtUpdate {
+  int slot, index, phys;
+};
+struct PtWriteParams {
+  int *page_table;
+  int max_pp, n;
+  PtUpdate upd[kPtUpdPerLaunch];
+};
+
+// ---- page selection --------------------------------------------------------
+struct SelectSeq {
+  int slot;
+  int qrow;       // row of this sequence in the call's q array
+  int nL;         // logical pages at selection time
+  int K_sel;      // pages to keep
+  int chunk_off;  // first scoring CTA of this sequence (0 chunks if nL<=K_sel)
+  int n_chunks;   // scoring CTAs per dynamic head
+};
+
+struct SelectParams {
+  const void *q;        // [n_seqs][Hq][d]
+  const void *meta;
+  const int *page_table;
+  int *selection;       // [max_seqs][Hd][ksel_max]
+  float *scores;        // [kSeqsPerLaunch][Hd][max_nL]
+  int *err;
+  int n_seqs, Hq, Hd, ell, R, max_pp, ksel_max, max_nL, pages_per_chunk,
+      num_phys;
+  int score_ctas;       // total scoring CTAs
+  unsigned char dyn_kv[kMaxKvHeads];
+  SelectSeq seqs[kSeqsPerLaunch];
+};
+
+// ---- split-K decode + combine ----------------------------------------------
+struct DecodeSeq {
+  int slot, L;
+  int nL0;        // logical pages when the selection was taken
+  int sel_count;  // pages in the stored selection
+  int item_off;   // first work item of this sequence
+  int ns_dyn;     // splits per dynamic head
+  int ns_str;     // splits per streaming head
+  int pps;        // attended pages per dynamic split
+  int tps;        // attended tokens per streaming split
+};
+
+struct DecodeParams {
+  const void *q;
+  float *out;           // [n_seqs][Hq][d]
+  const void *k_pool, *v_pool, *stream_k, *stream_v;
+  const int *page_table, *selection;
+  float *part_o;
+  float2 *part_ml;
+  int *tickets;
+  int *err;
+  int n_seqs, Hq, Hkv, Hd, Hs, ell, P, R, max_pp, ksel_max, S, W, num_phys;
+  int total_items;
+  float scale_log2;     // log2(e) / sqrt(d)
+  unsigned char kv_kind[kMaxKvHeads];  // 0 dynamic, 1 streaming
+  unsigned char kv_sub[kMaxKvHeads];   // index within its kind
+  unsigned char dyn_kv[kMaxKvHeads];
+  unsigned char str_kv[kMaxKvHeads];
+  DecodeSeq seqs[kSeqsPerLaunch];
+};
+
+// Launchers (kernels.cu).  dtype: 0 fp16, 1 bf16.  Return cudaGetLastError().
+cudaError_t launch_pt_write(const PtWriteParams &p, cudaStream_t s);
+cudaError_t launch_append(const AppendParams &p, int dtype, int d,
+                          cudaStream_t s);
+cudaError_t launch_select(const SelectParams &p, int dtype, int d, int G,
+                          cudaStream_t s);
+cudaError_t launch_decode(const DecodeParams &p, int dtype, int d, int G,
+                          cudaStream_t s);
+
+}  // namespace spd

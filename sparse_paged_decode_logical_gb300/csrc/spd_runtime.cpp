@@ -1,0 +1,695 @@
+// Host runtime of the sparse paged decode attention library: configuration
+// checks, the fixed physical page pool with its free list, per-sequence
+// tables (length, page list, step counter, selection bookkeeping), the
+// split-K work partitioning and the C ABI declared in include/spd.h.
+//
+// Hierarchical paging follows "LServe long-sequence LLM serving system",
+// section 2.2: a physical page of P tokens is the allocation unit and holds
+// R = P / l consecutive logical pages of one sequence (the selection unit).
+// The pool is fixed; an allocation that does not fit reports exhaustion and
+// changes nothing (the free-list pager of "Long-context inference
+// optimization for LLMs", section 3.4, raises on an empty list).
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "spd.h"
+#include "spd_internal.h"
+
+using namespace spd;
+
+namespace {
+
+struct Seq {
+  bool live = false;
+  long long L = 0;
+  long long counter = 0;   // decode steps taken (attention calls)
+  bool has_sel = false;
+  int nL0 = 0;             // logical pages when the selection was taken
+  int sel_count = 0;       // pages kept at that selection
+  std::vector<int> pages;  // physical page per P-token block
+};
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+uint64_t splitmix64(uint64_t &s) {
+  uint64_t z = (s += 0x9e3779b97f4a7c15ull);
+  z = (z ^ (z >> 30)) * 0xbf58476d1ce4e5b9ull;
+  z = (z ^ (z >> 27)) * 0x94d049bb133111ebull;
+  return z ^ (z >> 31);
+}
+
+struct Derived {
+  int G = 0, Hd = 0, Hs = 0, R = 0, max_pp = 0, ksel_max = 0, max_nL = 0,
+      seqs_per_launch = 0;
+  unsigned char kv_kind[kMaxKvHeads] = {}, kv_sub[kMaxKvHeads] = {},
+                dyn_kv[kMaxKvHeads] = {}, str_kv[kMaxKvHeads] = {};
+  ScratchLayout sl{};
+  spd_sizes sizes{};
+};
+
+// Validates cfg and fills the derived quantities; returns an error string or
+// nullptr.
+const char *derive(const spd_config *c, Derived *d) {
+  if (!c) return "config is NULL";
+  if (c->num_kv_heads < 1 || c->num_kv_heads > kMaxKvHeads)
+    return "num_kv_heads must be in [1, 128]";
+  if (c->num_q_heads < 1 || c->num_q_heads % c->num_kv_heads)
+    return "num_q_heads must be a positive multiple of num_kv_heads";
+  d->G = c->num_q_heads / c->num_kv_heads;
+  if (d->G != 1 && d->G != 2 && d->G != 4 && d->G != 8)
+    return "num_q_heads / num_kv_heads must be 1, 2, 4 or 8";
+  if (c->head_dim != 64 && c->head_dim != 128) return "head_dim must be 64 or 128";
+  if (c->dtype != SPD_F16 && c->dtype != SPD_BF16) return "dtype must be SPD_F16 or SPD_BF16";
+  if (c->logical_page != 16 && c->logical_page != 32 && c->logical_page != 64)
+    return "logical_page must be 16, 32 or 64";
+  if (c->physical_page < c->logical_page || c->physical_page % c->logical_page ||
+      c->physical_page > 4096)
+    return "physical_page must be a multiple of logical_page, at most 4096";
+  if (c->max_seqs < 1) return "max_seqs must be >= 1";
+  if (c->max_context < 1 || c->max_context > (1 << 28)) return "max_context must be in [1, 2^28]";
+  if (c->reuse_interval < 1) return "reuse_interval must be >= 1";
+  d->Hd = d->Hs = 0;
+  for (int h = 0; h < c->num_kv_heads; ++h) {
+    const bool str = c->kv_head_is_streaming && c->kv_head_is_streaming[h];
+    d->kv_kind[h] = str ? 1 : 0;
+    if (str) {
+      d->kv_sub[h] = (unsigned char)d->Hs;
+      d->str_kv[d->Hs++] = (unsigned char)h;
+    } else {
+      d->kv_sub[h] = (unsigned char)d->Hd;
+      d->dyn_kv[d->Hd++] = (unsigned char)h;
+    }
+  }
+  if (d->Hs > 0 && (c->sink < 0 || c->window < 1 || (long long)c->sink + c->window > (1 << 24)))
+    return "streaming heads need sink >= 0 and window >= 1";
+  if (d->Hd > 0 && c->num_physical_pages < 1) return "num_physical_pages must be >= 1";
+  if (c->num_physical_pages < 0) return "num_physical_pages must be >= 0";
+  d->R = c->physical_page / c->logical_page;
+  d->max_pp = (c->max_context + c->physical_page - 1) / c->physical_page;
+  d->max_nL = (c->max_context + c->logical_page - 1) / c->logical_page;
+  long long budget = c->token_budget > 0 ? c->token_budget
+                                         : std::min<long long>(4096, c->max_context / 32);
+  d->ksel_max = (int)std::max<long long>(1, budget / c->logical_page);
+  d->seqs_per_launch = std::min(c->max_seqs, kSeqsPerLaunch);
+
+  const size_t e = 2, dim = (size_t)c->head_dim;
+  const int S = d->Hs ? c->sink : 0, W = d->Hs ? c->window : 0;
+  spd_sizes &z = d->sizes;
+  z.k_pool = z.v_pool = (size_t)c->num_physical_pages * d->Hd * c->physical_page * dim * e;
+  z.meta = (size_t)c->num_physical_pages * d->Hd * d->R * 2 * dim * e;
+  z.stream_k = z.stream_v = (size_t)c->max_seqs * d->Hs * (size_t)(S + W) * dim * e;
+  z.page_table = d->Hd ? (size_t)c->max_seqs * d->max_pp * 4 : 0;
+  z.selection = d->Hd ? (size_t)c->max_seqs * d->Hd * d->ksel_max * 4 : 0;
+  ScratchLayout &sl = d->sl;
+  size_t off = kScratchHeader;
+  sl.tickets_dec = off;
+  off = round_up(off + (size_t)d->seqs_per_launch * c->num_kv_heads * 4, 256);
+  sl.tickets_sel = off;
+  off = round_up(off + (size_t)d->seqs_per_launch * d->Hd * 4, 256);
+  sl.part_ml = off;
+  off = round_up(off + (size_t)kMaxItems * d->G * 8, 256);
+  sl.part_o = off;
+  off = round_up(off + (size_t)kMaxItems * d->G * dim * 4, 256);
+  sl.scores = off;
+  off = round_up(off + (size_t)d->seqs_per_launch * d->Hd * d->max_nL * 4, 256);
+  sl.total = off;
+  z.scratch = off;
+  return nullptr;
+}
+
+}  // namespace
+
+struct spd_ctx {
+  spd_config cfg{};
+  std::vector<unsigned char> streaming;
+  Derived dv;
+  spd_buffers buf{};
+  std::vector<int> free_pages;  // back() is handed out next
+  std::vector<Seq> seqs;
+  std::vector<PtUpdate> pending_pt;
+  bool device_ready = false;
+  int device = 0;
+  int num_sms = 152;
+  std::string err;
+
+  spd_status fail(spd_status s, const char *fmt, ...) {
+    char b[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(b, sizeof b, fmt, ap);
+    va_end(ap);
+    err = b;
+    return s;
+  }
+  int *err_word() { return reinterpret_cast<int *>(buf.scratch); }
+  char *scratch(size_t off) { return static_cast<char *>(buf.scratch) + off; }
+};
+
+namespace {
+
+spd_status cuda_fail(spd_ctx *c, cudaError_t e, const char *what) {
+  return c->fail(SPD_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// First GPU-side call: bind the device that owns the buffers, learn the SM
+// count, and zero the scratch header (error word) and ticket counters.
+spd_status ensure_device(spd_ctx *c, cudaStream_t st) {
+  if (c->device_ready) return SPD_OK;
+  cudaPointerAttributes a{};
+  cudaError_t e = cudaPointerGetAttributes(&a, c->buf.scratch);
+  if (e != cudaSuccess) return cuda_fail(c, e, "cudaPointerGetAttributes(scratch)");
+  if (a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeManaged)
+    return c->fail(SPD_ERR_INVALID_ARG, "scratch is not device memory");
+  c->device = a.device;
+  if ((e = cudaSetDevice(c->device)) != cudaSuccess) return cuda_fail(c, e, "cudaSetDevice");
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, c->device) == cudaSuccess &&
+      sms > 0)
+    c->num_sms = sms;
+  e = cudaMemsetAsync(c->buf.scratch, 0, c->dv.sl.part_ml, st);
+  if (e != cudaSuccess) return cuda_fail(c, e, "cudaMemsetAsync(scratch header)");
+  c->device_ready = true;
+  return SPD_OK;
+}
+
+spd_status check_seqs(spd_ctx *c, const int *ids, int n) {
+  if (!ids || n < 1) return c->fail(SPD_ERR_INVALID_ARG, "seq_ids must list at least one sequence");
+  for (int i = 0; i < n; ++i) {
+    const int s = ids[i];
+    if (s < 0 || s >= (int)c->seqs.size() || !c->seqs[s].live)
+      return c->fail(SPD_ERR_BAD_SEQ, "sequence %d is not live", s);
+    for (int j = 0; j < i; ++j)
+      if (ids[j] == s) return c->fail(SPD_ERR_BAD_SEQ, "sequence %d listed twice", s);
+  }
+  return SPD_OK;
+}
+
+long long pages_needed(const spd_ctx *c, const Seq &s, long long n_tokens) {
+  if (c->dv.Hd == 0) return 0;
+  const long long P = c->cfg.physical_page;
+  const long long need = (s.L + n_tokens + P - 1) / P;
+  return std::max<long long>(0, need - (long long)s.pages.size());
+}
+
+void take_pages(spd_ctx *c, int slot, long long n_tokens) {
+  Seq &s = c->seqs[slot];
+  long long k = pages_needed(c, s, n_tokens);
+  for (; k > 0; --k) {
+    const int phys = c->free_pages.back();
+    c->free_pages.pop_back();
+    c->pending_pt.push_back(PtUpdate{slot, (int)s.pages.size(), phys});
+    s.pages.push_back(phys);
+  }
+}
+
+spd_status flush_page_table(spd_ctx *c, cudaStream_t st) {
+  size_t i = 0;
+  while (i < c->pending_pt.size()) {
+    PtWriteParams p{};
+    p.page_table = static_cast<int *>(c->buf.page_table);
+    p.max_pp = c->dv.max_pp;
+    p.n = (int)std::min<size_t>(kPtUpdPerLaunch, c->pending_pt.size() - i);
+    for (int k = 0; k < p.n; ++k) p.upd[k] = c->pending_pt[i + k];
+    cudaError_t e = launch_pt_write(p, st);
+    if (e != cudaSuccess) return cuda_fail(c, e, "pt_write launch");
+    i += p.n;
+  }
+  c->pending_pt.clear();
+  return SPD_OK;
+}
+
+int nL_of(long long L, int ell) { return (int)((L + ell - 1) / ell); }
+
+int budget_pages(const spd_ctx *c, long long L) {
+  long long budget = c->cfg.token_budget > 0 ? c->cfg.token_budget
+                                             : std::min<long long>(4096, L / 32);
+  return (int)std::max<long long>(1, budget / c->cfg.logical_page);
+}
+
+spd_status append_impl(spd_ctx *c, const int *ids, int n, int n_tokens, const void *k,
+                       const void *v, cudaStream_t st) {
+  spd_status r = ensure_device(c, st);
+  if (r != SPD_OK) return r;
+  for (int i = 0; i < n; ++i) take_pages(c, ids[i], n_tokens);
+  if ((r = flush_page_table(c, st)) != SPD_OK) return r;
+  const Derived &dv = c->dv;
+  const size_t row = (size_t)c->cfg.num_kv_heads * c->cfg.head_dim * 2;  // bytes per token
+  for (int b = 0; b < n; b += dv.seqs_per_launch) {
+    AppendParams p{};
+    p.n_seqs = std::min(dv.seqs_per_launch, n - b);
+    p.k = static_cast<const char *>(k) + (size_t)b * n_tokens * row;
+    p.v = static_cast<const char *>(v) + (size_t)b * n_tokens * row;
+    p.k_pool = c->buf.k_pool;
+    p.v_pool = c->buf.v_pool;
+    p.meta = c->buf.meta;
+    p.stream_k = c->buf.stream_k;
+    p.stream_v = c->buf.stream_v;
+    p.page_table = static_cast<const int *>(c->buf.page_table);
+    p.err = c->err_word();
+    p.n_tokens = n_tokens;
+    p.Hkv = c->cfg.num_kv_heads;
+    p.Hd = dv.Hd;
+    p.Hs = dv.Hs;
+    p.ell = c->cfg.logical_page;
+    p.P = c->cfg.physical_page;
+    p.R = dv.R;
+    p.max_pp = dv.max_pp;
+    p.S = dv.Hs ? c->cfg.sink : 0;
+    p.W = dv.Hs ? c->cfg.window : 0;
+    p.num_phys = c->cfg.num_physical_pages;
+    memcpy(p.dyn_kv, dv.dyn_kv, sizeof p.dyn_kv);
+    memcpy(p.str_kv, dv.str_kv, sizeof p.str_kv);
+    long long ctas = 0;
+    for (int i = 0; i < p.n_seqs; ++i) {
+      const Seq &s = c->seqs[ids[b + i]];
+      p.seqs[i].slot = ids[b + i];
+      p.seqs[i].L_old = (int)s.L;
+      p.seqs[i].cta_off = (int)ctas;
+      const long long j0 = s.L / p.ell, j1 = (s.L + n_tokens + p.ell - 1) / p.ell;
+      ctas += (j1 - j0) * dv.Hd;
+    }
+    if (ctas > 0x7fffffffLL - p.n_seqs * dv.Hs)
+      return c->fail(SPD_ERR_CAPACITY, "append too large for one launch");
+    p.dyn_ctas = (int)ctas;
+    cudaError_t e = launch_append(p, c->cfg.dtype, c->cfg.head_dim, st);
+    if (e != cudaSuccess) return cuda_fail(c, e, "append launch");
+  }
+  for (int i = 0; i < n; ++i) c->seqs[ids[i]].L += n_tokens;
+  return SPD_OK;
+}
+
+spd_status select_impl(spd_ctx *c, const void *q, const int *ids, int n, bool force,
+                       cudaStream_t st) {
+  const Derived &dv = c->dv;
+  std::vector<int> due;  // positions in the call
+  for (int i = 0; i < n; ++i) {
+    const Seq &s = c->seqs[ids[i]];
+    if (force || s.counter % c->cfg.reuse_interval == 0) due.push_back(i);
+  }
+  if (due.empty()) return SPD_OK;
+  if (dv.Hd > 0) {
+    spd_status r = ensure_device(c, st);
+    if (r != SPD_OK) return r;
+    const int ppc = 64;
+    for (size_t b = 0; b < due.size(); b += dv.seqs_per_launch) {
+      SelectParams p{};
+      p.n_seqs = (int)std::min<size_t>(dv.seqs_per_launch, due.size() - b);
+      p.q = q;
+      p.meta = c->buf.meta;
+      p.page_table = static_cast<const int *>(c->buf.page_table);
+      p.selection = static_cast<int *>(c->buf.selection);
+      p.scores = reinterpret_cast<float *>(c->scratch(dv.sl.scores));
+      p.err = c->err_word();
+      p.Hq = c->cfg.num_q_heads;
+      p.Hd = dv.Hd;
+      p.ell = c->cfg.logical_page;
+      p.R = dv.R;
+      p.max_pp = dv.max_pp;
+      p.ksel_max = dv.ksel_max;
+      p.max_nL = dv.max_nL;
+      p.pages_per_chunk = ppc;
+      p.num_phys = c->cfg.num_physical_pages;
+      memcpy(p.dyn_kv, dv.dyn_kv, sizeof p.dyn_kv);
+      int off = 0;
+      for (int i = 0; i < p.n_seqs; ++i) {
+        const int pos = due[b + i];
+        const Seq &s = c->seqs[ids[pos]];
+        SelectSeq &d = p.seqs[i];
+        d.slot = ids[pos];
+        d.qrow = pos;
+        d.nL = nL_of(s.L, p.ell);
+        d.K_sel = budget_pages(c, s.L);
+        d.chunk_off = off;
+        d.n_chunks = d.nL > d.K_sel ? (d.nL - 1 + ppc - 1) / ppc : 0;
+        off += d.n_chunks * dv.Hd;
+      }
+      p.score_ctas = off;
+      cudaError_t e = launch_select(p, c->cfg.dtype, c->cfg.head_dim, dv.G, st);
+      if (e != cudaSuccess) return cuda_fail(c, e, "select launch");
+    }
+  }
+  for (int pos : due) {
+    Seq &s = c->seqs[ids[pos]];
+    const int nL = nL_of(s.L, c->cfg.logical_page);
+    s.nL0 = nL;
+    s.sel_count = std::min(nL, budget_pages(c, s.L));
+    s.has_sel = true;
+  }
+  return SPD_OK;
+}
+
+// Split policy: aim for about four CTAs per SM in total, at least 64 tokens
+// per split, at most 64 splits per (sequence, kv head) and kMaxItems per
+// launch.  Splits never come out empty.
+void plan_splits(const spd_ctx *c, DecodeParams &p, const int *ids) {
+  const Derived &dv = c->dv;
+  const int ell = c->cfg.logical_page;
+  long long total = 0;
+  for (int i = 0; i < p.n_seqs; ++i) {
+    const Seq &s = c->seqs[ids[i]];
+    if (dv.Hd) total += (long long)dv.Hd * (s.sel_count + nL_of(s.L, ell) - s.nL0) * ell;
+    if (dv.Hs) total += (long long)dv.Hs * std::min<long long>(s.L, (long long)p.S + p.W);
+  }
+  long long chunk = std::max<long long>(64, (total + 4LL * c->num_sms - 1) / (4LL * c->num_sms));
+  for (;;) {
+    int items = 0;
+    for (int i = 0; i < p.n_seqs; ++i) {
+      const Seq &s = c->seqs[ids[i]];
+      DecodeSeq &d = p.seqs[i];
+      d.item_off = items;
+      d.ns_dyn = d.ns_str = d.pps = d.tps = 0;
+      if (dv.Hd) {
+        const int n_att = s.sel_count + nL_of(s.L, ell) - s.nL0;
+        long long ns = std::min<long long>({64, (long long)n_att,
+                                            std::max<long long>(1, ((long long)n_att * ell + chunk - 1) / chunk)});
+        d.pps = (int)((n_att + ns - 1) / ns);
+        d.ns_dyn = (n_att + d.pps - 1) / d.pps;
+      }
+      if (dv.Hs) {
+        const long long n_tok = std::min<long long>(s.L, (long long)p.S + p.W);
+        long long ns = std::min<long long>({64, n_tok, std::max<long long>(1, (n_tok + chunk - 1) / chunk)});
+        d.tps = (int)((n_tok + ns - 1) / ns);
+        d.ns_str = (int)((n_tok + d.tps - 1) / d.tps);
+      }
+      items += dv.Hd * d.ns_dyn + dv.Hs * d.ns_str;
+    }
+    p.total_items = items;
+    if (items <= kMaxItems) return;
+    chunk *= 2;
+  }
+}
+
+spd_status attention_impl(spd_ctx *c, const void *q, const int *ids, int n, float *out,
+                          cudaStream_t st) {
+  spd_status r = ensure_device(c, st);
+  if (r != SPD_OK) return r;
+  const Derived &dv = c->dv;
+  const size_t qrow = (size_t)c->cfg.num_q_heads * c->cfg.head_dim;
+  for (int b = 0; b < n; b += dv.seqs_per_launch) {
+    DecodeParams p{};
+    p.n_seqs = std::min(dv.seqs_per_launch, n - b);
+    p.q = static_cast<const char *>(q) + (size_t)b * qrow * 2;
+    p.out = out + (size_t)b * qrow;
+    p.k_pool = c->buf.k_pool;
+    p.v_pool = c->buf.v_pool;
+    p.stream_k = c->buf.stream_k;
+    p.stream_v = c->buf.stream_v;
+    p.page_table = static_cast<const int *>(c->buf.page_table);
+    p.selection = static_cast<const int *>(c->buf.selection);
+    p.part_o = reinterpret_cast<float *>(c->scratch(dv.sl.part_o));
+    p.part_ml = reinterpret_cast<float2 *>(c->scratch(dv.sl.part_ml));
+    p.tickets = reinterpret_cast<int *>(c->scratch(dv.sl.tickets_dec));
+    p.err = c->err_word();
+    p.Hq = c->cfg.num_q_heads;
+    p.Hkv = c->cfg.num_kv_heads;
+    p.Hd = dv.Hd;
+    p.Hs = dv.Hs;
+    p.ell = c->cfg.logical_page;
+    p.P = c->cfg.physical_page;
+    p.R = dv.R;
+    p.max_pp = dv.max_pp;
+    p.ksel_max = dv.ksel_max;
+    p.S = dv.Hs ? c->cfg.sink : 0;
+    p.W = dv.Hs ? c->cfg.window : 0;
+    p.num_phys = c->cfg.num_physical_pages;
+    p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)c->cfg.head_dim));
+    memcpy(p.kv_kind, dv.kv_kind, sizeof p.kv_kind);
+    memcpy(p.kv_sub, dv.kv_sub, sizeof p.kv_sub);
+    memcpy(p.dyn_kv, dv.dyn_kv, sizeof p.dyn_kv);
+    memcpy(p.str_kv, dv.str_kv, sizeof p.str_kv);
+    for (int i = 0; i < p.n_seqs; ++i) {
+      const Seq &s = c->seqs[ids[b + i]];
+      DecodeSeq &d = p.seqs[i];
+      d.slot = ids[b + i];
+      d.L = (int)s.L;
+      d.nL0 = s.nL0;
+      d.sel_count = s.sel_count;
+    }
+    plan_splits(c, p, ids + b);
+    cudaError_t e = launch_decode(p, c->cfg.dtype, c->cfg.head_dim, dv.G, st);
+    if (e != cudaSuccess) return cuda_fail(c, e, "decode launch");
+  }
+  for (int i = 0; i < n; ++i) c->seqs[ids[i]].counter += 1;
+  return SPD_OK;
+}
+
+// will_append: the call appends one token first (so the length will be >= 1)
+// and selects the sequences that are due before attending.
+spd_status check_attend_state(spd_ctx *c, const int *ids, int n, bool will_append) {
+  const bool will_select = will_append;
+  for (int i = 0; i < n; ++i) {
+    const Seq &s = c->seqs[ids[i]];
+    if (s.L < 1 && !will_append)
+      return c->fail(SPD_ERR_STATE, "sequence %d has no tokens", ids[i]);
+    const bool due = s.counter % c->cfg.reuse_interval == 0;
+    if (c->dv.Hd > 0 && !s.has_sel && !(will_select && due))
+      return c->fail(SPD_ERR_STATE, "sequence %d has no page selection yet", ids[i]);
+  }
+  return SPD_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+spd_status spd_query_sizes(const spd_config *cfg, spd_sizes *out) {
+  if (!out) return SPD_ERR_INVALID_ARG;
+  Derived d;
+  if (derive(cfg, &d)) return SPD_ERR_INVALID_ARG;
+  *out = d.sizes;
+  return SPD_OK;
+}
+
+spd_status spd_create(const spd_config *cfg, const spd_buffers *bufs, spd_ctx **out) {
+  if (!out || !bufs) return SPD_ERR_INVALID_ARG;
+  *out = nullptr;
+  Derived d;
+  if (derive(cfg, &d)) return SPD_ERR_INVALID_ARG;
+  const void *ptrs[8] = {bufs->k_pool, bufs->v_pool, bufs->meta, bufs->stream_k,
+                         bufs->stream_v, bufs->page_table, bufs->selection, bufs->scratch};
+  const size_t sizes[8] = {d.sizes.k_pool, d.sizes.v_pool, d.sizes.meta, d.sizes.stream_k,
+                           d.sizes.stream_v, d.sizes.page_table, d.sizes.selection,
+                           d.sizes.scratch};
+  for (int i = 0; i < 8; ++i) {
+    if (sizes[i] && !ptrs[i]) return SPD_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(ptrs[i]) % 256) return SPD_ERR_INVALID_ARG;
+  }
+  spd_ctx *c = new (std::nothrow) spd_ctx();
+  if (!c) return SPD_ERR_INVALID_ARG;
+  c->cfg = *cfg;
+  c->dv = d;
+  if (cfg->kv_head_is_streaming)
+    c->streaming.assign(cfg->kv_head_is_streaming, cfg->kv_head_is_streaming + cfg->num_kv_heads);
+  c->cfg.kv_head_is_streaming = c->streaming.empty() ? nullptr : c->streaming.data();
+  c->buf = *bufs;
+  const int N = d.Hd ? cfg->num_physical_pages : 0;
+  c->free_pages.resize(N);
+  for (int i = 0; i < N; ++i) c->free_pages[i] = N - 1 - i;  // page 0 first
+  if (cfg->free_list_seed) {
+    uint64_t st = cfg->free_list_seed;
+    for (int i = N - 1; i > 0; --i) {
+      const int j = (int)(splitmix64(st) % (uint64_t)(i + 1));
+      std::swap(c->free_pages[i], c->free_pages[j]);
+    }
+  }
+  c->seqs.resize(cfg->max_seqs);
+  *out = c;
+  return SPD_OK;
+}
+
+void spd_destroy(spd_ctx *ctx) { delete ctx; }
+
+spd_status spd_seq_create(spd_ctx *c, int *seq_id_out) {
+  if (!c || !seq_id_out) return SPD_ERR_INVALID_ARG;
+  for (int i = 0; i < (int)c->seqs.size(); ++i)
+    if (!c->seqs[i].live) {
+      c->seqs[i] = Seq();
+      c->seqs[i].live = true;
+      *seq_id_out = i;
+      return SPD_OK;
+    }
+  return c->fail(SPD_ERR_CAPACITY, "all %d sequence slots are live", (int)c->seqs.size());
+}
+
+spd_status spd_seq_free(spd_ctx *c, int seq_id) {
+  if (!c) return SPD_ERR_INVALID_ARG;
+  if (seq_id < 0 || seq_id >= (int)c->seqs.size() || !c->seqs[seq_id].live)
+    return c->fail(SPD_ERR_BAD_SEQ, "sequence %d is not live", seq_id);
+  Seq &s = c->seqs[seq_id];
+  for (auto it = s.pages.rbegin(); it != s.pages.rend(); ++it) c->free_pages.push_back(*it);
+  // drop queued page-table writes of this sequence (its pages are free again)
+  c->pending_pt.erase(std::remove_if(c->pending_pt.begin(), c->pending_pt.end(),
+                                     [&](const PtUpdate &u) { return u.slot == seq_id; }),
+                      c->pending_pt.end());
+  s = Seq();
+  return SPD_OK;
+}
+
+spd_status spd_seq_reserve(spd_ctx *c, int seq_id, int n_tokens) {
+  if (!c || n_tokens < 0) return SPD_ERR_INVALID_ARG;
+  spd_status r = check_seqs(c, &seq_id, 1);
+  if (r != SPD_OK) return r;
+  const Seq &s = c->seqs[seq_id];
+  if (s.L + n_tokens > c->cfg.max_context)
+    return c->fail(SPD_ERR_CAPACITY, "sequence %d: %lld + %d tokens exceed max_context %d", seq_id,
+                   s.L, n_tokens, c->cfg.max_context);
+  const long long need = pages_needed(c, s, n_tokens);
+  if (need > (long long)c->free_pages.size())
+    return c->fail(SPD_ERR_NO_PAGES, "need %lld physical pages, %zu free", need,
+                   c->free_pages.size());
+  take_pages(c, seq_id, n_tokens);
+  return SPD_OK;
+}
+
+spd_status spd_seq_info(spd_ctx *c, int seq_id, long long *length, long long *step_counter,
+                        int *pages_at_selection, int *pages_kept) {
+  if (!c) return SPD_ERR_INVALID_ARG;
+  spd_status r = check_seqs(c, &seq_id, 1);
+  if (r != SPD_OK) return r;
+  const Seq &s = c->seqs[seq_id];
+  if (length) *length = s.L;
+  if (step_counter) *step_counter = s.counter;
+  if (pages_at_selection) *pages_at_selection = s.has_sel ? s.nL0 : 0;
+  if (pages_kept) *pages_kept = s.has_sel ? s.sel_count : 0;
+  return SPD_OK;
+}
+
+spd_status spd_get_page_table(spd_ctx *c, int seq_id, int *phys_host, int cap, int *n_host) {
+  if (!c || !n_host) return SPD_ERR_INVALID_ARG;
+  spd_status r = check_seqs(c, &seq_id, 1);
+  if (r != SPD_OK) return r;
+  const Seq &s = c->seqs[seq_id];
+  *n_host = (int)s.pages.size();
+  if (phys_host)
+    for (int i = 0; i < std::min(cap, (int)s.pages.size()); ++i) phys_host[i] = s.pages[i];
+  return SPD_OK;
+}
+
+spd_status spd_free_pages(spd_ctx *c, int *n_free) {
+  if (!c || !n_free) return SPD_ERR_INVALID_ARG;
+  *n_free = (int)c->free_pages.size();
+  return SPD_OK;
+}
+
+static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+static spd_status check_append(spd_ctx *c, const int *ids, int n, int n_tokens, const void *k,
+                               const void *v) {
+  if (n_tokens < 1 || !k || !v) return c->fail(SPD_ERR_INVALID_ARG, "n_tokens >= 1 and k, v required");
+  if (!aligned16(k) || !aligned16(v)) return c->fail(SPD_ERR_INVALID_ARG, "k, v must be 16-byte aligned");
+  spd_status r = check_seqs(c, ids, n);
+  if (r != SPD_OK) return r;
+  long long need = 0;
+  for (int i = 0; i < n; ++i) {
+    const Seq &s = c->seqs[ids[i]];
+    if (s.L + n_tokens > c->cfg.max_context)
+      return c->fail(SPD_ERR_CAPACITY, "sequence %d: %lld + %d tokens exceed max_context %d",
+                     ids[i], s.L, n_tokens, c->cfg.max_context);
+    need += pages_needed(c, s, n_tokens);
+  }
+  if (need > (long long)c->free_pages.size())
+    return c->fail(SPD_ERR_NO_PAGES, "need %lld physical pages, %zu free", need,
+                   c->free_pages.size());
+  return SPD_OK;
+}
+
+spd_status spd_kv_append(spd_ctx *c, const int *seq_ids, int n_seqs, int n_tokens, const void *k,
+                         const void *v, spd_stream stream) {
+  if (!c) return SPD_ERR_INVALID_ARG;
+  spd_status r = check_append(c, seq_ids, n_seqs, n_tokens, k, v);
+  if (r != SPD_OK) return r;
+  return append_impl(c, seq_ids, n_seqs, n_tokens, k, v, (cudaStream_t)stream);
+}
+
+spd_status spd_select_pages(spd_ctx *c, const void *q, const int *seq_ids, int n_seqs, int force,
+                            spd_stream stream) {
+  if (!c) return SPD_ERR_INVALID_ARG;
+  if (!q || !aligned16(q)) return c->fail(SPD_ERR_INVALID_ARG, "q must be a 16-byte aligned pointer");
+  spd_status r = check_seqs(c, seq_ids, n_seqs);
+  if (r != SPD_OK) return r;
+  for (int i = 0; i < n_seqs; ++i)
+    if (c->seqs[seq_ids[i]].L < 1)
+      return c->fail(SPD_ERR_STATE, "sequence %d has no tokens", seq_ids[i]);
+  return select_impl(c, q, seq_ids, n_seqs, force != 0, (cudaStream_t)stream);
+}
+
+spd_status spd_sparse_decode_attention(spd_ctx *c, const void *q, const int *seq_ids, int n_seqs,
+                                       float *out, spd_stream stream) {
+  if (!c) return SPD_ERR_INVALID_ARG;
+  if (!q || !out || !aligned16(q) || !aligned16(out))
+    return c->fail(SPD_ERR_INVALID_ARG, "q and out must be 16-byte aligned pointers");
+  spd_status r = check_seqs(c, seq_ids, n_seqs);
+  if (r != SPD_OK) return r;
+  if ((r = check_attend_state(c, seq_ids, n_seqs, false)) != SPD_OK) return r;
+  return attention_impl(c, q, seq_ids, n_seqs, out, (cudaStream_t)stream);
+}
+
+spd_status spd_decode_step(spd_ctx *c, const void *q, const void *k, const void *v,
+                           const int *seq_ids, int n_seqs, float *out, spd_stream stream) {
+  if (!c) return SPD_ERR_INVALID_ARG;
+  if (!q || !out || !aligned16(q) || !aligned16(out))
+    return c->fail(SPD_ERR_INVALID_ARG, "q and out must be 16-byte aligned pointers");
+  spd_status r = check_append(c, seq_ids, n_seqs, 1, k, v);
+  if (r != SPD_OK) return r;
+  if ((r = check_attend_state(c, seq_ids, n_seqs, true)) != SPD_OK) return r;
+  cudaStream_t st = (cudaStream_t)stream;
+  if ((r = append_impl(c, seq_ids, n_seqs, 1, k, v, st)) != SPD_OK) return r;
+  if ((r = select_impl(c, q, seq_ids, n_seqs, false, st)) != SPD_OK) return r;
+  return attention_impl(c, q, seq_ids, n_seqs, out, st);
+}
+
+spd_status spd_get_selection(spd_ctx *c, int seq_id, int kv_head, int *idx_host, int cap,
+                             int *count_host, spd_stream stream) {
+  if (!c || !count_host) return SPD_ERR_INVALID_ARG;
+  spd_status r = check_seqs(c, &seq_id, 1);
+  if (r != SPD_OK) return r;
+  if (kv_head < 0 || kv_head >= c->cfg.num_kv_heads || c->dv.kv_kind[kv_head] != 0)
+    return c->fail(SPD_ERR_INVALID_ARG, "kv head %d is not a dynamic head", kv_head);
+  const Seq &s = c->seqs[seq_id];
+  if (!s.has_sel) return c->fail(SPD_ERR_STATE, "sequence %d has no selection", seq_id);
+  *count_host = s.sel_count;
+  if (!idx_host) return SPD_OK;
+  cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(c, e, "cudaStreamSynchronize");
+  const int *src = static_cast<const int *>(c->buf.selection) +
+                   ((size_t)seq_id * c->dv.Hd + c->dv.kv_sub[kv_head]) * c->dv.ksel_max;
+  e = cudaMemcpy(idx_host, src, sizeof(int) * std::min(cap, s.sel_count), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(c, e, "cudaMemcpy(selection)");
+  return SPD_OK;
+}
+
+spd_status spd_check_status(spd_ctx *c, spd_stream stream) {
+  if (!c) return SPD_ERR_INVALID_ARG;
+  if (!c->device_ready) return SPD_OK;
+  cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(c, e, "cudaStreamSynchronize");
+  int w[4] = {0, 0, 0, 0};
+  e = cudaMemcpy(w, c->buf.scratch, sizeof w, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(c, e, "cudaMemcpy(error word)");
+  if (w[0] == 0) return SPD_OK;
+  cudaMemset(c->buf.scratch, 0, sizeof w);
+  return c->fail(SPD_ERR_DEVICE_CHECK, "device check %d (details %d %d %d)", w[0], w[1], w[2], w[3]);
+}
+
+const char *spd_status_string(spd_status s) {
+  switch (s) {
+    case SPD_OK: return "ok";
+    case SPD_ERR_INVALID_ARG: return "invalid argument";
+    case SPD_ERR_NO_PAGES: return "no free physical pages";
+    case SPD_ERR_BAD_SEQ: return "bad sequence id";
+    case SPD_ERR_CAPACITY: return "capacity exceeded";
+    case SPD_ERR_CUDA: return "CUDA error";
+    case SPD_ERR_DEVICE_CHECK: return "device bounds check failed";
+    case SPD_ERR_STATE: return "call out of order";
+  }
+  return "unknown status";
+}
+
+const char *spd_last_error(spd_ctx *c) { return c ? c->err.c_str() : ""; }
+
+}  // extern "C"
