@@ -228,6 +228,8 @@ spd_status spd_get_selection(spd_ctx *ctx, int seq_id, int kv_head,
 spd_status spd_check_status(spd_ctx *ctx, spd_stream stream);
 
 const char *spd_status_string(spd_status s);
+/* Number of kernels this context has enqueued since it was created. */
+spd_status spd_launch_count(spd_ctx *ctx, long long *n);
 /* Human-readable detail of the last error on this context ("" if none). */
 const char *spd_last_error(spd_ctx *ctx);
 

@@ -84,6 +84,7 @@ def lib():
         "spd_decode_step": [vp, vp, vp, vp, ip, i, vp, vp],
         "spd_get_selection": [vp, i, i, ip, i, ip, vp],
         "spd_check_status": [vp, vp],
+        "spd_launch_count": [vp, ll],
     }
     for name, args in sig.items():
         f = getattr(L, name)
@@ -229,6 +230,12 @@ def spd_check_status(ctx, stream=0):
     _check(lib().spd_check_status(ctx, stream or None), "spd_check_status", ctx)
 
 
+def spd_launch_count(ctx):
+    n = ctypes.c_longlong()
+    _check(lib().spd_launch_count(ctx, ctypes.byref(n)), "spd_launch_count", ctx)
+    return n.value
+
+
 # ---- high level: torch-allocated buffers ----------------------------------------
 
 class SparsePagedKVCache:
@@ -332,3 +339,6 @@ class SparsePagedKVCache:
 
     def check_status(self, stream=None):
         spd_check_status(self.ctx, self._stream(stream))
+
+    def launch_count(self):
+        return spd_launch_count(self.ctx)

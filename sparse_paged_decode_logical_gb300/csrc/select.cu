@@ -1,0 +1,303 @@
+// Query-aware page selection for sm_103a ("LServe long-sequence LLM serving
+// system", section 2.1 dynamic sparsity; section 3.2 reusable selector and
+// dynamic budget).
+//
+// Score.  For a logical page j with channel-wise key bounds kmin <= kmax and
+// a query head q,
+//     s(j) = sum_c max(q_c kmax_c, q_c kmin_c) = sum_c (q+_c kmax_c + q-_c kmin_c)
+// with q+ = max(q, 0), q- = min(q, 0): for q_c >= 0 the larger product is the
+// one with kmax, for q_c < 0 the one with kmin.  So the score is a dot
+// product of the page's 2d-long metadata row [kmin ; kmax] with [q- ; q+],
+// and the G heads of a kv head make it a [pages x 2d] x [2d x G] contraction:
+// mma.sync m16n8k16 with the pages as M, the heads (padded to 8) as N.  The
+// products of 16-bit values are exact; the sum is fp32.  S(j) = max over the
+// G heads.
+//
+// Fragments are loaded straight from global memory: the k order inside each
+// pair of k-steps is permuted (both operands alike, which leaves the sum
+// unchanged) so that every thread reads 16 contiguous bytes of a metadata
+// row per load.
+//
+// Top-k.  Each scoring CTA writes its pages' scores, then takes a ticket;
+// the last CTA of a (sequence, head) runs an exact radix select for the
+// K_sel - 1 highest scores among pages [0, nL-1) (ties to the lower page
+// index, -0 folded onto +0), adds the newest page nL-1, and writes the set in
+// ascending order.  No CTA ever waits for another.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <math_constants.h>
+
+#include "ptx.cuh"
+#include "spd_internal.h"
+
+namespace spd {
+namespace {
+
+constexpr int kSelThreads = 256;
+constexpr int kSelWarps = kSelThreads / 32;
+constexpr int kPagesPerWarp = 16;
+constexpr int kPagesPerCta = kSelWarps * kPagesPerWarp;  // 128
+
+template <typename T> struct IsBf { static constexpr bool v = false; };
+template <> struct IsBf<__nv_bfloat16> { static constexpr bool v = true; };
+
+template <typename T> struct Neg;
+template <> struct Neg<__half> {
+  static __device__ __forceinline__ bool neg(uint16_t b) { return (b & 0x8000u) && (b & 0x7fffu); }
+};
+template <> struct Neg<__nv_bfloat16> {
+  static __device__ __forceinline__ bool neg(uint16_t b) { return (b & 0x8000u) && (b & 0x7fffu); }
+};
+
+__device__ __forceinline__ void set_err(int *err, int code, int a, int b, int c) {
+  if (atomicCAS(err, 0, code) == 0) {
+    err[1] = a;
+    err[2] = b;
+    err[3] = c;
+  }
+}
+
+__device__ __forceinline__ uint32_t score_key(float f) {
+  if (f != f) return 0u;
+  if (f == 0.f) f = 0.f;
+  const uint32_t b = __float_as_uint(f);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+// Exclusive scan over the CTA (kSelThreads threads); *total = sum.
+__device__ __forceinline__ int cta_excl_scan(int v, int *sh, int *total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) sh[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < kSelWarps ? sh[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    if (lane < kSelWarps) sh[lane] = w;
+    if (lane == kSelWarps - 1) sh[32] = w;
+  }
+  __syncthreads();
+  const int res = x - v + (warp > 0 ? sh[warp - 1] : 0);
+  *total = sh[32];
+  __syncthreads();
+  return res;
+}
+
+// Radix select of the k highest of n scores (k >= 1, n > k); writes the
+// chosen indices ascending to out[0..k).  Returns the count written.
+__device__ int cta_topk(const float *sc, int n, int k, int *out) {
+  __shared__ int hist[256];
+  __shared__ int sh[33];
+  __shared__ uint32_t s_prefix;
+  __shared__ int s_remaining;
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    s_prefix = 0;
+    s_remaining = k;
+  }
+  uint32_t mask = 0;
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int b = tid; b < 256; b += kSelThreads) hist[b] = 0;
+    __syncthreads();
+    const uint32_t prefix = s_prefix;
+    for (int j = tid; j < n; j += kSelThreads) {
+      const uint32_t u = score_key(__ldcg(sc + j));
+      if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & 0xffu], 1);
+    }
+    __syncthreads();
+    if (tid == 0) {
+      int rem = s_remaining, cum = 0, b = 255;
+      for (; b > 0; --b) {
+        if (cum + hist[b] >= rem) break;
+        cum += hist[b];
+      }
+      s_remaining = rem - cum;
+      s_prefix = prefix | ((uint32_t)b << shift);
+    }
+    mask |= 0xffu << shift;
+    __syncthreads();
+  }
+  const uint32_t T = s_prefix;
+  const int take_eq = s_remaining;
+  int eq_seen = 0, taken = 0;
+  for (int base = 0; base < n; base += kSelThreads) {
+    const int j = base + tid;
+    const uint32_t u = j < n ? score_key(__ldcg(sc + j)) : 0u;
+    const int gt = j < n && u > T;
+    const int eq = j < n && u == T;
+    int tot_eq, tot_take;
+    const int eq_rank = cta_excl_scan(eq, sh, &tot_eq) + eq_seen;
+    const int take = gt || (eq && eq_rank < take_eq);
+    const int pos = cta_excl_scan(take, sh, &tot_take) + taken;
+    if (take && pos < k) out[pos] = j;
+    eq_seen += tot_eq;
+    taken += tot_take;
+  }
+  return taken;
+}
+
+template <typename T, int D, int G>
+__global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_constant__ SelectParams p) {
+  __shared__ int s_last;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int i = 0;
+  while (i + 1 < p.n_seqs && p.seqs[i + 1].chunk_off <= (int)blockIdx.x) ++i;
+  const SelectSeq s = p.seqs[i];
+  const int local = blockIdx.x - s.chunk_off;
+  const int per_head = max(1, s.n_chunks);
+  const int hd = local / per_head;
+  const int chunk = local % per_head;
+  const int h = p.dyn_kv[hd];
+  int *out = p.selection + ((size_t)s.slot * p.Hd + hd) * p.ksel_max;
+  if (s.n_chunks == 0) {
+    // every page is kept (nL <= K_sel), or only the newest one (K_sel = 1)
+    if (s.nL <= s.K_sel) {
+      for (int j = tid; j < s.nL; j += kSelThreads) out[j] = j;
+    } else if (tid == 0) {
+      out[0] = s.nL - 1;
+    }
+    return;
+  }
+  const int n = s.nL - 1;  // candidate pages
+  float *scores = p.scores + ((size_t)i * p.Hd + hd) * p.max_nL;
+
+  // ---- B operand: [q- ; q+] over 2D rows of k, heads as the 8 columns ----
+  // k-step pair s2 covers metadata elements [32*s2, 32*s2 + 32); thread t4
+  // of a k-step pair owns elements 32*s2 + 8*t4 + [0, 8): the first four are
+  // its k indices {2t4, 2t4+1, 2t4+8, 2t4+9} of step 2*s2, the last four the
+  // same k indices of step 2*s2+1.
+  constexpr int KSTEPS = 2 * D / 16;
+  const int g8 = lane >> 2, t4 = lane & 3;
+  uint32_t qb[KSTEPS][2];
+  {
+    const uint16_t *qp = reinterpret_cast<const uint16_t *>(p.q) + ((size_t)s.qrow * p.Hq + h * G) * D;
+#pragma unroll
+    for (int kk = 0; kk < KSTEPS; ++kk) {
+      uint16_t e[4] = {0, 0, 0, 0};
+      if (g8 < G) {
+        const int base = 32 * (kk >> 1) + 8 * t4 + 4 * (kk & 1);  // metadata element
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+          const int m = base + x;  // < D: a kmin element, else kmax
+          const uint16_t qv = qp[g8 * D + (m % D)];
+          const bool neg = Neg<T>::neg(qv);
+          e[x] = (m < D) == neg ? qv : (uint16_t)0;  // kmin takes q-, kmax takes q+
+        }
+      }
+      qb[kk][0] = (uint32_t)e[0] | ((uint32_t)e[1] << 16);
+      qb[kk][1] = (uint32_t)e[2] | ((uint32_t)e[3] << 16);
+    }
+  }
+
+  // ---- score 16 pages per warp ----
+  const int j0 = chunk * kPagesPerCta + warp * kPagesPerWarp;
+  if (j0 < n) {
+    const uint16_t *meta = static_cast<const uint16_t *>(p.meta);
+    const uint4 *rowp[2];
+    bool ok[2];
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const int j = j0 + g8 + 8 * hh;
+      ok[hh] = j < n;
+      rowp[hh] = nullptr;
+      if (ok[hh]) {
+        const int blk = j / p.R;
+        const int phys = p.page_table[(size_t)s.slot * p.max_pp + blk];
+        if (phys < 0 || phys >= p.num_phys) {
+          set_err(p.err, kDevBadPhys, s.slot, blk, phys);
+          ok[hh] = false;
+        } else {
+          rowp[hh] = reinterpret_cast<const uint4 *>(
+              meta + (((size_t)phys * p.Hd + hd) * p.R + (j % p.R)) * 2 * D);
+        }
+      }
+    }
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    constexpr int PAIRS = KSTEPS / 2;
+    uint4 ra[PAIRS], rb[PAIRS];
+#pragma unroll
+    for (int s2 = 0; s2 < PAIRS; ++s2) {
+      ra[s2] = ok[0] ? __ldg(rowp[0] + 4 * s2 + t4) : make_uint4(0, 0, 0, 0);
+      rb[s2] = ok[1] ? __ldg(rowp[1] + 4 * s2 + t4) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int s2 = 0; s2 < PAIRS; ++s2) {
+      const uint32_t a0[4] = {ra[s2].x, rb[s2].x, ra[s2].y, rb[s2].y};
+      mma_16816<IsBf<T>::v>(acc, a0, qb[2 * s2][0], qb[2 * s2][1]);
+      const uint32_t a1[4] = {ra[s2].z, rb[s2].z, ra[s2].w, rb[s2].w};
+      mma_16816<IsBf<T>::v>(acc, a1, qb[2 * s2 + 1][0], qb[2 * s2 + 1][1]);
+    }
+    // acc: [0],[1] page g8 heads 2t4, 2t4+1; [2],[3] page g8+8
+    float s0 = -CUDART_INF_F, s1 = -CUDART_INF_F;
+    if (2 * t4 < G) {
+      s0 = acc[0];
+      s1 = acc[2];
+    }
+    if (2 * t4 + 1 < G) {
+      s0 = fmaxf(s0, acc[1]);
+      s1 = fmaxf(s1, acc[3]);
+    }
+    s0 = fmaxf(s0, __shfl_xor_sync(0xffffffffu, s0, 1));
+    s0 = fmaxf(s0, __shfl_xor_sync(0xffffffffu, s0, 2));
+    s1 = fmaxf(s1, __shfl_xor_sync(0xffffffffu, s1, 1));
+    s1 = fmaxf(s1, __shfl_xor_sync(0xffffffffu, s1, 2));
+    if (t4 == 0) {
+      if (ok[0]) scores[j0 + g8] = s0;
+      if (ok[1]) scores[j0 + g8 + 8] = s1;
+    }
+  }
+
+  // ---- the last scoring CTA of this (sequence, head) selects ----
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    const int prev = atomicAdd(&p.tickets[i * p.Hd + hd], 1);
+    s_last = prev == s.n_chunks - 1;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const int k = s.K_sel - 1;
+  const int got = cta_topk(scores, n, k, out);
+  if (tid == 0) {
+    out[k] = s.nL - 1;
+    if (got != k) set_err(p.err, kDevTopkCount, s.slot, hd, got);
+    p.tickets[i * p.Hd + hd] = 0;
+  }
+}
+
+template <typename T, int D>
+cudaError_t launch_g(const SelectParams &p, int G, cudaStream_t st) {
+  const int grid = p.score_ctas;
+  switch (G) {
+    case 1: select_kernel<T, D, 1><<<grid, kSelThreads, 0, st>>>(p); break;
+    case 2: select_kernel<T, D, 2><<<grid, kSelThreads, 0, st>>>(p); break;
+    case 4: select_kernel<T, D, 4><<<grid, kSelThreads, 0, st>>>(p); break;
+    case 8: select_kernel<T, D, 8><<<grid, kSelThreads, 0, st>>>(p); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int select_pages_per_cta() { return kPagesPerCta; }
+
+cudaError_t launch_select_fused(const SelectParams &p, int dtype, int d, int G, cudaStream_t s,
+                                long long *n) {
+  if (p.n_seqs == 0 || p.Hd == 0 || p.score_ctas == 0) return cudaSuccess;
+  *n += 1;
+  if (dtype == 0) return d == 64 ? launch_g<__half, 64>(p, G, s) : launch_g<__half, 128>(p, G, s);
+  return d == 64 ? launch_g<__nv_bfloat16, 64>(p, G, s) : launch_g<__nv_bfloat16, 128>(p, G, s);
+}
+
+}  // namespace spd

@@ -3,6 +3,7 @@
 // value, so a launch needs no host staging buffer and can be captured into a
 // CUDA graph as is.
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -22,6 +23,7 @@ enum DevErr : int {
   kDevBadPage = 2,      // logical page beyond the page table row
   kDevBadSelection = 3, // selection entry out of range
   kDevTopkCount = 4,    // top-k produced a count different from K_sel
+  kDevTimeout = 5,      // a bounded mbarrier wait gave up
 };
 
 struct ScratchLayout {
@@ -67,8 +69,9 @@ struct SelectSeq {
   int qrow;       // row of this sequence in the call's q array
   int nL;         // logical pages at selection time
   int K_sel;      // pages to keep
-  int chunk_off;  // first scoring CTA of this sequence (0 chunks if nL<=K_sel)
-  int n_chunks;   // scoring CTAs per dynamic head
+  int chunk_off;  // first CTA of this sequence
+  int n_chunks;   // scoring CTAs per dynamic head (0: nothing to score, one CTA
+                  // writes the trivial selection)
 };
 
 struct SelectParams {
@@ -77,6 +80,7 @@ struct SelectParams {
   const int *page_table;
   int *selection;       // [max_seqs][Hd][ksel_max]
   float *scores;        // [kSeqsPerLaunch][Hd][max_nL]
+  int *tickets;         // [kSeqsPerLaunch][Hd], zero between launches
   int *err;
   int n_seqs, Hq, Hd, ell, R, max_pp, ksel_max, max_nL, pages_per_chunk,
       num_phys;
@@ -85,22 +89,25 @@ struct SelectParams {
   SelectSeq seqs[kSeqsPerLaunch];
 };
 
-// ---- split-K decode + combine ----------------------------------------------
-struct DecodeSeq {
+// ---- split-K decode over 16-row tiles (decode.cu) ---------------------------
+struct TileSeq {
   int slot, L;
   int nL0;        // logical pages when the selection was taken
   int sel_count;  // pages in the stored selection
   int item_off;   // first work item of this sequence
-  int ns_dyn;     // splits per dynamic head
-  int ns_str;     // splits per streaming head
-  int pps;        // attended pages per dynamic split
-  int tps;        // attended tokens per streaming split
+  int ns_dyn;     // items per dynamic head
+  int ns_str;     // items per streaming head
+  int tpi_dyn;    // tiles per dynamic item
+  int tpi_str;    // tiles per streaming item
 };
 
-struct DecodeParams {
-  const void *q;
-  float *out;           // [n_seqs][Hq][d]
-  const void *k_pool, *v_pool, *stream_k, *stream_v;
+struct TileDecodeParams {
+  CUtensorMap tm_k, tm_v;    // pool:      dims {d, P, Nphys*Hd}, box {64, 16, 1}
+  CUtensorMap tm_sk, tm_sv;  // streaming: dims {d, max_seqs*Hs*(S+W), 1}, box {64, 16, 1}
+  const void *q;             // [n_seqs][Hq][d]
+  const void *k_new, *v_new; // [n_seqs][Hkv][d] for a fused append, else null
+  float *out;                // [n_seqs][Hq][d]
+  void *k_pool, *v_pool, *meta, *stream_k, *stream_v;
   const int *page_table, *selection;
   float *part_o;
   float2 *part_ml;
@@ -108,21 +115,26 @@ struct DecodeParams {
   int *err;
   int n_seqs, Hq, Hkv, Hd, Hs, ell, P, R, max_pp, ksel_max, S, W, num_phys;
   int total_items;
-  float scale_log2;     // log2(e) / sqrt(d)
-  unsigned char kv_kind[kMaxKvHeads];  // 0 dynamic, 1 streaming
-  unsigned char kv_sub[kMaxKvHeads];   // index within its kind
+  float scale_log2;
   unsigned char dyn_kv[kMaxKvHeads];
   unsigned char str_kv[kMaxKvHeads];
-  DecodeSeq seqs[kSeqsPerLaunch];
+  TileSeq seqs[kSeqsPerLaunch];
 };
 
-// Launchers (kernels.cu).  dtype: 0 fp16, 1 bf16.  Return cudaGetLastError().
-cudaError_t launch_pt_write(const PtWriteParams &p, cudaStream_t s);
-cudaError_t launch_append(const AppendParams &p, int dtype, int d,
-                          cudaStream_t s);
-cudaError_t launch_select(const SelectParams &p, int dtype, int d, int G,
-                          cudaStream_t s);
-cudaError_t launch_decode(const DecodeParams &p, int dtype, int d, int G,
-                          cudaStream_t s);
+constexpr int kTileRows = 16;
+constexpr int kMaxTilesPerItem = 8;
+
+cudaError_t prepare_decode_kernels();
+cudaError_t launch_decode_tiles(const TileDecodeParams &p, int dtype, int d, int G,
+                                cudaStream_t s, long long *launches);
+
+// Launchers.  dtype: 0 fp16, 1 bf16.  Return cudaGetLastError() and add the
+// number of kernels enqueued to *launches.
+cudaError_t launch_pt_write(const PtWriteParams &p, cudaStream_t s, long long *launches);
+cudaError_t launch_append(const AppendParams &p, int dtype, int d, cudaStream_t s,
+                          long long *launches);
+int select_pages_per_cta();
+cudaError_t launch_select_fused(const SelectParams &p, int dtype, int d, int G, cudaStream_t s,
+                                long long *launches);
 
 }  // namespace spd

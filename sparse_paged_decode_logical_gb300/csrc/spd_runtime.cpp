@@ -17,6 +17,8 @@
 #include <string>
 #include <vector>
 
+#include <cudaTypedefs.h>
+
 #include "spd.h"
 #include "spd_internal.h"
 
@@ -96,6 +98,12 @@ const char *derive(const spd_config *c, Derived *d) {
                                          : std::min<long long>(4096, c->max_context / 32);
   d->ksel_max = (int)std::max<long long>(1, budget / c->logical_page);
   d->seqs_per_launch = std::min(c->max_seqs, kSeqsPerLaunch);
+  // one unit (sequence, kv head) must fit in one launch's work items
+  const long long unit_cap = (long long)kMaxItems * kMaxTilesPerItem * kTileRows / 2;
+  if (d->Hs > 0 && (long long)c->sink + c->window > unit_cap) return "sink + window too large";
+  if ((long long)d->ksel_max * c->logical_page > unit_cap) return "token budget too large";
+  if (d->Hs > 0 && (long long)c->max_seqs * d->Hs * (c->sink + c->window) >= (1LL << 31))
+    return "streaming buffers exceed 2^31 rows";
 
   const size_t e = 2, dim = (size_t)c->head_dim;
   const int S = d->Hs ? c->sink : 0, W = d->Hs ? c->window : 0;
@@ -135,6 +143,8 @@ struct spd_ctx {
   bool device_ready = false;
   int device = 0;
   int num_sms = 152;
+  long long launches = 0;  // kernels enqueued by this context
+  CUtensorMap tm_k{}, tm_v{}, tm_sk{}, tm_sv{};
   std::string err;
 
   spd_status fail(spd_status s, const char *fmt, ...) {
@@ -156,6 +166,51 @@ spd_status cuda_fail(spd_ctx *c, cudaError_t e, const char *what) {
   return c->fail(SPD_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
+// TMA descriptors over the paged pool and the streaming buffers: 3-D tiled
+// maps, boxes of 64 channels x 16 rows, 128-byte swizzle.
+spd_status encode_map(spd_ctx *c, CUtensorMap *m, void *base, uint64_t rows_per_plane,
+                      uint64_t planes) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  if (!encode) {
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                     cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+      return c->fail(SPD_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  const uint64_t d = (uint64_t)c->cfg.head_dim;
+  cuuint64_t dims[3] = {d, rows_per_plane, planes};
+  cuuint64_t strides[2] = {d * 2, rows_per_plane * d * 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)kTileRows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = encode(m,
+                      c->cfg.dtype == SPD_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                               : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                      3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return c->fail(SPD_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return SPD_OK;
+}
+
+spd_status make_tensor_maps(spd_ctx *c) {
+  const Derived &dv = c->dv;
+  spd_status r;
+  if (dv.Hd > 0) {
+    const uint64_t planes = (uint64_t)c->cfg.num_physical_pages * dv.Hd;
+    if ((r = encode_map(c, &c->tm_k, c->buf.k_pool, c->cfg.physical_page, planes)) != SPD_OK) return r;
+    if ((r = encode_map(c, &c->tm_v, c->buf.v_pool, c->cfg.physical_page, planes)) != SPD_OK) return r;
+  }
+  if (dv.Hs > 0) {
+    const uint64_t rows = (uint64_t)c->cfg.max_seqs * dv.Hs * (c->cfg.sink + c->cfg.window);
+    if ((r = encode_map(c, &c->tm_sk, c->buf.stream_k, rows, 1)) != SPD_OK) return r;
+    if ((r = encode_map(c, &c->tm_sv, c->buf.stream_v, rows, 1)) != SPD_OK) return r;
+  }
+  return SPD_OK;
+}
+
 // First GPU-side call: bind the device that owns the buffers, learn the SM
 // count, and zero the scratch header (error word) and ticket counters.
 spd_status ensure_device(spd_ctx *c, cudaStream_t st) {
@@ -171,6 +226,9 @@ spd_status ensure_device(spd_ctx *c, cudaStream_t st) {
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, c->device) == cudaSuccess &&
       sms > 0)
     c->num_sms = sms;
+  if ((e = prepare_decode_kernels()) != cudaSuccess) return cuda_fail(c, e, "kernel attributes");
+  spd_status r = make_tensor_maps(c);
+  if (r != SPD_OK) return r;
   e = cudaMemsetAsync(c->buf.scratch, 0, c->dv.sl.part_ml, st);
   if (e != cudaSuccess) return cuda_fail(c, e, "cudaMemsetAsync(scratch header)");
   c->device_ready = true;
@@ -215,7 +273,7 @@ spd_status flush_page_table(spd_ctx *c, cudaStream_t st) {
     p.max_pp = c->dv.max_pp;
     p.n = (int)std::min<size_t>(kPtUpdPerLaunch, c->pending_pt.size() - i);
     for (int k = 0; k < p.n; ++k) p.upd[k] = c->pending_pt[i + k];
-    cudaError_t e = launch_pt_write(p, st);
+    cudaError_t e = launch_pt_write(p, st, &c->launches);
     if (e != cudaSuccess) return cuda_fail(c, e, "pt_write launch");
     i += p.n;
   }
@@ -276,7 +334,7 @@ spd_status append_impl(spd_ctx *c, const int *ids, int n, int n_tokens, const vo
     if (ctas > 0x7fffffffLL - p.n_seqs * dv.Hs)
       return c->fail(SPD_ERR_CAPACITY, "append too large for one launch");
     p.dyn_ctas = (int)ctas;
-    cudaError_t e = launch_append(p, c->cfg.dtype, c->cfg.head_dim, st);
+    cudaError_t e = launch_append(p, c->cfg.dtype, c->cfg.head_dim, st, &c->launches);
     if (e != cudaSuccess) return cuda_fail(c, e, "append launch");
   }
   for (int i = 0; i < n; ++i) c->seqs[ids[i]].L += n_tokens;
@@ -295,7 +353,7 @@ spd_status select_impl(spd_ctx *c, const void *q, const int *ids, int n, bool fo
   if (dv.Hd > 0) {
     spd_status r = ensure_device(c, st);
     if (r != SPD_OK) return r;
-    const int ppc = 64;
+    const int ppc = select_pages_per_cta();
     for (size_t b = 0; b < due.size(); b += dv.seqs_per_launch) {
       SelectParams p{};
       p.n_seqs = (int)std::min<size_t>(dv.seqs_per_launch, due.size() - b);
@@ -304,6 +362,7 @@ spd_status select_impl(spd_ctx *c, const void *q, const int *ids, int n, bool fo
       p.page_table = static_cast<const int *>(c->buf.page_table);
       p.selection = static_cast<int *>(c->buf.selection);
       p.scores = reinterpret_cast<float *>(c->scratch(dv.sl.scores));
+      p.tickets = reinterpret_cast<int *>(c->scratch(dv.sl.tickets_sel));
       p.err = c->err_word();
       p.Hq = c->cfg.num_q_heads;
       p.Hd = dv.Hd;
@@ -325,11 +384,11 @@ spd_status select_impl(spd_ctx *c, const void *q, const int *ids, int n, bool fo
         d.nL = nL_of(s.L, p.ell);
         d.K_sel = budget_pages(c, s.L);
         d.chunk_off = off;
-        d.n_chunks = d.nL > d.K_sel ? (d.nL - 1 + ppc - 1) / ppc : 0;
-        off += d.n_chunks * dv.Hd;
+        d.n_chunks = (d.nL > d.K_sel && d.K_sel > 1) ? (d.nL - 1 + ppc - 1) / ppc : 0;
+        off += std::max(1, d.n_chunks) * dv.Hd;
       }
       p.score_ctas = off;
-      cudaError_t e = launch_select(p, c->cfg.dtype, c->cfg.head_dim, dv.G, st);
+      cudaError_t e = launch_select_fused(p, c->cfg.dtype, c->cfg.head_dim, dv.G, st, &c->launches);
       if (e != cudaSuccess) return cuda_fail(c, e, "select launch");
     }
   }
@@ -343,60 +402,99 @@ spd_status select_impl(spd_ctx *c, const void *q, const int *ids, int n, bool fo
   return SPD_OK;
 }
 
-// Split policy: aim for about four CTAs per SM in total, at least 64 tokens
-// per split, at most 64 splits per (sequence, kv head) and kMaxItems per
-// launch.  Splits never come out empty.
-void plan_splits(const spd_ctx *c, DecodeParams &p, const int *ids) {
-  const Derived &dv = c->dv;
+// Tiles of 16 rows a unit (sequence, kv head) attends to.
+int unit_tiles_dyn(const spd_ctx *c, const Seq &s) {
   const int ell = c->cfg.logical_page;
-  long long total = 0;
-  for (int i = 0; i < p.n_seqs; ++i) {
-    const Seq &s = c->seqs[ids[i]];
-    if (dv.Hd) total += (long long)dv.Hd * (s.sel_count + nL_of(s.L, ell) - s.nL0) * ell;
-    if (dv.Hs) total += (long long)dv.Hs * std::min<long long>(s.L, (long long)p.S + p.W);
-  }
-  long long chunk = std::max<long long>(64, (total + 4LL * c->num_sms - 1) / (4LL * c->num_sms));
-  for (;;) {
-    int items = 0;
-    for (int i = 0; i < p.n_seqs; ++i) {
-      const Seq &s = c->seqs[ids[i]];
-      DecodeSeq &d = p.seqs[i];
-      d.item_off = items;
-      d.ns_dyn = d.ns_str = d.pps = d.tps = 0;
-      if (dv.Hd) {
-        const int n_att = s.sel_count + nL_of(s.L, ell) - s.nL0;
-        long long ns = std::min<long long>({64, (long long)n_att,
-                                            std::max<long long>(1, ((long long)n_att * ell + chunk - 1) / chunk)});
-        d.pps = (int)((n_att + ns - 1) / ns);
-        d.ns_dyn = (n_att + d.pps - 1) / d.pps;
-      }
-      if (dv.Hs) {
-        const long long n_tok = std::min<long long>(s.L, (long long)p.S + p.W);
-        long long ns = std::min<long long>({64, n_tok, std::max<long long>(1, (n_tok + chunk - 1) / chunk)});
-        d.tps = (int)((n_tok + ns - 1) / ns);
-        d.ns_str = (int)((n_tok + d.tps - 1) / d.tps);
-      }
-      items += dv.Hd * d.ns_dyn + dv.Hs * d.ns_str;
-    }
-    p.total_items = items;
-    if (items <= kMaxItems) return;
-    chunk *= 2;
-  }
+  const int n_att = s.sel_count + nL_of(s.L, ell) - s.nL0;
+  const int last_rows = (int)((s.L - 1) % ell) + 1;
+  return (n_att - 1) * (ell / kTileRows) + (last_rows + kTileRows - 1) / kTileRows;
 }
 
+int unit_tiles_str(const spd_ctx *c, const Seq &s) {
+  const long long S = c->cfg.sink, W = c->cfg.window, L = s.L;
+  long long n0 = std::min(S, L), n1 = 0, n2 = 0;
+  if (L > S) {
+    const long long w0 = std::max(S, L - W), n_win = L - w0, a0 = (w0 - S) % W;
+    n1 = std::min(n_win, W - a0);
+    n2 = n_win - n1;
+  }
+  auto t = [](long long n) { return (int)((n + kTileRows - 1) / kTileRows); };
+  return t(n0) + t(n1) + t(n2);
+}
+
+// Split policy: tiles per item chosen so the launch has about two items per
+// SM (at most 8 tiles = 128 rows per item, the shared-memory stage).  Items
+// of a unit are consecutive; none is empty.
+int plan_tiles(const spd_ctx *c, TileDecodeParams &p, const int *ids, int n) {
+  const Derived &dv = c->dv;
+  long long total = 0;
+  for (int i = 0; i < n; ++i) {
+    const Seq &s = c->seqs[ids[i]];
+    if (dv.Hd) total += (long long)dv.Hd * unit_tiles_dyn(c, s);
+    if (dv.Hs) total += (long long)dv.Hs * unit_tiles_str(c, s);
+  }
+  int tpi = (int)std::min<long long>(kMaxTilesPerItem,
+                                     std::max<long long>(1, (total + 2LL * c->num_sms - 1) /
+                                                                (2LL * c->num_sms)));
+  int items = 0;
+  for (int i = 0; i < n; ++i) {
+    const Seq &s = c->seqs[ids[i]];
+    TileSeq &d = p.seqs[i];
+    d.slot = ids[i];
+    d.L = (int)s.L;
+    d.nL0 = s.nL0;
+    d.sel_count = s.sel_count;
+    d.item_off = items;
+    d.ns_dyn = d.ns_str = 0;
+    d.tpi_dyn = d.tpi_str = tpi;
+    if (dv.Hd) {
+      const int nt = unit_tiles_dyn(c, s);
+      d.ns_dyn = (nt + tpi - 1) / tpi;
+      d.tpi_dyn = (nt + d.ns_dyn - 1) / d.ns_dyn;
+      d.ns_dyn = (nt + d.tpi_dyn - 1) / d.tpi_dyn;
+    }
+    if (dv.Hs) {
+      const int nt = unit_tiles_str(c, s);
+      d.ns_str = (nt + tpi - 1) / tpi;
+      d.tpi_str = (nt + d.ns_str - 1) / d.ns_str;
+      d.ns_str = (nt + d.tpi_str - 1) / d.tpi_str;
+    }
+    items += dv.Hd * d.ns_dyn + dv.Hs * d.ns_str;
+  }
+  p.total_items = items;
+  return items;
+}
+
+// Enqueue split-K decode attention for seqs `ids` (lengths already final).
+// With k_new/v_new the kernel also appends each sequence's newest token.
 spd_status attention_impl(spd_ctx *c, const void *q, const int *ids, int n, float *out,
-                          cudaStream_t st) {
+                          const void *k_new, const void *v_new, cudaStream_t st) {
   spd_status r = ensure_device(c, st);
   if (r != SPD_OK) return r;
   const Derived &dv = c->dv;
   const size_t qrow = (size_t)c->cfg.num_q_heads * c->cfg.head_dim;
-  for (int b = 0; b < n; b += dv.seqs_per_launch) {
-    DecodeParams p{};
-    p.n_seqs = std::min(dv.seqs_per_launch, n - b);
+  const size_t kvrow = (size_t)c->cfg.num_kv_heads * c->cfg.head_dim;
+  int b = 0;
+  while (b < n) {
+    // grow the batch while it fits one parameter block and kMaxItems
+    int m = std::min(dv.seqs_per_launch, n - b);
+    static thread_local TileDecodeParams p;
+    for (;;) {
+      if (plan_tiles(c, p, ids + b, m) <= kMaxItems || m == 1) break;
+      m = (m + 1) / 2;
+    }
+    p.n_seqs = m;
+    p.tm_k = c->tm_k;
+    p.tm_v = c->tm_v;
+    p.tm_sk = c->tm_sk;
+    p.tm_sv = c->tm_sv;
     p.q = static_cast<const char *>(q) + (size_t)b * qrow * 2;
+    p.k_new = k_new ? static_cast<const char *>(k_new) + (size_t)b * kvrow * 2 : nullptr;
+    p.v_new = v_new ? static_cast<const char *>(v_new) + (size_t)b * kvrow * 2 : nullptr;
     p.out = out + (size_t)b * qrow;
     p.k_pool = c->buf.k_pool;
     p.v_pool = c->buf.v_pool;
+    p.meta = c->buf.meta;
     p.stream_k = c->buf.stream_k;
     p.stream_v = c->buf.stream_v;
     p.page_table = static_cast<const int *>(c->buf.page_table);
@@ -418,21 +516,11 @@ spd_status attention_impl(spd_ctx *c, const void *q, const int *ids, int n, floa
     p.W = dv.Hs ? c->cfg.window : 0;
     p.num_phys = c->cfg.num_physical_pages;
     p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)c->cfg.head_dim));
-    memcpy(p.kv_kind, dv.kv_kind, sizeof p.kv_kind);
-    memcpy(p.kv_sub, dv.kv_sub, sizeof p.kv_sub);
     memcpy(p.dyn_kv, dv.dyn_kv, sizeof p.dyn_kv);
     memcpy(p.str_kv, dv.str_kv, sizeof p.str_kv);
-    for (int i = 0; i < p.n_seqs; ++i) {
-      const Seq &s = c->seqs[ids[b + i]];
-      DecodeSeq &d = p.seqs[i];
-      d.slot = ids[b + i];
-      d.L = (int)s.L;
-      d.nL0 = s.nL0;
-      d.sel_count = s.sel_count;
-    }
-    plan_splits(c, p, ids + b);
-    cudaError_t e = launch_decode(p, c->cfg.dtype, c->cfg.head_dim, dv.G, st);
+    cudaError_t e = launch_decode_tiles(p, c->cfg.dtype, c->cfg.head_dim, dv.G, st, &c->launches);
     if (e != cudaSuccess) return cuda_fail(c, e, "decode launch");
+    b += m;
   }
   for (int i = 0; i < n; ++i) c->seqs[ids[i]].counter += 1;
   return SPD_OK;
@@ -626,7 +714,7 @@ spd_status spd_sparse_decode_attention(spd_ctx *c, const void *q, const int *seq
   spd_status r = check_seqs(c, seq_ids, n_seqs);
   if (r != SPD_OK) return r;
   if ((r = check_attend_state(c, seq_ids, n_seqs, false)) != SPD_OK) return r;
-  return attention_impl(c, q, seq_ids, n_seqs, out, (cudaStream_t)stream);
+  return attention_impl(c, q, seq_ids, n_seqs, out, nullptr, nullptr, (cudaStream_t)stream);
 }
 
 spd_status spd_decode_step(spd_ctx *c, const void *q, const void *k, const void *v,
@@ -638,9 +726,15 @@ spd_status spd_decode_step(spd_ctx *c, const void *q, const void *k, const void 
   if (r != SPD_OK) return r;
   if ((r = check_attend_state(c, seq_ids, n_seqs, true)) != SPD_OK) return r;
   cudaStream_t st = (cudaStream_t)stream;
-  if ((r = append_impl(c, seq_ids, n_seqs, 1, k, v, st)) != SPD_OK) return r;
+  if ((r = ensure_device(c, st)) != SPD_OK) return r;
+  // pages for the new token, then the token itself is appended by the decode
+  // kernel (after this step's selection, which never reads it: the page
+  // holding it is always kept)
+  for (int i = 0; i < n_seqs; ++i) take_pages(c, seq_ids[i], 1);
+  if ((r = flush_page_table(c, st)) != SPD_OK) return r;
+  for (int i = 0; i < n_seqs; ++i) c->seqs[seq_ids[i]].L += 1;
   if ((r = select_impl(c, q, seq_ids, n_seqs, false, st)) != SPD_OK) return r;
-  return attention_impl(c, q, seq_ids, n_seqs, out, st);
+  return attention_impl(c, q, seq_ids, n_seqs, out, k, v, st);
 }
 
 spd_status spd_get_selection(spd_ctx *c, int seq_id, int kv_head, int *idx_host, int cap,
@@ -691,5 +785,11 @@ const char *spd_status_string(spd_status s) {
 }
 
 const char *spd_last_error(spd_ctx *c) { return c ? c->err.c_str() : ""; }
+
+spd_status spd_launch_count(spd_ctx *c, long long *n) {
+  if (!c || !n) return SPD_ERR_INVALID_ARG;
+  *n = c->launches;
+  return SPD_OK;
+}
 
 }  // extern "C"
