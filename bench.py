@@ -58,6 +58,24 @@ def parse():
     return ap.parse_args()
 
 
+# ---- multi-rank aggregation (replicas: no data-path collective) -------------
+
+def reduce_max(x, dist=None, device="cpu"):
+    """Max of a host float over all ranks (identity on one process)."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(bytes_per_rank, ms_max, world):
+    """Weak scaling: every rank moves the same bytes; the job takes the
+    slowest rank's time."""
+    return bytes_per_rank * world / (ms_max * 1e-3) / 1e9
+
+
 # ---- algorithmic bytes ------------------------------------------------------
 
 def step_bytes(wl, L, n_att, selected):
@@ -239,11 +257,7 @@ def run_ours(args, rank, world, device):
             dist.barrier()
 
     def max_over_ranks(x):
-        if dist is None:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return reduce_max(x, dist, device)
 
     # warm-up: W steps, enqueued on `stream`
     warm = layers.inputs(args.warmup)
@@ -282,7 +296,7 @@ def run_ours(args, rank, world, device):
     for c in layers.caches:
         c.check_status(stream)
     total_bytes = float(tot.sum())
-    gbs = total_bytes / (ms * 1e-3) / 1e9 * world
+    gbs = whole_job_gbs(total_bytes, ms, world)
 
     # roofline: the decode kernel alone (read-only, replayable), events around
     # every launch inside one graph
@@ -450,7 +464,7 @@ def run_e2e(layers, stream, n_steps, barrier, max_over_ranks, world):
     barrier()
     ms = max_over_ranks(a.elapsed_time(b))
     assert all(torch.isfinite(host_out[-1][layer]).all() for layer in range(n))
-    return {"value": round(tot / (ms * 1e-3) / 1e9 * world, 2), "unit": "GB/s",
+    return {"value": round(whole_job_gbs(tot, ms, world), 2), "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "us_per_step": round(ms / n_steps * 1e3, 2),
             "how": "per step: H2D of q/k/v for all layers from pinned host memory, the "

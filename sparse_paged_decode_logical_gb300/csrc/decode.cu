@@ -124,6 +124,7 @@ __global__ void __launch_bounds__(128) decode_tiles_kernel(const __grid_constant
   float *l_w = m_w + kWarps * G;
   int *s_flag = reinterpret_cast<int *>(smem + Sm::kFlag);
 
+  pdl_launch_dependents();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int item = blockIdx.x;
   int i = 0;
@@ -176,6 +177,10 @@ __global__ void __launch_bounds__(128) decode_tiles_kernel(const __grid_constant
   const int nt = max(0, min(n_tiles, tile0 + tpi) - tile0);
   const bool owns_newest = tile0 + nt == n_tiles;
   const bool do_append = p.k_new != nullptr && owns_newest;
+
+  // everything above used only the parameter block; from here on global
+  // memory written by earlier kernels is read
+  pdl_wait();
 
   // ---- issue every TMA load of the item ----
   if (tid == 0) {
@@ -516,8 +521,9 @@ cudaError_t prep_g() {
 
 template <typename T, int D, int G>
 cudaError_t launch_one(const TileDecodeParams &p, cudaStream_t st) {
-  decode_tiles_kernel<T, D, G><<<p.total_items, 128, Smem<D, G>::kAlloc, st>>>(p);
-  return cudaGetLastError();
+  cudaError_t e = launch_pdl(decode_tiles_kernel<T, D, G>, p.total_items, 128,
+                             (size_t)Smem<D, G>::kAlloc, st, p);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <typename T, int D>

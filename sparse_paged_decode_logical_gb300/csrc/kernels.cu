@@ -11,6 +11,7 @@
 #include <cuda_fp16.h>
 #include <math_constants.h>
 
+#include "ptx.cuh"
 #include "spd_internal.h"
 
 namespace spd {
@@ -59,6 +60,8 @@ __device__ __forceinline__ void set_err(int *err, int code, int a, int b, int c)
 
 // ---- page table ------------------------------------------------------------
 __global__ void pt_write_kernel(const __grid_constant__ PtWriteParams p) {
+  pdl_launch_dependents();
+  pdl_wait();
   for (int i = threadIdx.x; i < p.n; i += blockDim.x) {
     const PtUpdate u = p.upd[i];
     p.page_table[(size_t)u.slot * p.max_pp + u.index] = u.phys;
@@ -70,6 +73,8 @@ __global__ void pt_write_kernel(const __grid_constant__ PtWriteParams p) {
 // thread c owns channel c.  Streaming part: one CTA per (sequence, head).
 template <typename T, int D>
 __global__ void __launch_bounds__(128) append_kernel(const __grid_constant__ AppendParams p) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int c = threadIdx.x;
   const T *kin = static_cast<const T *>(p.k);
   const T *vin = static_cast<const T *>(p.v);
@@ -151,9 +156,9 @@ __global__ void __launch_bounds__(128) append_kernel(const __grid_constant__ App
 }  // namespace
 
 cudaError_t launch_pt_write(const PtWriteParams &p, cudaStream_t s, long long *n) {
-  pt_write_kernel<<<1, 256, 0, s>>>(p);
+  cudaError_t e = launch_pdl(pt_write_kernel, 1, 256, 0, s, p);
   *n += 1;
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_append(const AppendParams &p, int dtype, int d, cudaStream_t s,
@@ -161,14 +166,14 @@ cudaError_t launch_append(const AppendParams &p, int dtype, int d, cudaStream_t 
   const int grid = p.dyn_ctas + p.n_seqs * p.Hs;
   if (grid == 0) return cudaSuccess;
   *n += 1;
-  if (dtype == 0) {
-    if (d == 64) append_kernel<__half, 64><<<grid, 128, 0, s>>>(p);
-    else append_kernel<__half, 128><<<grid, 128, 0, s>>>(p);
-  } else {
-    if (d == 64) append_kernel<__nv_bfloat16, 64><<<grid, 128, 0, s>>>(p);
-    else append_kernel<__nv_bfloat16, 128><<<grid, 128, 0, s>>>(p);
-  }
-  return cudaGetLastError();
+  cudaError_t e;
+  if (dtype == 0)
+    e = d == 64 ? launch_pdl(append_kernel<__half, 64>, grid, 128, 0, s, p)
+                : launch_pdl(append_kernel<__half, 128>, grid, 128, 0, s, p);
+  else
+    e = d == 64 ? launch_pdl(append_kernel<__nv_bfloat16, 64>, grid, 128, 0, s, p)
+                : launch_pdl(append_kernel<__nv_bfloat16, 128>, grid, 128, 0, s, p);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace spd

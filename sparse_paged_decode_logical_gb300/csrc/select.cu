@@ -148,6 +148,8 @@ __device__ int cta_topk(const float *sc, int n, int k, int *out) {
 template <typename T, int D, int G>
 __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_constant__ SelectParams p) {
   __shared__ int s_last;
+  pdl_launch_dependents();
+  pdl_wait();  // q, metadata and the page table come from earlier kernels
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   int i = 0;
   while (i + 1 < p.n_seqs && p.seqs[i + 1].chunk_off <= (int)blockIdx.x) ++i;
@@ -278,14 +280,15 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_consta
 template <typename T, int D>
 cudaError_t launch_g(const SelectParams &p, int G, cudaStream_t st) {
   const int grid = p.score_ctas;
+  cudaError_t e;
   switch (G) {
-    case 1: select_kernel<T, D, 1><<<grid, kSelThreads, 0, st>>>(p); break;
-    case 2: select_kernel<T, D, 2><<<grid, kSelThreads, 0, st>>>(p); break;
-    case 4: select_kernel<T, D, 4><<<grid, kSelThreads, 0, st>>>(p); break;
-    case 8: select_kernel<T, D, 8><<<grid, kSelThreads, 0, st>>>(p); break;
+    case 1: e = launch_pdl(select_kernel<T, D, 1>, grid, kSelThreads, 0, st, p); break;
+    case 2: e = launch_pdl(select_kernel<T, D, 2>, grid, kSelThreads, 0, st, p); break;
+    case 4: e = launch_pdl(select_kernel<T, D, 4>, grid, kSelThreads, 0, st, p); break;
+    case 8: e = launch_pdl(select_kernel<T, D, 8>, grid, kSelThreads, 0, st, p); break;
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace
