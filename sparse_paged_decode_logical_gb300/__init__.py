@@ -250,7 +250,10 @@ class SparsePagedKVCache:
         self.torch = torch
         self.cfg_dict = dict(cfg)
         self.cfg = make_config(**cfg)
-        self.device = torch.device(device)
+        dev = torch.device(device)
+        if dev.type == "cuda" and dev.index is None:
+            dev = torch.device("cuda", torch.cuda.current_device())
+        self.device = dev
         self.sizes = spd_query_sizes(self.cfg)
         self.buffers = {}
         addrs = {}
