@@ -96,7 +96,9 @@ const char *derive(const spd_config *c, Derived *d) {
   d->max_nL = (c->max_context + c->logical_page - 1) / c->logical_page;
   long long budget = c->token_budget > 0 ? c->token_budget
                                          : std::min<long long>(4096, c->max_context / 32);
-  d->ksel_max = (int)std::max<long long>(1, budget / c->logical_page);
+  // pages kept never exceed the pages a sequence can have
+  d->ksel_max = (int)std::min<long long>(std::max<long long>(1, budget / c->logical_page),
+                                         d->max_nL);
   d->seqs_per_launch = std::min(c->max_seqs, kSeqsPerLaunch);
   // one unit (sequence, kv head) must fit in one launch's work items
   const long long unit_cap = (long long)kMaxItems * kMaxTilesPerItem * kTileRows / 2;
