@@ -182,49 +182,51 @@ __global__ void __launch_bounds__(128) decode_tiles_kernel(const __grid_constant
   // memory written by earlier kernels is read
   pdl_wait();
 
-  // ---- issue every TMA load of the item ----
+  // ---- issue every TMA load of the item: thread t sets up tile t ----
   if (tid == 0) {
     s_flag[1] = 0;  // set if a bounded wait gives up
     for (int t = 0; t < nt; ++t) mbar_init(&bars[t], 1);
     fence_mbar_init();
+  }
+  __syncthreads();
+  if (tid < nt) {
+    const int t = tid;
     const CUtensorMap *mk = dyn ? &p.tm_k : &p.tm_sk;
     const CUtensorMap *mv = dyn ? &p.tm_v : &p.tm_sv;
-    for (int t = 0; t < nt; ++t) {
-      const int tau = tile0 + t;
-      TileDesc td{0, 0, 0, 0};
-      if (dyn) {
-        const int pi = tau / tpp, st = tau % tpp;
-        const int *sel = p.selection + ((size_t)s.slot * p.Hd + sub) * p.ksel_max;
-        const int j = pi < s.sel_count ? sel[pi] : s.nL0 + (pi - s.sel_count);
-        const int blk = j / p.R;
-        if (j < 0 || j >= nL || blk >= p.max_pp) {
-          set_err(p.err, kDevBadSelection, s.slot, sub, j);
-        } else {
-          const int phys = p.page_table[(size_t)s.slot * p.max_pp + blk];
-          if (phys < 0 || phys >= p.num_phys) {
-            set_err(p.err, kDevBadPhys, s.slot, blk, phys);
-          } else {
-            td.y = (j % p.R) * p.ell + st * kRows;
-            td.z = phys * p.Hd + sub;
-            td.n_valid = min(kRows, L - (j * p.ell + st * kRows));
-          }
-        }
+    const int tau = tile0 + t;
+    TileDesc td{0, 0, 0, 0};
+    if (dyn) {
+      const int pi = tau / tpp, st = tau % tpp;
+      const int *sel = p.selection + ((size_t)s.slot * p.Hd + sub) * p.ksel_max;
+      const int j = pi < s.sel_count ? sel[pi] : s.nL0 + (pi - s.sel_count);
+      const int blk = j / p.R;
+      if (j < 0 || j >= nL || blk >= p.max_pp) {
+        set_err(p.err, kDevBadSelection, s.slot, sub, j);
       } else {
-        int r = 0, k = tau;
-        while (r < 2 && k >= run_tiles[r]) k -= run_tiles[r++];
-        td.y = ((s.slot * p.Hs + sub) * (p.S + p.W)) + run_start[r] + k * kRows;
-        td.z = 0;
-        td.n_valid = min(kRows, run_len[r] - k * kRows);
-      }
-      tdesc[t] = td;
-      if (td.n_valid > 0) {
-        uint8_t *kt = smem + t * Gm::kTileBytes;
-        uint8_t *vt = kt + Gm::kBoxes * Gm::kBoxBytes;
-        mbar_arrive_expect_tx(&bars[t], Gm::kTileBytes);
-        for (int b = 0; b < Gm::kBoxes; ++b) {
-          tma_load_3d(kt + b * Gm::kBoxBytes, mk, b * 64, td.y, td.z, &bars[t]);
-          tma_load_3d(vt + b * Gm::kBoxBytes, mv, b * 64, td.y, td.z, &bars[t]);
+        const int phys = p.page_table[(size_t)s.slot * p.max_pp + blk];
+        if (phys < 0 || phys >= p.num_phys) {
+          set_err(p.err, kDevBadPhys, s.slot, blk, phys);
+        } else {
+          td.y = (j % p.R) * p.ell + st * kRows;
+          td.z = phys * p.Hd + sub;
+          td.n_valid = min(kRows, L - (j * p.ell + st * kRows));
         }
+      }
+    } else {
+      int r = 0, k = tau;
+      while (r < 2 && k >= run_tiles[r]) k -= run_tiles[r++];
+      td.y = ((s.slot * p.Hs + sub) * (p.S + p.W)) + run_start[r] + k * kRows;
+      td.z = 0;
+      td.n_valid = min(kRows, run_len[r] - k * kRows);
+    }
+    tdesc[t] = td;
+    if (td.n_valid > 0) {
+      uint8_t *kt = smem + t * Gm::kTileBytes;
+      uint8_t *vt = kt + Gm::kBoxes * Gm::kBoxBytes;
+      mbar_arrive_expect_tx(&bars[t], Gm::kTileBytes);
+      for (int b = 0; b < Gm::kBoxes; ++b) {
+        tma_load_3d(kt + b * Gm::kBoxBytes, mk, b * 64, td.y, td.z, &bars[t]);
+        tma_load_3d(vt + b * Gm::kBoxBytes, mv, b * 64, td.y, td.z, &bars[t]);
       }
     }
   }
@@ -487,19 +489,85 @@ __global__ void __launch_bounds__(128) decode_tiles_kernel(const __grid_constant
   __syncthreads();
   if (!*s_flag) return;
   __threadfence();
-  for (int x = tid; x < G * D; x += blockDim.x) {
-    const int g = x / D, c = x % D;
-    float M = -CUDART_INF_F;
-    for (int k = 0; k < ns; ++k) M = fmaxf(M, __ldcg(&p.part_ml[(size_t)(unit_item0 + k) * G + g].x));
-    float O = 0.f, Ls = 0.f;
-    for (int k = 0; k < ns; ++k) {
-      const float2 ml = __ldcg(&p.part_ml[(size_t)(unit_item0 + k) * G + g]);
-      if (ml.x == -CUDART_INF_F) continue;
-      const float f = exp2f(ml.x - M);
-      O += f * __ldcg(&p.part_o[((size_t)(unit_item0 + k) * G + g) * D + c]);
-      Ls += f * ml.y;
+  // (1) per-head maximum over the unit's items, (2) per-item weights
+  // 2^(m_k - M) and the weighted row sum, (3) the weighted sum of the o
+  // partials with many independent L2 loads in flight per thread.
+  constexpr int kChunk = 256;                       // items per pass
+  constexpr int OPT = (G * D + 127) / 128;          // outputs per thread
+  float *Mh = m_w;                                  // [G] (the warp buffers are free now)
+  float *Lh = l_w;                                  // [G]
+  float *wk = reinterpret_cast<float *>(smem);      // [kChunk][G] weights
+  float *red = wk + kChunk * G;                     // [128] reduction scratch
+  const float2 *pml = p.part_ml + (size_t)unit_item0 * G;
+  const float *po = p.part_o + (size_t)unit_item0 * G * D;
+  float mloc[G];
+#pragma unroll
+  for (int g = 0; g < G; ++g) mloc[g] = -CUDART_INF_F;
+  for (int x = tid; x < ns * G; x += blockDim.x) {
+    const float mv = __ldcg(&pml[x].x);
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+      if (x % G == g) mloc[g] = fmaxf(mloc[g], mv);
+  }
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    float v = mloc[g];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+    if (lane == 0) red[warp * G + g] = v;
+  }
+  __syncthreads();
+  if (tid < G) {
+    float v = red[tid];
+    for (int w = 1; w < kWarps; ++w) v = fmaxf(v, red[w * G + tid]);
+    Mh[tid] = v;
+    Lh[tid] = 0.f;
+  }
+  __syncthreads();
+  float acc_o[OPT];
+#pragma unroll
+  for (int j = 0; j < OPT; ++j) acc_o[j] = 0.f;
+  for (int base = 0; base < ns; base += kChunk) {
+    const int cnt = min(kChunk, ns - base);
+    for (int x = tid; x < cnt * G; x += blockDim.x) {
+      const float2 ml = __ldcg(&pml[(size_t)base * G + x]);
+      const float w = ml.x == -CUDART_INF_F ? 0.f : exp2f(ml.x - Mh[x % G]);
+      wk[x] = w;
+      atomicAdd(&Lh[x % G], w * ml.y);
     }
-    out[x] = O / Ls;
+    __syncthreads();
+    const float *pb = po + (size_t)base * G * D;
+    int k = 0;
+    for (; k + 4 <= cnt; k += 4) {
+      float v[4][OPT];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int j = 0; j < OPT; ++j) {
+          const int x = tid + 128 * j;
+          v[u][j] = x < G * D ? __ldcg(pb + (size_t)(k + u) * G * D + x) : 0.f;
+        }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int j = 0; j < OPT; ++j) {
+          const int x = tid + 128 * j;
+          if (x < G * D) acc_o[j] = fmaf(wk[(k + u) * G + x / D], v[u][j], acc_o[j]);
+        }
+    }
+    for (; k < cnt; ++k)
+#pragma unroll
+      for (int j = 0; j < OPT; ++j) {
+        const int x = tid + 128 * j;
+        if (x < G * D)
+          acc_o[j] = fmaf(wk[k * G + x / D], __ldcg(pb + (size_t)k * G * D + x), acc_o[j]);
+      }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int j = 0; j < OPT; ++j) {
+    const int x = tid + 128 * j;
+    if (x < G * D) out[x] = acc_o[j] / Lh[x / D];
   }
   if (tid == 0) p.tickets[unit] = 0;
 }

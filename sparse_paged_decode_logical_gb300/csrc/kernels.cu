@@ -76,8 +76,8 @@ __global__ void __launch_bounds__(128) append_kernel(const __grid_constant__ App
   pdl_launch_dependents();
   pdl_wait();
   const int c = threadIdx.x;
-  const T *kin = static_cast<const T *>(p.k);
-  const T *vin = static_cast<const T *>(p.v);
+  const T *__restrict__ kin = static_cast<const T *>(p.k);
+  const T *__restrict__ vin = static_cast<const T *>(p.v);
   const int n = p.n_tokens;
   if ((int)blockIdx.x < p.dyn_ctas) {
     int i = 0;
@@ -101,9 +101,9 @@ __global__ void __launch_bounds__(128) append_kernel(const __grid_constant__ App
       return;
     }
     const size_t page_base = ((size_t)phys * p.Hd + hd) * p.P;  // in rows
-    T *kp = static_cast<T *>(p.k_pool);
-    T *vp = static_cast<T *>(p.v_pool);
-    T *meta = static_cast<T *>(p.meta) +
+    T *__restrict__ kp = static_cast<T *>(p.k_pool);
+    T *__restrict__ vp = static_cast<T *>(p.v_pool);
+    T *__restrict__ meta = static_cast<T *>(p.meta) +
               (((size_t)phys * p.Hd + hd) * p.R + (j % p.R)) * 2 * D;
     if (c >= D) return;
     T bmin, bmax;
@@ -118,12 +118,13 @@ __global__ void __launch_bounds__(128) append_kernel(const __grid_constant__ App
       bmin = bmax = kin[(((size_t)i * n + (t - s.L_old)) * p.Hkv + h) * D + c];
       vmin = vmax = Elem<T>::to_f(bmin);
     }
+#pragma unroll 8
     for (; t < t1; ++t) {
       const size_t src = (((size_t)i * n + (t - s.L_old)) * p.Hkv + h) * D + c;
-      const T kx = kin[src];
+      const T kx = __ldg(kin + src);
       const size_t dst = (page_base + (t % p.P)) * D + c;
       kp[dst] = kx;
-      vp[dst] = vin[src];
+      vp[dst] = __ldg(vin + src);
       const float x = Elem<T>::to_f(kx);
       if (x < vmin) { vmin = x; bmin = kx; }
       if (x > vmax) { vmax = x; bmax = kx; }

@@ -92,35 +92,51 @@ __device__ __forceinline__ int cta_excl_scan(int v, int *sh, int *total) {
   return res;
 }
 
-// Radix select of the k highest of n scores (k >= 1, n > k); writes the
-// chosen indices ascending to out[0..k).  Returns the count written.
+constexpr int kMaxKeys = 8192;  // candidate pages handled in shared memory
+
+// Radix select of the k highest of n scores (1 <= k < n <= kMaxKeys); writes
+// the chosen indices ascending to out[0..k).  Keys live in shared memory;
+// each pass builds a 256-bin histogram of one key byte (warp-aggregated
+// atomics), and one block scan over the bins finds the byte of the k-th
+// largest key.  Ties at the threshold go to the lower indices.  Returns the
+// count written.
 __device__ int cta_topk(const float *sc, int n, int k, int *out) {
+  __shared__ uint32_t keys[kMaxKeys];
   __shared__ int hist[256];
   __shared__ int sh[33];
   __shared__ uint32_t s_prefix;
   __shared__ int s_remaining;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31;
+  for (int j = tid; j < n; j += kSelThreads) keys[j] = score_key(__ldcg(sc + j));
   if (tid == 0) {
     s_prefix = 0;
     s_remaining = k;
   }
+  __syncthreads();
   uint32_t mask = 0;
   for (int shift = 24; shift >= 0; shift -= 8) {
-    for (int b = tid; b < 256; b += kSelThreads) hist[b] = 0;
+    hist[tid] = 0;  // kSelThreads == 256 bins
     __syncthreads();
     const uint32_t prefix = s_prefix;
-    for (int j = tid; j < n; j += kSelThreads) {
-      const uint32_t u = score_key(__ldcg(sc + j));
-      if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & 0xffu], 1);
+    for (int base = 0; base < n; base += kSelThreads) {
+      const int j = base + tid;
+      const uint32_t u = j < n ? keys[j] : 0u;
+      const bool in = j < n && (u & mask) == prefix;
+      const unsigned bin = in ? (u >> shift) & 0xffu : 256u + lane;  // unique when out
+      const unsigned peers = __match_any_sync(0xffffffffu, bin);
+      if (in && (__ffs(peers) - 1) == lane) atomicAdd(&hist[bin], __popc(peers));
     }
     __syncthreads();
-    if (tid == 0) {
-      int rem = s_remaining, cum = 0, b = 255;
-      for (; b > 0; --b) {
-        if (cum + hist[b] >= rem) break;
-        cum += hist[b];
-      }
-      s_remaining = rem - cum;
+    // suffix counts: bins above b hold `above` keys; pick b with
+    // above < remaining <= above + hist[b]
+    const int b = 255 - tid;  // thread t owns bin 255 - t (descending order)
+    const int hb = hist[b];
+    int tot;
+    const int above = cta_excl_scan(hb, sh, &tot);
+    const int rem = s_remaining;
+    __syncthreads();
+    if (above < rem && rem <= above + hb) {
+      s_remaining = rem - above;
       s_prefix = prefix | ((uint32_t)b << shift);
     }
     mask |= 0xffu << shift;
@@ -128,6 +144,72 @@ __device__ int cta_topk(const float *sc, int n, int k, int *out) {
   }
   const uint32_t T = s_prefix;
   const int take_eq = s_remaining;
+  // thread t owns keys [t*per, (t+1)*per): ascending output order falls out
+  const int per = (n + kSelThreads - 1) / kSelThreads;
+  const int j0 = min(n, tid * per), j1 = min(n, j0 + per);
+  int n_gt = 0, n_eq = 0;
+  for (int j = j0; j < j1; ++j) {
+    n_gt += keys[j] > T;
+    n_eq += keys[j] == T;
+  }
+  int tot_eq;
+  int eq_before = cta_excl_scan(n_eq, sh, &tot_eq);
+  int mine = n_gt + max(0, min(n_eq, take_eq - eq_before));
+  int total;
+  int pos = cta_excl_scan(mine, sh, &total);
+  for (int j = j0; j < j1 && mine > 0; ++j) {
+    const uint32_t u = keys[j];
+    bool take = u > T;
+    if (u == T) {
+      take = eq_before < take_eq;
+      ++eq_before;
+    }
+    if (take) {
+      if (pos < k) out[pos] = j;
+      ++pos;
+      --mine;
+    }
+  }
+  return total;
+}
+
+// Fallback for more candidates than shared memory holds: the same radix
+// select, reading the keys from global memory in every pass.
+__device__ int cta_topk_global(const float *sc, int n, int k, int *out) {
+  __shared__ int ghist[256];
+  __shared__ int gsh[33];
+  __shared__ uint32_t g_prefix;
+  __shared__ int g_remaining;
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    g_prefix = 0;
+    g_remaining = k;
+  }
+  uint32_t mask = 0;
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    ghist[tid] = 0;
+    __syncthreads();
+    const uint32_t prefix = g_prefix;
+    for (int j = tid; j < n; j += kSelThreads) {
+      const uint32_t u = score_key(__ldcg(sc + j));
+      if ((u & mask) == prefix) atomicAdd(&ghist[(u >> shift) & 0xffu], 1);
+    }
+    __syncthreads();
+    const int b = 255 - tid;
+    const int hb = ghist[b];
+    int tot;
+    const int above = cta_excl_scan(hb, gsh, &tot);
+    const int rem = g_remaining;
+    __syncthreads();
+    if (above < rem && rem <= above + hb) {
+      g_remaining = rem - above;
+      g_prefix = prefix | ((uint32_t)b << shift);
+    }
+    mask |= 0xffu << shift;
+    __syncthreads();
+  }
+  const uint32_t T = g_prefix;
+  const int take_eq = g_remaining;
   int eq_seen = 0, taken = 0;
   for (int base = 0; base < n; base += kSelThreads) {
     const int j = base + tid;
@@ -135,9 +217,9 @@ __device__ int cta_topk(const float *sc, int n, int k, int *out) {
     const int gt = j < n && u > T;
     const int eq = j < n && u == T;
     int tot_eq, tot_take;
-    const int eq_rank = cta_excl_scan(eq, sh, &tot_eq) + eq_seen;
+    const int eq_rank = cta_excl_scan(eq, gsh, &tot_eq) + eq_seen;
     const int take = gt || (eq && eq_rank < take_eq);
-    const int pos = cta_excl_scan(take, sh, &tot_take) + taken;
+    const int pos = cta_excl_scan(take, gsh, &tot_take) + taken;
     if (take && pos < k) out[pos] = j;
     eq_seen += tot_eq;
     taken += tot_take;
@@ -269,7 +351,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_consta
   if (!s_last) return;
   __threadfence();
   const int k = s.K_sel - 1;
-  const int got = cta_topk(scores, n, k, out);
+  const int got = n <= kMaxKeys ? cta_topk(scores, n, k, out) : cta_topk_global(scores, n, k, out);
   if (tid == 0) {
     out[k] = s.nL - 1;
     if (got != k) set_err(p.err, kDevTopkCount, s.slot, hd, got);
