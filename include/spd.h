@@ -208,6 +208,32 @@ spd_status spd_sparse_decode_attention(spd_ctx *ctx, const void *q,
                                        float *out, spd_stream stream);
 
 /*
+ * Sparse decode attention without any device allocation by the caller or
+ * the library for its temporaries.  No counterpart in the paper: this entry
+ * point exists for callers that cannot allocate device memory when they run
+ * attention -- code running while a CUDA stream is being captured (device
+ * allocation is not allowed there), integrations whose device memory plan is
+ * fixed at start-up, and plugins inside a host framework that owns every
+ * device allocation.  It computes exactly what spd_sparse_decode_attention
+ * computes (same arguments, same step-counter advance), but the split
+ * partials and tickets of the fused combine live in a library-owned
+ * file-scope device array of 4,292,608 bytes, held on every GPU that loads
+ * the library until the process exits, instead of the context's scratch.
+ * Limits: at most 1024 split items per launch (an item is up to 128 attended
+ * rows of one kv head); a sequence whose work needs more is rejected with
+ * SPD_ERR_CAPACITY before anything is enqueued.  The first call on a device
+ * looks up the array's device address (cudaGetSymbolAddress with that device
+ * current); make it before any stream capture.  All calls share the array
+ * and it keeps the last call's contents: tickets are cleared at each call,
+ * and calls whose GPU work overlaps (other streams, other contexts) race --
+ * issue them in order on one stream.  It calls no cudaMalloc, cudaFree or
+ * allocating library routine.
+ */
+spd_status spd_sparse_decode_attention_static(spd_ctx *ctx, const void *q,
+                                              const int *seq_ids, int n_seqs,
+                                              float *out, spd_stream stream);
+
+/*
  * One decode step for each listed sequence: append one token (k, v device
  * [n_seqs][Hkv][d]), select if due, attend.  Same results as calling the
  * three entry points above in that order; enqueues fewer launches.

@@ -81,6 +81,7 @@ def lib():
         "spd_kv_append": [vp, ip, i, i, vp, vp, vp],
         "spd_select_pages": [vp, vp, ip, i, i, vp],
         "spd_sparse_decode_attention": [vp, vp, ip, i, vp, vp],
+        "spd_sparse_decode_attention_static": [vp, vp, ip, i, vp, vp],
         "spd_decode_step": [vp, vp, vp, vp, ip, i, vp, vp],
         "spd_get_selection": [vp, i, i, ip, i, ip, vp],
         "spd_check_status": [vp, vp],
@@ -208,6 +209,15 @@ def spd_sparse_decode_attention(ctx, q_ptr, seq_ids, out_ptr, stream=0):
     ids, n = _ids(seq_ids)
     _check(lib().spd_sparse_decode_attention(ctx, q_ptr, ids, n, out_ptr, stream or None),
            "spd_sparse_decode_attention", ctx)
+
+
+def spd_sparse_decode_attention_static(ctx, q_ptr, seq_ids, out_ptr, stream=0):
+    """spd_sparse_decode_attention with its temporaries in the library-owned
+    device array: for callers that cannot allocate device memory at call
+    time (see include/spd.h)."""
+    ids, n = _ids(seq_ids)
+    _check(lib().spd_sparse_decode_attention_static(ctx, q_ptr, ids, n, out_ptr, stream or None),
+           "spd_sparse_decode_attention_static", ctx)
 
 
 def spd_decode_step(ctx, q_ptr, k_ptr, v_ptr, seq_ids, out_ptr, stream=0):

@@ -7,6 +7,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "spd.h"
+
 namespace spd {
 
 constexpr int kSeqsPerLaunch = 64;    // sequences described per parameter block
@@ -127,6 +129,23 @@ constexpr int kMaxTilesPerItem = 8;
 cudaError_t prepare_decode_kernels();
 cudaError_t launch_decode_tiles(const TileDecodeParams &p, int dtype, int d, int G,
                                 cudaStream_t s, long long *launches);
+
+// Temporaries of a decode launch (split partials and the per-unit tickets)
+// supplied from outside the context's scratch buffer.
+struct DecodeScratch {
+  float *part_o;   // [max_items][G][d]
+  float2 *part_ml; // [max_items][G]
+  int *tickets;    // [kSeqsPerLaunch][Hkv], zero before the launch
+  int max_items;   // split items one launch may use
+};
+
+// Runtime hooks (spd_runtime.cpp) for entry points defined in other files.
+spd_status check_attention_call(spd_ctx *c, const void *q, const int *ids, int n,
+                                const float *out);
+spd_status bind_device(spd_ctx *c, cudaStream_t st, int *device);
+spd_status attention_with_scratch(spd_ctx *c, const void *q, const int *ids, int n, float *out,
+                                  cudaStream_t st, const DecodeScratch &scratch);
+spd_status fail_message(spd_ctx *c, spd_status s, const char *msg);
 
 // Launchers.  dtype: 0 fp16, 1 bf16.  Return cudaGetLastError() and add the
 // number of kernels enqueued to *launches.

@@ -38,6 +38,8 @@ struct Seq {
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
 uint64_t splitmix64(uint64_t &s) {
   uint64_t z = (s += 0x9e3779b97f4a7c15ull);
   z = (z ^ (z >> 30)) * 0xbf58476d1ce4e5b9ull;
@@ -469,22 +471,29 @@ int plan_tiles(const spd_ctx *c, TileDecodeParams &p, const int *ids, int n) {
 
 // Enqueue split-K decode attention for seqs `ids` (lengths already final).
 // With k_new/v_new the kernel also appends each sequence's newest token.
+// `scr` (optional) replaces the context's scratch for the split partials and
+// tickets; a launch then holds at most scr->max_items items.
 spd_status attention_impl(spd_ctx *c, const void *q, const int *ids, int n, float *out,
-                          const void *k_new, const void *v_new, cudaStream_t st) {
+                          const void *k_new, const void *v_new, cudaStream_t st,
+                          const DecodeScratch *scr = nullptr) {
   spd_status r = ensure_device(c, st);
   if (r != SPD_OK) return r;
   const Derived &dv = c->dv;
   const size_t qrow = (size_t)c->cfg.num_q_heads * c->cfg.head_dim;
   const size_t kvrow = (size_t)c->cfg.num_kv_heads * c->cfg.head_dim;
+  const int max_items = scr ? scr->max_items : kMaxItems;
   int b = 0;
   while (b < n) {
-    // grow the batch while it fits one parameter block and kMaxItems
+    // grow the batch while it fits one parameter block and max_items
     int m = std::min(dv.seqs_per_launch, n - b);
     static thread_local TileDecodeParams p;
     for (;;) {
-      if (plan_tiles(c, p, ids + b, m) <= kMaxItems || m == 1) break;
+      if (plan_tiles(c, p, ids + b, m) <= max_items || m == 1) break;
       m = (m + 1) / 2;
     }
+    if (scr && p.total_items > max_items)
+      return c->fail(SPD_ERR_CAPACITY, "sequence %d needs %d split items, the library-owned "
+                     "scratch holds %d", ids[b], p.total_items, max_items);
     p.n_seqs = m;
     p.tm_k = c->tm_k;
     p.tm_v = c->tm_v;
@@ -501,9 +510,9 @@ spd_status attention_impl(spd_ctx *c, const void *q, const int *ids, int n, floa
     p.stream_v = c->buf.stream_v;
     p.page_table = static_cast<const int *>(c->buf.page_table);
     p.selection = static_cast<const int *>(c->buf.selection);
-    p.part_o = reinterpret_cast<float *>(c->scratch(dv.sl.part_o));
-    p.part_ml = reinterpret_cast<float2 *>(c->scratch(dv.sl.part_ml));
-    p.tickets = reinterpret_cast<int *>(c->scratch(dv.sl.tickets_dec));
+    p.part_o = scr ? scr->part_o : reinterpret_cast<float *>(c->scratch(dv.sl.part_o));
+    p.part_ml = scr ? scr->part_ml : reinterpret_cast<float2 *>(c->scratch(dv.sl.part_ml));
+    p.tickets = scr ? scr->tickets : reinterpret_cast<int *>(c->scratch(dv.sl.tickets_dec));
     p.err = c->err_word();
     p.Hq = c->cfg.num_q_heads;
     p.Hkv = c->cfg.num_kv_heads;
@@ -544,6 +553,34 @@ spd_status check_attend_state(spd_ctx *c, const int *ids, int n, bool will_appen
 }
 
 }  // namespace
+
+namespace spd {
+
+spd_status check_attention_call(spd_ctx *c, const void *q, const int *ids, int n,
+                                const float *out) {
+  if (!q || !out || !aligned16(q) || !aligned16(out))
+    return c->fail(SPD_ERR_INVALID_ARG, "q and out must be 16-byte aligned pointers");
+  spd_status r = check_seqs(c, ids, n);
+  if (r != SPD_OK) return r;
+  return check_attend_state(c, ids, n, false);
+}
+
+spd_status bind_device(spd_ctx *c, cudaStream_t st, int *device) {
+  spd_status r = ensure_device(c, st);
+  if (r == SPD_OK) *device = c->device;
+  return r;
+}
+
+spd_status attention_with_scratch(spd_ctx *c, const void *q, const int *ids, int n, float *out,
+                                  cudaStream_t st, const DecodeScratch &scratch) {
+  return attention_impl(c, q, ids, n, out, nullptr, nullptr, st, &scratch);
+}
+
+spd_status fail_message(spd_ctx *c, spd_status s, const char *msg) {
+  return c->fail(s, "%s", msg);
+}
+
+}  // namespace spd
 
 extern "C" {
 
@@ -665,8 +702,6 @@ spd_status spd_free_pages(spd_ctx *c, int *n_free) {
   *n_free = (int)c->free_pages.size();
   return SPD_OK;
 }
-
-static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 static spd_status check_append(spd_ctx *c, const int *ids, int n, int n_tokens, const void *k,
                                const void *v) {
