@@ -53,6 +53,8 @@ def parse():
     ap.add_argument("--layers", type=int, default=32)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-roofline", action="store_true")
+    ap.add_argument("--no-eager", action="store_true")
     ap.add_argument("--roofline-iters", type=int, default=40)
     ap.add_argument("--cpu-sample-steps", type=int, default=16)
     return ap.parse_args()
@@ -301,7 +303,7 @@ def run_ours(args, rank, world, device):
 
     # roofline: the decode kernel alone (read-only, replayable), events around
     # every launch inside one graph
-    rl = roofline(layers, stream, args.roofline_iters)
+    rl = None if args.no_roofline else roofline(layers, stream, args.roofline_iters)
     clk = clocks.stop()
 
     # end to end: pinned host inputs -> device -> step -> pinned host outputs
@@ -310,14 +312,16 @@ def run_ours(args, rank, world, device):
         e2e = run_e2e(layers, stream, args.steps, barrier, max_over_ranks, world)
 
     # eager launches (no graph), for context
-    eager_rows = layers.inputs(4)
-    torch.cuda.synchronize()
-    te0 = time.perf_counter()
-    with torch.cuda.stream(stream):
-        for row in eager_rows:
-            layers.step(row)
-    stream.synchronize()
-    eager_us = (time.perf_counter() - te0) / len(eager_rows) * 1e6
+    eager_us = float("nan")
+    if not args.no_eager:
+        eager_rows = layers.inputs(4)
+        torch.cuda.synchronize()
+        te0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            for row in eager_rows:
+                layers.step(row)
+        stream.synchronize()
+        eager_us = (time.perf_counter() - te0) / len(eager_rows) * 1e6
 
     peak, peak_kind = measured_peaks()
     res = {
