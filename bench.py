@@ -191,6 +191,10 @@ class Layers:
         self.caches, self.seqs = [], []
         for layer in range(n_layers):
             c = spd.SparsePagedKVCache(device=device, **cfg)
+            # every kernel on the stream is this library's and each layer's
+            # cache is written only through its own context: the next layer
+            # may stage its K/V tiles while the previous layer finishes
+            c.set_early_kv_staging(True)
             s = c.seq_create()
             K, V = W.device_context(wl, 0, L0, layer, device)
             c.kv_append([s], K[None], V[None])
@@ -365,7 +369,7 @@ def arm_config(wl, n_layers, n_sel=None, bytes_per_step=None, world=1):
         "token_budget": "min(4096, L/32)", "reuse_interval": wl.C,
         "l2": "inputs larger than L2: %d layers x ~19 MB touched per step" % n_layers,
         "timing": "timed window captured once into a CUDA graph and run once; "
-                  "CUDA events on the launching stream",
+                  "CUDA events on the launching stream; early KV staging on",
         "parallelism": "replicas" if world > 1 else "single GPU",
     }
     if n_sel is not None:

@@ -32,6 +32,10 @@
  *     order on one stream.  A context is not thread-safe.
  *   - Argument errors are detected on the host before anything is enqueued
  *     and leave the context unchanged.
+ *   - Kernels are launched with programmatic dependent launch: each waits
+ *     for the preceding kernel on the stream before touching global memory
+ *     and only then lets the next kernel start (see
+ *     spd_set_early_kv_staging for the one exception).
  */
 #ifndef SPD_H
 #define SPD_H
@@ -254,6 +258,21 @@ spd_status spd_get_selection(spd_ctx *ctx, int seq_id, int kv_head,
 spd_status spd_check_status(spd_ctx *ctx, spd_stream stream);
 
 const char *spd_status_string(spd_status s);
+/*
+ * Early KV staging (off by default).  When on, a decode kernel of this
+ * context whose preceding kernel on the stream was not enqueued by this
+ * context starts loading its K/V tiles (reading the page table, selection and
+ * pools) before that kernel has finished; q, the new token and all writes
+ * still wait for it.  This overlaps the attention's HBM reads with the tail
+ * of the kernel before it -- in a model, the projection that produces q.
+ * Turn it on only if (a) nothing but this library's calls on this context
+ * writes its KV-cache buffers, and (b) other code's kernels on the stream do
+ * not release their dependents (programmatic dependent launch) before they
+ * have waited for their own predecessor.  All of this library's kernels
+ * meet (b).  SPD_ERR_INVALID_ARG for a NULL context.
+ */
+spd_status spd_set_early_kv_staging(spd_ctx *ctx, int enable);
+
 /* Number of kernels this context has enqueued since it was created. */
 spd_status spd_launch_count(spd_ctx *ctx, long long *n);
 /* Human-readable detail of the last error on this context ("" if none). */

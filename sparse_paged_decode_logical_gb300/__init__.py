@@ -86,6 +86,7 @@ def lib():
         "spd_get_selection": [vp, i, i, ip, i, ip, vp],
         "spd_check_status": [vp, vp],
         "spd_launch_count": [vp, ll],
+        "spd_set_early_kv_staging": [vp, i],
     }
     for name, args in sig.items():
         f = getattr(L, name)
@@ -240,6 +241,10 @@ def spd_check_status(ctx, stream=0):
     _check(lib().spd_check_status(ctx, stream or None), "spd_check_status", ctx)
 
 
+def spd_set_early_kv_staging(ctx, enable):
+    _check(lib().spd_set_early_kv_staging(ctx, 1 if enable else 0), "spd_set_early_kv_staging", ctx)
+
+
 def spd_launch_count(ctx):
     n = ctypes.c_longlong()
     _check(lib().spd_launch_count(ctx, ctypes.byref(n)), "spd_launch_count", ctx)
@@ -355,3 +360,6 @@ class SparsePagedKVCache:
 
     def launch_count(self):
         return spd_launch_count(self.ctx)
+
+    def set_early_kv_staging(self, enable=True):
+        spd_set_early_kv_staging(self.ctx, enable)

@@ -124,7 +124,6 @@ __global__ void __launch_bounds__(128) decode_tiles_kernel(const __grid_constant
   float *l_w = m_w + kWarps * G;
   int *s_flag = reinterpret_cast<int *>(smem + Sm::kFlag);
 
-  pdl_launch_dependents();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int item = blockIdx.x;
   int i = 0;
@@ -178,9 +177,17 @@ __global__ void __launch_bounds__(128) decode_tiles_kernel(const __grid_constant
   const bool owns_newest = tile0 + nt == n_tiles;
   const bool do_append = p.k_new != nullptr && owns_newest;
 
-  // everything above used only the parameter block; from here on global
-  // memory written by earlier kernels is read
-  pdl_wait();
+  // Everything above used only the parameter block.  The KV cache (page
+  // table, selection, pools) is read next: before the wait for the previous
+  // kernel on the stream when the host knows that kernel cannot have written
+  // this context's cache (p.early), after it otherwise.  q, the new token and
+  // every write come after the wait.  Dependents are released only after the
+  // wait, so when this kernel runs, every kernel before its immediate
+  // predecessor has finished.
+  if (!p.early) {
+    pdl_wait();
+    pdl_launch_dependents();
+  }
 
   // ---- issue every TMA load of the item: thread t sets up tile t ----
   if (tid == 0) {
@@ -229,6 +236,11 @@ __global__ void __launch_bounds__(128) decode_tiles_kernel(const __grid_constant
         tma_load_3d(vt + b * Gm::kBoxBytes, mv, b * 64, td.y, td.z, &bars[t]);
       }
     }
+  }
+
+  if (p.early) {
+    pdl_wait();
+    pdl_launch_dependents();
   }
 
   // ---- q^T fragments (B operand), heads padded to 8 columns ----

@@ -60,8 +60,8 @@ __device__ __forceinline__ void set_err(int *err, int code, int a, int b, int c)
 
 // ---- page table ------------------------------------------------------------
 __global__ void pt_write_kernel(const __grid_constant__ PtWriteParams p) {
-  pdl_launch_dependents();
   pdl_wait();
+  pdl_launch_dependents();
   for (int i = threadIdx.x; i < p.n; i += blockDim.x) {
     const PtUpdate u = p.upd[i];
     p.page_table[(size_t)u.slot * p.max_pp + u.index] = u.phys;
@@ -73,8 +73,8 @@ __global__ void pt_write_kernel(const __grid_constant__ PtWriteParams p) {
 // thread c owns channel c.  Streaming part: one CTA per (sequence, head).
 template <typename T, int D>
 __global__ void __launch_bounds__(128) append_kernel(const __grid_constant__ AppendParams p) {
-  pdl_launch_dependents();
   pdl_wait();
+  pdl_launch_dependents();
   const int c = threadIdx.x;
   const T *__restrict__ kin = static_cast<const T *>(p.k);
   const T *__restrict__ vin = static_cast<const T *>(p.v);

@@ -10,10 +10,11 @@
 
 namespace spd {
 
-// Programmatic dependent launch: let the next kernel in the stream be
-// scheduled now; and wait until every kernel this one depends on has
-// finished and its writes are visible.  A kernel issues the wait before its
-// first global-memory access, so nothing it reads can be stale.
+// Programmatic dependent launch: wait until the kernel this one depends on
+// has finished and its writes are visible; and let the next kernel in the
+// stream be scheduled.  Every kernel here releases its dependents only after
+// its own wait, so a running kernel knows that all kernels before its
+// immediate predecessor have finished.
 __device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }

@@ -230,8 +230,8 @@ __device__ int cta_topk_global(const float *sc, int n, int k, int *out) {
 template <typename T, int D, int G>
 __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_constant__ SelectParams p) {
   __shared__ int s_last;
-  pdl_launch_dependents();
   pdl_wait();  // q, metadata and the page table come from earlier kernels
+  pdl_launch_dependents();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   int i = 0;
   while (i + 1 < p.n_seqs && p.seqs[i + 1].chunk_off <= (int)blockIdx.x) ++i;

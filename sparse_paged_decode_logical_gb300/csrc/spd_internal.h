@@ -117,6 +117,7 @@ struct TileDecodeParams {
   int *err;
   int n_seqs, Hq, Hkv, Hd, Hs, ell, P, R, max_pp, ksel_max, S, W, num_phys;
   int total_items;
+  int early;          // 1: stage K/V tiles before waiting for the previous kernel
   float scale_log2;
   unsigned char dyn_kv[kMaxKvHeads];
   unsigned char str_kv[kMaxKvHeads];

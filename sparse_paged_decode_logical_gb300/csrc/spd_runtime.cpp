@@ -11,6 +11,8 @@
 // optimization for LLMs", section 3.4, raises on an empty list).
 #include <algorithm>
 #include <cmath>
+#include <mutex>
+#include <unordered_map>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -148,6 +150,7 @@ struct spd_ctx {
   int device = 0;
   int num_sms = 152;
   long long launches = 0;  // kernels enqueued by this context
+  bool early_staging = false;
   CUtensorMap tm_k{}, tm_v{}, tm_sk{}, tm_sv{};
   std::string err;
 
@@ -165,6 +168,30 @@ struct spd_ctx {
 };
 
 namespace {
+
+// Stream -> the context whose kernel this library enqueued last on it.  A
+// decode kernel may read its own KV cache before the previous kernel on the
+// stream has finished only when that kernel came from another context (or
+// from other code): nothing but this context's own launches writes its cache.
+std::mutex g_last_mu;
+std::unordered_map<cudaStream_t, const spd_ctx *> g_last_launcher;
+
+bool previous_launcher_is(const spd_ctx *c, cudaStream_t st) {
+  std::lock_guard<std::mutex> lock(g_last_mu);
+  auto it = g_last_launcher.find(st);
+  return it != g_last_launcher.end() && it->second == c;
+}
+
+void note_launcher(const spd_ctx *c, cudaStream_t st) {
+  std::lock_guard<std::mutex> lock(g_last_mu);
+  g_last_launcher[st] = c;
+}
+
+void forget_launcher(const spd_ctx *c) {
+  std::lock_guard<std::mutex> lock(g_last_mu);
+  for (auto it = g_last_launcher.begin(); it != g_last_launcher.end();)
+    it = it->second == c ? g_last_launcher.erase(it) : std::next(it);
+}
 
 spd_status cuda_fail(spd_ctx *c, cudaError_t e, const char *what) {
   return c->fail(SPD_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
@@ -279,6 +306,7 @@ spd_status flush_page_table(spd_ctx *c, cudaStream_t st) {
     for (int k = 0; k < p.n; ++k) p.upd[k] = c->pending_pt[i + k];
     cudaError_t e = launch_pt_write(p, st, &c->launches);
     if (e != cudaSuccess) return cuda_fail(c, e, "pt_write launch");
+    note_launcher(c, st);
     i += p.n;
   }
   c->pending_pt.clear();
@@ -340,6 +368,7 @@ spd_status append_impl(spd_ctx *c, const int *ids, int n, int n_tokens, const vo
     p.dyn_ctas = (int)ctas;
     cudaError_t e = launch_append(p, c->cfg.dtype, c->cfg.head_dim, st, &c->launches);
     if (e != cudaSuccess) return cuda_fail(c, e, "append launch");
+    note_launcher(c, st);
   }
   for (int i = 0; i < n; ++i) c->seqs[ids[i]].L += n_tokens;
   return SPD_OK;
@@ -394,6 +423,7 @@ spd_status select_impl(spd_ctx *c, const void *q, const int *ids, int n, bool fo
       p.score_ctas = off;
       cudaError_t e = launch_select_fused(p, c->cfg.dtype, c->cfg.head_dim, dv.G, st, &c->launches);
       if (e != cudaSuccess) return cuda_fail(c, e, "select launch");
+      note_launcher(c, st);
     }
   }
   for (int pos : due) {
@@ -529,8 +559,10 @@ spd_status attention_impl(spd_ctx *c, const void *q, const int *ids, int n, floa
     p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)c->cfg.head_dim));
     memcpy(p.dyn_kv, dv.dyn_kv, sizeof p.dyn_kv);
     memcpy(p.str_kv, dv.str_kv, sizeof p.str_kv);
+    p.early = c->early_staging && !previous_launcher_is(c, st) ? 1 : 0;
     cudaError_t e = launch_decode_tiles(p, c->cfg.dtype, c->cfg.head_dim, dv.G, st, &c->launches);
     if (e != cudaSuccess) return cuda_fail(c, e, "decode launch");
+    note_launcher(c, st);
     b += m;
   }
   for (int i = 0; i < n; ++i) c->seqs[ids[i]].counter += 1;
@@ -629,7 +661,10 @@ spd_status spd_create(const spd_config *cfg, const spd_buffers *bufs, spd_ctx **
   return SPD_OK;
 }
 
-void spd_destroy(spd_ctx *ctx) { delete ctx; }
+void spd_destroy(spd_ctx *ctx) {
+  if (ctx) forget_launcher(ctx);
+  delete ctx;
+}
 
 spd_status spd_seq_create(spd_ctx *c, int *seq_id_out) {
   if (!c || !seq_id_out) return SPD_ERR_INVALID_ARG;
@@ -822,6 +857,12 @@ const char *spd_status_string(spd_status s) {
 }
 
 const char *spd_last_error(spd_ctx *c) { return c ? c->err.c_str() : ""; }
+
+spd_status spd_set_early_kv_staging(spd_ctx *c, int enable) {
+  if (!c) return SPD_ERR_INVALID_ARG;
+  c->early_staging = enable != 0;
+  return SPD_OK;
+}
 
 spd_status spd_launch_count(spd_ctx *c, long long *n) {
   if (!c || !n) return SPD_ERR_INVALID_ARG;

@@ -176,3 +176,27 @@ def test_launch_counts():
     # a selection step: fused score+top-k, then the fused append+decode kernel
     # (plus a page-table write when the token opens a physical page)
     assert pr.cache.launch_count() - n0 in (2, 3)
+
+
+@needs_gpu
+def test_early_kv_staging_interleaved_contexts_bit_identical():
+    # three contexts stepped round-robin on one stream (like consecutive
+    # layers): with early staging each decode kernel loads its tiles while the
+    # previous context's kernel finishes; outputs must equal the default path
+    wl = synth(batch=2, lens=[700, 1500], steps=9, ell=32, P=128)
+    res = []
+    for early in (False, True):
+        prs = [Pair(wl, layer=layer) for layer in range(3)]
+        for pr in prs:
+            pr.cache.set_early_kv_staging(early)
+        outs = []
+        for s in range(wl.steps):
+            for layer, pr in enumerate(prs):
+                q, k, v = W.step_tokens(wl, s, layer)
+                outs.append(pr.cache.decode_step(tdev(q, wl.dtype), tdev(k, wl.dtype),
+                                                 tdev(v, wl.dtype), pr.gids))
+        torch.cuda.synchronize()
+        for pr in prs:
+            pr.cache.check_status()
+        res.append(torch.stack([o.cpu() for o in outs]))
+    assert torch.equal(res[0], res[1])
