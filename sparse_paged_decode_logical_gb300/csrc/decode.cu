@@ -67,17 +67,30 @@ struct TileDesc {
   int pad;
 };
 
+// Shared memory: a small fixed region (barriers, tile descriptors, P and
+// rescale buffers, per-warp row max / sum, flags), then the K/V tiles at a
+// 1024-byte aligned offset.  The launch sizes the tile region for the largest
+// item it holds, at least big enough for the warp-merge and combine buffers.
 template <int D, int G>
 struct Smem {
-  static constexpr int kTiles = kMaxTiles * Geo<D>::kTileBytes;
-  static constexpr int kBars = kTiles;                              // uint64 x kMaxTiles
+  static constexpr int kBars = 0;                                   // uint64 x kMaxTiles
   static constexpr int kDesc = kBars + kMaxTiles * 8;               // TileDesc x kMaxTiles
   static constexpr int kP = kDesc + kMaxTiles * (int)sizeof(TileDesc);  // float [W][16][GP]
   static constexpr int kC = kP + kWarps * kRows * GP<G>::v * 4;     // float [W][GP]
   static constexpr int kML = kC + kWarps * GP<G>::v * 4;            // float [2][W][G]
-  static constexpr int kFlag = kML + 2 * kWarps * G * 4;
-  static constexpr int kTotal = kFlag + 16;
-  static constexpr int kAlloc = kTotal + 1024;                      // alignment slack
+  static constexpr int kFlag = kML + 2 * kWarps * G * 4;            // int [4]
+  static constexpr int kTiles = (kFlag + 16 + 1023) / 1024 * 1024;  // tiles start here
+  // warp-merge buffer [W][G][D] floats, or the combine's (m, l) and weight
+  // buffers for 256 items
+  static constexpr int kMinTileRegion = (kWarps * G * D * 4 > 256 * G * 12 + 64)
+                                            ? kWarps * G * D * 4
+                                            : 256 * G * 12 + 64;
+  static constexpr int bytes(int tiles) {
+    return kTiles + (tiles * Geo<D>::kTileBytes > kMinTileRegion ? tiles * Geo<D>::kTileBytes
+                                                                  : kMinTileRegion) +
+           1024;  // alignment slack
+  }
+  static constexpr int kAlloc = bytes(kMaxTiles);
 };
 
 template <typename T> struct IsBF16 { static constexpr bool v = false; };
@@ -116,6 +129,7 @@ __global__ void __launch_bounds__(128) decode_tiles_kernel(const __grid_constant
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t *tiles = smem + Sm::kTiles;
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Sm::kBars);
   TileDesc *tdesc = reinterpret_cast<TileDesc *>(smem + Sm::kDesc);
   float *P_all = reinterpret_cast<float *>(smem + Sm::kP);
@@ -125,6 +139,13 @@ __global__ void __launch_bounds__(128) decode_tiles_kernel(const __grid_constant
   int *s_flag = reinterpret_cast<int *>(smem + Sm::kFlag);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) {
+    prefetch_tmap(&p.tm_k);
+    prefetch_tmap(&p.tm_v);
+    prefetch_tmap(&p.tm_sk);
+    prefetch_tmap(&p.tm_sv);
+    s_flag[1] = 0;  // set if a bounded wait gives up
+  }
   const int item = blockIdx.x;
   int i = 0;
   while (i + 1 < p.n_seqs && p.seqs[i + 1].item_off <= item) ++i;
@@ -190,14 +211,10 @@ __global__ void __launch_bounds__(128) decode_tiles_kernel(const __grid_constant
   }
 
   // ---- issue every TMA load of the item: thread t sets up tile t ----
-  if (tid == 0) {
-    s_flag[1] = 0;  // set if a bounded wait gives up
-    for (int t = 0; t < nt; ++t) mbar_init(&bars[t], 1);
-    fence_mbar_init();
-  }
-  __syncthreads();
   if (tid < nt) {
     const int t = tid;
+    mbar_init(&bars[t], 1);
+    fence_mbar_init();
     const CUtensorMap *mk = dyn ? &p.tm_k : &p.tm_sk;
     const CUtensorMap *mv = dyn ? &p.tm_v : &p.tm_sv;
     const int tau = tile0 + t;
@@ -228,7 +245,7 @@ __global__ void __launch_bounds__(128) decode_tiles_kernel(const __grid_constant
     }
     tdesc[t] = td;
     if (td.n_valid > 0) {
-      uint8_t *kt = smem + t * Gm::kTileBytes;
+      uint8_t *kt = tiles + t * Gm::kTileBytes;
       uint8_t *vt = kt + Gm::kBoxes * Gm::kBoxBytes;
       mbar_arrive_expect_tx(&bars[t], Gm::kTileBytes);
       for (int b = 0; b < Gm::kBoxes; ++b) {
@@ -282,7 +299,7 @@ __global__ void __launch_bounds__(128) decode_tiles_kernel(const __grid_constant
       }
       continue;
     }
-    uint8_t *kt = smem + t * Gm::kTileBytes;
+    uint8_t *kt = tiles + t * Gm::kTileBytes;
     uint8_t *vt = kt + Gm::kBoxes * Gm::kBoxBytes;
     const int nv = td.n_valid;
 
@@ -337,6 +354,18 @@ __global__ void __launch_bounds__(128) decode_tiles_kernel(const __grid_constant
           mrow[e] = bmin;
           mrow[D + e] = bmax;
         }
+      }
+      __syncwarp();
+    }
+
+    if (nv < kRows) {
+      // rows past the tile's attended tokens: zero V so the unrolled P.V
+      // below adds exactly 0 for them (their weights are 0 as well)
+      for (int x = lane; x < (kRows - nv) * 8 * Gm::kBoxes; x += 32) {
+        const int box = x / ((kRows - nv) * 8), rem = x % ((kRows - nv) * 8);
+        const int r = nv + rem / 8, ch = rem % 8;
+        *reinterpret_cast<uint4 *>(vt + box * Gm::kBoxBytes + r * 128 + ch * 16) =
+            make_uint4(0, 0, 0, 0);
       }
       __syncwarp();
     }
@@ -401,7 +430,8 @@ __global__ void __launch_bounds__(128) decode_tiles_kernel(const __grid_constant
       const int cb = lane * CPL;
       const uint32_t voff = (uint32_t)((cb >> 6) * Gm::kBoxBytes) + ((cb & 7) * 2);
       const int chunk = (cb & 63) >> 3;
-      for (int r = 0; r < nv; ++r) {
+#pragma unroll
+      for (int r = 0; r < kRows; ++r) {
         float vf[CPL];
         const uint8_t *vp = vt + voff + swz128(r, chunk);
         if constexpr (CPL == 4) {
@@ -449,7 +479,7 @@ __global__ void __launch_bounds__(128) decode_tiles_kernel(const __grid_constant
         if (tdesc[t].n_valid > 0) mbar_wait(&bars[t], 0, kWaitLimit);
     __syncthreads();
   }
-  float *o_w = reinterpret_cast<float *>(smem);  // [W][G][D]
+  float *o_w = reinterpret_cast<float *>(tiles);  // [W][G][D]
   if (g8 == 0) {
     if (2 * t4 < G) {
       m_w[warp * G + 2 * t4] = m0;
@@ -492,94 +522,102 @@ __global__ void __launch_bounds__(128) decode_tiles_kernel(const __grid_constant
   if (ns == 1) return;
 
   // ---- last item of the unit merges the partials ----
-  __threadfence();
-  __syncthreads();
+  __syncthreads();  // every partial write of this CTA precedes the release below
   if (tid == 0) {
-    const int prev = atomicAdd(&p.tickets[unit], 1);
+    const int prev = atom_add_acq_rel_gpu(&p.tickets[unit], 1);
     *s_flag = prev == ns - 1;
   }
-  __syncthreads();
+  __syncthreads();  // ... and the acquire above precedes every read below
   if (!*s_flag) return;
-  __threadfence();
-  // (1) per-head maximum over the unit's items, (2) per-item weights
-  // 2^(m_k - M) and the weighted row sum, (3) the weighted sum of the o
-  // partials with many independent L2 loads in flight per thread.
+  // Merge in three steps, each a single round of independent L2 loads:
+  // (1) every (m, l) pair of the chunk into shared memory, (2) per-head max
+  // M and weights 2^(m_k - M) with the weighted row sum (shared memory
+  // only), (3) the weighted sum of the o partials, kU items per round.
   constexpr int kChunk = 256;                       // items per pass
-  constexpr int OPT = (G * D + 127) / 128;          // outputs per thread
+  constexpr int OPT4 = (G * D / 4 + 127) / 128;     // float4 outputs per thread
+  constexpr int kU = 16;                            // o-partial items in flight
   float *Mh = m_w;                                  // [G] (the warp buffers are free now)
   float *Lh = l_w;                                  // [G]
-  float *wk = reinterpret_cast<float *>(smem);      // [kChunk][G] weights
-  float *red = wk + kChunk * G;                     // [128] reduction scratch
+  float2 *mlk = reinterpret_cast<float2 *>(tiles);  // [kChunk][G] (m, l) of the chunk
+  float *wk = reinterpret_cast<float *>(mlk + kChunk * G);  // [kChunk][G] weights
   const float2 *pml = p.part_ml + (size_t)unit_item0 * G;
   const float *po = p.part_o + (size_t)unit_item0 * G * D;
-  float mloc[G];
+  float4 acc_o[OPT4];
 #pragma unroll
-  for (int g = 0; g < G; ++g) mloc[g] = -CUDART_INF_F;
-  for (int x = tid; x < ns * G; x += blockDim.x) {
-    const float mv = __ldcg(&pml[x].x);
-#pragma unroll
-    for (int g = 0; g < G; ++g)
-      if (x % G == g) mloc[g] = fmaxf(mloc[g], mv);
-  }
-#pragma unroll
-  for (int g = 0; g < G; ++g) {
-    float v = mloc[g];
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
-    if (lane == 0) red[warp * G + g] = v;
-  }
-  __syncthreads();
+  for (int j = 0; j < OPT4; ++j) acc_o[j] = make_float4(0.f, 0.f, 0.f, 0.f);
   if (tid < G) {
-    float v = red[tid];
-    for (int w = 1; w < kWarps; ++w) v = fmaxf(v, red[w * G + tid]);
-    Mh[tid] = v;
+    Mh[tid] = -CUDART_INF_F;
     Lh[tid] = 0.f;
   }
-  __syncthreads();
-  float acc_o[OPT];
-#pragma unroll
-  for (int j = 0; j < OPT; ++j) acc_o[j] = 0.f;
   for (int base = 0; base < ns; base += kChunk) {
     const int cnt = min(kChunk, ns - base);
-    for (int x = tid; x < cnt * G; x += blockDim.x) {
-      const float2 ml = __ldcg(&pml[(size_t)base * G + x]);
-      const float w = ml.x == -CUDART_INF_F ? 0.f : exp2f(ml.x - Mh[x % G]);
-      wk[x] = w;
-      atomicAdd(&Lh[x % G], w * ml.y);
+    for (int x = tid; x < cnt * G; x += blockDim.x) mlk[x] = __ldcg(&pml[(size_t)base * G + x]);
+    __syncthreads();
+    // one thread per head: running max over the chunk, rescale what came before
+    if (tid < G) {
+      const int g = tid;
+      float M = Mh[g];
+      for (int k = 0; k < cnt; ++k) M = fmaxf(M, mlk[k * G + g].x);
+      const float resc = Mh[g] == -CUDART_INF_F ? 0.f : exp2f(Mh[g] - M);
+      float Ls = Lh[g] * resc;
+      for (int k = 0; k < cnt; ++k) {
+        const float2 ml = mlk[k * G + g];
+        const float w = ml.x == -CUDART_INF_F ? 0.f : exp2f(ml.x - M);
+        wk[k * G + g] = w;
+        Ls = fmaf(w, ml.y, Ls);
+      }
+      wk[kChunk * G + g] = resc;  // factor for the o accumulated so far
+      Mh[g] = M;
+      Lh[g] = Ls;
     }
     __syncthreads();
-    const float *pb = po + (size_t)base * G * D;
-    int k = 0;
-    for (; k + 4 <= cnt; k += 4) {
-      float v[4][OPT];
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
+    for (int j = 0; j < OPT4; ++j) {
+      const int x4 = tid + 128 * j;
+      if (x4 < G * D / 4) {
+        const float r = wk[kChunk * G + (4 * x4) / D];
+        acc_o[j].x *= r;
+        acc_o[j].y *= r;
+        acc_o[j].z *= r;
+        acc_o[j].w *= r;
+      }
+    }
+    const float4 *pb = reinterpret_cast<const float4 *>(po + (size_t)base * G * D);
+    for (int k = 0; k < cnt; k += kU) {
+      float4 v[kU][OPT4];
 #pragma unroll
-        for (int j = 0; j < OPT; ++j) {
-          const int x = tid + 128 * j;
-          v[u][j] = x < G * D ? __ldcg(pb + (size_t)(k + u) * G * D + x) : 0.f;
+      for (int u = 0; u < kU; ++u)
+#pragma unroll
+        for (int j = 0; j < OPT4; ++j) {
+          const int x4 = tid + 128 * j;
+          v[u][j] = (k + u < cnt && x4 < G * D / 4)
+                        ? __ldcg(pb + (size_t)(k + u) * (G * D / 4) + x4)
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
+      for (int u = 0; u < kU; ++u)
 #pragma unroll
-        for (int j = 0; j < OPT; ++j) {
-          const int x = tid + 128 * j;
-          if (x < G * D) acc_o[j] = fmaf(wk[(k + u) * G + x / D], v[u][j], acc_o[j]);
+        for (int j = 0; j < OPT4; ++j) {
+          const int x4 = tid + 128 * j;
+          if (k + u < cnt && x4 < G * D / 4) {
+            const float w = wk[(k + u) * G + (4 * x4) / D];
+            acc_o[j].x = fmaf(w, v[u][j].x, acc_o[j].x);
+            acc_o[j].y = fmaf(w, v[u][j].y, acc_o[j].y);
+            acc_o[j].z = fmaf(w, v[u][j].z, acc_o[j].z);
+            acc_o[j].w = fmaf(w, v[u][j].w, acc_o[j].w);
+          }
         }
     }
-    for (; k < cnt; ++k)
-#pragma unroll
-      for (int j = 0; j < OPT; ++j) {
-        const int x = tid + 128 * j;
-        if (x < G * D)
-          acc_o[j] = fmaf(wk[k * G + x / D], __ldcg(pb + (size_t)k * G * D + x), acc_o[j]);
-      }
     __syncthreads();
   }
 #pragma unroll
-  for (int j = 0; j < OPT; ++j) {
-    const int x = tid + 128 * j;
-    if (x < G * D) out[x] = acc_o[j] / Lh[x / D];
+  for (int j = 0; j < OPT4; ++j) {
+    const int x4 = tid + 128 * j;
+    if (x4 < G * D / 4) {
+      const float inv = 1.f / Lh[(4 * x4) / D];
+      reinterpret_cast<float4 *>(out)[x4] =
+          make_float4(acc_o[j].x * inv, acc_o[j].y * inv, acc_o[j].z * inv, acc_o[j].w * inv);
+    }
   }
   if (tid == 0) p.tickets[unit] = 0;
 }
@@ -601,8 +639,12 @@ cudaError_t prep_g() {
 
 template <typename T, int D, int G>
 cudaError_t launch_one(const TileDecodeParams &p, cudaStream_t st) {
+  int tiles = 1;
+  for (int i = 0; i < p.n_seqs; ++i)
+    tiles = max(tiles, max(p.seqs[i].ns_dyn ? p.seqs[i].tpi_dyn : 0,
+                           p.seqs[i].ns_str ? p.seqs[i].tpi_str : 0));
   cudaError_t e = launch_pdl(decode_tiles_kernel<T, D, G>, p.total_items, 128,
-                             (size_t)Smem<D, G>::kAlloc, st, p);
+                             (size_t)Smem<D, G>::bytes(min(tiles, kMaxTiles)), st, p);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

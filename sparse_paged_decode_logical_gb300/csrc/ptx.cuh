@@ -72,6 +72,19 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, i
       : "memory");
 }
 
+// Atomic add with acquire-release semantics at GPU scope (returns the old
+// value).  Issued by one thread after a CTA barrier it publishes the CTA's
+// prior writes to other CTAs and, if it observes their releases, makes
+// their writes visible to this CTA after the next barrier.
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int *addr, int v) {
+  int old;
+  asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], %2;"
+               : "=r"(old)
+               : "l"(addr), "r"(v)
+               : "memory");
+  return old;
+}
+
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

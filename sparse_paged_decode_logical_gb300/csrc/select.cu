@@ -94,59 +94,63 @@ __device__ __forceinline__ int cta_excl_scan(int v, int *sh, int *total) {
 
 constexpr int kMaxKeys = 8192;  // candidate pages handled in shared memory
 
-// Radix select of the k highest of n scores (1 <= k < n <= kMaxKeys); writes
-// the chosen indices ascending to out[0..k).  Keys live in shared memory;
-// each pass builds a 256-bin histogram of one key byte (warp-aggregated
-// atomics), and one block scan over the bins finds the byte of the k-th
-// largest key.  Ties at the threshold go to the lower indices.  Returns the
-// count written.
+// Exact selection of the k highest of n scores (1 <= k < n <= kMaxKeys);
+// writes the chosen indices ascending to out[0..k).  The k-th largest key T
+// is found 4 bits at a time, from the top: at each step every thread counts
+// its keys (a contiguous range of indices) that match the bits fixed so far,
+// per value of the next 4 bits; warp sums come from redux.sync and one
+// thread picks the digit.  Keys equal to T are taken lowest index first.
+// Returns the count written.
 __device__ int cta_topk(const float *sc, int n, int k, int *out) {
   __shared__ uint32_t keys[kMaxKeys];
-  __shared__ int hist[256];
+  __shared__ uint32_t wcnt[kSelWarps][16];
   __shared__ int sh[33];
   __shared__ uint32_t s_prefix;
   __shared__ int s_remaining;
-  const int tid = threadIdx.x, lane = tid & 31;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   for (int j = tid; j < n; j += kSelThreads) keys[j] = score_key(__ldcg(sc + j));
   if (tid == 0) {
     s_prefix = 0;
     s_remaining = k;
   }
   __syncthreads();
-  uint32_t mask = 0;
-  for (int shift = 24; shift >= 0; shift -= 8) {
-    hist[tid] = 0;  // kSelThreads == 256 bins
-    __syncthreads();
+  const int per = (n + kSelThreads - 1) / kSelThreads;
+  const int j0 = min(n, tid * per), j1 = min(n, j0 + per);
+  for (int shift = 28; shift >= 0; shift -= 4) {
     const uint32_t prefix = s_prefix;
-    for (int base = 0; base < n; base += kSelThreads) {
-      const int j = base + tid;
-      const uint32_t u = j < n ? keys[j] : 0u;
-      const bool in = j < n && (u & mask) == prefix;
-      const unsigned bin = in ? (u >> shift) & 0xffu : 256u + lane;  // unique when out
-      const unsigned peers = __match_any_sync(0xffffffffu, bin);
-      if (in && (__ffs(peers) - 1) == lane) atomicAdd(&hist[bin], __popc(peers));
+    const uint32_t hi_mask = shift == 28 ? 0u : ~((1u << (shift + 4)) - 1u);
+    uint32_t cnt[16];
+#pragma unroll
+    for (int b = 0; b < 16; ++b) cnt[b] = 0;
+    for (int j = tid; j < n; j += kSelThreads) {  // strided: no bank conflicts
+      const uint32_t u = keys[j];
+      if ((u & hi_mask) == prefix) {
+        const uint32_t d = (u >> shift) & 15u;
+#pragma unroll
+        for (int b = 0; b < 16; ++b) cnt[b] += d == (uint32_t)b;
+      }
+    }
+#pragma unroll
+    for (int b = 0; b < 16; ++b) {
+      const uint32_t w = __reduce_add_sync(0xffffffffu, cnt[b]);
+      if (lane == 0) wcnt[warp][b] = w;
     }
     __syncthreads();
-    // suffix counts: bins above b hold `above` keys; pick b with
-    // above < remaining <= above + hist[b]
-    const int b = 255 - tid;  // thread t owns bin 255 - t (descending order)
-    const int hb = hist[b];
-    int tot;
-    const int above = cta_excl_scan(hb, sh, &tot);
-    const int rem = s_remaining;
-    __syncthreads();
-    if (above < rem && rem <= above + hb) {
+    if (tid == 0) {
+      int rem = s_remaining, above = 0, b = 15;
+      for (; b > 0; --b) {
+        int c = 0;
+        for (int w = 0; w < kSelWarps; ++w) c += (int)wcnt[w][b];
+        if (above + c >= rem) break;
+        above += c;
+      }
       s_remaining = rem - above;
       s_prefix = prefix | ((uint32_t)b << shift);
     }
-    mask |= 0xffu << shift;
     __syncthreads();
   }
   const uint32_t T = s_prefix;
   const int take_eq = s_remaining;
-  // thread t owns keys [t*per, (t+1)*per): ascending output order falls out
-  const int per = (n + kSelThreads - 1) / kSelThreads;
-  const int j0 = min(n, tid * per), j1 = min(n, j0 + per);
   int n_gt = 0, n_eq = 0;
   for (int j = j0; j < j1; ++j) {
     n_gt += keys[j] > T;
@@ -262,8 +266,13 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_consta
   constexpr int KSTEPS = 2 * D / 16;
   const int g8 = lane >> 2, t4 = lane & 3;
   uint32_t qb[KSTEPS][2];
+  __shared__ __align__(16) uint16_t q_s[G * D];
   {
-    const uint16_t *qp = reinterpret_cast<const uint16_t *>(p.q) + ((size_t)s.qrow * p.Hq + h * G) * D;
+    // the group's G query rows: one coalesced 16-byte load per thread
+    const uint4 *qg = reinterpret_cast<const uint4 *>(
+        reinterpret_cast<const uint16_t *>(p.q) + ((size_t)s.qrow * p.Hq + h * G) * D);
+    for (int x = tid; x < G * D / 8; x += kSelThreads) reinterpret_cast<uint4 *>(q_s)[x] = qg[x];
+    __syncthreads();
 #pragma unroll
     for (int kk = 0; kk < KSTEPS; ++kk) {
       uint16_t e[4] = {0, 0, 0, 0};
@@ -272,7 +281,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_consta
 #pragma unroll
         for (int x = 0; x < 4; ++x) {
           const int m = base + x;  // < D: a kmin element, else kmax
-          const uint16_t qv = qp[g8 * D + (m % D)];
+          const uint16_t qv = q_s[g8 * D + (m % D)];
           const bool neg = Neg<T>::neg(qv);
           e[x] = (m < D) == neg ? qv : (uint16_t)0;  // kmin takes q-, kmax takes q+
         }
