@@ -419,15 +419,20 @@ def roofline(layers, stream, iters):
     achieved = (dyn + strm) / (avg_ms * 1e-3) / 1e9
     peak, kind = measured_peaks()
     traffic = None
-    tp = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    tp = os.path.join(ROOT, "profiles", "decode_traffic.txt")
     if os.path.exists(tp):
-        try:
-            with open(tp) as f:
-                tj = json.load(f)
-            if tj.get("kernel_source_hash") == kernel_hash():
-                traffic = tj.get("traffic_bytes_per_launch")
-        except Exception:
-            traffic = None
+        # "key: value" lines written from an ncu capture of this kernel; the
+        # figure is used only while the kernel sources are unchanged
+        kv = {}
+        for ln in open(tp):
+            if ":" in ln and not ln.startswith("#"):
+                k, v = ln.split(":", 1)
+                kv[k.strip()] = v.strip()
+        if kv.get("kernel_source_hash") == kernel_hash():
+            try:
+                traffic = float(kv["traffic_bytes_per_launch"])
+            except (KeyError, ValueError):
+                traffic = None
     return {"kernel": "decode_tiles_kernel (split-K sparse attention, fused combine), one layer",
             "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
             "peak_kind": kind + " (MEASURED_PEAKS.json hbm_gbs, burst copy)" if kind == "measured" else kind,

@@ -259,12 +259,12 @@ spd_status spd_check_status(spd_ctx *ctx, spd_stream stream);
 
 const char *spd_status_string(spd_status s);
 /*
- * Early KV staging (off by default).  When on, a decode kernel of this
- * context whose preceding kernel on the stream was not enqueued by this
- * context starts loading its K/V tiles (reading the page table, selection and
- * pools) before that kernel has finished; q, the new token and all writes
- * still wait for it.  This overlaps the attention's HBM reads with the tail
- * of the kernel before it -- in a model, the projection that produces q.
+ * Early KV staging (off by default).  When on, a decode or selection kernel
+ * of this context whose preceding kernel on the stream was not enqueued by
+ * this context starts loading KV-cache data (page table, selection, K/V
+ * tiles, page metadata) before that kernel has finished; q, the new token and
+ * all writes still wait for it.  This overlaps the HBM reads with the tail of
+ * the kernel before it -- in a model, the projection that produces q.
  * Turn it on only if (a) nothing but this library's calls on this context
  * writes its KV-cache buffers, and (b) other code's kernels on the stream do
  * not release their dependents (programmatic dependent launch) before they

@@ -11,24 +11,36 @@
 //   streaming head three runs of ring-buffer slots -- sink [0, min(S, L)),
 //                  the window's slots up to the ring's end, and its wrapped
 //                  remainder -- each run tiled from its start.
-// A CTA (4 warps) takes up to 8 consecutive tiles of one unit (an "item").
+// A unit is split over nc clusters of CS CTAs (a thread-block cluster; CS and
+// the CTAs' tile ranges are chosen by the host so the launch fills the GPU);
+// a CTA ("item") takes a contiguous range of the unit's tiles.
 //
-// Data movement.  One thread issues every TMA tensor load of the item at
-// kernel start (2-D boxes of 64 channels x 16 rows, 128-byte swizzle, one
-// mbarrier per tile), so the whole item is in flight at once; K/V bytes are
-// read from HBM exactly once.
+// Data movement.  Each of the 8 warps owns one shared-memory stage; the CTA's
+// tiles go round-robin to the warps, every stage is filled by a TMA tensor
+// load (64 channels x 16 rows boxes, 128-byte swizzle, one mbarrier per
+// stage) and refilled as soon as its warp has consumed it; the later tiles
+// are prefetched into L2 at kernel start, so refills read L2.  K/V bytes are
+// read from HBM once.
 //
-// Math (per warp, per tile, all G query heads of the kv head at once):
+// Math (per warp and tile, all G query heads of the kv head at once):
 //   q.K^T   mma.sync m16n8k16, A = K tile rows (ldmatrix from the swizzled
-//           tile), B = q^T held in registers (heads padded to 8 columns),
-//           fp32 accumulate -- the products of 16-bit inputs are exact;
-//   softmax online, in fp32, base-2 with log2(e)/sqrt(d) folded in;
-//   P.V     fp32 FMAs on CUDA cores (P stays fp32: no rounding of weights).
-// Split combine.  Each item writes (o, m, l) for its unit; the last item of a
-// unit to finish (atomic ticket, no waiting) merges them with a
-// log-sum-exp rescale and writes the fp32 output -- the row max / row sum
-// export of the Novita KV-sparsity article ("attention mechanism
-// modifications").
+//           tile), B = q^T in registers (heads padded to 8 columns), fp32
+//           accumulate -- the products of 16-bit inputs are exact;
+//   softmax online, in fp32, base 2 with log2(e)/sqrt(d) folded in;
+//   P.V     mma.sync m16n8k16 as O^T = V^T P^T: A = V tile (ldmatrix.trans),
+//           B = P^T with the 16 tokens as k and the heads as the 8 columns;
+//           P is split into a 16-bit high part and the 16-bit rounding of
+//           the rest, two mma each, so the weights carry ~2^-16 relative
+//           error instead of 2^-9 (fp32 accumulate).
+// Merge.  The 8 warps merge in shared memory into the CTA's (m, l, o).  The
+// CTAs of a cluster then merge over distributed shared memory: every CTA
+// pushes each channel slice of its (m, l, o) into the inbox of the CTA that
+// owns that slice (remote shared-memory stores), and after one cluster
+// barrier each CTA combines its slice locally -- the row max / row sum export
+// of the Novita KV-sparsity article's modified FlashAttention ("attention
+// mechanism modifications").  When a
+// unit has several clusters (nc > 1), their results meet in global memory:
+// the last cluster to finish (atomic ticket, no waiting) merges them.
 //
 // Fused append (decode step).  The CTA that owns a unit's newest token also
 // appends it: the row is written to the pool / ring, patched into the
@@ -43,17 +55,19 @@
 namespace spd {
 namespace {
 
-constexpr int kRows = 16;          // rows per tile (one mma M tile)
-constexpr int kMaxTiles = 8;       // tiles per item
-constexpr int kWarps = 4;
+constexpr int kRows = 16;                  // rows per tile (one mma M tile)
+constexpr int kWarps = 8;                  // 256 threads
+constexpr int kThreads = kWarps * 32;
+constexpr int kStages = kWarps;            // one shared-memory stage per warp
+constexpr int kMaxDesc = 256;              // tiles one CTA may take
 constexpr uint32_t kWaitLimit = 1u << 24;  // bounded mbarrier polls
 
 template <int D>
 struct Geo {
-  static constexpr int kBoxes = D / 64;                 // 64-channel boxes per row
-  static constexpr int kBoxBytes = kRows * 128;         // one box: 16 rows x 128 B
+  static constexpr int kBoxes = D / 64;                      // 64-channel boxes per row
+  static constexpr int kBoxBytes = kRows * 128;              // one box: 16 rows x 128 B
   static constexpr int kTileBytes = 2 * kBoxes * kBoxBytes;  // K boxes then V boxes
-  static constexpr int kCPL = D / 32;                   // channels per lane in P.V
+  static constexpr int kCPL = D / 32;                        // channels per lane in P.V
 };
 
 template <int G>
@@ -67,30 +81,30 @@ struct TileDesc {
   int pad;
 };
 
-// Shared memory: a small fixed region (barriers, tile descriptors, P and
-// rescale buffers, per-warp row max / sum, flags), then the K/V tiles at a
-// 1024-byte aligned offset.  The launch sizes the tile region for the largest
-// item it holds, at least big enough for the warp-merge and combine buffers.
+// Shared memory: a fixed region (stage barriers, tile descriptors, P and
+// rescale buffers, per-warp and per-CTA row max / sum / output, flags), then
+// the stages at a 1024-byte aligned offset.  After the tile loop the stage
+// region holds the warp-merge buffer and later the global-merge buffers.
 template <int D, int G>
 struct Smem {
-  static constexpr int kBars = 0;                                   // uint64 x kMaxTiles
-  static constexpr int kDesc = kBars + kMaxTiles * 8;               // TileDesc x kMaxTiles
-  static constexpr int kP = kDesc + kMaxTiles * (int)sizeof(TileDesc);  // float [W][16][GP]
-  static constexpr int kC = kP + kWarps * kRows * GP<G>::v * 4;     // float [W][GP]
-  static constexpr int kML = kC + kWarps * GP<G>::v * 4;            // float [2][W][G]
-  static constexpr int kFlag = kML + 2 * kWarps * G * 4;            // int [4]
-  static constexpr int kTiles = (kFlag + 16 + 1023) / 1024 * 1024;  // tiles start here
-  // warp-merge buffer [W][G][D] floats, or the combine's (m, l) and weight
-  // buffers for 256 items
-  static constexpr int kMinTileRegion = (kWarps * G * D * 4 > 256 * G * 12 + 64)
-                                            ? kWarps * G * D * 4
-                                            : 256 * G * 12 + 64;
-  static constexpr int bytes(int tiles) {
-    return kTiles + (tiles * Geo<D>::kTileBytes > kMinTileRegion ? tiles * Geo<D>::kTileBytes
-                                                                  : kMinTileRegion) +
-           1024;  // alignment slack
-  }
-  static constexpr int kAlloc = bytes(kMaxTiles);
+  static constexpr int kBars = 0;                                      // uint64 [kStages]
+  static constexpr int kDesc = kBars + kStages * 8;                    // TileDesc [kMaxDesc]
+  static constexpr int kP = kDesc + kMaxDesc * (int)sizeof(TileDesc);  // float [W][16][GP]
+  static constexpr int kC = kP + kWarps * kRows * GP<G>::v * 4;        // float [W][GP]
+  static constexpr int kML = kC + kWarps * GP<G>::v * 4;               // float [2][W][G]
+  // inbox: what the cluster's CTAs send this CTA: M[16][G], L[16][G] and
+  // O[16 ranks][G][D / CS] (= G * D floats for any CS)
+  static constexpr int kInbox = (kML + 2 * kWarps * G * 4 + 15) / 16 * 16;
+  static constexpr int kFlag = kInbox + (32 * G + G * D) * 4;          // int [4]
+  static constexpr int kTiles = (kFlag + 16 + 1023) / 1024 * 1024;
+  static constexpr int kStageRegion = kStages * Geo<D>::kTileBytes;
+  static constexpr int kMergeRegion = kWarps * G * D * 4;              // o of every warp
+  static constexpr int kCombineRegion = 256 * G * 12 + 64;             // (m, l), weights
+  static constexpr int kRegion =
+      kStageRegion > kMergeRegion
+          ? (kStageRegion > kCombineRegion ? kStageRegion : kCombineRegion)
+          : (kMergeRegion > kCombineRegion ? kMergeRegion : kCombineRegion);
+  static constexpr int kAlloc = kTiles + kRegion + 1024;  // + alignment slack
 };
 
 template <typename T> struct IsBF16 { static constexpr bool v = false; };
@@ -101,9 +115,13 @@ __device__ __forceinline__ float tof(T x);
 template <> __device__ __forceinline__ float tof(__half x) { return __half2float(x); }
 template <> __device__ __forceinline__ float tof(__nv_bfloat16 x) { return __bfloat162float(x); }
 
-__device__ __forceinline__ uint32_t pack2(uint16_t lo, uint16_t hi) {
-  return (uint32_t)lo | ((uint32_t)hi << 16);
-}
+template <typename T> struct Cvt;
+template <> struct Cvt<__half> {
+  static __device__ __forceinline__ __half from(float x) { return __float2half_rn(x); }
+};
+template <> struct Cvt<__nv_bfloat16> {
+  static __device__ __forceinline__ __nv_bfloat16 from(float x) { return __float2bfloat16_rn(x); }
+};
 
 __device__ __forceinline__ void set_err(int *err, int code, int a, int b, int c) {
   if (atomicCAS(err, 0, code) == 0) {
@@ -121,24 +139,27 @@ __device__ __forceinline__ uint32_t chan_off(int r, int ch) {
 }
 
 template <typename T, int D, int G>
-__global__ void __launch_bounds__(128) decode_tiles_kernel(const __grid_constant__ TileDecodeParams p) {
+__global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_constant__ TileDecodeParams p) {
   using Gm = Geo<D>;
   using Sm = Smem<D, G>;
-  constexpr int CPL = Gm::kCPL;
+  constexpr int CPL = Gm::kCPL;  // channels per lane of the fused append
   constexpr int GPAD = GP<G>::v;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t *tiles = smem + Sm::kTiles;
+  uint8_t *stages = smem + Sm::kTiles;
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Sm::kBars);
   TileDesc *tdesc = reinterpret_cast<TileDesc *>(smem + Sm::kDesc);
   float *P_all = reinterpret_cast<float *>(smem + Sm::kP);
-  float *C_all = reinterpret_cast<float *>(smem + Sm::kC);
   float *m_w = reinterpret_cast<float *>(smem + Sm::kML);
   float *l_w = m_w + kWarps * G;
+  float *in_M = reinterpret_cast<float *>(smem + Sm::kInbox);  // [rank][G]
+  float *in_L = in_M + 16 * G;                                   // [rank][G]
+  float *in_O = in_L + 16 * G;                                   // [rank][G][slice]
   int *s_flag = reinterpret_cast<int *>(smem + Sm::kFlag);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  cluster_arrive_relaxed();  // paired with the wait before the first remote store
   if (tid == 0) {
     prefetch_tmap(&p.tm_k);
     prefetch_tmap(&p.tm_v);
@@ -167,6 +188,10 @@ __global__ void __launch_bounds__(128) decode_tiles_kernel(const __grid_constant
     tpi = s.tpi_str;
     unit_item0 = s.item_off + p.Hd * s.ns_dyn + sub * s.ns_str;
   }
+  const int CS = p.cluster;        // CTAs per cluster (units' item counts are multiples)
+  const int rank = split % CS;     // == %cluster_ctarank: clusters start at multiples of CS
+  const int ci = split / CS;       // cluster index within the unit
+  const int nc = ns / CS;          // clusters of this unit
   const int h = dyn ? p.dyn_kv[sub] : p.str_kv[sub];
   const int L = s.L;
 
@@ -194,8 +219,8 @@ __global__ void __launch_bounds__(128) decode_tiles_kernel(const __grid_constant
     n_tiles = run_tiles[0] + run_tiles[1] + run_tiles[2];
   }
   const int tile0 = split * tpi;
-  const int nt = max(0, min(n_tiles, tile0 + tpi) - tile0);
-  const bool owns_newest = tile0 + nt == n_tiles;
+  const int nt = min(kMaxDesc, max(0, min(n_tiles, tile0 + tpi) - tile0));
+  const bool owns_newest = nt > 0 && tile0 + nt == n_tiles;
   const bool do_append = p.k_new != nullptr && owns_newest;
 
   // Everything above used only the parameter block.  The KV cache (page
@@ -210,13 +235,8 @@ __global__ void __launch_bounds__(128) decode_tiles_kernel(const __grid_constant
     pdl_launch_dependents();
   }
 
-  // ---- issue every TMA load of the item: thread t sets up tile t ----
-  if (tid < nt) {
-    const int t = tid;
-    mbar_init(&bars[t], 1);
-    fence_mbar_init();
-    const CUtensorMap *mk = dyn ? &p.tm_k : &p.tm_sk;
-    const CUtensorMap *mv = dyn ? &p.tm_v : &p.tm_sv;
+  // ---- tile descriptors (threads in parallel), stage barriers ----
+  for (int t = tid; t < nt; t += kThreads) {
     const int tau = tile0 + t;
     TileDesc td{0, 0, 0, 0};
     if (dyn) {
@@ -244,13 +264,37 @@ __global__ void __launch_bounds__(128) decode_tiles_kernel(const __grid_constant
       td.n_valid = min(kRows, run_len[r] - k * kRows);
     }
     tdesc[t] = td;
-    if (td.n_valid > 0) {
-      uint8_t *kt = tiles + t * Gm::kTileBytes;
-      uint8_t *vt = kt + Gm::kBoxes * Gm::kBoxBytes;
-      mbar_arrive_expect_tx(&bars[t], Gm::kTileBytes);
+  }
+  if (tid < kStages) {
+    mbar_init(&bars[tid], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  const CUtensorMap *mk = dyn ? &p.tm_k : &p.tm_sk;
+  const CUtensorMap *mv = dyn ? &p.tm_v : &p.tm_sv;
+  uint8_t *kt = stages + warp * Gm::kTileBytes;  // the warp's stage: K boxes, then V boxes
+  uint8_t *vt = kt + Gm::kBoxes * Gm::kBoxBytes;
+  // the warp's stage holds its tiles warp, warp + kWarps, ... in turn
+  auto issue = [&](int t) {
+    const TileDesc td = tdesc[t];
+    if (td.n_valid <= 0) return;
+    mbar_arrive_expect_tx(&bars[warp], Gm::kTileBytes);
+    for (int b = 0; b < Gm::kBoxes; ++b) {
+      tma_load_3d(kt + b * Gm::kBoxBytes, mk, b * 64, td.y, td.z, &bars[warp]);
+      tma_load_3d(vt + b * Gm::kBoxBytes, mv, b * 64, td.y, td.z, &bars[warp]);
+    }
+  };
+  if (lane == 0 && warp < nt) {
+    issue(warp);
+    // the warp's later tiles start their way from HBM into L2 now; their
+    // stage refills then read L2
+    for (int t = warp + kWarps; t < nt; t += kWarps) {
+      const TileDesc td = tdesc[t];
+      if (td.n_valid <= 0) continue;
       for (int b = 0; b < Gm::kBoxes; ++b) {
-        tma_load_3d(kt + b * Gm::kBoxBytes, mk, b * 64, td.y, td.z, &bars[t]);
-        tma_load_3d(vt + b * Gm::kBoxBytes, mv, b * 64, td.y, td.z, &bars[t]);
+        tma_prefetch_l2_3d(mk, b * 64, td.y, td.z);
+        tma_prefetch_l2_3d(mv, b * 64, td.y, td.z);
       }
     }
   }
@@ -264,222 +308,228 @@ __global__ void __launch_bounds__(128) decode_tiles_kernel(const __grid_constant
   const int g8 = lane >> 2, t4 = lane & 3;
   uint32_t qb[D / 16][2];
   {
-    const uint16_t *qp = reinterpret_cast<const uint16_t *>(p.q) + ((size_t)i * p.Hq + h * G) * D;
+    const uint32_t *qp = reinterpret_cast<const uint32_t *>(
+        reinterpret_cast<const uint16_t *>(p.q) + ((size_t)i * p.Hq + h * G) * D);
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
       if (g8 < G) {
-        const uint16_t *row = qp + g8 * D + kk * 16 + 2 * t4;
-        qb[kk][0] = pack2(row[0], row[1]);
-        qb[kk][1] = pack2(row[8], row[9]);
+        qb[kk][0] = qp[(g8 * D + kk * 16 + 2 * t4) / 2];
+        qb[kk][1] = qp[(g8 * D + kk * 16 + 2 * t4 + 8) / 2];
       } else {
         qb[kk][0] = qb[kk][1] = 0u;
       }
     }
   }
-  __syncthreads();
 
   // ---- per-warp online softmax over its tiles ----
   float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F, l0 = 0.f, l1 = 0.f;  // heads 2t4, 2t4+1
-  float o[G][CPL];
+  // O^T accumulators: m-tile m holds channels 16m + g8 (and + 8) x heads
+  // 2t4, 2t4 + 1 -- the two heads whose running max this lane tracks
+  constexpr int MT = D / 16;
+  float oacc[MT][4];
 #pragma unroll
-  for (int g = 0; g < G; ++g)
+  for (int m = 0; m < MT; ++m)
 #pragma unroll
-    for (int e = 0; e < CPL; ++e) o[g][e] = 0.f;
+    for (int e = 0; e < 4; ++e) oacc[m][e] = 0.f;
   float *Pw = P_all + warp * kRows * GPAD;
-  float *Cw = C_all + warp * GPAD;
   const float sc = p.scale_log2;
 
+  int use = 0;  // loads this warp's stage has completed (mbarrier phase)
   for (int t = warp; t < nt; t += kWarps) {
     const TileDesc td = tdesc[t];
-    if (td.n_valid <= 0) continue;
-    if (!mbar_wait(&bars[t], 0, kWaitLimit)) {
-      if (lane == 0) {
-        set_err(p.err, kDevTimeout, s.slot, h, t);
-        s_flag[1] = 1;
+    if (td.n_valid > 0) {
+      if (!mbar_wait(&bars[warp], use & 1, kWaitLimit)) {
+        if (lane == 0) {
+          set_err(p.err, kDevTimeout, s.slot, h, t);
+          s_flag[1] = 1;
+        }
+        break;
       }
-      continue;
-    }
-    uint8_t *kt = tiles + t * Gm::kTileBytes;
-    uint8_t *vt = kt + Gm::kBoxes * Gm::kBoxBytes;
-    const int nv = td.n_valid;
+      ++use;
+      const int nv = td.n_valid;
 
-    if (do_append && t == nt - 1) {
-      // the newest token is row nv-1 of the unit's last tile
-      const int r = nv - 1;
-      const int cb = lane * CPL;
-      const size_t src = ((size_t)i * p.Hkv + h) * D + cb;
-      const uint16_t *kn = reinterpret_cast<const uint16_t *>(p.k_new) + src;
-      const uint16_t *vn = reinterpret_cast<const uint16_t *>(p.v_new) + src;
-      uint16_t kx[CPL], vx[CPL];
-#pragma unroll
-      for (int e = 0; e < CPL; ++e) {
-        kx[e] = kn[e];
-        vx[e] = vn[e];
-      }
-#pragma unroll
-      for (int e = 0; e < CPL; ++e) {
-        *reinterpret_cast<uint16_t *>(kt + chan_off<D>(r, cb + e)) = kx[e];
-        *reinterpret_cast<uint16_t *>(vt + chan_off<D>(r, cb + e)) = vx[e];
-      }
-      size_t grow;
-      uint16_t *kg, *vg;
-      if (dyn) {
-        grow = ((size_t)td.z * p.P + td.y + r) * D + cb;
-        kg = static_cast<uint16_t *>(p.k_pool) + grow;
-        vg = static_cast<uint16_t *>(p.v_pool) + grow;
-      } else {
-        grow = ((size_t)td.y + r) * D + cb;
-        kg = static_cast<uint16_t *>(p.stream_k) + grow;
-        vg = static_cast<uint16_t *>(p.stream_v) + grow;
-      }
-#pragma unroll
-      for (int e = 0; e < CPL; ++e) {
-        kg[e] = kx[e];
-        vg[e] = vx[e];
-      }
-      if (dyn) {
-        const int j = nL - 1;
-        uint16_t *mrow = static_cast<uint16_t *>(p.meta) +
-                         ((size_t)td.z * p.R + (j % p.R)) * 2 * D + cb;
-        const bool fresh = (L - 1) % p.ell == 0;
+      if (do_append && t == nt - 1) {
+        // the newest token is row nv-1 of the unit's last tile
+        const int r = nv - 1;
+        const int cb = lane * CPL;
+        const size_t src = ((size_t)i * p.Hkv + h) * D + cb;
+        const uint16_t *kn = reinterpret_cast<const uint16_t *>(p.k_new) + src;
+        const uint16_t *vn = reinterpret_cast<const uint16_t *>(p.v_new) + src;
+        uint16_t kx[CPL], vx[CPL];
 #pragma unroll
         for (int e = 0; e < CPL; ++e) {
-          uint16_t bmin = kx[e], bmax = kx[e];
-          if (!fresh) {
-            const uint16_t omin = mrow[e], omax = mrow[D + e];
-            const float x = tof(*reinterpret_cast<const T *>(&kx[e]));
-            bmin = x < tof(*reinterpret_cast<const T *>(&omin)) ? kx[e] : omin;
-            bmax = x > tof(*reinterpret_cast<const T *>(&omax)) ? kx[e] : omax;
-          }
-          mrow[e] = bmin;
-          mrow[D + e] = bmax;
+          kx[e] = kn[e];
+          vx[e] = vn[e];
         }
-      }
-      __syncwarp();
-    }
-
-    if (nv < kRows) {
-      // rows past the tile's attended tokens: zero V so the unrolled P.V
-      // below adds exactly 0 for them (their weights are 0 as well)
-      for (int x = lane; x < (kRows - nv) * 8 * Gm::kBoxes; x += 32) {
-        const int box = x / ((kRows - nv) * 8), rem = x % ((kRows - nv) * 8);
-        const int r = nv + rem / 8, ch = rem % 8;
-        *reinterpret_cast<uint4 *>(vt + box * Gm::kBoxBytes + r * 128 + ch * 16) =
-            make_uint4(0, 0, 0, 0);
-      }
-      __syncwarp();
-    }
-
-    // q.K^T for 16 rows x 8 (padded) heads
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    {
-      const int row = (lane & 7) + ((lane >> 3) & 1) * 8;
-      const int chalf = lane >> 4;
-      const uint32_t kbase = smem_u32(kt);
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const int box = kk >> 2;
-        const int chunk = 2 * (kk & 3) + chalf;
-        uint32_t a[4];
-        ldmatrix_x4(kbase + box * Gm::kBoxBytes + swz128(row, chunk), a[0], a[1], a[2], a[3]);
-        mma_16816<IsBF16<T>::v>(acc, a, qb[kk][0], qb[kk][1]);
-      }
-    }
-    // acc: [0] row g8 head 2t4, [1] row g8 head 2t4+1, [2] row g8+8 head 2t4, [3] row g8+8 head 2t4+1
-    const bool v_lo = g8 < nv, v_hi = g8 + 8 < nv;
-    const float z0 = v_lo ? acc[0] * sc : -CUDART_INF_F;
-    const float z1 = v_lo ? acc[1] * sc : -CUDART_INF_F;
-    const float z2 = v_hi ? acc[2] * sc : -CUDART_INF_F;
-    const float z3 = v_hi ? acc[3] * sc : -CUDART_INF_F;
-    float mx0 = fmaxf(z0, z2), mx1 = fmaxf(z1, z3);
-#pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-    }
-    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-    const float c0 = exp2f(m0 - mn0), c1 = exp2f(m1 - mn1);
-    const float p0 = exp2f(z0 - mn0), p1 = exp2f(z1 - mn1);
-    const float p2 = exp2f(z2 - mn0), p3 = exp2f(z3 - mn1);
-    l0 = l0 * c0 + p0 + p2;
-    l1 = l1 * c1 + p1 + p3;
-    m0 = mn0;
-    m1 = mn1;
-    const int h0 = 2 * t4, h1 = 2 * t4 + 1;
-    if (h0 < G) {
-      Pw[g8 * GPAD + h0] = p0;
-      Pw[(g8 + 8) * GPAD + h0] = p2;
-      if (g8 == 0) Cw[h0] = c0;
-    }
-    if (h1 < G) {
-      Pw[g8 * GPAD + h1] = p1;
-      Pw[(g8 + 8) * GPAD + h1] = p3;
-      if (g8 == 0) Cw[h1] = c1;
-    }
-    __syncwarp();
-
-    // P.V: lane owns channels [lane*CPL, lane*CPL + CPL) of every head
-    {
-      float cr[G];
-#pragma unroll
-      for (int g = 0; g < G; ++g) cr[g] = Cw[g];
-#pragma unroll
-      for (int g = 0; g < G; ++g)
-#pragma unroll
-        for (int e = 0; e < CPL; ++e) o[g][e] *= cr[g];
-      const int cb = lane * CPL;
-      const uint32_t voff = (uint32_t)((cb >> 6) * Gm::kBoxBytes) + ((cb & 7) * 2);
-      const int chunk = (cb & 63) >> 3;
-#pragma unroll
-      for (int r = 0; r < kRows; ++r) {
-        float vf[CPL];
-        const uint8_t *vp = vt + voff + swz128(r, chunk);
-        if constexpr (CPL == 4) {
-          const uint2 raw = *reinterpret_cast<const uint2 *>(vp);
-          const T *e2 = reinterpret_cast<const T *>(&raw);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) vf[e] = tof(e2[e]);
+        for (int e = 0; e < CPL; ++e) {
+          *reinterpret_cast<uint16_t *>(kt + chan_off<D>(r, cb + e)) = kx[e];
+          *reinterpret_cast<uint16_t *>(vt + chan_off<D>(r, cb + e)) = vx[e];
+        }
+        size_t grow;
+        uint16_t *kg, *vg;
+        if (dyn) {
+          grow = ((size_t)td.z * p.P + td.y + r) * D + cb;
+          kg = static_cast<uint16_t *>(p.k_pool) + grow;
+          vg = static_cast<uint16_t *>(p.v_pool) + grow;
         } else {
-          const uint32_t raw = *reinterpret_cast<const uint32_t *>(vp);
-          const T *e2 = reinterpret_cast<const T *>(&raw);
-#pragma unroll
-          for (int e = 0; e < 2; ++e) vf[e] = tof(e2[e]);
-        }
-        float pr[GPAD];
-        const float4 *prow = reinterpret_cast<const float4 *>(Pw + r * GPAD);
-#pragma unroll
-        for (int g4 = 0; g4 < GPAD / 4; ++g4) {
-          const float4 x = prow[g4];
-          pr[4 * g4] = x.x;
-          pr[4 * g4 + 1] = x.y;
-          pr[4 * g4 + 2] = x.z;
-          pr[4 * g4 + 3] = x.w;
+          grow = ((size_t)td.y + r) * D + cb;
+          kg = static_cast<uint16_t *>(p.stream_k) + grow;
+          vg = static_cast<uint16_t *>(p.stream_v) + grow;
         }
 #pragma unroll
-        for (int g = 0; g < G; ++g)
+        for (int e = 0; e < CPL; ++e) {
+          kg[e] = kx[e];
+          vg[e] = vx[e];
+        }
+        if (dyn) {
+          const int j = nL - 1;
+          uint16_t *mrow = static_cast<uint16_t *>(p.meta) +
+                           ((size_t)td.z * p.R + (j % p.R)) * 2 * D + cb;
+          const bool fresh = (L - 1) % p.ell == 0;
 #pragma unroll
-          for (int e = 0; e < CPL; ++e) o[g][e] = fmaf(pr[g], vf[e], o[g][e]);
+          for (int e = 0; e < CPL; ++e) {
+            uint16_t bmin = kx[e], bmax = kx[e];
+            if (!fresh) {
+              const uint16_t omin = mrow[e], omax = mrow[D + e];
+              const float x = tof(*reinterpret_cast<const T *>(&kx[e]));
+              bmin = x < tof(*reinterpret_cast<const T *>(&omin)) ? kx[e] : omin;
+              bmax = x > tof(*reinterpret_cast<const T *>(&omax)) ? kx[e] : omax;
+            }
+            mrow[e] = bmin;
+            mrow[D + e] = bmax;
+          }
+        }
+        __syncwarp();
       }
+      if (nv < kRows) {
+        // rows past the tile's attended tokens: zero V so the unrolled P.V
+        // below adds exactly 0 for them (their weights are 0 as well)
+        for (int x = lane; x < (kRows - nv) * 8 * Gm::kBoxes; x += 32) {
+          const int box = x / ((kRows - nv) * 8), rem = x % ((kRows - nv) * 8);
+          const int r = nv + rem / 8, ch = rem % 8;
+          *reinterpret_cast<uint4 *>(vt + box * Gm::kBoxBytes + r * 128 + ch * 16) =
+              make_uint4(0, 0, 0, 0);
+        }
+        __syncwarp();
+      }
+
+      // q.K^T for 16 rows x 8 (padded) heads
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      {
+        const int row = (lane & 7) + ((lane >> 3) & 1) * 8;
+        const int chalf = lane >> 4;
+        const uint32_t kbase = smem_u32(kt);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const int box = kk >> 2;
+          const int chunk = 2 * (kk & 3) + chalf;
+          uint32_t a[4];
+          ldmatrix_x4(kbase + box * Gm::kBoxBytes + swz128(row, chunk), a[0], a[1], a[2], a[3]);
+          mma_16816<IsBF16<T>::v>(acc, a, qb[kk][0], qb[kk][1]);
+        }
+      }
+      // acc: [0] row g8 head 2t4, [1] row g8 head 2t4+1, [2] row g8+8 head 2t4, [3] row g8+8 head 2t4+1
+      const bool v_lo = g8 < nv, v_hi = g8 + 8 < nv;
+      const float z0 = v_lo ? acc[0] * sc : -CUDART_INF_F;
+      const float z1 = v_lo ? acc[1] * sc : -CUDART_INF_F;
+      const float z2 = v_hi ? acc[2] * sc : -CUDART_INF_F;
+      const float z3 = v_hi ? acc[3] * sc : -CUDART_INF_F;
+      float mx0 = fmaxf(z0, z2), mx1 = fmaxf(z1, z3);
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+      }
+      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+      const float c0 = exp2f(m0 - mn0), c1 = exp2f(m1 - mn1);
+      const float p0 = exp2f(z0 - mn0), p1 = exp2f(z1 - mn1);
+      const float p2 = exp2f(z2 - mn0), p3 = exp2f(z3 - mn1);
+      l0 = l0 * c0 + p0 + p2;
+      l1 = l1 * c1 + p1 + p3;
+      m0 = mn0;
+      m1 = mn1;
+      const int h0 = 2 * t4, h1 = 2 * t4 + 1;
+      if (h0 < G) {
+        Pw[g8 * GPAD + h0] = p0;
+        Pw[(g8 + 8) * GPAD + h0] = p2;
+      }
+      if (h1 < G) {
+        Pw[g8 * GPAD + h1] = p1;
+        Pw[(g8 + 8) * GPAD + h1] = p3;
+      }
+      __syncwarp();
+
+      // P.V on tensor cores: rescale, then O^T += V^T (P_hi + P_lo)^T
+#pragma unroll
+      for (int m = 0; m < MT; ++m) {
+        oacc[m][0] *= c0;
+        oacc[m][1] *= c1;
+        oacc[m][2] *= c0;
+        oacc[m][3] *= c1;
+      }
+      uint32_t bh0, bh1, bl0, bl1;  // B = P^T: k = tokens 2t4.. / 2t4+8.., n = head g8
+      {
+        float pv[4] = {0.f, 0.f, 0.f, 0.f};
+        if (g8 < G) {
+          pv[0] = Pw[(2 * t4) * GPAD + g8];
+          pv[1] = Pw[(2 * t4 + 1) * GPAD + g8];
+          pv[2] = Pw[(2 * t4 + 8) * GPAD + g8];
+          pv[3] = Pw[(2 * t4 + 9) * GPAD + g8];
+        }
+        uint16_t hi[4], lo[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const T th = Cvt<T>::from(pv[e]);
+          hi[e] = *reinterpret_cast<const uint16_t *>(&th);
+          const T tl = Cvt<T>::from(pv[e] - tof(th));
+          lo[e] = *reinterpret_cast<const uint16_t *>(&tl);
+        }
+        bh0 = (uint32_t)hi[0] | ((uint32_t)hi[1] << 16);
+        bh1 = (uint32_t)hi[2] | ((uint32_t)hi[3] << 16);
+        bl0 = (uint32_t)lo[0] | ((uint32_t)lo[1] << 16);
+        bl1 = (uint32_t)lo[2] | ((uint32_t)lo[3] << 16);
+      }
+      {
+        // A = V^T for m-tile m: matrix j of ldmatrix.x4.trans takes token rows
+        // (lane & 7) + 8 * (j >> 1) and channel chunk 2m + (j & 1)
+        const int j = lane >> 3;
+        const int row = (lane & 7) + 8 * (j >> 1);
+        const uint32_t vbase = smem_u32(vt);
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+          const int box = m >> 2;
+          const int chunk = 2 * (m & 3) + (j & 1);
+          uint32_t a[4];
+          ldmatrix_x4_trans(vbase + box * Gm::kBoxBytes + swz128(row, chunk), a[0], a[1], a[2],
+                            a[3]);
+          mma_16816<IsBF16<T>::v>(oacc[m], a, bh0, bh1);
+          mma_16816<IsBF16<T>::v>(oacc[m], a, bl0, bl1);
+        }
+      }
+      __syncwarp();
     }
-    __syncwarp();
+    // refill this warp's stage with its next tile
+    if (t + kWarps < nt) {
+      fence_proxy_async_smem();  // the warp's reads of the stage precede the TMA write
+      if (lane == 0) issue(t + kWarps);
+    }
   }
 
-  // ---- merge the warps ----
+  // ---- merge the warps into this CTA's (M, L, O) ----
 #pragma unroll
   for (int off = 4; off < 32; off <<= 1) {
     l0 += __shfl_xor_sync(0xffffffffu, l0, off);
     l1 += __shfl_xor_sync(0xffffffffu, l1, off);
   }
-  __syncthreads();  // every warp is done with the tiles: reuse them for o
+  __syncthreads();  // every warp is done with its stage: reuse the region for o
   if (s_flag[1]) {
     // a wait gave up: give the loads still in flight one more bounded wait
     // before their destination is reused
-    if (tid == 0)
-      for (int t = 0; t < nt; ++t)
-        if (tdesc[t].n_valid > 0) mbar_wait(&bars[t], 0, kWaitLimit);
+    if (lane == 0 && warp < nt) mbar_wait(&bars[warp], use & 1, kWaitLimit);
     __syncthreads();
   }
-  float *o_w = reinterpret_cast<float *>(tiles);  // [W][G][D]
+  float *o_w = reinterpret_cast<float *>(stages);  // [W][G][D]
   if (g8 == 0) {
     if (2 * t4 < G) {
       m_w[warp * G + 2 * t4] = m0;
@@ -491,14 +541,24 @@ __global__ void __launch_bounds__(128) decode_tiles_kernel(const __grid_constant
     }
   }
 #pragma unroll
-  for (int g = 0; g < G; ++g)
-#pragma unroll
-    for (int e = 0; e < CPL; ++e) o_w[(warp * G + g) * D + lane * CPL + e] = o[g][e];
+  for (int m = 0; m < MT; ++m) {
+    const int ch = 16 * m + g8;
+    if (2 * t4 < G) {
+      o_w[(warp * G + 2 * t4) * D + ch] = oacc[m][0];
+      o_w[(warp * G + 2 * t4) * D + ch + 8] = oacc[m][2];
+    }
+    if (2 * t4 + 1 < G) {
+      o_w[(warp * G + 2 * t4 + 1) * D + ch] = oacc[m][1];
+      o_w[(warp * G + 2 * t4 + 1) * D + ch + 8] = oacc[m][3];
+    }
+  }
   __syncthreads();
-
-  const int unit = i * p.Hkv + h;
-  float *out = p.out + ((size_t)i * p.Hq + h * G) * D;
-  for (int x = tid; x < G * D; x += blockDim.x) {
+  cluster_wait();  // every CTA of the cluster has started: its inbox may be written
+  // this CTA's (M, L, O), pushed straight into the inbox of the cluster CTA
+  // that owns each channel slice (remote shared-memory stores)
+  const int slice = D / CS;
+  const uint32_t aM = smem_u32(in_M), aL = smem_u32(in_L), aO = smem_u32(in_O);
+  for (int x = tid; x < G * D; x += kThreads) {
     const int g = x / D, c = x % D;
     float M = m_w[g];
 #pragma unroll
@@ -512,36 +572,66 @@ __global__ void __launch_bounds__(128) decode_tiles_kernel(const __grid_constant
         Ls += f * l_w[w * G + g];
       }
     }
-    if (ns == 1) {
-      out[x] = O / Ls;
-    } else {
-      p.part_o[((size_t)item * G + g) * D + c] = O;
-      if (c == 0) p.part_ml[(size_t)item * G + g] = make_float2(M, Ls);
+    const int owner = c / slice;
+    st_dsmem_f32(map_rank(aO + 4 * ((rank * G + g) * slice + c % slice), owner), O);
+    if (c % slice == 0) {
+      st_dsmem_f32(map_rank(aM + 4 * (rank * G + g), owner), M);
+      st_dsmem_f32(map_rank(aL + 4 * (rank * G + g), owner), Ls);
     }
   }
-  if (ns == 1) return;
 
-  // ---- last item of the unit merges the partials ----
-  __syncthreads();  // every partial write of this CTA precedes the release below
+  // ---- merge the cluster: this CTA combines channels [rank*slice, +slice) ----
+  cluster_sync();  // every push has landed; nothing remote is touched after this
+  const int unit = i * p.Hkv + h;
+  float *out = p.out + ((size_t)i * p.Hq + h * G) * D;
+  const size_t cpart = (size_t)unit_item0 + (size_t)ci * CS;  // global slot of this cluster
+  for (int x = tid; x < G * slice; x += kThreads) {
+    const int g = x / slice, cl = x % slice, c = rank * slice + cl;
+    float mr[16];
+    float M = -CUDART_INF_F;
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      mr[r] = r < CS ? in_M[r * G + g] : -CUDART_INF_F;
+      M = fmaxf(M, mr[r]);
+    }
+    float O = 0.f, Ls = 0.f;
+    if (M != -CUDART_INF_F) {
+#pragma unroll
+      for (int r = 0; r < 16; ++r) {
+        if (r < CS && mr[r] != -CUDART_INF_F) {
+          const float f = exp2f(mr[r] - M);
+          Ls = fmaf(f, in_L[r * G + g], Ls);
+          O = fmaf(f, in_O[(r * G + g) * slice + cl], O);
+        }
+      }
+    }
+    if (nc == 1) {
+      out[g * D + c] = O / Ls;
+    } else {
+      p.part_o[(cpart * G + g) * D + c] = O;
+      if (rank == 0 && cl == 0) p.part_ml[cpart * G + g] = make_float2(M, Ls);
+    }
+  }
+  if (nc == 1) return;
+  cluster_sync();  // every rank's slice is written before rank 0 releases it
+  if (rank != 0) return;
+
+  // ---- several clusters: the last one to finish merges their results ----
   if (tid == 0) {
     const int prev = atom_add_acq_rel_gpu(&p.tickets[unit], 1);
-    *s_flag = prev == ns - 1;
+    *s_flag = prev == nc - 1;
   }
   __syncthreads();  // ... and the acquire above precedes every read below
   if (!*s_flag) return;
-  // Merge in three steps, each a single round of independent L2 loads:
-  // (1) every (m, l) pair of the chunk into shared memory, (2) per-head max
-  // M and weights 2^(m_k - M) with the weighted row sum (shared memory
-  // only), (3) the weighted sum of the o partials, kU items per round.
-  constexpr int kChunk = 256;                       // items per pass
-  constexpr int OPT4 = (G * D / 4 + 127) / 128;     // float4 outputs per thread
-  constexpr int kU = 16;                            // o-partial items in flight
-  float *Mh = m_w;                                  // [G] (the warp buffers are free now)
+  // (1) every (m, l) pair into shared memory, (2) per-head max, weights and
+  // row sum, (3) the weighted sum of the o partials, kU at a time.
+  constexpr int kChunk = 256;                       // clusters per pass
+  constexpr int OPT4 = (G * D / 4 + kThreads - 1) / kThreads;
+  constexpr int kU = 8;
+  float *Mh = m_w;                                  // [G]
   float *Lh = l_w;                                  // [G]
-  float2 *mlk = reinterpret_cast<float2 *>(tiles);  // [kChunk][G] (m, l) of the chunk
-  float *wk = reinterpret_cast<float *>(mlk + kChunk * G);  // [kChunk][G] weights
-  const float2 *pml = p.part_ml + (size_t)unit_item0 * G;
-  const float *po = p.part_o + (size_t)unit_item0 * G * D;
+  float2 *mlk = reinterpret_cast<float2 *>(stages); // [kChunk][G]
+  float *wk = reinterpret_cast<float *>(mlk + kChunk * G);  // [kChunk][G] + [G]
   float4 acc_o[OPT4];
 #pragma unroll
   for (int j = 0; j < OPT4; ++j) acc_o[j] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -549,11 +639,13 @@ __global__ void __launch_bounds__(128) decode_tiles_kernel(const __grid_constant
     Mh[tid] = -CUDART_INF_F;
     Lh[tid] = 0.f;
   }
-  for (int base = 0; base < ns; base += kChunk) {
-    const int cnt = min(kChunk, ns - base);
-    for (int x = tid; x < cnt * G; x += blockDim.x) mlk[x] = __ldcg(&pml[(size_t)base * G + x]);
+  for (int base = 0; base < nc; base += kChunk) {
+    const int cnt = min(kChunk, nc - base);
+    for (int x = tid; x < cnt * G; x += kThreads) {
+      const int k = x / G, g = x % G;
+      mlk[x] = __ldcg(&p.part_ml[((size_t)unit_item0 + (size_t)(base + k) * CS) * G + g]);
+    }
     __syncthreads();
-    // one thread per head: running max over the chunk, rescale what came before
     if (tid < G) {
       const int g = tid;
       float M = Mh[g];
@@ -566,14 +658,14 @@ __global__ void __launch_bounds__(128) decode_tiles_kernel(const __grid_constant
         wk[k * G + g] = w;
         Ls = fmaf(w, ml.y, Ls);
       }
-      wk[kChunk * G + g] = resc;  // factor for the o accumulated so far
+      wk[kChunk * G + g] = resc;
       Mh[g] = M;
       Lh[g] = Ls;
     }
     __syncthreads();
 #pragma unroll
     for (int j = 0; j < OPT4; ++j) {
-      const int x4 = tid + 128 * j;
+      const int x4 = tid + kThreads * j;
       if (x4 < G * D / 4) {
         const float r = wk[kChunk * G + (4 * x4) / D];
         acc_o[j].x *= r;
@@ -582,23 +674,23 @@ __global__ void __launch_bounds__(128) decode_tiles_kernel(const __grid_constant
         acc_o[j].w *= r;
       }
     }
-    const float4 *pb = reinterpret_cast<const float4 *>(po + (size_t)base * G * D);
     for (int k = 0; k < cnt; k += kU) {
       float4 v[kU][OPT4];
 #pragma unroll
       for (int u = 0; u < kU; ++u)
 #pragma unroll
         for (int j = 0; j < OPT4; ++j) {
-          const int x4 = tid + 128 * j;
-          v[u][j] = (k + u < cnt && x4 < G * D / 4)
-                        ? __ldcg(pb + (size_t)(k + u) * (G * D / 4) + x4)
-                        : make_float4(0.f, 0.f, 0.f, 0.f);
+          const int x4 = tid + kThreads * j;
+          const float4 *src = reinterpret_cast<const float4 *>(
+              p.part_o + ((size_t)unit_item0 + (size_t)(base + k + u) * CS) * G * D);
+          v[u][j] = (k + u < cnt && x4 < G * D / 4) ? __ldcg(src + x4)
+                                                     : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
       for (int u = 0; u < kU; ++u)
 #pragma unroll
         for (int j = 0; j < OPT4; ++j) {
-          const int x4 = tid + 128 * j;
+          const int x4 = tid + kThreads * j;
           if (k + u < cnt && x4 < G * D / 4) {
             const float w = wk[(k + u) * G + (4 * x4) / D];
             acc_o[j].x = fmaf(w, v[u][j].x, acc_o[j].x);
@@ -612,7 +704,7 @@ __global__ void __launch_bounds__(128) decode_tiles_kernel(const __grid_constant
   }
 #pragma unroll
   for (int j = 0; j < OPT4; ++j) {
-    const int x4 = tid + 128 * j;
+    const int x4 = tid + kThreads * j;
     if (x4 < G * D / 4) {
       const float inv = 1.f / Lh[(4 * x4) / D];
       reinterpret_cast<float4 *>(out)[x4] =
@@ -622,29 +714,50 @@ __global__ void __launch_bounds__(128) decode_tiles_kernel(const __grid_constant
   if (tid == 0) p.tickets[unit] = 0;
 }
 
+int g_max_cluster[2][2][4];  // [dtype][d == 128][log2 G]: co-schedulable cluster size
+
 template <typename T, int D, int G>
-cudaError_t prep_one() {
-  return cudaFuncSetAttribute(decode_tiles_kernel<T, D, G>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<D, G>::kAlloc);
+cudaError_t prep_one(int *max_cluster) {
+  auto k = decode_tiles_kernel<T, D, G>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       Smem<D, G>::kAlloc);
+  if (e != cudaSuccess) return e;
+  int cs = 8;  // portable cluster size
+  if (cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+      cudaSuccess) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(16);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = Smem<D, G>::kAlloc;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 16;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int q = 0;
+    if (cudaOccupancyMaxPotentialClusterSize(&q, k, &cfg) == cudaSuccess && q >= 1) cs = q;
+  }
+  (void)cudaGetLastError();
+  *max_cluster = cs;
+  return cudaSuccess;
 }
 
 template <typename T, int D>
-cudaError_t prep_g() {
+cudaError_t prep_g(int dt) {
   cudaError_t e;
-  if ((e = prep_one<T, D, 1>()) != cudaSuccess) return e;
-  if ((e = prep_one<T, D, 2>()) != cudaSuccess) return e;
-  if ((e = prep_one<T, D, 4>()) != cudaSuccess) return e;
-  return prep_one<T, D, 8>();
+  const int di = D == 128;
+  if ((e = prep_one<T, D, 1>(&g_max_cluster[dt][di][0])) != cudaSuccess) return e;
+  if ((e = prep_one<T, D, 2>(&g_max_cluster[dt][di][1])) != cudaSuccess) return e;
+  if ((e = prep_one<T, D, 4>(&g_max_cluster[dt][di][2])) != cudaSuccess) return e;
+  return prep_one<T, D, 8>(&g_max_cluster[dt][di][3]);
 }
 
 template <typename T, int D, int G>
 cudaError_t launch_one(const TileDecodeParams &p, cudaStream_t st) {
-  int tiles = 1;
-  for (int i = 0; i < p.n_seqs; ++i)
-    tiles = max(tiles, max(p.seqs[i].ns_dyn ? p.seqs[i].tpi_dyn : 0,
-                           p.seqs[i].ns_str ? p.seqs[i].tpi_str : 0));
-  cudaError_t e = launch_pdl(decode_tiles_kernel<T, D, G>, p.total_items, 128,
-                             (size_t)Smem<D, G>::bytes(min(tiles, kMaxTiles)), st, p);
+  cudaError_t e = launch_pdl_cluster(decode_tiles_kernel<T, D, G>, p.total_items, kThreads,
+                                     (size_t)Smem<D, G>::kAlloc, p.cluster, st, p);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
@@ -663,11 +776,22 @@ cudaError_t launch_g(const TileDecodeParams &p, int G, cudaStream_t st) {
 
 cudaError_t prepare_decode_kernels() {
   cudaError_t e;
-  if ((e = prep_g<__half, 64>()) != cudaSuccess) return e;
-  if ((e = prep_g<__half, 128>()) != cudaSuccess) return e;
-  if ((e = prep_g<__nv_bfloat16, 64>()) != cudaSuccess) return e;
-  return prep_g<__nv_bfloat16, 128>();
+  if ((e = prep_g<__half, 64>(0)) != cudaSuccess) return e;
+  if ((e = prep_g<__half, 128>(0)) != cudaSuccess) return e;
+  if ((e = prep_g<__nv_bfloat16, 64>(1)) != cudaSuccess) return e;
+  return prep_g<__nv_bfloat16, 128>(1);
 }
+
+// Largest power-of-two cluster (<= 16) the decode kernel can be launched with.
+int decode_max_cluster(int dtype, int d, int G) {
+  const int gi = G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : 3;
+  const int cs = g_max_cluster[dtype ? 1 : 0][d == 128][gi];
+  int p2 = 1;
+  while (p2 * 2 <= cs && p2 < 16) p2 *= 2;
+  return p2;
+}
+
+int decode_max_tiles_per_cta() { return kMaxDesc; }
 
 cudaError_t launch_decode_tiles(const TileDecodeParams &p, int dtype, int d, int G,
                                 cudaStream_t s, long long *n) {

@@ -94,6 +94,10 @@ __device__ __forceinline__ int cta_excl_scan(int v, int *sh, int *total) {
 
 constexpr int kMaxKeys = 8192;  // candidate pages handled in shared memory
 
+// Keys sit at j + j/16 in shared memory: a thread's contiguous run of 16 and
+// a warp's strided sweep both hit distinct banks.
+__device__ __forceinline__ int kpos(int j) { return j + (j >> 4); }
+
 // Exact selection of the k highest of n scores (1 <= k < n <= kMaxKeys);
 // writes the chosen indices ascending to out[0..k).  The k-th largest key T
 // is found 4 bits at a time, from the top: at each step every thread counts
@@ -102,13 +106,13 @@ constexpr int kMaxKeys = 8192;  // candidate pages handled in shared memory
 // thread picks the digit.  Keys equal to T are taken lowest index first.
 // Returns the count written.
 __device__ int cta_topk(const float *sc, int n, int k, int *out) {
-  __shared__ uint32_t keys[kMaxKeys];
+  __shared__ uint32_t keys[kMaxKeys + kMaxKeys / 16];
   __shared__ uint32_t wcnt[kSelWarps][16];
   __shared__ int sh[33];
   __shared__ uint32_t s_prefix;
   __shared__ int s_remaining;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  for (int j = tid; j < n; j += kSelThreads) keys[j] = score_key(__ldcg(sc + j));
+  for (int j = tid; j < n; j += kSelThreads) keys[kpos(j)] = score_key(__ldcg(sc + j));
   if (tid == 0) {
     s_prefix = 0;
     s_remaining = k;
@@ -119,33 +123,57 @@ __device__ int cta_topk(const float *sc, int n, int k, int *out) {
   for (int shift = 28; shift >= 0; shift -= 4) {
     const uint32_t prefix = s_prefix;
     const uint32_t hi_mask = shift == 28 ? 0u : ~((1u << (shift + 4)) - 1u);
-    uint32_t cnt[16];
+    // per-thread counts of the 16 digit values, 8-bit fields packed in two
+    // 64-bit words (a thread holds at most kMaxKeys / 256 = 32 keys)
+    unsigned long long c_lo = 0, c_hi = 0;
+#pragma unroll 4
+    for (int j = tid; j < n; j += kSelThreads) {  // strided sweep
+      const uint32_t u = keys[kpos(j)];
+      const uint32_t d = (u >> shift) & 15u;
+      // branch-free: a key outside the prefix adds 0
+      const unsigned long long inc =
+          ((u & hi_mask) == prefix ? 1ull : 0ull) << (8 * (d & 7u));
+      c_lo += d < 8 ? inc : 0ull;
+      c_hi += d < 8 ? 0ull : inc;
+    }
+    // widen to 16-bit fields (a warp holds at most 1024 keys) and sum the warp
+    uint32_t w16[8];
 #pragma unroll
-    for (int b = 0; b < 16; ++b) cnt[b] = 0;
-    for (int j = tid; j < n; j += kSelThreads) {  // strided: no bank conflicts
-      const uint32_t u = keys[j];
-      if ((u & hi_mask) == prefix) {
-        const uint32_t d = (u >> shift) & 15u;
+    for (int r = 0; r < 8; ++r) {
+      const unsigned long long src = r < 4 ? c_lo : c_hi;
+      const int f = (r & 3) * 2;  // two 8-bit fields per 32-bit word
+      const uint32_t lo = (uint32_t)(src >> (8 * f)) & 0xffu;
+      const uint32_t hi = (uint32_t)(src >> (8 * (f + 1))) & 0xffu;
+      w16[r] = __reduce_add_sync(0xffffffffu, lo | (hi << 16));
+    }
+    if (lane == 0)
 #pragma unroll
-        for (int b = 0; b < 16; ++b) cnt[b] += d == (uint32_t)b;
+      for (int r = 0; r < 8; ++r) {
+        wcnt[warp][2 * r] = w16[r] & 0xffffu;
+        wcnt[warp][2 * r + 1] = w16[r] >> 16;
       }
-    }
-#pragma unroll
-    for (int b = 0; b < 16; ++b) {
-      const uint32_t w = __reduce_add_sync(0xffffffffu, cnt[b]);
-      if (lane == 0) wcnt[warp][b] = w;
-    }
     __syncthreads();
-    if (tid == 0) {
-      int rem = s_remaining, above = 0, b = 15;
-      for (; b > 0; --b) {
-        int c = 0;
-        for (int w = 0; w < kSelWarps; ++w) c += (int)wcnt[w][b];
-        if (above + c >= rem) break;
-        above += c;
+    if (warp == 0) {
+      // lane l holds the total of digit 15 - l; an inclusive scan over the
+      // lanes is then the count of keys with a digit >= 15 - l
+      int v = 0;
+      if (lane < 16)
+#pragma unroll
+        for (int w = 0; w < kSelWarps; ++w) v += (int)wcnt[w][15 - lane];
+      int incl = v;
+#pragma unroll
+      for (int o = 1; o < 16; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
       }
-      s_remaining = rem - above;
-      s_prefix = prefix | ((uint32_t)b << shift);
+      const int rem = s_remaining;
+      const int excl = incl - v;
+      const bool hit = lane < 16 && excl < rem && rem <= incl;
+      const unsigned who = __ballot_sync(0xffffffffu, hit);
+      if (hit && (unsigned)lane == (unsigned)(__ffs(who) - 1)) {
+        s_remaining = rem - excl;
+        s_prefix = prefix | ((uint32_t)(15 - lane) << shift);
+      }
     }
     __syncthreads();
   }
@@ -153,8 +181,9 @@ __device__ int cta_topk(const float *sc, int n, int k, int *out) {
   const int take_eq = s_remaining;
   int n_gt = 0, n_eq = 0;
   for (int j = j0; j < j1; ++j) {
-    n_gt += keys[j] > T;
-    n_eq += keys[j] == T;
+    const uint32_t u = keys[kpos(j)];
+    n_gt += u > T;
+    n_eq += u == T;
   }
   int tot_eq;
   int eq_before = cta_excl_scan(n_eq, sh, &tot_eq);
@@ -162,7 +191,7 @@ __device__ int cta_topk(const float *sc, int n, int k, int *out) {
   int total;
   int pos = cta_excl_scan(mine, sh, &total);
   for (int j = j0; j < j1 && mine > 0; ++j) {
-    const uint32_t u = keys[j];
+    const uint32_t u = keys[kpos(j)];
     bool take = u > T;
     if (u == T) {
       take = eq_before < take_eq;
@@ -234,8 +263,7 @@ __device__ int cta_topk_global(const float *sc, int n, int k, int *out) {
 template <typename T, int D, int G>
 __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_constant__ SelectParams p) {
   __shared__ int s_last;
-  pdl_wait();  // q, metadata and the page table come from earlier kernels
-  pdl_launch_dependents();
+  __shared__ __align__(16) uint16_t q_s[G * D];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   int i = 0;
   while (i + 1 < p.n_seqs && p.seqs[i + 1].chunk_off <= (int)blockIdx.x) ++i;
@@ -246,6 +274,14 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_consta
   const int chunk = local % per_head;
   const int h = p.dyn_kv[hd];
   int *out = p.selection + ((size_t)s.slot * p.Hd + hd) * p.ksel_max;
+  // Metadata and the page table are read before the wait for the previous
+  // kernel on the stream only when the host knows that kernel cannot have
+  // written this context's cache (p.early); q and every write come after it.
+  const bool early = p.early && s.n_chunks != 0;
+  if (!early) {
+    pdl_wait();
+    pdl_launch_dependents();
+  }
   if (s.n_chunks == 0) {
     // every page is kept (nL <= K_sel), or only the newest one (K_sel = 1)
     if (s.nL <= s.K_sel) {
@@ -257,16 +293,49 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_consta
   }
   const int n = s.nL - 1;  // candidate pages
   float *scores = p.scores + ((size_t)i * p.Hd + hd) * p.max_nL;
+  constexpr int KSTEPS = 2 * D / 16;
+  constexpr int PAIRS = KSTEPS / 2;
+  const int g8 = lane >> 2, t4 = lane & 3;
 
-  // ---- B operand: [q- ; q+] over 2D rows of k, heads as the 8 columns ----
+  // ---- this warp's 16 pages: metadata rows straight into A fragments ----
   // k-step pair s2 covers metadata elements [32*s2, 32*s2 + 32); thread t4
   // of a k-step pair owns elements 32*s2 + 8*t4 + [0, 8): the first four are
   // its k indices {2t4, 2t4+1, 2t4+8, 2t4+9} of step 2*s2, the last four the
   // same k indices of step 2*s2+1.
-  constexpr int KSTEPS = 2 * D / 16;
-  const int g8 = lane >> 2, t4 = lane & 3;
+  const int j0 = chunk * kPagesPerCta + warp * kPagesPerWarp;
+  bool ok[2] = {false, false};
+  uint4 ra[PAIRS], rb[PAIRS];
+  if (j0 < n) {
+    const uint16_t *meta = static_cast<const uint16_t *>(p.meta);
+    const uint4 *rowp[2] = {nullptr, nullptr};
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const int j = j0 + g8 + 8 * hh;
+      if (j < n) {
+        const int blk = j / p.R;
+        const int phys = p.page_table[(size_t)s.slot * p.max_pp + blk];
+        if (phys < 0 || phys >= p.num_phys) {
+          set_err(p.err, kDevBadPhys, s.slot, blk, phys);
+        } else {
+          ok[hh] = true;
+          rowp[hh] = reinterpret_cast<const uint4 *>(
+              meta + (((size_t)phys * p.Hd + hd) * p.R + (j % p.R)) * 2 * D);
+        }
+      }
+    }
+#pragma unroll
+    for (int s2 = 0; s2 < PAIRS; ++s2) {
+      ra[s2] = ok[0] ? __ldg(rowp[0] + 4 * s2 + t4) : make_uint4(0, 0, 0, 0);
+      rb[s2] = ok[1] ? __ldg(rowp[1] + 4 * s2 + t4) : make_uint4(0, 0, 0, 0);
+    }
+  }
+  if (early) {
+    pdl_wait();
+    pdl_launch_dependents();
+  }
+
+  // ---- B operand: [q- ; q+] over the 2D metadata elements, heads as columns ----
   uint32_t qb[KSTEPS][2];
-  __shared__ __align__(16) uint16_t q_s[G * D];
   {
     // the group's G query rows: one coalesced 16-byte load per thread
     const uint4 *qg = reinterpret_cast<const uint4 *>(
@@ -292,36 +361,8 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_consta
   }
 
   // ---- score 16 pages per warp ----
-  const int j0 = chunk * kPagesPerCta + warp * kPagesPerWarp;
   if (j0 < n) {
-    const uint16_t *meta = static_cast<const uint16_t *>(p.meta);
-    const uint4 *rowp[2];
-    bool ok[2];
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      const int j = j0 + g8 + 8 * hh;
-      ok[hh] = j < n;
-      rowp[hh] = nullptr;
-      if (ok[hh]) {
-        const int blk = j / p.R;
-        const int phys = p.page_table[(size_t)s.slot * p.max_pp + blk];
-        if (phys < 0 || phys >= p.num_phys) {
-          set_err(p.err, kDevBadPhys, s.slot, blk, phys);
-          ok[hh] = false;
-        } else {
-          rowp[hh] = reinterpret_cast<const uint4 *>(
-              meta + (((size_t)phys * p.Hd + hd) * p.R + (j % p.R)) * 2 * D);
-        }
-      }
-    }
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    constexpr int PAIRS = KSTEPS / 2;
-    uint4 ra[PAIRS], rb[PAIRS];
-#pragma unroll
-    for (int s2 = 0; s2 < PAIRS; ++s2) {
-      ra[s2] = ok[0] ? __ldg(rowp[0] + 4 * s2 + t4) : make_uint4(0, 0, 0, 0);
-      rb[s2] = ok[1] ? __ldg(rowp[1] + 4 * s2 + t4) : make_uint4(0, 0, 0, 0);
-    }
 #pragma unroll
     for (int s2 = 0; s2 < PAIRS; ++s2) {
       const uint32_t a0[4] = {ra[s2].x, rb[s2].x, ra[s2].y, rb[s2].y};
@@ -350,15 +391,13 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_consta
   }
 
   // ---- the last scoring CTA of this (sequence, head) selects ----
-  __threadfence();
-  __syncthreads();
+  __syncthreads();  // every score of this CTA precedes the release below
   if (tid == 0) {
-    const int prev = atomicAdd(&p.tickets[i * p.Hd + hd], 1);
+    const int prev = atom_add_acq_rel_gpu(&p.tickets[i * p.Hd + hd], 1);
     s_last = prev == s.n_chunks - 1;
   }
-  __syncthreads();
+  __syncthreads();  // ... and the acquire above precedes every read below
   if (!s_last) return;
-  __threadfence();
   const int k = s.K_sel - 1;
   const int got = n <= kMaxKeys ? cta_topk(scores, n, k, out) : cta_topk_global(scores, n, k, out);
   if (tid == 0) {

@@ -87,6 +87,7 @@ struct SelectParams {
   int n_seqs, Hq, Hd, ell, R, max_pp, ksel_max, max_nL, pages_per_chunk,
       num_phys;
   int score_ctas;       // total scoring CTAs
+  int early;            // 1: read metadata before waiting for the previous kernel
   unsigned char dyn_kv[kMaxKvHeads];
   SelectSeq seqs[kSeqsPerLaunch];
 };
@@ -97,8 +98,8 @@ struct TileSeq {
   int nL0;        // logical pages when the selection was taken
   int sel_count;  // pages in the stored selection
   int item_off;   // first work item of this sequence
-  int ns_dyn;     // items per dynamic head
-  int ns_str;     // items per streaming head
+  int ns_dyn;     // items (CTAs) per dynamic head: clusters x cluster size
+  int ns_str;     // items (CTAs) per streaming head
   int tpi_dyn;    // tiles per dynamic item
   int tpi_str;    // tiles per streaming item
 };
@@ -117,6 +118,7 @@ struct TileDecodeParams {
   int *err;
   int n_seqs, Hq, Hkv, Hd, Hs, ell, P, R, max_pp, ksel_max, S, W, num_phys;
   int total_items;
+  int cluster;        // CTAs per thread-block cluster; every unit's item count is a multiple
   int early;          // 1: stage K/V tiles before waiting for the previous kernel
   float scale_log2;
   unsigned char dyn_kv[kMaxKvHeads];
@@ -128,6 +130,8 @@ constexpr int kTileRows = 16;
 constexpr int kMaxTilesPerItem = 8;
 
 cudaError_t prepare_decode_kernels();
+int decode_max_cluster(int dtype, int d, int G);  // after prepare_decode_kernels()
+int decode_max_tiles_per_cta();
 cudaError_t launch_decode_tiles(const TileDecodeParams &p, int dtype, int d, int G,
                                 cudaStream_t s, long long *launches);
 

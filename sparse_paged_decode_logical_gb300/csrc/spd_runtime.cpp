@@ -421,6 +421,7 @@ spd_status select_impl(spd_ctx *c, const void *q, const int *ids, int n, bool fo
         off += std::max(1, d.n_chunks) * dv.Hd;
       }
       p.score_ctas = off;
+      p.early = c->early_staging && !previous_launcher_is(c, st) ? 1 : 0;
       cudaError_t e = launch_select_fused(p, c->cfg.dtype, c->cfg.head_dim, dv.G, st, &c->launches);
       if (e != cudaSuccess) return cuda_fail(c, e, "select launch");
       note_launcher(c, st);
@@ -456,9 +457,12 @@ int unit_tiles_str(const spd_ctx *c, const Seq &s) {
   return t(n0) + t(n1) + t(n2);
 }
 
-// Split policy: tiles per item chosen so the launch has about two items per
-// SM (at most 8 tiles = 128 rows per item, the shared-memory stage).  Items
-// of a unit are consecutive; none is empty.
+// Split policy.  Every unit (sequence, kv head) gets nc clusters of CS CTAs;
+// CS, the same for the whole launch, is the largest power of two (up to the
+// size the kernel can be co-scheduled with) that keeps units x CS within one
+// CTA per SM; nc is 1 unless a unit holds much more than its share of the
+// launch's tiles (uneven batches), in which case its clusters are merged in
+// global memory.  Tiles are then spread evenly over the unit's CTAs.
 int plan_tiles(const spd_ctx *c, TileDecodeParams &p, const int *ids, int n) {
   const Derived &dv = c->dv;
   long long total = 0;
@@ -467,9 +471,18 @@ int plan_tiles(const spd_ctx *c, TileDecodeParams &p, const int *ids, int n) {
     if (dv.Hd) total += (long long)dv.Hd * unit_tiles_dyn(c, s);
     if (dv.Hs) total += (long long)dv.Hs * unit_tiles_str(c, s);
   }
-  int tpi = (int)std::min<long long>(kMaxTilesPerItem,
-                                     std::max<long long>(1, (total + 2LL * c->num_sms - 1) /
-                                                                (2LL * c->num_sms)));
+  const long long units = (long long)n * (dv.Hd + dv.Hs);
+  int cs = 1;
+  const int cs_max = decode_max_cluster(c->cfg.dtype, c->cfg.head_dim, dv.G);
+  while (cs * 2 <= cs_max && units * cs * 2 <= c->num_sms) cs *= 2;
+  const long long tpc = std::max<long long>(1, (total + c->num_sms - 1) / c->num_sms);
+  const int max_tiles = decode_max_tiles_per_cta();
+  auto split = [&](int nt, int *ns, int *tpi) {
+    long long nc = std::max<long long>(1, (nt + cs * tpc / 2) / (cs * tpc));  // rounded
+    nc = std::max<long long>(nc, (nt + (long long)cs * max_tiles - 1) / ((long long)cs * max_tiles));
+    *ns = (int)(nc * cs);
+    *tpi = std::max(1, (nt + *ns - 1) / *ns);
+  };
   int items = 0;
   for (int i = 0; i < n; ++i) {
     const Seq &s = c->seqs[ids[i]];
@@ -480,27 +493,16 @@ int plan_tiles(const spd_ctx *c, TileDecodeParams &p, const int *ids, int n) {
     d.sel_count = s.sel_count;
     d.item_off = items;
     d.ns_dyn = d.ns_str = 0;
-    d.tpi_dyn = d.tpi_str = tpi;
-    if (dv.Hd) {
-      const int nt = unit_tiles_dyn(c, s);
-      d.ns_dyn = (nt + tpi - 1) / tpi;
-      d.tpi_dyn = (nt + d.ns_dyn - 1) / d.ns_dyn;
-      d.ns_dyn = (nt + d.tpi_dyn - 1) / d.tpi_dyn;
-    }
-    if (dv.Hs) {
-      const int nt = unit_tiles_str(c, s);
-      d.ns_str = (nt + tpi - 1) / tpi;
-      d.tpi_str = (nt + d.ns_str - 1) / d.ns_str;
-      d.ns_str = (nt + d.tpi_str - 1) / d.tpi_str;
-    }
+    d.tpi_dyn = d.tpi_str = 1;
+    if (dv.Hd) split(unit_tiles_dyn(c, s), &d.ns_dyn, &d.tpi_dyn);
+    if (dv.Hs) split(unit_tiles_str(c, s), &d.ns_str, &d.tpi_str);
     items += dv.Hd * d.ns_dyn + dv.Hs * d.ns_str;
   }
+  p.cluster = cs;
   p.total_items = items;
   return items;
 }
 
-// Enqueue split-K decode attention for seqs `ids` (lengths already final).
-// With k_new/v_new the kernel also appends each sequence's newest token.
 // `scr` (optional) replaces the context's scratch for the split partials and
 // tickets; a launch then holds at most scr->max_items items.
 spd_status attention_impl(spd_ctx *c, const void *q, const int *ids, int n, float *out,

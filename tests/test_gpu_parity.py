@@ -200,3 +200,20 @@ def test_early_kv_staging_interleaved_contexts_bit_identical():
             pr.cache.check_status()
         res.append(torch.stack([o.cpu() for o in outs]))
     assert torch.equal(res[0], res[1])
+
+
+@needs_gpu
+def test_llama2_mha_full_256k():
+    # Llama-2-7B attention (MHA 32/32, d 128, fp16) at 262144 tokens, logical
+    # page 64: the full-size workload, two selections (steps 0 and 4)
+    run(W.workload("llama2_7b_mha_256k"), steps=5, layout_every=5)
+
+
+@needs_gpu
+def test_continuous_batch_full_lengths():
+    # 16 sequences at their seeded log-uniform lengths in [8K, 128K], shared
+    # permuted pool, budget min(4096, L/32): full-size, first selection plus
+    # one reuse step
+    wl = W.workload("cont_batch_16")
+    pr = run(wl, steps=2, layout_every=2)
+    assert max(pr.lens) > 65536 and min(pr.lens) < 16384

@@ -67,19 +67,31 @@ def test_static_scratch_matches_default_entry_point_on_two_calls():
 
 @needs_gpu
 def test_static_scratch_rejects_work_beyond_its_capacity():
-    # four streaming heads with a 40000-token window need more split items
-    # than the 1024 the array holds; the call is refused before any launch
-    # and the sequence's step counter does not move
-    c, ids, g = _cache([True] * 4, sink=0, window=40000, context=45000)
-    q = _step(c, ids, g)
-    before = c.seq_info(ids[0])["step_counter"]
-    out = torch.empty((1, 8, 128), dtype=torch.float32, device="cuda")
+    # 33 streaming kv heads with a 131072-token window: one sequence needs
+    # more split items than the 1024 the array holds (each CTA takes at most
+    # 256 tiles of 16 rows), so the call is refused before any launch and the
+    # sequence's step counter does not move; the default entry point runs it
+    W_ = 131072
+    cfg = dict(num_q_heads=33, num_kv_heads=33, head_dim=64, dtype="bf16", logical_page=32,
+               physical_page=128, num_physical_pages=1, max_seqs=1, max_context=W_ + 64,
+               streaming=[True] * 33, sink=0, window=W_, token_budget=0, reuse_interval=4)
+    c = spd.SparsePagedKVCache(device="cuda", **cfg)
+    sid = c.seq_create()
+    g = torch.Generator(device="cuda").manual_seed(11)
+    k = torch.randn((1, W_ + 16, 33, 64), generator=g, device="cuda").to(torch.bfloat16)
+    v = torch.randn((1, W_ + 16, 33, 64), generator=g, device="cuda").to(torch.bfloat16)
+    c.kv_append([sid], k, v)
+    del k, v
+    q = torch.randn((1, 33, 64), generator=g, device="cuda").to(torch.bfloat16)
+    before = c.seq_info(sid)["step_counter"]
+    out = torch.empty((1, 33, 64), dtype=torch.float32, device="cuda")
     stream = torch.cuda.current_stream().cuda_stream
     with pytest.raises(spd.SpdError) as e:
-        spd.spd_sparse_decode_attention_static(c.ctx, q[:1].data_ptr(), ids[:1], out.data_ptr(),
+        spd.spd_sparse_decode_attention_static(c.ctx, q.data_ptr(), [sid], out.data_ptr(),
                                                stream)
     assert e.value.name == "SPD_ERR_CAPACITY"
-    assert c.seq_info(ids[0])["step_counter"] == before
-    spd.spd_sparse_decode_attention(c.ctx, q[:1].data_ptr(), ids[:1], out.data_ptr(), stream)
+    assert c.seq_info(sid)["step_counter"] == before
+    spd.spd_sparse_decode_attention(c.ctx, q.data_ptr(), [sid], out.data_ptr(), stream)
     torch.cuda.synchronize()
+    c.check_status()
     assert torch.isfinite(out).all()
