@@ -264,7 +264,11 @@ const char *spd_status_string(spd_status s);
  * this context starts loading KV-cache data (page table, selection, K/V
  * tiles, page metadata) before that kernel has finished; q, the new token and
  * all writes still wait for it.  This overlaps the HBM reads with the tail of
- * the kernel before it -- in a model, the projection that produces q.
+ * the kernel before it -- in a model, the projection that produces q.  The
+ * streaming heads of a decode kernel also start early when the kernel before
+ * it is this context's own selection or page-table flush: neither writes the
+ * streaming buffers, and q and the new token are final by then (that kernel
+ * waited for its own predecessor), so they run without waiting at all.
  * Turn it on only if (a) nothing but this library's calls on this context
  * writes its KV-cache buffers, and (b) other code's kernels on the stream do
  * not release their dependents (programmatic dependent launch) before they

@@ -15,12 +15,15 @@
 // the CTAs' tile ranges are chosen by the host so the launch fills the GPU);
 // a CTA ("item") takes a contiguous range of the unit's tiles.
 //
-// Data movement.  Each of the 8 warps owns one shared-memory stage; the CTA's
-// tiles go round-robin to the warps, every stage is filled by a TMA tensor
-// load (64 channels x 16 rows boxes, 128-byte swizzle, one mbarrier per
-// stage) and refilled as soon as its warp has consumed it; the later tiles
-// are prefetched into L2 at kernel start, so refills read L2.  K/V bytes are
-// read from HBM once.
+// Data movement.  The CTA's tiles stream through a ring of kStages shared-
+// memory stages: tile t lives in stage t mod kStages, filled by TMA tensor
+// loads (64 channels x 16 rows boxes, 128-byte swizzle, one mbarrier per
+// stage, its phase counting the stage's uses).  The first kStages tiles are
+// requested at kernel start, the later ones are prefetched into L2 then, and
+// the warp that finishes tile t refills its stage with tile t + kStages.
+// Warps take tiles from a shared counter, so a CTA with more tiles than warps
+// spreads the extra ones over whichever warps are free.  K/V bytes are read
+// from HBM once.
 //
 // Math (per warp and tile, all G query heads of the kv head at once):
 //   q.K^T   mma.sync m16n8k16, A = K tile rows (ldmatrix from the swizzled
@@ -58,7 +61,7 @@ namespace {
 constexpr int kRows = 16;                  // rows per tile (one mma M tile)
 constexpr int kWarps = 8;                  // 256 threads
 constexpr int kThreads = kWarps * 32;
-constexpr int kStages = kWarps;            // one shared-memory stage per warp
+constexpr int kStages = 12;                // shared-memory stage ring
 constexpr int kMaxDesc = 256;              // tiles one CTA may take
 constexpr uint32_t kWaitLimit = 1u << 24;  // bounded mbarrier polls
 
@@ -95,8 +98,8 @@ struct Smem {
   // inbox: what the cluster's CTAs send this CTA: M[16][G], L[16][G] and
   // O[16 ranks][G][D / CS] (= G * D floats for any CS)
   static constexpr int kInbox = (kML + 2 * kWarps * G * 4 + 15) / 16 * 16;
-  static constexpr int kFlag = kInbox + (32 * G + G * D) * 4;          // int [4]
-  static constexpr int kTiles = (kFlag + 16 + 1023) / 1024 * 1024;
+  static constexpr int kFlag = kInbox + (32 * G + G * D) * 4;          // int [4 + kStages]
+  static constexpr int kTiles = (kFlag + (4 + kStages) * 4 + 1023) / 1024 * 1024;
   static constexpr int kStageRegion = kStages * Geo<D>::kTileBytes;
   static constexpr int kMergeRegion = kWarps * G * D * 4;              // o of every warp
   static constexpr int kCombineRegion = 256 * G * 12 + 64;             // (m, l), weights
@@ -131,6 +134,14 @@ __device__ __forceinline__ void set_err(int *err, int code, int a, int b, int c)
   }
 }
 
+// Bounded wait until another warp of the CTA has counted more than `u` uses
+// of a stage (its load for use u is issued).
+__device__ __forceinline__ bool wait_issued(const int *count, int u, uint32_t limit) {
+  for (uint32_t i = 0; i < limit; ++i)
+    if (*reinterpret_cast<const volatile int *>(count) > u) return true;
+  return false;
+}
+
 // Byte offset, inside a tile half (K or V), of channel `ch` of row `r`.
 template <int D>
 __device__ __forceinline__ uint32_t chan_off(int r, int ch) {
@@ -156,7 +167,8 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
   float *in_M = reinterpret_cast<float *>(smem + Sm::kInbox);  // [rank][G]
   float *in_L = in_M + 16 * G;                                   // [rank][G]
   float *in_O = in_L + 16 * G;                                   // [rank][G][slice]
-  int *s_flag = reinterpret_cast<int *>(smem + Sm::kFlag);
+  int *s_flag = reinterpret_cast<int *>(smem + Sm::kFlag);  // [1] a wait gave up, [2] next tile
+  int *s_iss = s_flag + 4;                                   // loads issued per stage
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   cluster_arrive_relaxed();  // paired with the wait before the first remote store
@@ -166,6 +178,7 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
     prefetch_tmap(&p.tm_sk);
     prefetch_tmap(&p.tm_sv);
     s_flag[1] = 0;  // set if a bounded wait gives up
+    s_flag[2] = kWarps;  // tiles 0..kWarps-1 go to warps 0..kWarps-1
   }
   const int item = blockIdx.x;
   int i = 0;
@@ -222,16 +235,22 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
   const int nt = min(kMaxDesc, max(0, min(n_tiles, tile0 + tpi) - tile0));
   const bool owns_newest = nt > 0 && tile0 + nt == n_tiles;
   const bool do_append = p.k_new != nullptr && owns_newest;
+  const bool early = (p.early >> (dyn ? 0 : 1)) & 1;
+  // bit 2: the previous kernel is this context's own selection or page-table
+  // kernel, which writes nothing a streaming unit reads; q is final once that
+  // kernel runs (it waited for its own predecessor before releasing this one)
+  const bool skip_wait = !dyn && ((p.early >> 2) & 1);
 
   // Everything above used only the parameter block.  The KV cache (page
   // table, selection, pools) is read next: before the wait for the previous
   // kernel on the stream when the host knows that kernel cannot have written
-  // this context's cache (p.early), after it otherwise.  q, the new token and
-  // every write come after the wait.  Dependents are released only after the
-  // wait, so when this kernel runs, every kernel before its immediate
-  // predecessor has finished.
-  if (!p.early) {
-    pdl_wait();
+  // the KV this unit reads (bit 0 of p.early for dynamic units, bit 1 for
+  // streaming ones), after it otherwise.  q, the new token and every write
+  // come after the wait.  Dependents are released only after the wait, so when
+  // this kernel runs, every kernel before its immediate predecessor has
+  // finished.
+  if (!early) {
+    if (!skip_wait) pdl_wait();
     pdl_launch_dependents();
   }
 
@@ -268,28 +287,35 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
   if (tid < kStages) {
     mbar_init(&bars[tid], 1);
     fence_mbar_init();
+    s_iss[tid] = 0;
   }
   __syncthreads();
 
   const CUtensorMap *mk = dyn ? &p.tm_k : &p.tm_sk;
   const CUtensorMap *mv = dyn ? &p.tm_v : &p.tm_sv;
-  uint8_t *kt = stages + warp * Gm::kTileBytes;  // the warp's stage: K boxes, then V boxes
-  uint8_t *vt = kt + Gm::kBoxes * Gm::kBoxBytes;
-  // the warp's stage holds its tiles warp, warp + kWarps, ... in turn
+  // stage s: K boxes, then V boxes; tile t uses stage t % kStages, and its
+  // use number t / kStages is the phase its waiter checks
   auto issue = [&](int t) {
+    const int st = t % kStages;
     const TileDesc td = tdesc[t];
-    if (td.n_valid <= 0) return;
-    mbar_arrive_expect_tx(&bars[warp], Gm::kTileBytes);
+    atomicAdd(&s_iss[st], 1);
+    if (td.n_valid <= 0) {  // nothing to load: complete the phase anyway
+      mbar_arrive_expect_tx(&bars[st], 0);
+      return;
+    }
+    uint8_t *kd = stages + st * Gm::kTileBytes;
+    uint8_t *vd = kd + Gm::kBoxes * Gm::kBoxBytes;
+    mbar_arrive_expect_tx(&bars[st], Gm::kTileBytes);
     for (int b = 0; b < Gm::kBoxes; ++b) {
-      tma_load_3d(kt + b * Gm::kBoxBytes, mk, b * 64, td.y, td.z, &bars[warp]);
-      tma_load_3d(vt + b * Gm::kBoxBytes, mv, b * 64, td.y, td.z, &bars[warp]);
+      tma_load_3d(kd + b * Gm::kBoxBytes, mk, b * 64, td.y, td.z, &bars[st]);
+      tma_load_3d(vd + b * Gm::kBoxBytes, mv, b * 64, td.y, td.z, &bars[st]);
     }
   };
-  if (lane == 0 && warp < nt) {
-    issue(warp);
-    // the warp's later tiles start their way from HBM into L2 now; their
-    // stage refills then read L2
-    for (int t = warp + kWarps; t < nt; t += kWarps) {
+  if (lane == 0) {
+    for (int t = warp; t < min(nt, kStages); t += kWarps) issue(t);
+    // the later tiles start their way from HBM into L2 now; their stage
+    // refills then read L2
+    for (int t = kStages + warp; t < nt; t += kWarps) {
       const TileDesc td = tdesc[t];
       if (td.n_valid <= 0) continue;
       for (int b = 0; b < Gm::kBoxes; ++b) {
@@ -299,8 +325,8 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
     }
   }
 
-  if (p.early) {
-    pdl_wait();
+  if (early) {
+    if (!skip_wait) pdl_wait();
     pdl_launch_dependents();
   }
 
@@ -334,18 +360,23 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
   float *Pw = P_all + warp * kRows * GPAD;
   const float sc = p.scale_log2;
 
-  int use = 0;  // loads this warp's stage has completed (mbarrier phase)
-  for (int t = warp; t < nt; t += kWarps) {
+  for (int t = warp; t < nt;) {
     const TileDesc td = tdesc[t];
-    if (td.n_valid > 0) {
-      if (!mbar_wait(&bars[warp], use & 1, kWaitLimit)) {
-        if (lane == 0) {
-          set_err(p.err, kDevTimeout, s.slot, h, t);
-          s_flag[1] = 1;
-        }
-        break;
+    const int st = t % kStages, u = t / kStages;  // stage and its use number
+    uint8_t *kt = stages + st * Gm::kTileBytes;
+    uint8_t *vt = kt + Gm::kBoxes * Gm::kBoxBytes;
+    // Use u of the stage is loaded only after use u-1 was consumed, so the
+    // barrier's parity identifies it once the load is known to be issued
+    // (a wait on the parity alone could match use u-2).  Every tile is waited
+    // for, empty ones too, so no copy is in flight when the loop ends.
+    if (!wait_issued(&s_iss[st], u, kWaitLimit) || !mbar_wait(&bars[st], u & 1, kWaitLimit)) {
+      if (lane == 0) {
+        set_err(p.err, kDevTimeout, s.slot, h, t);
+        s_flag[1] = 1;
       }
-      ++use;
+      break;
+    }
+    if (td.n_valid > 0) {
       const int nv = td.n_valid;
 
       if (do_append && t == nt - 1) {
@@ -509,11 +540,14 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
       }
       __syncwarp();
     }
-    // refill this warp's stage with its next tile
-    if (t + kWarps < nt) {
+    // refill the stage with the tile kStages further on, then take the next tile
+    if (t + kStages < nt) {
       fence_proxy_async_smem();  // the warp's reads of the stage precede the TMA write
-      if (lane == 0) issue(t + kWarps);
+      if (lane == 0) issue(t + kStages);
     }
+    int nx = 0;
+    if (lane == 0) nx = atomicAdd(&s_flag[2], 1);
+    t = __shfl_sync(0xffffffffu, nx, 0);
   }
 
   // ---- merge the warps into this CTA's (M, L, O) ----
@@ -524,9 +558,11 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
   }
   __syncthreads();  // every warp is done with its stage: reuse the region for o
   if (s_flag[1]) {
-    // a wait gave up: give the loads still in flight one more bounded wait
-    // before their destination is reused
-    if (lane == 0 && warp < nt) mbar_wait(&bars[warp], use & 1, kWaitLimit);
+    // a wait gave up: give the last load issued to each stage one more
+    // bounded wait before the stage region is reused
+    if (lane == 0)
+      for (int st = warp; st < kStages; st += kWarps)
+        if (s_iss[st] > 0) mbar_wait(&bars[st], (s_iss[st] - 1) & 1, kWaitLimit);
     __syncthreads();
   }
   float *o_w = reinterpret_cast<float *>(stages);  // [W][G][D]

@@ -92,118 +92,196 @@ __device__ __forceinline__ int cta_excl_scan(int v, int *sh, int *total) {
   return res;
 }
 
-constexpr int kMaxKeys = 8192;  // candidate pages handled in shared memory
+constexpr int kMaxKeys = 8192;  // candidate pages selected in shared memory
+constexpr int kRankMax = 128;   // candidates finished by direct ranking
+constexpr uint32_t kCopyWaitLimit = 1u << 24;
 
-// Keys sit at j + j/16 in shared memory: a thread's contiguous run of 16 and
-// a warp's strided sweep both hit distinct banks.
-__device__ __forceinline__ int kpos(int j) { return j + (j >> 4); }
+// Exclusive scan over the CTA, thread order; *total = the sum.  One barrier;
+// `sh` must not be reused before the next barrier.
+__device__ __forceinline__ int cta_scan1(int v, int *sh, int *total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    x += lane >= o ? y : 0;
+  }
+  if (lane == 31) sh[warp] = x;
+  __syncthreads();
+  int before = 0, tot = 0;
+#pragma unroll
+  for (int w = 0; w < kSelWarps; ++w) {
+    const int t = sh[w];
+    before += w < warp ? t : 0;
+    tot += t;
+  }
+  *total = tot;
+  return before + x - v;
+}
 
 // Exact selection of the k highest of n scores (1 <= k < n <= kMaxKeys);
-// writes the chosen indices ascending to out[0..k).  The k-th largest key T
-// is found 4 bits at a time, from the top: at each step every thread counts
-// its keys (a contiguous range of indices) that match the bits fixed so far,
-// per value of the next 4 bits; warp sums come from redux.sync and one
-// thread picks the digit.  Keys equal to T are taken lowest index first.
-// Returns the count written.
-__device__ int cta_topk(const float *sc, int n, int k, int *out) {
-  __shared__ uint32_t keys[kMaxKeys + kMaxKeys / 16];
-  __shared__ uint32_t wcnt[kSelWarps][16];
-  __shared__ int sh[33];
-  __shared__ uint32_t s_prefix;
-  __shared__ int s_remaining;
+// writes the chosen indices ascending to out[0..k) and returns the count.
+// `sc` is 16-byte aligned and readable up to n rounded up to 4 floats.
+//   1. One bulk copy brings the scores into shared memory; they become
+//      order-preserving keys in place (NaN lowest, -0 folded onto +0).
+//   2. The bits on which the largest and smallest key agree are shared by
+//      every key: the search starts below them.
+//   3. The k-th largest key T is narrowed 8 bits at a time: a 256-bin
+//      histogram (shared-memory atomics) of the keys that match the bits
+//      fixed so far, a CTA scan from the top bin down, and the bin where the
+//      running count reaches k is fixed.
+//   4. Once at most kRankMax keys still match, they are ranked directly
+//      (greater key first, lower index first among equal keys); if every bit
+//      is fixed with more matching keys, all equal T and the lowest indices
+//      are taken.
+//   5. The chosen pages are marked in a bitmap; a scan of its words' bit
+//      counts writes them in ascending order.
+// The loops are short and rolled: this runs in one CTA per head, on an SM
+// whose instruction cache has not seen it.
+__device__ int cta_topk(const float *sc, int n, int k, int *out, int *err) {
+  __shared__ __align__(16) uint32_t skey[kMaxKeys];
+  __shared__ int hist[2][256];
+  __shared__ int sh[3][kSelWarps];
+  __shared__ uint32_t mm[2][kSelWarps];
+  __shared__ int dec[3];
+  __shared__ uint2 cand[kRankMax];
+  __shared__ int ncand;
+  __shared__ uint32_t chosen[kMaxKeys / 32];
+  __shared__ uint32_t equal[kMaxKeys / 32];
+  __shared__ __align__(8) uint64_t bar;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  for (int j = tid; j < n; j += kSelThreads) keys[kpos(j)] = score_key(__ldcg(sc + j));
   if (tid == 0) {
-    s_prefix = 0;
-    s_remaining = k;
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    const uint32_t bytes = (uint32_t)((n * 4 + 15) & ~15);
+    mbar_arrive_expect_tx(&bar, bytes);
+    bulk_load_1d(skey, sc, bytes, &bar);
+  }
+  hist[0][tid] = 0;
+  hist[1][tid] = 0;
+  for (int x = tid; x < kMaxKeys / 32; x += kSelThreads) chosen[x] = equal[x] = 0u;
+  if (tid == 0) ncand = 0;
+  __syncthreads();  // the barrier is initialised before anyone polls it
+  if (!mbar_wait(&bar, 0, kCopyWaitLimit)) {
+    if (tid == 0) set_err(err, kDevTimeout, -1, n, k);
+    return 0;
+  }
+  uint32_t kmax = 0u, kmin = 0xffffffffu;
+  for (int j = tid; j < n; j += kSelThreads) {
+    const uint32_t key = score_key(__uint_as_float(skey[j]));
+    skey[j] = key;
+    kmax = max(kmax, key);
+    kmin = min(kmin, key);
+  }
+  kmax = __reduce_max_sync(0xffffffffu, kmax);
+  kmin = __reduce_min_sync(0xffffffffu, kmin);
+  if (lane == 0) {
+    mm[0][warp] = kmax;
+    mm[1][warp] = kmin;
   }
   __syncthreads();
-  const int per = (n + kSelThreads - 1) / kSelThreads;
-  const int j0 = min(n, tid * per), j1 = min(n, j0 + per);
-  for (int shift = 28; shift >= 0; shift -= 4) {
-    const uint32_t prefix = s_prefix;
-    const uint32_t hi_mask = shift == 28 ? 0u : ~((1u << (shift + 4)) - 1u);
-    // per-thread counts of the 16 digit values, 8-bit fields packed in two
-    // 64-bit words (a thread holds at most kMaxKeys / 256 = 32 keys)
-    unsigned long long c_lo = 0, c_hi = 0;
+#pragma unroll
+  for (int w = 0; w < kSelWarps; ++w) {
+    kmax = max(kmax, mm[0][w]);
+    kmin = min(kmin, mm[1][w]);
+  }
+  // `lo` low bits are unresolved; the bits above them equal `prefix` for T
+  int lo = (kmax ^ kmin) ? 32 - __clz(kmax ^ kmin) : 0;
+  uint32_t prefix = lo == 32 ? 0u : kmax & ~((1u << lo) - 1u);
+  int remaining = k;  // keys still to take among those matching prefix
+  int active = n;     // keys matching prefix
+  for (int rnd = 0; lo > 0 && active > kRankMax; ++rnd) {
+    const int w = min(8, lo);
+    const int shift = lo - w;
+    const uint32_t fmask = lo == 32 ? 0u : ~((1u << lo) - 1u);
+    const uint32_t dmask = (1u << w) - 1u;
+    int *hc = hist[rnd & 1];
 #pragma unroll 4
-    for (int j = tid; j < n; j += kSelThreads) {  // strided sweep
-      const uint32_t u = keys[kpos(j)];
-      const uint32_t d = (u >> shift) & 15u;
-      // branch-free: a key outside the prefix adds 0
-      const unsigned long long inc =
-          ((u & hi_mask) == prefix ? 1ull : 0ull) << (8 * (d & 7u));
-      c_lo += d < 8 ? inc : 0ull;
-      c_hi += d < 8 ? 0ull : inc;
-    }
-    // widen to 16-bit fields (a warp holds at most 1024 keys) and sum the warp
-    uint32_t w16[8];
-#pragma unroll
-    for (int r = 0; r < 8; ++r) {
-      const unsigned long long src = r < 4 ? c_lo : c_hi;
-      const int f = (r & 3) * 2;  // two 8-bit fields per 32-bit word
-      const uint32_t lo = (uint32_t)(src >> (8 * f)) & 0xffu;
-      const uint32_t hi = (uint32_t)(src >> (8 * (f + 1))) & 0xffu;
-      w16[r] = __reduce_add_sync(0xffffffffu, lo | (hi << 16));
-    }
-    if (lane == 0)
-#pragma unroll
-      for (int r = 0; r < 8; ++r) {
-        wcnt[warp][2 * r] = w16[r] & 0xffffu;
-        wcnt[warp][2 * r + 1] = w16[r] >> 16;
-      }
-    __syncthreads();
-    if (warp == 0) {
-      // lane l holds the total of digit 15 - l; an inclusive scan over the
-      // lanes is then the count of keys with a digit >= 15 - l
-      int v = 0;
-      if (lane < 16)
-#pragma unroll
-        for (int w = 0; w < kSelWarps; ++w) v += (int)wcnt[w][15 - lane];
-      int incl = v;
-#pragma unroll
-      for (int o = 1; o < 16; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      const int rem = s_remaining;
-      const int excl = incl - v;
-      const bool hit = lane < 16 && excl < rem && rem <= incl;
-      const unsigned who = __ballot_sync(0xffffffffu, hit);
-      if (hit && (unsigned)lane == (unsigned)(__ffs(who) - 1)) {
-        s_remaining = rem - excl;
-        s_prefix = prefix | ((uint32_t)(15 - lane) << shift);
-      }
+    for (int j = tid; j < n; j += kSelThreads) {
+      const uint32_t u = skey[j];
+      if ((u & fmask) == prefix) atomicAdd(&hc[(u >> shift) & dmask], 1);
     }
     __syncthreads();
-  }
-  const uint32_t T = s_prefix;
-  const int take_eq = s_remaining;
-  int n_gt = 0, n_eq = 0;
-  for (int j = j0; j < j1; ++j) {
-    const uint32_t u = keys[kpos(j)];
-    n_gt += u > T;
-    n_eq += u == T;
-  }
-  int tot_eq;
-  int eq_before = cta_excl_scan(n_eq, sh, &tot_eq);
-  int mine = n_gt + max(0, min(n_eq, take_eq - eq_before));
-  int total;
-  int pos = cta_excl_scan(mine, sh, &total);
-  for (int j = j0; j < j1 && mine > 0; ++j) {
-    const uint32_t u = keys[kpos(j)];
-    bool take = u > T;
-    if (u == T) {
-      take = eq_before < take_eq;
-      ++eq_before;
+    // thread i takes bin 255 - i: the scan is then over bins from the top
+    const int v = hc[255 - tid];
+    hist[(rnd + 1) & 1][tid] = 0;  // the next round's bins (last read a round ago)
+    int tot;
+    const int excl = cta_scan1(v, sh[rnd & 1], &tot);
+    if (excl < remaining && remaining <= excl + v) {  // exactly one thread
+      dec[0] = 255 - tid;
+      dec[1] = remaining - excl;
+      dec[2] = v;
     }
-    if (take) {
-      if (pos < k) out[pos] = j;
+    __syncthreads();
+    prefix |= (uint32_t)dec[0] << shift;
+    remaining = dec[1];
+    active = dec[2];
+    lo = shift;
+  }
+  const uint32_t fmask = lo == 32 ? 0u : ~((1u << lo) - 1u);
+  const bool ranked = active <= kRankMax;
+#pragma unroll 4
+  for (int j = tid; j < n; j += kSelThreads) {
+    const uint32_t u = skey[j];
+    const uint32_t hb = u & fmask;
+    if (hb > prefix) atomicOr(&chosen[j >> 5], 1u << (j & 31));
+    if (hb == prefix) {
+      if (ranked) {
+        const int e = atomicAdd(&ncand, 1);
+        if (e < kRankMax) cand[e] = make_uint2(u, (uint32_t)j);
+      } else {
+        atomicOr(&equal[j >> 5], 1u << (j & 31));
+      }
+    }
+  }
+  __syncthreads();
+  const int nw = (n + 31) / 32;
+  if (ranked) {
+    if (tid < active) {
+      const uint2 me = cand[tid];
+      int rank = 0;
+#pragma unroll 8
+      for (int e = 0; e < active; ++e) {
+        const uint2 o = cand[e];
+        rank += (o.x > me.x) | ((o.x == me.x) & (o.y < me.y));
+      }
+      if (rank < remaining) atomicOr(&chosen[me.y >> 5], 1u << (me.y & 31u));
+    }
+  } else {
+    int taken = 0;
+    for (int w0 = 0; w0 < nw; w0 += kSelThreads) {
+      const int wd = w0 + tid;
+      uint32_t bits = wd < nw ? equal[wd] : 0u;
+      int tot;
+      int before = cta_scan1(__popc(bits), sh[2], &tot) + taken;
+      uint32_t add = 0u;
+      while (bits && before < remaining) {
+        const uint32_t low = bits & (0u - bits);
+        add |= low;
+        bits ^= low;
+        ++before;
+      }
+      if (add) chosen[wd] |= add;
+      taken += tot;
+      __syncthreads();
+    }
+  }
+  __syncthreads();
+  int written = 0;
+  for (int w0 = 0; w0 < nw; w0 += kSelThreads) {
+    const int wd = w0 + tid;
+    uint32_t bits = wd < nw ? chosen[wd] : 0u;
+    int tot;
+    int pos = cta_scan1(__popc(bits), sh[(w0 / kSelThreads) & 1], &tot) + written;
+    while (bits) {
+      const int b = __ffs(bits) - 1;
+      bits &= bits - 1;
+      if (pos < k) out[pos] = wd * 32 + b;
       ++pos;
-      --mine;
     }
+    written += tot;
   }
-  return total;
+  return written;
 }
 
 // Fallback for more candidates than shared memory holds: the same radix
@@ -292,7 +370,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_consta
     return;
   }
   const int n = s.nL - 1;  // candidate pages
-  float *scores = p.scores + ((size_t)i * p.Hd + hd) * p.max_nL;
+  float *scores = p.scores + ((size_t)i * p.Hd + hd) * p.score_stride;
   constexpr int KSTEPS = 2 * D / 16;
   constexpr int PAIRS = KSTEPS / 2;
   const int g8 = lane >> 2, t4 = lane & 3;
@@ -399,7 +477,8 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_consta
   __syncthreads();  // ... and the acquire above precedes every read below
   if (!s_last) return;
   const int k = s.K_sel - 1;
-  const int got = n <= kMaxKeys ? cta_topk(scores, n, k, out) : cta_topk_global(scores, n, k, out);
+  const int got = n <= kMaxKeys ? cta_topk(scores, n, k, out, p.err)
+                                : cta_topk_global(scores, n, k, out);
   if (tid == 0) {
     out[k] = s.nL - 1;
     if (got != k) set_err(p.err, kDevTopkCount, s.slot, hd, got);

@@ -33,7 +33,7 @@ struct ScratchLayout {
   size_t tickets_sel;  // int [kSeqsPerLaunch * Hd]
   size_t part_ml;      // float2 [kMaxItems * G]   (row max in log2 units, sum)
   size_t part_o;       // float  [kMaxItems * G * d]
-  size_t scores;       // float  [kSeqsPerLaunch * Hd * max_nL]
+  size_t scores;       // float  [kSeqsPerLaunch * Hd * score_stride]
   size_t total;
 };
 
@@ -81,10 +81,10 @@ struct SelectParams {
   const void *meta;
   const int *page_table;
   int *selection;       // [max_seqs][Hd][ksel_max]
-  float *scores;        // [kSeqsPerLaunch][Hd][max_nL]
+  float *scores;        // [kSeqsPerLaunch][Hd][score_stride], rows 16-byte aligned
   int *tickets;         // [kSeqsPerLaunch][Hd], zero between launches
   int *err;
-  int n_seqs, Hq, Hd, ell, R, max_pp, ksel_max, max_nL, pages_per_chunk,
+  int n_seqs, Hq, Hd, ell, R, max_pp, ksel_max, score_stride, pages_per_chunk,
       num_phys;
   int score_ctas;       // total scoring CTAs
   int early;            // 1: read metadata before waiting for the previous kernel
@@ -119,7 +119,9 @@ struct TileDecodeParams {
   int n_seqs, Hq, Hkv, Hd, Hs, ell, P, R, max_pp, ksel_max, S, W, num_phys;
   int total_items;
   int cluster;        // CTAs per thread-block cluster; every unit's item count is a multiple
-  int early;          // 1: stage K/V tiles before waiting for the previous kernel
+  int early;          // stage K/V tiles before waiting for the previous kernel:
+                      // bit 0 dynamic units, bit 1 streaming units; bit 2:
+                      // streaming units do not wait at all
   float scale_log2;
   unsigned char dyn_kv[kMaxKvHeads];
   unsigned char str_kv[kMaxKvHeads];

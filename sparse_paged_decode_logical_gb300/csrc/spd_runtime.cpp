@@ -130,7 +130,7 @@ const char *derive(const spd_config *c, Derived *d) {
   sl.part_o = off;
   off = round_up(off + (size_t)kMaxItems * d->G * dim * 4, 256);
   sl.scores = off;
-  off = round_up(off + (size_t)d->seqs_per_launch * d->Hd * d->max_nL * 4, 256);
+  off = round_up(off + (size_t)d->seqs_per_launch * d->Hd * round_up((size_t)d->max_nL, 4) * 4, 256);
   sl.total = off;
   z.scratch = off;
   return nullptr;
@@ -169,28 +169,38 @@ struct spd_ctx {
 
 namespace {
 
-// Stream -> the context whose kernel this library enqueued last on it.  A
-// decode kernel may read its own KV cache before the previous kernel on the
-// stream has finished only when that kernel came from another context (or
-// from other code): nothing but this context's own launches writes its cache.
+// Stream -> the context whose kernel this library enqueued last on it, and
+// which kernel.  A kernel may read its own KV cache before the previous kernel
+// on the stream has finished only when that kernel cannot have written what
+// it reads: a kernel of another context (or other code) writes nothing of
+// this cache; this context's selection kernel writes only the selection, and
+// its page-table flush only the page table, neither of which a streaming
+// head reads.
+enum LaunchKind { kKindOther = 0, kKindSelect = 1, kKindPageTable = 2 };
+struct LastLaunch {
+  const spd_ctx *ctx;
+  LaunchKind kind;
+};
 std::mutex g_last_mu;
-std::unordered_map<cudaStream_t, const spd_ctx *> g_last_launcher;
+std::unordered_map<cudaStream_t, LastLaunch> g_last_launcher;
 
-bool previous_launcher_is(const spd_ctx *c, cudaStream_t st) {
+bool previous_launcher_is(const spd_ctx *c, cudaStream_t st, LaunchKind *kind = nullptr) {
   std::lock_guard<std::mutex> lock(g_last_mu);
   auto it = g_last_launcher.find(st);
-  return it != g_last_launcher.end() && it->second == c;
+  const bool mine = it != g_last_launcher.end() && it->second.ctx == c;
+  if (kind) *kind = mine ? it->second.kind : kKindOther;
+  return mine;
 }
 
-void note_launcher(const spd_ctx *c, cudaStream_t st) {
+void note_launcher(const spd_ctx *c, cudaStream_t st, LaunchKind kind = kKindOther) {
   std::lock_guard<std::mutex> lock(g_last_mu);
-  g_last_launcher[st] = c;
+  g_last_launcher[st] = LastLaunch{c, kind};
 }
 
 void forget_launcher(const spd_ctx *c) {
   std::lock_guard<std::mutex> lock(g_last_mu);
   for (auto it = g_last_launcher.begin(); it != g_last_launcher.end();)
-    it = it->second == c ? g_last_launcher.erase(it) : std::next(it);
+    it = it->second.ctx == c ? g_last_launcher.erase(it) : std::next(it);
 }
 
 spd_status cuda_fail(spd_ctx *c, cudaError_t e, const char *what) {
@@ -306,7 +316,7 @@ spd_status flush_page_table(spd_ctx *c, cudaStream_t st) {
     for (int k = 0; k < p.n; ++k) p.upd[k] = c->pending_pt[i + k];
     cudaError_t e = launch_pt_write(p, st, &c->launches);
     if (e != cudaSuccess) return cuda_fail(c, e, "pt_write launch");
-    note_launcher(c, st);
+    note_launcher(c, st, kKindPageTable);
     i += p.n;
   }
   c->pending_pt.clear();
@@ -403,7 +413,7 @@ spd_status select_impl(spd_ctx *c, const void *q, const int *ids, int n, bool fo
       p.R = dv.R;
       p.max_pp = dv.max_pp;
       p.ksel_max = dv.ksel_max;
-      p.max_nL = dv.max_nL;
+      p.score_stride = (int)round_up((size_t)dv.max_nL, 4);  // 16-byte aligned rows
       p.pages_per_chunk = ppc;
       p.num_phys = c->cfg.num_physical_pages;
       memcpy(p.dyn_kv, dv.dyn_kv, sizeof p.dyn_kv);
@@ -424,7 +434,7 @@ spd_status select_impl(spd_ctx *c, const void *q, const int *ids, int n, bool fo
       p.early = c->early_staging && !previous_launcher_is(c, st) ? 1 : 0;
       cudaError_t e = launch_select_fused(p, c->cfg.dtype, c->cfg.head_dim, dv.G, st, &c->launches);
       if (e != cudaSuccess) return cuda_fail(c, e, "select launch");
-      note_launcher(c, st);
+      note_launcher(c, st, kKindSelect);
     }
   }
   for (int pos : due) {
@@ -561,7 +571,14 @@ spd_status attention_impl(spd_ctx *c, const void *q, const int *ids, int n, floa
     p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)c->cfg.head_dim));
     memcpy(p.dyn_kv, dv.dyn_kv, sizeof p.dyn_kv);
     memcpy(p.str_kv, dv.str_kv, sizeof p.str_kv);
-    p.early = c->early_staging && !previous_launcher_is(c, st) ? 1 : 0;
+    // bit 0: dynamic units may stage before the wait, bit 1: streaming units;
+    // bit 2: streaming units need not wait at all (the previous kernel is this
+    // context's selection or page-table flush, which q and the streaming
+    // buffers do not depend on)
+    LaunchKind prev = kKindOther;
+    if (!c->early_staging) p.early = 0;
+    else if (!previous_launcher_is(c, st, &prev)) p.early = 3;
+    else p.early = (prev == kKindSelect || prev == kKindPageTable) ? 2 | 4 : 0;
     cudaError_t e = launch_decode_tiles(p, c->cfg.dtype, c->cfg.head_dim, dv.G, st, &c->launches);
     if (e != cudaSuccess) return cuda_fail(c, e, "decode launch");
     note_launcher(c, st);
