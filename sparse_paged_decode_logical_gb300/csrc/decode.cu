@@ -240,6 +240,17 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
   // kernel, which writes nothing a streaming unit reads; q is final once that
   // kernel runs (it waited for its own predecessor before releasing this one)
   const bool skip_wait = !dyn && ((p.early >> 2) & 1);
+  if (tid == 0) {
+    // q (and the new token) start their way into L2 now; they are read only
+    // after the wait, and L2 is coherent, so this is a hint and nothing more
+    prefetch_l2_bulk(static_cast<const uint16_t *>(p.q) + ((size_t)i * p.Hq + h * G) * D,
+                     G * D * 2);
+    if (do_append) {
+      const size_t row = ((size_t)i * p.Hkv + h) * D;
+      prefetch_l2_bulk(static_cast<const uint16_t *>(p.k_new) + row, D * 2);
+      prefetch_l2_bulk(static_cast<const uint16_t *>(p.v_new) + row, D * 2);
+    }
+  }
 
   // Everything above used only the parameter block.  The KV cache (page
   // table, selection, pools) is read next: before the wait for the previous

@@ -83,6 +83,15 @@ __device__ __forceinline__ void bulk_load_1d(void *dst, const void *src, uint32_
       : "memory");
 }
 
+// Bulk prefetch of [src, src + bytes) into L2 (16-byte aligned, bytes a
+// multiple of 16).  A hint: it reads nothing into registers, so it may be
+// issued before the data's producer has finished (L2 is coherent).
+__device__ __forceinline__ void prefetch_l2_bulk(const void *src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)),
+               "r"(bytes)
+               : "memory");
+}
+
 // Atomic add with acquire-release semantics at GPU scope (returns the old
 // value).  Issued by one thread after a CTA barrier it publishes the CTA's
 // prior writes to other CTAs and, if it observes their releases, makes

@@ -57,11 +57,12 @@ __device__ __forceinline__ void set_err(int *err, int code, int a, int b, int c)
   }
 }
 
+// Order-preserving unsigned key of a score: NaN lowest (0), -0 folded onto +0.
 __device__ __forceinline__ uint32_t score_key(float f) {
-  if (f != f) return 0u;
-  if (f == 0.f) f = 0.f;
-  const uint32_t b = __float_as_uint(f);
-  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+  const uint32_t b = __float_as_uint(f), a = b & 0x7fffffffu;
+  uint32_t key = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+  key = a == 0u ? 0x80000000u : key;
+  return a > 0x7f800000u ? 0u : key;
 }
 
 // Exclusive scan over the CTA (kSelThreads threads); *total = sum.
@@ -134,8 +135,9 @@ __device__ __forceinline__ int cta_scan1(int v, int *sh, int *total) {
 //      (greater key first, lower index first among equal keys); if every bit
 //      is fixed with more matching keys, all equal T and the lowest indices
 //      are taken.
-//   5. The chosen pages are marked in a bitmap; a scan of its words' bit
-//      counts writes them in ascending order.
+//   5. The chosen pages are marked in a bitmap (a warp's 32 consecutive
+//      pages make one word, by ballot); a scan of its words' bit counts
+//      writes them in ascending order.
 // The loops are short and rolled: this runs in one CTA per head, on an SM
 // whose instruction cache has not seen it.
 __device__ int cta_topk(const float *sc, int n, int k, int *out, int *err) {
@@ -159,7 +161,6 @@ __device__ int cta_topk(const float *sc, int n, int k, int *out, int *err) {
   }
   hist[0][tid] = 0;
   hist[1][tid] = 0;
-  for (int x = tid; x < kMaxKeys / 32; x += kSelThreads) chosen[x] = equal[x] = 0u;
   if (tid == 0) ncand = 0;
   __syncthreads();  // the barrier is initialised before anyone polls it
   if (!mbar_wait(&bar, 0, kCopyWaitLimit)) {
@@ -220,17 +221,26 @@ __device__ int cta_topk(const float *sc, int n, int k, int *out, int *err) {
   }
   const uint32_t fmask = lo == 32 ? 0u : ~((1u << lo) - 1u);
   const bool ranked = active <= kRankMax;
-#pragma unroll 4
-  for (int j = tid; j < n; j += kSelThreads) {
-    const uint32_t u = skey[j];
+  // warp w of pass r holds pages 256r + 32w + lane: its ballots are bitmap
+  // word 8r + w (every word below the rounded-up n is written once)
+  for (int j0 = 0; j0 < n; j0 += kSelThreads) {
+    const int j = j0 + tid;
+    const uint32_t u = j < n ? skey[j] : 0u;
     const uint32_t hb = u & fmask;
-    if (hb > prefix) atomicOr(&chosen[j >> 5], 1u << (j & 31));
-    if (hb == prefix) {
-      if (ranked) {
-        const int e = atomicAdd(&ncand, 1);
+    const unsigned above = __ballot_sync(0xffffffffu, j < n && hb > prefix);
+    const unsigned eq = __ballot_sync(0xffffffffu, j < n && hb == prefix);
+    const int wd = (j0 >> 5) + warp;
+    if (lane == 0) {
+      chosen[wd] = above;
+      equal[wd] = ranked ? 0u : eq;
+    }
+    if (ranked && eq) {
+      int base = 0;
+      if (lane == 0) base = atomicAdd(&ncand, __popc(eq));
+      base = __shfl_sync(0xffffffffu, base, 0);
+      if ((eq >> lane) & 1u) {
+        const int e = base + __popc(eq & ((1u << lane) - 1u));
         if (e < kRankMax) cand[e] = make_uint2(u, (uint32_t)j);
-      } else {
-        atomicOr(&equal[j >> 5], 1u << (j & 31));
       }
     }
   }
@@ -356,6 +366,9 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_consta
   // kernel on the stream only when the host knows that kernel cannot have
   // written this context's cache (p.early); q and every write come after it.
   const bool early = p.early && s.n_chunks != 0;
+  if (threadIdx.x == 0 && s.n_chunks != 0)  // a hint: q is read only after the wait
+    prefetch_l2_bulk(static_cast<const uint16_t *>(p.q) + ((size_t)s.qrow * p.Hq + h * G) * D,
+                     G * D * 2);
   if (!early) {
     pdl_wait();
     pdl_launch_dependents();
