@@ -54,6 +54,7 @@
 
 #include "ptx.cuh"
 #include "spd_internal.h"
+#include "topk.cuh"
 
 namespace spd {
 namespace {
@@ -99,14 +100,17 @@ struct Smem {
   // O[16 ranks][G][D / CS] (= G * D floats for any CS)
   static constexpr int kInbox = (kML + 2 * kWarps * G * 4 + 15) / 16 * 16;
   static constexpr int kFlag = kInbox + (32 * G + G * D) * 4;          // int [4 + kStages]
-  static constexpr int kTiles = (kFlag + (4 + kStages) * 4 + 1023) / 1024 * 1024;
+  static constexpr int kTopkBar = (kFlag + (4 + kStages) * 4 + 7) / 8 * 8;  // uint64
+  static constexpr int kTiles = (kTopkBar + 8 + 1023) / 1024 * 1024;
   static constexpr int kStageRegion = kStages * Geo<D>::kTileBytes;
   static constexpr int kMergeRegion = kWarps * G * D * 4;              // o of every warp
   static constexpr int kCombineRegion = 256 * G * 12 + 64;             // (m, l), weights
-  static constexpr int kRegion =
-      kStageRegion > kMergeRegion
-          ? (kStageRegion > kCombineRegion ? kStageRegion : kCombineRegion)
-          : (kMergeRegion > kCombineRegion ? kMergeRegion : kCombineRegion);
+  // before the tiles of a fused selection step: the top-k buffers, then the
+  // unit's selected pages
+  static constexpr int kTopkRegion = kTopkSmemBytes + kFusedMaxSel * 4;
+  static constexpr int kR1 = kStageRegion > kMergeRegion ? kStageRegion : kMergeRegion;
+  static constexpr int kR2 = kCombineRegion > kTopkRegion ? kCombineRegion : kTopkRegion;
+  static constexpr int kRegion = kR1 > kR2 ? kR1 : kR2;
   static constexpr int kAlloc = kTiles + kRegion + 1024;  // + alignment slack
 };
 
@@ -235,7 +239,8 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
   const int nt = min(kMaxDesc, max(0, min(n_tiles, tile0 + tpi) - tile0));
   const bool owns_newest = nt > 0 && tile0 + nt == n_tiles;
   const bool do_append = p.k_new != nullptr && owns_newest;
-  const bool early = (p.early >> (dyn ? 0 : 1)) & 1;
+  // (a unit that selects its pages here reads this step's scores: never early)
+  const bool early = ((p.early >> (dyn ? 0 : 1)) & 1) && !(dyn && s.topk_n > 0);
   // bit 2: the previous kernel is this context's own selection or page-table
   // kernel, which writes nothing a streaming unit reads; q is final once that
   // kernel runs (it waited for its own predecessor before releasing this one)
@@ -265,13 +270,42 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
     pdl_launch_dependents();
   }
 
+  // ---- a fused selection step: this CTA selects the unit's pages ----
+  // (every CTA of the unit computes the same selection from the same scores;
+  // the stage region holds the work and the result until the tiles arrive)
+  const int *sel_s = nullptr;
+  if (dyn && s.topk_n > 0) {
+    TopkSmem tm = carve_topk_smem(stages);
+    tm.bar = reinterpret_cast<uint64_t *>(smem + Sm::kTopkBar);  // never repurposed
+    int *list = reinterpret_cast<int *>(stages + kTopkSmemBytes);
+    const int k = s.sel_count - 1;
+    const float *scr = p.scores + ((size_t)s.topk_row * p.Hd + sub) * p.score_stride;
+    const uint32_t bound =
+        s.topk_bounds > 0
+            ? min_chunk_bound(p.bounds + ((size_t)s.topk_row * p.Hd + sub) * p.bound_stride,
+                              s.topk_bounds, tm)
+            : 0u;
+    const int got = cta_topk(scr, s.topk_n, k, bound, list, p.err, tm);
+    __syncthreads();
+    if (tid == 0) {
+      list[k] = s.nL0 - 1;  // the newest page is always kept
+      if (got != k) set_err(p.err, kDevTopkCount, s.slot, sub, got);
+    }
+    __syncthreads();
+    if (split == 0) {  // one CTA of the unit stores it for the steps that reuse it
+      int *gsel = const_cast<int *>(p.selection) + ((size_t)s.slot * p.Hd + sub) * p.ksel_max;
+      for (int t = tid; t < s.sel_count; t += kThreads) gsel[t] = list[t];
+    }
+    sel_s = list;
+  }
+
   // ---- tile descriptors (threads in parallel), stage barriers ----
   for (int t = tid; t < nt; t += kThreads) {
     const int tau = tile0 + t;
     TileDesc td{0, 0, 0, 0};
     if (dyn) {
       const int pi = tau / tpp, st = tau % tpp;
-      const int *sel = p.selection + ((size_t)s.slot * p.Hd + sub) * p.ksel_max;
+      const int *sel = sel_s ? sel_s : p.selection + ((size_t)s.slot * p.Hd + sub) * p.ksel_max;
       const int j = pi < s.sel_count ? sel[pi] : s.nL0 + (pi - s.sel_count);
       const int blk = j / p.R;
       if (j < 0 || j >= nL || blk >= p.max_pp) {
@@ -323,6 +357,9 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
     }
   };
   if (lane == 0) {
+    // the stage region was read and written through the generic proxy (the
+    // selection above): order that before the TMA writes
+    if (sel_s) fence_proxy_async_smem();
     for (int t = warp; t < min(nt, kStages); t += kWarps) issue(t);
     // the later tiles start their way from HBM into L2 now; their stage
     // refills then read L2
@@ -576,7 +613,7 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
         if (s_iss[st] > 0) mbar_wait(&bars[st], (s_iss[st] - 1) & 1, kWaitLimit);
     __syncthreads();
   }
-  float *o_w = reinterpret_cast<float *>(stages);  // [W][G][D]
+  float *o_w = reinterpret_cast<float *>(stages);  // [W][D][G]
   if (g8 == 0) {
     if (2 * t4 < G) {
       m_w[warp * G + 2 * t4] = m0;
@@ -587,16 +624,21 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
       l_w[warp * G + 2 * t4 + 1] = l1;
     }
   }
+  // a lane's two heads are adjacent: one 8-byte store per channel, and a
+  // half-warp's stores cover 32 distinct banks
 #pragma unroll
   for (int m = 0; m < MT; ++m) {
     const int ch = 16 * m + g8;
     if (2 * t4 < G) {
-      o_w[(warp * G + 2 * t4) * D + ch] = oacc[m][0];
-      o_w[(warp * G + 2 * t4) * D + ch + 8] = oacc[m][2];
-    }
-    if (2 * t4 + 1 < G) {
-      o_w[(warp * G + 2 * t4 + 1) * D + ch] = oacc[m][1];
-      o_w[(warp * G + 2 * t4 + 1) * D + ch + 8] = oacc[m][3];
+      if constexpr (G >= 2) {
+        *reinterpret_cast<float2 *>(&o_w[(warp * D + ch) * G + 2 * t4]) =
+            make_float2(oacc[m][0], oacc[m][1]);
+        *reinterpret_cast<float2 *>(&o_w[(warp * D + ch + 8) * G + 2 * t4]) =
+            make_float2(oacc[m][2], oacc[m][3]);
+      } else {
+        o_w[warp * D + ch] = oacc[m][0];
+        o_w[warp * D + ch + 8] = oacc[m][2];
+      }
     }
   }
   __syncthreads();
@@ -606,7 +648,7 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
   const int slice = D / CS;
   const uint32_t aM = smem_u32(in_M), aL = smem_u32(in_L), aO = smem_u32(in_O);
   for (int x = tid; x < G * D; x += kThreads) {
-    const int g = x / D, c = x % D;
+    const int c = x / G, g = x % G;
     float M = m_w[g];
 #pragma unroll
     for (int w = 1; w < kWarps; ++w) M = fmaxf(M, m_w[w * G + g]);
@@ -615,7 +657,7 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
 #pragma unroll
       for (int w = 0; w < kWarps; ++w) {
         const float f = exp2f(m_w[w * G + g] - M);
-        O += f * o_w[(w * G + g) * D + c];
+        O += f * o_w[(w * D + c) * G + g];
         Ls += f * l_w[w * G + g];
       }
     }
@@ -632,31 +674,40 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
   const int unit = i * p.Hkv + h;
   float *out = p.out + ((size_t)i * p.Hq + h * G) * D;
   const size_t cpart = (size_t)unit_item0 + (size_t)ci * CS;  // global slot of this cluster
-  for (int x = tid; x < G * slice; x += kThreads) {
-    const int g = x / slice, cl = x % slice, c = rank * slice + cl;
-    float mr[16];
+  // TPE adjacent lanes share one output element and split the CS ranks
+  // between them (fewer serial steps than one lane walking all ranks)
+  const int E = G * slice;
+  int TPE = 1;
+  while (TPE * 2 <= CS && E * TPE * 2 <= kThreads) TPE *= 2;
+  for (int base = 0; base < E * TPE; base += kThreads) {
+    const int xt = base + tid, x = xt / TPE, r0 = xt % TPE;
+    const bool valid = x < E;
+    const int g = valid ? x / slice : 0, cl = valid ? x % slice : 0, c = rank * slice + cl;
     float M = -CUDART_INF_F;
-#pragma unroll
-    for (int r = 0; r < 16; ++r) {
-      mr[r] = r < CS ? in_M[r * G + g] : -CUDART_INF_F;
-      M = fmaxf(M, mr[r]);
-    }
+    if (valid)
+      for (int r = r0; r < CS; r += TPE) M = fmaxf(M, in_M[r * G + g]);
+    for (int o = 1; o < TPE; o <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     float O = 0.f, Ls = 0.f;
-    if (M != -CUDART_INF_F) {
-#pragma unroll
-      for (int r = 0; r < 16; ++r) {
-        if (r < CS && mr[r] != -CUDART_INF_F) {
-          const float f = exp2f(mr[r] - M);
+    if (valid && M != -CUDART_INF_F)
+      for (int r = r0; r < CS; r += TPE) {
+        const float mr = in_M[r * G + g];
+        if (mr != -CUDART_INF_F) {
+          const float f = exp2f(mr - M);
           Ls = fmaf(f, in_L[r * G + g], Ls);
           O = fmaf(f, in_O[(r * G + g) * slice + cl], O);
         }
       }
+    for (int o = 1; o < TPE; o <<= 1) {
+      O += __shfl_xor_sync(0xffffffffu, O, o);
+      Ls += __shfl_xor_sync(0xffffffffu, Ls, o);
     }
-    if (nc == 1) {
-      out[g * D + c] = O / Ls;
-    } else {
-      p.part_o[(cpart * G + g) * D + c] = O;
-      if (rank == 0 && cl == 0) p.part_ml[cpart * G + g] = make_float2(M, Ls);
+    if (valid && r0 == 0) {
+      if (nc == 1) {
+        out[g * D + c] = O / Ls;
+      } else {
+        p.part_o[(cpart * G + g) * D + c] = O;
+        if (rank == 0 && cl == 0) p.part_ml[cpart * G + g] = make_float2(M, Ls);
+      }
     }
   }
   if (nc == 1) return;

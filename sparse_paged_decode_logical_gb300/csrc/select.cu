@@ -29,12 +29,11 @@
 
 #include "ptx.cuh"
 #include "spd_internal.h"
+#include "topk.cuh"
 
 namespace spd {
 namespace {
 
-constexpr int kSelThreads = 256;
-constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kPagesPerWarp = 16;
 constexpr int kPagesPerCta = kSelWarps * kPagesPerWarp;  // 128
 
@@ -57,13 +56,6 @@ __device__ __forceinline__ void set_err(int *err, int code, int a, int b, int c)
   }
 }
 
-// Order-preserving unsigned key of a score: NaN lowest (0), -0 folded onto +0.
-__device__ __forceinline__ uint32_t score_key(float f) {
-  const uint32_t b = __float_as_uint(f), a = b & 0x7fffffffu;
-  uint32_t key = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-  key = a == 0u ? 0x80000000u : key;
-  return a > 0x7f800000u ? 0u : key;
-}
 
 // Exclusive scan over the CTA (kSelThreads threads); *total = sum.
 __device__ __forceinline__ int cta_excl_scan(int v, int *sh, int *total) {
@@ -91,207 +83,6 @@ __device__ __forceinline__ int cta_excl_scan(int v, int *sh, int *total) {
   *total = sh[32];
   __syncthreads();
   return res;
-}
-
-constexpr int kMaxKeys = 8192;  // candidate pages selected in shared memory
-constexpr int kRankMax = 128;   // candidates finished by direct ranking
-constexpr uint32_t kCopyWaitLimit = 1u << 24;
-
-// Exclusive scan over the CTA, thread order; *total = the sum.  One barrier;
-// `sh` must not be reused before the next barrier.
-__device__ __forceinline__ int cta_scan1(int v, int *sh, int *total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, x, o);
-    x += lane >= o ? y : 0;
-  }
-  if (lane == 31) sh[warp] = x;
-  __syncthreads();
-  int before = 0, tot = 0;
-#pragma unroll
-  for (int w = 0; w < kSelWarps; ++w) {
-    const int t = sh[w];
-    before += w < warp ? t : 0;
-    tot += t;
-  }
-  *total = tot;
-  return before + x - v;
-}
-
-// Exact selection of the k highest of n scores (1 <= k < n <= kMaxKeys);
-// writes the chosen indices ascending to out[0..k) and returns the count.
-// `sc` is 16-byte aligned and readable up to n rounded up to 4 floats.
-//   1. One bulk copy brings the scores into shared memory; they become
-//      order-preserving keys in place (NaN lowest, -0 folded onto +0).
-//   2. The bits on which the largest and smallest key agree are shared by
-//      every key: the search starts below them.
-//   3. The k-th largest key T is narrowed 8 bits at a time: a 256-bin
-//      histogram (shared-memory atomics) of the keys that match the bits
-//      fixed so far, a CTA scan from the top bin down, and the bin where the
-//      running count reaches k is fixed.
-//   4. Once at most kRankMax keys still match, they are ranked directly
-//      (greater key first, lower index first among equal keys); if every bit
-//      is fixed with more matching keys, all equal T and the lowest indices
-//      are taken.
-//   5. The chosen pages are marked in a bitmap (a warp's 32 consecutive
-//      pages make one word, by ballot); a scan of its words' bit counts
-//      writes them in ascending order.
-// The loops are short and rolled: this runs in one CTA per head, on an SM
-// whose instruction cache has not seen it.
-__device__ int cta_topk(const float *sc, int n, int k, int *out, int *err) {
-  __shared__ __align__(16) uint32_t skey[kMaxKeys];
-  __shared__ int hist[2][256];
-  __shared__ int sh[3][kSelWarps];
-  __shared__ uint32_t mm[2][kSelWarps];
-  __shared__ int dec[3];
-  __shared__ uint2 cand[kRankMax];
-  __shared__ int ncand;
-  __shared__ uint32_t chosen[kMaxKeys / 32];
-  __shared__ uint32_t equal[kMaxKeys / 32];
-  __shared__ __align__(8) uint64_t bar;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (tid == 0) {
-    mbar_init(&bar, 1);
-    fence_mbar_init();
-    const uint32_t bytes = (uint32_t)((n * 4 + 15) & ~15);
-    mbar_arrive_expect_tx(&bar, bytes);
-    bulk_load_1d(skey, sc, bytes, &bar);
-  }
-  hist[0][tid] = 0;
-  hist[1][tid] = 0;
-  if (tid == 0) ncand = 0;
-  __syncthreads();  // the barrier is initialised before anyone polls it
-  if (!mbar_wait(&bar, 0, kCopyWaitLimit)) {
-    if (tid == 0) set_err(err, kDevTimeout, -1, n, k);
-    return 0;
-  }
-  uint32_t kmax = 0u, kmin = 0xffffffffu;
-  for (int j = tid; j < n; j += kSelThreads) {
-    const uint32_t key = score_key(__uint_as_float(skey[j]));
-    skey[j] = key;
-    kmax = max(kmax, key);
-    kmin = min(kmin, key);
-  }
-  kmax = __reduce_max_sync(0xffffffffu, kmax);
-  kmin = __reduce_min_sync(0xffffffffu, kmin);
-  if (lane == 0) {
-    mm[0][warp] = kmax;
-    mm[1][warp] = kmin;
-  }
-  __syncthreads();
-#pragma unroll
-  for (int w = 0; w < kSelWarps; ++w) {
-    kmax = max(kmax, mm[0][w]);
-    kmin = min(kmin, mm[1][w]);
-  }
-  // `lo` low bits are unresolved; the bits above them equal `prefix` for T
-  int lo = (kmax ^ kmin) ? 32 - __clz(kmax ^ kmin) : 0;
-  uint32_t prefix = lo == 32 ? 0u : kmax & ~((1u << lo) - 1u);
-  int remaining = k;  // keys still to take among those matching prefix
-  int active = n;     // keys matching prefix
-  for (int rnd = 0; lo > 0 && active > kRankMax; ++rnd) {
-    const int w = min(8, lo);
-    const int shift = lo - w;
-    const uint32_t fmask = lo == 32 ? 0u : ~((1u << lo) - 1u);
-    const uint32_t dmask = (1u << w) - 1u;
-    int *hc = hist[rnd & 1];
-#pragma unroll 4
-    for (int j = tid; j < n; j += kSelThreads) {
-      const uint32_t u = skey[j];
-      if ((u & fmask) == prefix) atomicAdd(&hc[(u >> shift) & dmask], 1);
-    }
-    __syncthreads();
-    // thread i takes bin 255 - i: the scan is then over bins from the top
-    const int v = hc[255 - tid];
-    hist[(rnd + 1) & 1][tid] = 0;  // the next round's bins (last read a round ago)
-    int tot;
-    const int excl = cta_scan1(v, sh[rnd & 1], &tot);
-    if (excl < remaining && remaining <= excl + v) {  // exactly one thread
-      dec[0] = 255 - tid;
-      dec[1] = remaining - excl;
-      dec[2] = v;
-    }
-    __syncthreads();
-    prefix |= (uint32_t)dec[0] << shift;
-    remaining = dec[1];
-    active = dec[2];
-    lo = shift;
-  }
-  const uint32_t fmask = lo == 32 ? 0u : ~((1u << lo) - 1u);
-  const bool ranked = active <= kRankMax;
-  // warp w of pass r holds pages 256r + 32w + lane: its ballots are bitmap
-  // word 8r + w (every word below the rounded-up n is written once)
-  for (int j0 = 0; j0 < n; j0 += kSelThreads) {
-    const int j = j0 + tid;
-    const uint32_t u = j < n ? skey[j] : 0u;
-    const uint32_t hb = u & fmask;
-    const unsigned above = __ballot_sync(0xffffffffu, j < n && hb > prefix);
-    const unsigned eq = __ballot_sync(0xffffffffu, j < n && hb == prefix);
-    const int wd = (j0 >> 5) + warp;
-    if (lane == 0) {
-      chosen[wd] = above;
-      equal[wd] = ranked ? 0u : eq;
-    }
-    if (ranked && eq) {
-      int base = 0;
-      if (lane == 0) base = atomicAdd(&ncand, __popc(eq));
-      base = __shfl_sync(0xffffffffu, base, 0);
-      if ((eq >> lane) & 1u) {
-        const int e = base + __popc(eq & ((1u << lane) - 1u));
-        if (e < kRankMax) cand[e] = make_uint2(u, (uint32_t)j);
-      }
-    }
-  }
-  __syncthreads();
-  const int nw = (n + 31) / 32;
-  if (ranked) {
-    if (tid < active) {
-      const uint2 me = cand[tid];
-      int rank = 0;
-#pragma unroll 8
-      for (int e = 0; e < active; ++e) {
-        const uint2 o = cand[e];
-        rank += (o.x > me.x) | ((o.x == me.x) & (o.y < me.y));
-      }
-      if (rank < remaining) atomicOr(&chosen[me.y >> 5], 1u << (me.y & 31u));
-    }
-  } else {
-    int taken = 0;
-    for (int w0 = 0; w0 < nw; w0 += kSelThreads) {
-      const int wd = w0 + tid;
-      uint32_t bits = wd < nw ? equal[wd] : 0u;
-      int tot;
-      int before = cta_scan1(__popc(bits), sh[2], &tot) + taken;
-      uint32_t add = 0u;
-      while (bits && before < remaining) {
-        const uint32_t low = bits & (0u - bits);
-        add |= low;
-        bits ^= low;
-        ++before;
-      }
-      if (add) chosen[wd] |= add;
-      taken += tot;
-      __syncthreads();
-    }
-  }
-  __syncthreads();
-  int written = 0;
-  for (int w0 = 0; w0 < nw; w0 += kSelThreads) {
-    const int wd = w0 + tid;
-    uint32_t bits = wd < nw ? chosen[wd] : 0u;
-    int tot;
-    int pos = cta_scan1(__popc(bits), sh[(w0 / kSelThreads) & 1], &tot) + written;
-    while (bits) {
-      const int b = __ffs(bits) - 1;
-      bits &= bits - 1;
-      if (pos < k) out[pos] = wd * 32 + b;
-      ++pos;
-    }
-    written += tot;
-  }
-  return written;
 }
 
 // Fallback for more candidates than shared memory holds: the same radix
@@ -352,6 +143,7 @@ template <typename T, int D, int G>
 __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_constant__ SelectParams p) {
   __shared__ int s_last;
   __shared__ __align__(16) uint16_t q_s[G * D];
+  __shared__ uint32_t ks[kPagesPerCta];  // this CTA's score keys, for its bound
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   int i = 0;
   while (i + 1 < p.n_seqs && p.seqs[i + 1].chunk_off <= (int)blockIdx.x) ++i;
@@ -478,8 +270,46 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_consta
     if (t4 == 0) {
       if (ok[0]) scores[j0 + g8] = s0;
       if (ok[1]) scores[j0 + g8 + 8] = s1;
+      ks[warp * kPagesPerWarp + g8] = ok[0] ? score_key(s0) : 0u;
+      ks[warp * kPagesPerWarp + g8 + 8] = ok[1] ? score_key(s1) : 0u;
     }
   }
+
+  // ---- this chunk's bound: its tau_m-th largest score key ----
+  // A full chunk holds tau_m keys at or above it, and tau_m x full chunks is
+  // at least the number of pages to choose, so the smallest bound over the
+  // chunks is a key that every chosen page reaches.
+  if (s.tau_m > 0) {
+    __syncthreads();
+    if (warp == 0) {
+      uint32_t a[kPagesPerCta / 32];
+#pragma unroll
+      for (int x = 0; x < kPagesPerCta / 32; ++x) a[x] = ks[lane + 32 * x];
+      uint32_t v = 0u;
+      for (int it = 0; it < s.tau_m; ++it) {  // take the largest tau_m times
+        uint32_t lm = a[0];
+#pragma unroll
+        for (int x = 1; x < kPagesPerCta / 32; ++x) lm = max(lm, a[x]);
+        v = __reduce_max_sync(0xffffffffu, lm);
+        const unsigned who = __ballot_sync(0xffffffffu, lm == v);
+        if (lane == __ffs(who) - 1) {
+          bool done = false;
+#pragma unroll
+          for (int x = 0; x < kPagesPerCta / 32; ++x)
+            if (!done && a[x] == v) {
+              a[x] = 0u;
+              done = true;
+            }
+        }
+      }
+      if (lane == 0) {
+        const bool full = (chunk + 1) * kPagesPerCta <= n;
+        p.bounds[((size_t)i * p.Hd + hd) * p.bound_stride + chunk] = full ? v : 0xffffffffu;
+      }
+    }
+  }
+
+  if (p.score_only) return;  // the decode kernel of this step selects from the scores
 
   // ---- the last scoring CTA of this (sequence, head) selects ----
   __syncthreads();  // every score of this CTA precedes the release below
@@ -490,8 +320,18 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_consta
   __syncthreads();  // ... and the acquire above precedes every read below
   if (!s_last) return;
   const int k = s.K_sel - 1;
-  const int got = n <= kMaxKeys ? cta_topk(scores, n, k, out, p.err)
-                                : cta_topk_global(scores, n, k, out);
+  int got;
+  if (n <= kMaxKeys) {
+    __shared__ __align__(16) uint8_t topk_smem[kTopkSmemBytes];
+    const TopkSmem tm = carve_topk_smem(topk_smem);
+    const uint32_t bound =
+        s.tau_m > 0 ? min_chunk_bound(p.bounds + ((size_t)i * p.Hd + hd) * p.bound_stride,
+                                      s.n_chunks, tm)
+                    : 0u;
+    got = cta_topk(scores, n, k, bound, out, p.err, tm);
+  } else {
+    got = cta_topk_global(scores, n, k, out);
+  }
   if (tid == 0) {
     out[k] = s.nL - 1;
     if (got != k) set_err(p.err, kDevTopkCount, s.slot, hd, got);

@@ -31,6 +31,7 @@ enum DevErr : int {
 struct ScratchLayout {
   size_t tickets_dec;  // int [kSeqsPerLaunch * Hkv]
   size_t tickets_sel;  // int [kSeqsPerLaunch * Hd]
+  size_t bounds;       // uint32 [kSeqsPerLaunch * Hd * bound_stride] per-chunk score bounds
   size_t part_ml;      // float2 [kMaxItems * G]   (row max in log2 units, sum)
   size_t part_o;       // float  [kMaxItems * G * d]
   size_t scores;       // float  [kSeqsPerLaunch * Hd * score_stride]
@@ -74,6 +75,8 @@ struct SelectSeq {
   int chunk_off;  // first CTA of this sequence
   int n_chunks;   // scoring CTAs per dynamic head (0: nothing to score, one CTA
                   // writes the trivial selection)
+  int tau_m;      // > 0: each full chunk publishes its tau_m-th largest score key
+                  // (tau_m x full chunks >= the pages to choose), 0: none
 };
 
 struct SelectParams {
@@ -83,10 +86,13 @@ struct SelectParams {
   int *selection;       // [max_seqs][Hd][ksel_max]
   float *scores;        // [kSeqsPerLaunch][Hd][score_stride], rows 16-byte aligned
   int *tickets;         // [kSeqsPerLaunch][Hd], zero between launches
+  uint32_t *bounds;     // [kSeqsPerLaunch][Hd][bound_stride]
+  int bound_stride;
   int *err;
   int n_seqs, Hq, Hd, ell, R, max_pp, ksel_max, score_stride, pages_per_chunk,
       num_phys;
   int score_ctas;       // total scoring CTAs
+  int score_only;       // 1: write the scores and stop (the decode kernel selects)
   int early;            // 1: read metadata before waiting for the previous kernel
   unsigned char dyn_kv[kMaxKvHeads];
   SelectSeq seqs[kSeqsPerLaunch];
@@ -102,6 +108,11 @@ struct TileSeq {
   int ns_str;     // items (CTAs) per streaming head
   int tpi_dyn;    // tiles per dynamic item
   int tpi_str;    // tiles per streaming item
+  int topk_n;     // > 0: this launch selects the pages itself, from topk_n candidate
+                  // scores in row topk_row of `scores` (sel_count - 1 of them plus
+                  // the newest page), and stores the selection
+  int topk_row;
+  int topk_bounds;  // per-chunk score bounds to read for it (0: none)
 };
 
 struct TileDecodeParams {
@@ -116,6 +127,10 @@ struct TileDecodeParams {
   float2 *part_ml;
   int *tickets;
   int *err;
+  const float *scores;       // [kSeqsPerLaunch][Hd][score_stride] page scores (fused steps)
+  int score_stride;
+  const uint32_t *bounds;    // [kSeqsPerLaunch][Hd][bound_stride] their per-chunk bounds
+  int bound_stride;
   int n_seqs, Hq, Hkv, Hd, Hs, ell, P, R, max_pp, ksel_max, S, W, num_phys;
   int total_items;
   int cluster;        // CTAs per thread-block cluster; every unit's item count is a multiple
@@ -127,6 +142,15 @@ struct TileDecodeParams {
   unsigned char str_kv[kMaxKvHeads];
   TileSeq seqs[kSeqsPerLaunch];
 };
+
+// A fused decode step (selection inside the decode kernel) holds at most this
+// many candidate scores and kept pages in shared memory; larger ones use the
+// selection kernel's own top-k.
+constexpr int kFusedMaxCandidates = 8192;
+constexpr int kFusedMaxSelected = 4096;
+// A selection bounds its candidates from each scoring chunk's m-th largest
+// score only while m (pages to choose / full chunks) is at most this.
+constexpr int kMaxBoundRank = 8;
 
 constexpr int kTileRows = 16;
 constexpr int kMaxTilesPerItem = 8;

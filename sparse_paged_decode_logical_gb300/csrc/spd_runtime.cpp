@@ -35,6 +35,9 @@ struct Seq {
   bool has_sel = false;
   int nL0 = 0;             // logical pages when the selection was taken
   int sel_count = 0;       // pages kept at that selection
+  int topk_pending = 0;    // candidates the next fused decode launch selects from (0: none)
+  int topk_row = 0;        // their row in the score scratch
+  int topk_bounds = 0;     // per-chunk score bounds written for them (0: none)
   std::vector<int> pages;  // physical page per P-token block
 };
 
@@ -60,6 +63,13 @@ struct Derived {
 
 // Validates cfg and fills the derived quantities; returns an error string or
 // nullptr.
+// Per-chunk score bounds a selection writes for each (sequence, head): one per
+// scoring CTA, rows padded to 16 bytes.
+int bound_stride_of(const Derived &d) {
+  const int ppc = select_pages_per_cta();
+  return (int)round_up((size_t)((d.max_nL + ppc - 1) / ppc), 4);
+}
+
 const char *derive(const spd_config *c, Derived *d) {
   if (!c) return "config is NULL";
   if (c->num_kv_heads < 1 || c->num_kv_heads > kMaxKvHeads)
@@ -125,6 +135,8 @@ const char *derive(const spd_config *c, Derived *d) {
   off = round_up(off + (size_t)d->seqs_per_launch * c->num_kv_heads * 4, 256);
   sl.tickets_sel = off;
   off = round_up(off + (size_t)d->seqs_per_launch * d->Hd * 4, 256);
+  sl.bounds = off;
+  off = round_up(off + (size_t)d->seqs_per_launch * d->Hd * bound_stride_of(*d) * 4, 256);
   sl.part_ml = off;
   off = round_up(off + (size_t)kMaxItems * d->G * 8, 256);
   sl.part_o = off;
@@ -384,15 +396,29 @@ spd_status append_impl(spd_ctx *c, const int *ids, int n, int n_tokens, const vo
   return SPD_OK;
 }
 
+// score_only: the decode kernel launched next (attention_impl with
+// fused_topk) selects the pages from the scores this launch writes; used when
+// every due sequence fits one selection launch and the kernel's shared-memory
+// limits (candidates, kept pages), otherwise the selection kernel selects.
 spd_status select_impl(spd_ctx *c, const void *q, const int *ids, int n, bool force,
-                       cudaStream_t st) {
+                       cudaStream_t st, bool score_only = false) {
   const Derived &dv = c->dv;
   std::vector<int> due;  // positions in the call
   for (int i = 0; i < n; ++i) {
-    const Seq &s = c->seqs[ids[i]];
+    Seq &s = c->seqs[ids[i]];
+    s.topk_pending = 0;
     if (force || s.counter % c->cfg.reuse_interval == 0) due.push_back(i);
   }
   if (due.empty()) return SPD_OK;
+  if (score_only) {
+    score_only = (int)due.size() <= dv.seqs_per_launch;
+    for (int pos : due) {
+      const Seq &s = c->seqs[ids[pos]];
+      const int nL = nL_of(s.L, c->cfg.logical_page);
+      if (nL - 1 > kFusedMaxCandidates || budget_pages(c, s.L) > kFusedMaxSelected)
+        score_only = false;
+    }
+  }
   if (dv.Hd > 0) {
     spd_status r = ensure_device(c, st);
     if (r != SPD_OK) return r;
@@ -406,6 +432,8 @@ spd_status select_impl(spd_ctx *c, const void *q, const int *ids, int n, bool fo
       p.selection = static_cast<int *>(c->buf.selection);
       p.scores = reinterpret_cast<float *>(c->scratch(dv.sl.scores));
       p.tickets = reinterpret_cast<int *>(c->scratch(dv.sl.tickets_sel));
+      p.bounds = reinterpret_cast<uint32_t *>(c->scratch(dv.sl.bounds));
+      p.bound_stride = bound_stride_of(dv);
       p.err = c->err_word();
       p.Hq = c->cfg.num_q_heads;
       p.Hd = dv.Hd;
@@ -428,9 +456,21 @@ spd_status select_impl(spd_ctx *c, const void *q, const int *ids, int n, bool fo
         d.K_sel = budget_pages(c, s.L);
         d.chunk_off = off;
         d.n_chunks = (d.nL > d.K_sel && d.K_sel > 1) ? (d.nL - 1 + ppc - 1) / ppc : 0;
+        // bound from each full chunk's tau_m-th key, when a few per chunk suffice
+        const int n_full = (d.nL - 1) / ppc;
+        const int tau_m = n_full > 0 ? (d.K_sel - 1 + n_full - 1) / n_full : 0;
+        d.tau_m = d.n_chunks > 0 && tau_m <= kMaxBoundRank ? tau_m : 0;
         off += std::max(1, d.n_chunks) * dv.Hd;
       }
       p.score_ctas = off;
+      p.score_only = score_only ? 1 : 0;
+      if (score_only)
+        for (int i = 0; i < p.n_seqs; ++i) {
+          Seq &s = c->seqs[ids[due[b + i]]];
+          s.topk_pending = p.seqs[i].n_chunks > 0 ? p.seqs[i].nL - 1 : 0;
+          s.topk_row = i;
+          s.topk_bounds = p.seqs[i].tau_m > 0 ? p.seqs[i].n_chunks : 0;
+        }
       p.early = c->early_staging && !previous_launcher_is(c, st) ? 1 : 0;
       cudaError_t e = launch_select_fused(p, c->cfg.dtype, c->cfg.head_dim, dv.G, st, &c->launches);
       if (e != cudaSuccess) return cuda_fail(c, e, "select launch");
@@ -515,9 +555,11 @@ int plan_tiles(const spd_ctx *c, TileDecodeParams &p, const int *ids, int n) {
 
 // `scr` (optional) replaces the context's scratch for the split partials and
 // tickets; a launch then holds at most scr->max_items items.
+// fused_topk: the selection launched just before wrote only scores for the
+// sequences marked topk_pending; this launch selects their pages.
 spd_status attention_impl(spd_ctx *c, const void *q, const int *ids, int n, float *out,
                           const void *k_new, const void *v_new, cudaStream_t st,
-                          const DecodeScratch *scr = nullptr) {
+                          const DecodeScratch *scr = nullptr, bool fused_topk = false) {
   spd_status r = ensure_device(c, st);
   if (r != SPD_OK) return r;
   const Derived &dv = c->dv;
@@ -556,6 +598,16 @@ spd_status attention_impl(spd_ctx *c, const void *q, const int *ids, int n, floa
     p.part_ml = scr ? scr->part_ml : reinterpret_cast<float2 *>(c->scratch(dv.sl.part_ml));
     p.tickets = scr ? scr->tickets : reinterpret_cast<int *>(c->scratch(dv.sl.tickets_dec));
     p.err = c->err_word();
+    p.scores = reinterpret_cast<const float *>(c->scratch(dv.sl.scores));
+    p.score_stride = (int)round_up((size_t)dv.max_nL, 4);
+    p.bounds = reinterpret_cast<const uint32_t *>(c->scratch(dv.sl.bounds));
+    p.bound_stride = bound_stride_of(dv);
+    for (int i = 0; i < m; ++i) {
+      const Seq &s = c->seqs[ids[b + i]];
+      p.seqs[i].topk_n = fused_topk ? s.topk_pending : 0;
+      p.seqs[i].topk_row = s.topk_row;
+      p.seqs[i].topk_bounds = fused_topk ? s.topk_bounds : 0;
+    }
     p.Hq = c->cfg.num_q_heads;
     p.Hkv = c->cfg.num_kv_heads;
     p.Hd = dv.Hd;
@@ -584,7 +636,10 @@ spd_status attention_impl(spd_ctx *c, const void *q, const int *ids, int n, floa
     note_launcher(c, st);
     b += m;
   }
-  for (int i = 0; i < n; ++i) c->seqs[ids[i]].counter += 1;
+  for (int i = 0; i < n; ++i) {
+    c->seqs[ids[i]].counter += 1;
+    c->seqs[ids[i]].topk_pending = 0;
+  }
   return SPD_OK;
 }
 
@@ -824,8 +879,8 @@ spd_status spd_decode_step(spd_ctx *c, const void *q, const void *k, const void 
   for (int i = 0; i < n_seqs; ++i) take_pages(c, seq_ids[i], 1);
   if ((r = flush_page_table(c, st)) != SPD_OK) return r;
   for (int i = 0; i < n_seqs; ++i) c->seqs[seq_ids[i]].L += 1;
-  if ((r = select_impl(c, q, seq_ids, n_seqs, false, st)) != SPD_OK) return r;
-  return attention_impl(c, q, seq_ids, n_seqs, out, k, v, st);
+  if ((r = select_impl(c, q, seq_ids, n_seqs, false, st, /*score_only=*/true)) != SPD_OK) return r;
+  return attention_impl(c, q, seq_ids, n_seqs, out, k, v, st, nullptr, /*fused_topk=*/true);
 }
 
 spd_status spd_get_selection(spd_ctx *c, int seq_id, int kv_head, int *idx_host, int cap,
