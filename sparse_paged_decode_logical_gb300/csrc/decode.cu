@@ -108,8 +108,12 @@ struct Smem {
   // before the tiles of a fused selection step: the top-k buffers, then the
   // unit's selected pages
   static constexpr int kTopkRegion = kTopkSmemBytes + kFusedMaxSel * 4;
+  static constexpr int kPtCache = 2048;                  // page-table entries cached with it
+  static constexpr int kPtCacheOff = kTopkRegion;        // bytes into the stage region
   static constexpr int kR1 = kStageRegion > kMergeRegion ? kStageRegion : kMergeRegion;
-  static constexpr int kR2 = kCombineRegion > kTopkRegion ? kCombineRegion : kTopkRegion;
+  static constexpr int kR2 = kCombineRegion > kTopkRegion + kPtCache * 4
+                                 ? kCombineRegion
+                                 : kTopkRegion + kPtCache * 4;
   static constexpr int kRegion = kR1 > kR2 ? kR1 : kR2;
   static constexpr int kAlloc = kTiles + kRegion + 1024;  // + alignment slack
 };
@@ -265,6 +269,15 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
   // come after the wait.  Dependents are released only after the wait, so when
   // this kernel runs, every kernel before its immediate predecessor has
   // finished.
+  // A unit that selects its pages here follows this context's own selection
+  // kernel, after the page-table flush had finished: the sequence's page
+  // table is final, so it is copied to shared memory before the wait.
+  int *pt_s = nullptr;
+  if (dyn && s.topk_n > 0 && p.max_pp <= Sm::kPtCache) {
+    pt_s = reinterpret_cast<int *>(stages + Sm::kPtCacheOff);
+    const int *row = p.page_table + (size_t)s.slot * p.max_pp;
+    for (int x = tid; x < p.max_pp; x += kThreads) pt_s[x] = row[x];
+  }
   if (!early) {
     if (!skip_wait) pdl_wait();
     pdl_launch_dependents();
@@ -311,7 +324,7 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
       if (j < 0 || j >= nL || blk >= p.max_pp) {
         set_err(p.err, kDevBadSelection, s.slot, sub, j);
       } else {
-        const int phys = p.page_table[(size_t)s.slot * p.max_pp + blk];
+        const int phys = pt_s ? pt_s[blk] : p.page_table[(size_t)s.slot * p.max_pp + blk];
         if (phys < 0 || phys >= p.num_phys) {
           set_err(p.err, kDevBadPhys, s.slot, blk, phys);
         } else {
