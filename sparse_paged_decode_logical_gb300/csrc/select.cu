@@ -40,12 +40,12 @@ constexpr int kPagesPerCta = kSelWarps * kPagesPerWarp;  // 128
 template <typename T> struct IsBf { static constexpr bool v = false; };
 template <> struct IsBf<__nv_bfloat16> { static constexpr bool v = true; };
 
-template <typename T> struct Neg;
-template <> struct Neg<__half> {
-  static __device__ __forceinline__ bool neg(uint16_t b) { return (b & 0x8000u) && (b & 0x7fffu); }
-};
-template <> struct Neg<__nv_bfloat16> {
-  static __device__ __forceinline__ bool neg(uint16_t b) { return (b & 0x8000u) && (b & 0x7fffu); }
+// Strictly negative 16-bit float (sign set, magnitude nonzero; -0 counts as
+// non-negative).  Same bit test for fp16 and bf16; written without branches.
+template <typename T> struct Neg {
+  static __device__ __forceinline__ bool neg(uint16_t b) {
+    return ((b >> 15) & (uint32_t)((b & 0x7fffu) != 0u)) != 0u;
+  }
 };
 
 __device__ __forceinline__ void set_err(int *err, int code, int a, int b, int c) {
@@ -142,7 +142,10 @@ __device__ int cta_topk_global(const float *sc, int n, int k, int *out) {
 template <typename T, int D, int G>
 __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_constant__ SelectParams p) {
   __shared__ int s_last;
-  __shared__ __align__(16) uint16_t q_s[G * D];
+  // the group's [q- ; q+] rows (2D elements each), padded by 32 bytes so that a
+  // warp's fragment loads meet at most two to a bank
+  constexpr int QS = 2 * D + 16;
+  __shared__ __align__(16) uint16_t q_s[G * QS];
   __shared__ uint32_t ks[kPagesPerCta];  // this CTA's score keys, for its bound
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   int i = 0;
@@ -223,23 +226,33 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_consta
     // the group's G query rows: one coalesced 16-byte load per thread
     const uint4 *qg = reinterpret_cast<const uint4 *>(
         reinterpret_cast<const uint16_t *>(p.q) + ((size_t)s.qrow * p.Hq + h * G) * D);
-    for (int x = tid; x < G * D / 8; x += kSelThreads) reinterpret_cast<uint4 *>(q_s)[x] = qg[x];
+    // staging: 8 elements of q per thread, split into q- (the kmin half of a
+    // metadata row) and q+ (the kmax half)
+    for (int x = tid; x < G * D / 8; x += kSelThreads) {
+      const uint4 v = qg[x];
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      uint32_t neg[4], pos[4];
+#pragma unroll
+      for (int y = 0; y < 4; ++y) {
+        const uint16_t lo = (uint16_t)(w[y] & 0xffffu), hi = (uint16_t)(w[y] >> 16);
+        const bool nl = Neg<T>::neg(lo), nh = Neg<T>::neg(hi);
+        neg[y] = (nl ? lo : 0u) | ((nh ? (uint32_t)hi : 0u) << 16);
+        pos[y] = (nl ? 0u : lo) | ((nh ? 0u : (uint32_t)hi) << 16);
+      }
+      uint16_t *row = &q_s[(x / (D / 8)) * QS + (x % (D / 8)) * 8];
+      *reinterpret_cast<uint4 *>(row) = make_uint4(neg[0], neg[1], neg[2], neg[3]);
+      *reinterpret_cast<uint4 *>(row + D) = make_uint4(pos[0], pos[1], pos[2], pos[3]);
+    }
     __syncthreads();
 #pragma unroll
     for (int kk = 0; kk < KSTEPS; ++kk) {
-      uint16_t e[4] = {0, 0, 0, 0};
+      uint2 f = make_uint2(0u, 0u);
       if (g8 < G) {
         const int base = 32 * (kk >> 1) + 8 * t4 + 4 * (kk & 1);  // metadata element
-#pragma unroll
-        for (int x = 0; x < 4; ++x) {
-          const int m = base + x;  // < D: a kmin element, else kmax
-          const uint16_t qv = q_s[g8 * D + (m % D)];
-          const bool neg = Neg<T>::neg(qv);
-          e[x] = (m < D) == neg ? qv : (uint16_t)0;  // kmin takes q-, kmax takes q+
-        }
+        f = *reinterpret_cast<const uint2 *>(&q_s[g8 * QS + base]);
       }
-      qb[kk][0] = (uint32_t)e[0] | ((uint32_t)e[1] << 16);
-      qb[kk][1] = (uint32_t)e[2] | ((uint32_t)e[3] << 16);
+      qb[kk][0] = f.x;
+      qb[kk][1] = f.y;
     }
   }
 
