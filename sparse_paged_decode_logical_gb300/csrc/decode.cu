@@ -658,7 +658,10 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
   cluster_wait();  // every CTA of the cluster has started: its inbox may be written
   // this CTA's (M, L, O), pushed straight into the inbox of the cluster CTA
   // that owns each channel slice (remote shared-memory stores)
-  const int slice = D / CS;
+  // CS, the slice and TPE below are powers of two: shifts and masks, not
+  // run-time integer division
+  const int lcs = __ffs(CS) - 1;
+  const int slice = D >> lcs, lsl = __ffs(slice) - 1;
   const uint32_t aM = smem_u32(in_M), aL = smem_u32(in_L), aO = smem_u32(in_O);
   for (int x = tid; x < G * D; x += kThreads) {
     const int c = x / G, g = x % G;
@@ -674,9 +677,9 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
         Ls += f * l_w[w * G + g];
       }
     }
-    const int owner = c / slice;
-    st_dsmem_f32(map_rank(aO + 4 * ((rank * G + g) * slice + c % slice), owner), O);
-    if (c % slice == 0) {
+    const int owner = c >> lsl, cs_ = c & (slice - 1);
+    st_dsmem_f32(map_rank(aO + 4 * ((rank * G + g) * slice + cs_), owner), O);
+    if (cs_ == 0) {
       st_dsmem_f32(map_rank(aM + 4 * (rank * G + g), owner), M);
       st_dsmem_f32(map_rank(aL + 4 * (rank * G + g), owner), Ls);
     }
@@ -692,10 +695,11 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
   const int E = G * slice;
   int TPE = 1;
   while (TPE * 2 <= CS && E * TPE * 2 <= kThreads) TPE *= 2;
+  const int ltpe = __ffs(TPE) - 1;
   for (int base = 0; base < E * TPE; base += kThreads) {
-    const int xt = base + tid, x = xt / TPE, r0 = xt % TPE;
+    const int xt = base + tid, x = xt >> ltpe, r0 = xt & (TPE - 1);
     const bool valid = x < E;
-    const int g = valid ? x / slice : 0, cl = valid ? x % slice : 0, c = rank * slice + cl;
+    const int g = valid ? x >> lsl : 0, cl = valid ? x & (slice - 1) : 0, c = rank * slice + cl;
     float M = -CUDART_INF_F;
     if (valid)
       for (int r = r0; r < CS; r += TPE) M = fmaxf(M, in_M[r * G + g]);
