@@ -6,6 +6,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import workloads as W
 from harness import Pair, tdev
 
@@ -217,3 +218,48 @@ def test_continuous_batch_full_lengths():
     wl = W.workload("cont_batch_16")
     pr = run(wl, steps=2, layout_every=2)
     assert max(pr.lens) > 65536 and min(pr.lens) < 16384
+
+
+# ---- selection fallbacks ------------------------------------------------------
+# A fused decode step has the decode kernel select the pages from a bounded
+# candidate list; these cases take the other routes, which must agree with the
+# oracle just the same.
+
+@needs_gpu
+def test_more_due_sequences_than_one_selection_launch():
+    # 70 sequences due in one step: more than one selection launch holds, so
+    # the selection kernel selects (in two launches) instead of the decode kernel
+    wl = synth(batch=70, context=300, ell=16, P=64, token_budget=64, steps=3,
+               streaming=[False, True, False, True])
+    run(wl, layout_every=3)
+
+
+@needs_gpu
+def test_tied_scores_keep_the_lowest_pages():
+    # constant keys: every page has the same bounds and every score ties, so
+    # all 1,250 candidates reach the bound (more than the bounded list holds)
+    # and the selection is the lowest pages plus the newest one
+    wl = synth(batch=1, context=20000, ell=16, P=256, streaming=[False] * 4,
+               token_budget=1024, steps=3, needle="none", needle_frac=0.0)
+    pr = Pair(wl, prefill=False)
+    rng = np.random.default_rng(5)
+    K = np.full((wl.context, wl.Hkv, wl.d), 0.5, np.float32)
+    V = rng.standard_normal((wl.context, wl.Hkv, wl.d), dtype=np.float32)
+    pr.append_seq(0, W.to_bits(K, wl.dtype), W.to_bits(V, wl.dtype))
+    for s in range(wl.steps):
+        pr.step(s)
+    k_sel = oracle.budget_pages(wl.context + 1, wl.token_budget, wl.ell)
+    for h in pr.dyn:
+        sel = np.array(pr.cache.selection(pr.gids[0], h))
+        assert np.array_equal(sel[:-1], np.arange(k_sel - 1)), sel[:8]
+    pr.check_layout()
+
+
+@needs_gpu
+def test_more_candidate_pages_than_a_fused_step_holds():
+    # 8,749 candidate pages (140,000 tokens of 16-token pages): beyond what a
+    # fused step keeps in shared memory, so the selection kernel's global-memory
+    # top-k selects
+    wl = synth(batch=1, Hq=2, Hkv=1, d=64, streaming=[False], context=140000, ell=16,
+               P=256, token_budget=4096, steps=2)
+    run(wl, layout_every=2)
