@@ -328,19 +328,29 @@ __device__ int cta_topk(const float *sc, int n, int k, uint32_t bound, int *out,
   int cnt = 0;
   if (bound != 0u) {
     // warp w sees pages 256r + 32w + lane: it appends its candidates to its
-    // own segment of the list (no atomics), keeping the count in registers
-#pragma unroll 4
-    for (int j0 = 0; j0 < n; j0 += kSelThreads) {
-      const int j = j0 + tid;
-      const uint32_t key = j < n ? score_key(__uint_as_float(m.skey[j])) : 0u;
-      const bool c = j < n && key >= bound;
-      const unsigned cm = __ballot_sync(0xffffffffu, c);
-      const int e = cnt + __popc(cm & ((1u << lane) - 1u));
-      if (c && e < kSeg) {
-        ck[e] = key;
-        ci[e] = j;
+    // own segment of the list (no atomics), keeping the count in registers.
+    // A batch of keys is read into registers first, so the shared-memory
+    // loads overlap and only the ballots and counts run in sequence.
+    constexpr int kBatch = 8;
+    for (int j0 = 0; j0 < n; j0 += kBatch * kSelThreads) {
+      uint32_t key[kBatch];
+#pragma unroll
+      for (int r = 0; r < kBatch; ++r) {
+        const int j = j0 + r * kSelThreads + tid;
+        key[r] = j < n ? score_key(__uint_as_float(m.skey[j])) : 0u;
       }
-      cnt += __popc(cm);
+#pragma unroll
+      for (int r = 0; r < kBatch; ++r) {
+        const int j = j0 + r * kSelThreads + tid;
+        const bool c = j < n && key[r] >= bound;
+        const unsigned cm = __ballot_sync(0xffffffffu, c);
+        const int e = cnt + __popc(cm & ((1u << lane) - 1u));
+        if (c && e < kSeg) {
+          ck[e] = key[r];
+          ci[e] = j;
+        }
+        cnt += __popc(cm);
+      }
     }
     if (lane == 0) m.sh[warp] = cnt;
   }
