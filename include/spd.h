@@ -238,6 +238,25 @@ spd_status spd_sparse_decode_attention_static(spd_ctx *ctx, const void *q,
                                               float *out, spd_stream stream);
 
 /*
+ * Sparse decode attention that also exports the per-head softmax statistics
+ * (the row max and row sum a split FlashAttention exports, Novita
+ * KV-sparsity article, "attention mechanism modifications").  Same outputs
+ * and step-counter effect as spd_sparse_decode_attention, plus, for every
+ * listed sequence and query head h with logits z_t = q_h . k_t / sqrt(d)
+ * over its attended positions T:
+ *   row_max[h] = max_{t in T} z_t            (natural units)
+ *   row_sum[h] = sum_{t in T} exp(z_t - row_max[h])
+ * so that log(row_sum) + row_max is the log-sum-exp of the logits.
+ *   row_max, row_sum  device [n_seqs][Hq] fp32, 4-byte aligned (caller-owned).
+ * Errors as spd_sparse_decode_attention; SPD_ERR_INVALID_ARG for a null or
+ * misaligned statistics pointer.
+ */
+spd_status spd_sparse_decode_attention_stats(spd_ctx *ctx, const void *q,
+                                             const int *seq_ids, int n_seqs,
+                                             float *out, float *row_max,
+                                             float *row_sum, spd_stream stream);
+
+/*
  * One decode step for each listed sequence: append one token (k, v device
  * [n_seqs][Hkv][d]), select if due, attend.  Same results as calling the
  * three entry points above in that order; enqueues fewer launches.

@@ -81,6 +81,8 @@ def lib():
         L.orc_streaming_tokens.restype = ci
         L.orc_attention.argtypes = [u16p, u16p, u16p, ci, ci, ci, i32p, ci, f64p]
         L.orc_attention.restype = ci
+        L.orc_softmax_stats.argtypes = [u16p, u16p, ci, ci, ci, i32p, ci, f64p, f64p]
+        L.orc_softmax_stats.restype = ci
         _lib = L
     return _lib
 
@@ -178,6 +180,19 @@ def attention(q, K, V, dtype, tokens):
                            tokens.size, out) != 0:
         raise ValueError("orc_attention: empty token set")
     return out
+
+
+def softmax_stats(q, K, dtype, tokens):
+    """fp64 (row_max [G], row_sum [G]) of the logits q . k_t / sqrt(d) over
+    rows `tokens` of K [L][d]: the max and the sum of exp(z - max)."""
+    q, K = _u16(q), _u16(K)
+    tokens = np.ascontiguousarray(tokens, dtype=np.int32)
+    G, d = q.shape
+    rm = np.empty(G, np.float64)
+    rs = np.empty(G, np.float64)
+    if lib().orc_softmax_stats(q, K, dtype_code(dtype), G, d, tokens, tokens.size, rm, rs) != 0:
+        raise ValueError("orc_softmax_stats: empty token set")
+    return rm, rs
 
 
 # ---- decode state on logical positions ------------------------------------
@@ -310,6 +325,20 @@ class OracleLayer:
         if advance:
             s.counter += 1
         return out
+
+    def softmax_stats(self, sid, q):
+        """(row_max [Hq], row_sum [Hq]) fp64 over each head's attended tokens
+        (does not advance the step counter)."""
+        s = self.seqs[sid]
+        q = _u16(q)
+        rm = np.empty(self.Hq, np.float64)
+        rs = np.empty(self.Hq, np.float64)
+        for h in range(self.Hkv):
+            T = self.tokens(sid, h)
+            a, b = softmax_stats(q[h * self.G:(h + 1) * self.G], s.K[h, :s.L], self.dtype, T)
+            rm[h * self.G:(h + 1) * self.G] = a
+            rs[h * self.G:(h + 1) * self.G] = b
+        return rm, rs
 
     def step(self, sid, q, k, v, threads=1):
         """One decode step: append one token, select if due, attend."""

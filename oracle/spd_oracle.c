@@ -316,3 +316,39 @@ int orc_attention(const uint16_t *q, const uint16_t *K, const uint16_t *V,
   free(qd);
   return 0;
 }
+
+/*
+ * Softmax statistics a split FlashAttention exports alongside its partial
+ * output (the row max and row sum; Novita KV-sparsity article, "attention
+ * mechanism modifications"), over the same logits as orc_attention:
+ *   z_i = q_g . k_{t_i} / sqrt(d),  row_max_g = max_i z_i,
+ *   row_sum_g = sum_i exp(z_i - row_max_g)          (fp64).
+ * Returns 0, or -1 if n <= 0.
+ */
+int orc_softmax_stats(const uint16_t *q, const uint16_t *K, int dtype, int G, int d,
+                      const int *tokens, int n, double *row_max, double *row_sum) {
+  if (n <= 0) return -1;
+  double scale = 1.0 / sqrt((double)d);
+  for (int g = 0; g < G; ++g) {
+    double m = -INFINITY;
+    for (int i = 0; i < n; ++i) {
+      const uint16_t *k = K + (long)tokens[i] * d;
+      double dot = 0.0;
+      for (int c = 0; c < d; ++c)
+        dot += orc_value(q[(long)g * d + c], dtype) * orc_value(k[c], dtype);
+      if (dot * scale > m) m = dot * scale;
+    }
+    double sum = 0.0;
+    for (int i = 0; i < n; ++i) {
+      const uint16_t *k = K + (long)tokens[i] * d;
+      double dot = 0.0;
+      for (int c = 0; c < d; ++c)
+        dot += orc_value(q[(long)g * d + c], dtype) * orc_value(k[c], dtype);
+      sum += exp(dot * scale - m);
+    }
+    row_max[g] = m;
+    row_sum[g] = sum;
+  }
+  return 0;
+}
+

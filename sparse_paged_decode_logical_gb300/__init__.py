@@ -82,6 +82,7 @@ def lib():
         "spd_select_pages": [vp, vp, ip, i, i, vp],
         "spd_sparse_decode_attention": [vp, vp, ip, i, vp, vp],
         "spd_sparse_decode_attention_static": [vp, vp, ip, i, vp, vp],
+        "spd_sparse_decode_attention_stats": [vp, vp, ip, i, vp, vp, vp, vp],
         "spd_decode_step": [vp, vp, vp, vp, ip, i, vp, vp],
         "spd_get_selection": [vp, i, i, ip, i, ip, vp],
         "spd_check_status": [vp, vp],
@@ -221,6 +222,14 @@ def spd_sparse_decode_attention_static(ctx, q_ptr, seq_ids, out_ptr, stream=0):
            "spd_sparse_decode_attention_static", ctx)
 
 
+def spd_sparse_decode_attention_stats(ctx, q_ptr, seq_ids, out_ptr, row_max_ptr, row_sum_ptr,
+                                      stream=0):
+    ids, n = _ids(seq_ids)
+    _check(lib().spd_sparse_decode_attention_stats(ctx, q_ptr, ids, n, out_ptr, row_max_ptr,
+                                                   row_sum_ptr, stream or None),
+           "spd_sparse_decode_attention_stats", ctx)
+
+
 def spd_decode_step(ctx, q_ptr, k_ptr, v_ptr, seq_ids, out_ptr, stream=0):
     ids, n = _ids(seq_ids)
     _check(lib().spd_decode_step(ctx, q_ptr, k_ptr, v_ptr, ids, n, out_ptr, stream or None),
@@ -339,6 +348,22 @@ class SparsePagedKVCache:
         op = self._ptr(out, (n, self.Hq, self.d), self.torch.float32)
         spd_sparse_decode_attention(self.ctx, qp, seq_ids, op, self._stream(stream))
         return out
+
+    def sparse_decode_attention_stats(self, q, seq_ids, stream=None):
+        """Attention plus the per-head softmax statistics: returns (out,
+        row_max, row_sum) with row_max = max logit, row_sum = sum of
+        exp(logit - row_max) over the attended tokens, [n][Hq] fp32."""
+        n = len(seq_ids)
+        qp = self._ptr(q, (n, self.Hq, self.d), self.dtype)
+        out = self.torch.empty((n, self.Hq, self.d), dtype=self.torch.float32, device=self.device)
+        rm = self.torch.empty((n, self.Hq), dtype=self.torch.float32, device=self.device)
+        rs = self.torch.empty((n, self.Hq), dtype=self.torch.float32, device=self.device)
+        spd_sparse_decode_attention_stats(self.ctx, qp, seq_ids,
+                                          self._ptr(out, (n, self.Hq, self.d), self.torch.float32),
+                                          self._ptr(rm, (n, self.Hq), self.torch.float32),
+                                          self._ptr(rs, (n, self.Hq), self.torch.float32),
+                                          self._stream(stream))
+        return out, rm, rs
 
     def decode_step(self, q, k, v, seq_ids, out=None, stream=None):
         n = len(seq_ids)

@@ -721,6 +721,13 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
     if (valid && r0 == 0) {
       if (nc == 1) {
         out[g * D + c] = O / Ls;
+        if (p.row_max && rank == 0 && cl == 0) {
+          // the logits' max in natural units (M is base 2, scale folded in)
+          // and the sum of exp(z - max) over the attended tokens
+          const size_t hq = (size_t)i * p.Hq + h * G + g;
+          p.row_max[hq] = M * 0.6931471805599453f;
+          p.row_sum[hq] = Ls;
+        }
       } else {
         p.part_o[(cpart * G + g) * D + c] = O;
         if (rank == 0 && cl == 0) p.part_ml[cpart * G + g] = make_float2(M, Ls);
@@ -825,6 +832,11 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
       reinterpret_cast<float4 *>(out)[x4] =
           make_float4(acc_o[j].x * inv, acc_o[j].y * inv, acc_o[j].z * inv, acc_o[j].w * inv);
     }
+  }
+  if (p.row_max && tid < G) {
+    const size_t hq = (size_t)i * p.Hq + h * G + tid;
+    p.row_max[hq] = Mh[tid] * 0.6931471805599453f;
+    p.row_sum[hq] = Lh[tid];
   }
   if (tid == 0) p.tickets[unit] = 0;
 }

@@ -121,6 +121,7 @@ struct TileDecodeParams {
   const void *q;             // [n_seqs][Hq][d]
   const void *k_new, *v_new; // [n_seqs][Hkv][d] for a fused append, else null
   float *out;                // [n_seqs][Hq][d]
+  float *row_max, *row_sum;  // [n_seqs][Hq] softmax statistics, or null
   void *k_pool, *v_pool, *meta, *stream_k, *stream_v;
   const int *page_table, *selection;
   float *part_o;

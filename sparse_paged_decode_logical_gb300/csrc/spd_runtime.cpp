@@ -44,6 +44,7 @@ struct Seq {
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3) == 0; }
 
 uint64_t splitmix64(uint64_t &s) {
   uint64_t z = (s += 0x9e3779b97f4a7c15ull);
@@ -559,7 +560,8 @@ int plan_tiles(const spd_ctx *c, TileDecodeParams &p, const int *ids, int n) {
 // sequences marked topk_pending; this launch selects their pages.
 spd_status attention_impl(spd_ctx *c, const void *q, const int *ids, int n, float *out,
                           const void *k_new, const void *v_new, cudaStream_t st,
-                          const DecodeScratch *scr = nullptr, bool fused_topk = false) {
+                          const DecodeScratch *scr = nullptr, bool fused_topk = false,
+                          float *row_max = nullptr, float *row_sum = nullptr) {
   spd_status r = ensure_device(c, st);
   if (r != SPD_OK) return r;
   const Derived &dv = c->dv;
@@ -587,6 +589,8 @@ spd_status attention_impl(spd_ctx *c, const void *q, const int *ids, int n, floa
     p.k_new = k_new ? static_cast<const char *>(k_new) + (size_t)b * kvrow * 2 : nullptr;
     p.v_new = v_new ? static_cast<const char *>(v_new) + (size_t)b * kvrow * 2 : nullptr;
     p.out = out + (size_t)b * qrow;
+    p.row_max = row_max ? row_max + (size_t)b * c->cfg.num_q_heads : nullptr;
+    p.row_sum = row_sum ? row_sum + (size_t)b * c->cfg.num_q_heads : nullptr;
     p.k_pool = c->buf.k_pool;
     p.v_pool = c->buf.v_pool;
     p.meta = c->buf.meta;
@@ -861,6 +865,18 @@ spd_status spd_sparse_decode_attention(spd_ctx *c, const void *q, const int *seq
   if (r != SPD_OK) return r;
   if ((r = check_attend_state(c, seq_ids, n_seqs, false)) != SPD_OK) return r;
   return attention_impl(c, q, seq_ids, n_seqs, out, nullptr, nullptr, (cudaStream_t)stream);
+}
+
+spd_status spd_sparse_decode_attention_stats(spd_ctx *c, const void *q, const int *seq_ids,
+                                             int n_seqs, float *out, float *row_max,
+                                             float *row_sum, spd_stream stream) {
+  if (!c) return SPD_ERR_INVALID_ARG;
+  if (!row_max || !row_sum || !aligned4(row_max) || !aligned4(row_sum))
+    return c->fail(SPD_ERR_INVALID_ARG, "row_max and row_sum must be 4-byte aligned pointers");
+  spd_status r = check_attention_call(c, q, seq_ids, n_seqs, out);
+  if (r != SPD_OK) return r;
+  return attention_impl(c, q, seq_ids, n_seqs, out, nullptr, nullptr, (cudaStream_t)stream,
+                        nullptr, false, row_max, row_sum);
 }
 
 spd_status spd_decode_step(spd_ctx *c, const void *q, const void *k, const void *v,

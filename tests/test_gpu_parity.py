@@ -263,3 +263,41 @@ def test_more_candidate_pages_than_a_fused_step_holds():
     wl = synth(batch=1, Hq=2, Hkv=1, d=64, streaming=[False], context=140000, ell=16,
                P=256, token_budget=4096, steps=2)
     run(wl, layout_every=2)
+
+
+# ---- softmax statistics export ------------------------------------------------
+# row max: fp32 logits of exact 16-bit products (<= 128 terms): relative error
+# <= 128 * 2^-24 < 1e-5 of the logit scale, so 1e-4 absolute per unit of |m|;
+# row sum: fp32 exponentials summed over <= 8K terms in a tree, 1e-3 relative.
+TOL_STAT_M, TOL_STAT_L = 1e-4, 1e-3
+
+
+def _check_stats(pr, q):
+    out, rm, rs = pr.cache.sparse_decode_attention_stats(tdev(q, pr.dt), pr.gids)
+    pr.cache.check_status()
+    out, rm, rs = (t.cpu().numpy().astype(np.float64) for t in (out, rm, rs))
+    for b in range(pr.wl.batch):
+        oid, s = pr.oids[b], pr.orc.seqs[pr.oids[b]]
+        own = {h: s.sel[h] for h in pr.dyn}
+        for h in pr.dyn:  # the oracle on the GPU's own selection
+            s.sel[h] = np.array(pr.cache.selection(pr.gids[b], h), np.int32)
+        m_o, l_o = pr.orc.softmax_stats(oid, q[b])
+        ref = pr.orc.attend(oid, q[b])
+        for h in pr.dyn:
+            s.sel[h] = own[h]
+        assert np.all(np.abs(rm[b] - m_o) <= TOL_STAT_M * np.maximum(1.0, np.abs(m_o))), b
+        assert np.all(np.abs(rs[b] - l_o) <= TOL_STAT_L * l_o), b
+        err = np.abs(out[b] - ref)
+        assert err.max() <= 2e-3 and err.mean() <= 2e-4, b
+
+
+@needs_gpu
+@pytest.mark.parametrize("which", ["synthetic", "llama3_8b_b4_32k"])
+def test_softmax_statistics_export(which):
+    wl = synth(batch=3, lens=[40, 700, 1500], steps=3) if which == "synthetic" \
+        else W.workload(which)
+    pr = Pair(wl)
+    for s in range(2):
+        pr.step(s)
+    q, _, _ = W.step_tokens(wl, 2)
+    _check_stats(pr, q)

@@ -446,3 +446,37 @@ def test_layer_step_dense_when_budget_covers_context():
     for h in range(2):
         ref = _sdpa(q[2 * h:2 * h + 2], ctx[:, h], vv[:, h], "f16")
         assert np.allclose(out[2 * h:2 * h + 2], ref, atol=1e-12)
+
+
+# ---- softmax statistics (row max, row sum) --------------------------------
+
+def test_softmax_stats_closed_forms():
+    # z = q.k / sqrt(4) = (0, 1, -1): max 1, sum 1/e + 1 + 1/e^2
+    q = f16([[2, 0, 0, 0]])
+    K = f16([[0, 0, 0, 0], [1, 0, 0, 0], [-1, 0, 0, 0]])
+    rm, rs = oracle.softmax_stats(q, K, "f16", [0, 1, 2])
+    assert rm[0] == 1.0
+    assert rs[0] == pytest.approx(math.exp(-1) + 1 + math.exp(-2), rel=1e-15)
+    # one token: the sum is exactly 1 and the max is that token's logit
+    rm, rs = oracle.softmax_stats(q, K, "f16", [2])
+    assert (rm[0], rs[0]) == (-1.0, 1.0)
+    # n identical keys: every logit equals the max, the sum is n
+    Kc = f16([[0.5, -1, 2, 0]] * 9)
+    rm, rs = oracle.softmax_stats(q, Kc, "f16", list(range(9)))
+    assert (rm[0], rs[0]) == (0.5, 9.0)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_softmax_stats_match_a_library_logsumexp(dtype):
+    # log(row_sum) + row_max is the log-sum-exp of the logits: compare with
+    # torch.logsumexp over logits computed independently (fp64 matmul)
+    r = np.random.default_rng(23)
+    L, d, G = 500, 64, 4
+    K = W.to_bits(r.standard_normal((L, d)).astype(np.float32), dtype)
+    q = W.to_bits(r.standard_normal((G, d)).astype(np.float32), dtype)
+    T = np.sort(r.choice(L, 123, replace=False)).astype(np.int32)
+    rm, rs = oracle.softmax_stats(q, K, dtype, T)
+    z = (torch.from_numpy(oracle.decode(q, dtype)) @
+         torch.from_numpy(oracle.decode(K, dtype))[T].T) / math.sqrt(d)
+    assert np.allclose(rm, z.max(dim=1).values.numpy(), rtol=0, atol=1e-12)
+    assert np.allclose(np.log(rs) + rm, torch.logsumexp(z, dim=1).numpy(), rtol=0, atol=1e-12)
