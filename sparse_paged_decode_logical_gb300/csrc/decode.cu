@@ -293,12 +293,9 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
     int *list = reinterpret_cast<int *>(stages + kTopkSmemBytes);
     const int k = s.sel_count - 1;
     const float *scr = p.scores + ((size_t)s.topk_row * p.Hd + sub) * p.score_stride;
-    const uint32_t bound =
-        s.topk_bounds > 0
-            ? min_chunk_bound(p.bounds + ((size_t)s.topk_row * p.Hd + sub) * p.bound_stride,
-                              s.topk_bounds, tm)
-            : 0u;
-    const int got = cta_topk(scr, s.topk_n, k, bound, list, p.err, tm);
+    const int got =
+        cta_topk(scr, s.topk_n, k, p.bounds + ((size_t)s.topk_row * p.Hd + sub) * p.bound_stride,
+                 s.topk_bounds, list, p.err, tm);
     __syncthreads();
     if (tid == 0) {
       list[k] = s.nL0 - 1;  // the newest page is always kept

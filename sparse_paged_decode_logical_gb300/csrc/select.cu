@@ -336,12 +336,8 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_consta
   int got;
   if (n <= kMaxKeys) {
     __shared__ __align__(16) uint8_t topk_smem[kTopkSmemBytes];
-    const TopkSmem tm = carve_topk_smem(topk_smem);
-    const uint32_t bound =
-        s.tau_m > 0 ? min_chunk_bound(p.bounds + ((size_t)i * p.Hd + hd) * p.bound_stride,
-                                      s.n_chunks, tm)
-                    : 0u;
-    got = cta_topk(scores, n, k, bound, out, p.err, tm);
+    got = cta_topk(scores, n, k, p.bounds + ((size_t)i * p.Hd + hd) * p.bound_stride,
+                   s.tau_m > 0 ? s.n_chunks : 0, out, p.err, carve_topk_smem(topk_smem));
   } else {
     got = cta_topk_global(scores, n, k, out);
   }

@@ -275,28 +275,6 @@ __device__ int topk_core(const uint32_t *keys, const int *idx, int C, int n, int
   return written;
 }
 
-// One bulk copy of n scores (16-byte aligned, readable up to n rounded up to
-// 4 floats) into m.skey.  The same result in every thread: false if the copy
-// did not land within the wait limit (the error word then says so).
-__device__ bool load_scores(const float *sc, int n, int k, int *err, const TopkSmem &m) {
-  const int tid = threadIdx.x;
-  if (tid == 0) {
-    mbar_init(m.bar, 1);
-    fence_mbar_init();
-    const uint32_t bytes = (uint32_t)((n * 4 + 15) & ~15);
-    mbar_arrive_expect_tx(m.bar, bytes);
-    bulk_load_1d(m.skey, sc, bytes, m.bar);
-    *m.nfilt = 0;
-  }
-  __syncthreads();  // the barrier is initialised before anyone polls it
-  const bool landed = mbar_wait(m.bar, 0, kCopyWaitLimit);
-  if (__syncthreads_or(!landed)) {
-    if (tid == 0) topk_set_err(err, kDevTimeout, -1, n, k);
-    return false;
-  }
-  return true;
-}
-
 // The smallest of `count` per-chunk bounds (0xffffffff: a chunk that gives
 // none), the same in every thread; 0 (no bound) if no chunk gives one.
 __device__ uint32_t min_chunk_bound(const uint32_t *b, int count, const TopkSmem &m) {
@@ -313,14 +291,43 @@ __device__ uint32_t min_chunk_bound(const uint32_t *b, int count, const TopkSmem
   return v == 0xffffffffu ? 0u : v;
 }
 
+// One bulk copy of n scores (16-byte aligned, readable up to n rounded up to
+// 4 floats) into m.skey; while it is in flight, the smallest of `nb` chunk
+// bounds (nb = 0: none) goes to *bound.  The same result in every thread:
+// false if the copy did not land within the wait limit (the error word then
+// says so).
+__device__ bool load_scores(const float *sc, int n, int k, const uint32_t *bounds, int nb,
+                            uint32_t *bound, int *err, const TopkSmem &m) {
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    mbar_init(m.bar, 1);
+    fence_mbar_init();
+    const uint32_t bytes = (uint32_t)((n * 4 + 15) & ~15);
+    mbar_arrive_expect_tx(m.bar, bytes);
+    bulk_load_1d(m.skey, sc, bytes, m.bar);
+    *m.nfilt = 0;
+  }
+  // (its barriers also make the mbarrier's initialisation visible)
+  *bound = nb > 0 ? min_chunk_bound(bounds, nb, m) : 0u;
+  if (nb == 0) __syncthreads();
+  const bool landed = mbar_wait(m.bar, 0, kCopyWaitLimit);
+  if (__syncthreads_or(!landed)) {
+    if (tid == 0) topk_set_err(err, kDevTimeout, -1, n, k);
+    return false;
+  }
+  return true;
+}
+
 // Exact top-k of n scores (1 <= k < n <= kMaxKeys) into out[0..k), ascending;
-// returns the count written.  `bound` is a key that at least k scores reach
-// (0: none known).  Every top-k key reaches it too, ties included, so only
-// the scores at or above it are candidates: up to kFilterCap of them are
-// selected as a list; more (or a bound of 0) select over all n.
-__device__ int cta_topk(const float *sc, int n, int k, uint32_t bound, int *out, int *err,
-                        const TopkSmem &m) {
-  if (!load_scores(sc, n, k, err, m)) return 0;
+// returns the count written.  The smallest of the nb chunk bounds (keys that
+// at least k scores reach; nb = 0: none) bounds the candidates: every top-k
+// key reaches it too, ties included, so only the scores at or above it are
+// candidates.  Up to kFilterCap of them are selected as a list; more (or no
+// bound) select over all n.
+__device__ int cta_topk(const float *sc, int n, int k, const uint32_t *bounds, int nb, int *out,
+                        int *err, const TopkSmem &m) {
+  uint32_t bound = 0u;
+  if (!load_scores(sc, n, k, bounds, nb, &bound, err, m)) return 0;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr int kSeg = kFilterCap / kSelWarps;  // candidates a warp may hold
   uint32_t *ck = m.ckey + warp * kSeg;
