@@ -269,6 +269,15 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
   // come after the wait.  Dependents are released only after the wait, so when
   // this kernel runs, every kernel before its immediate predecessor has
   // finished.
+  // stage barriers: set up before any wait (the cluster-scope fence that
+  // publishes them to the TMA unit stays off the path after it); they live
+  // outside the stage region, and every use follows a CTA barrier below
+  if (tid < kStages) {
+    mbar_init(&bars[tid], 1);
+    fence_mbar_init();
+    s_iss[tid] = 0;
+  }
+
   // A unit that selects its pages here follows this context's own selection
   // kernel, after the page-table flush had finished: the sequence's page
   // table is final, so it is copied to shared memory before the wait.
@@ -339,12 +348,7 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
     }
     tdesc[t] = td;
   }
-  if (tid < kStages) {
-    mbar_init(&bars[tid], 1);
-    fence_mbar_init();
-    s_iss[tid] = 0;
-  }
-  __syncthreads();
+  __syncthreads();  // descriptors written; the stage barriers set up at the start
 
   const CUtensorMap *mk = dyn ? &p.tm_k : &p.tm_sk;
   const CUtensorMap *mv = dyn ? &p.tm_v : &p.tm_sv;
