@@ -17,8 +17,9 @@
 //
 // Data movement.  The CTA's tiles stream through a ring of kStages shared-
 // memory stages: tile t lives in stage t mod kStages, filled by TMA tensor
-// loads (64 channels x 16 rows boxes, 128-byte swizzle, one mbarrier per
-// stage, its phase counting the stage's uses).  The first kStages tiles are
+// loads (one per tile of K and of V: boxes of 64 channels x 16 rows x the
+// channel halves, 128-byte swizzle; one mbarrier per stage, its phase
+// counting the stage's uses).  The first kStages tiles are
 // requested at kernel start, the later ones are prefetched into L2 then, and
 // the warp that finishes tile t refills its stage with tile t + kStages.
 // Warps take tiles from a shared counter, so a CTA with more tiles than warps
@@ -365,10 +366,10 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
     uint8_t *kd = stages + st * Gm::kTileBytes;
     uint8_t *vd = kd + Gm::kBoxes * Gm::kBoxBytes;
     mbar_arrive_expect_tx(&bars[st], Gm::kTileBytes);
-    for (int b = 0; b < Gm::kBoxes; ++b) {
-      tma_load_3d(kd + b * Gm::kBoxBytes, mk, b * 64, td.y, td.z, &bars[st]);
-      tma_load_3d(vd + b * Gm::kBoxBytes, mv, b * 64, td.y, td.z, &bars[st]);
-    }
+    // one copy per tile of K and one of V: the map's third dimension walks
+    // the 64-channel halves, which land box after box
+    tma_load_4d(kd, mk, 0, td.y, 0, td.z, &bars[st]);
+    tma_load_4d(vd, mv, 0, td.y, 0, td.z, &bars[st]);
   };
   if (lane == 0) {
     // the stage region was read and written through the generic proxy (the
@@ -380,10 +381,8 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
     for (int t = kStages + warp; t < nt; t += kWarps) {
       const TileDesc td = tdesc[t];
       if (td.n_valid <= 0) continue;
-      for (int b = 0; b < Gm::kBoxes; ++b) {
-        tma_prefetch_l2_3d(mk, b * 64, td.y, td.z);
-        tma_prefetch_l2_3d(mv, b * 64, td.y, td.z);
-      }
+      tma_prefetch_l2_4d(mk, 0, td.y, 0, td.z);
+      tma_prefetch_l2_4d(mv, 0, td.y, 0, td.z);
     }
   }
 

@@ -92,6 +92,25 @@ __device__ __forceinline__ void prefetch_l2_bulk(const void *src, uint32_t bytes
                : "memory");
 }
 
+// 4-D tiled TMA load global -> shared, completion counted on `bar`.
+__device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, int x, int y,
+                                            int z, int w, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// 4-D tiled TMA prefetch of a box into L2.
+__device__ __forceinline__ void tma_prefetch_l2_4d(const CUtensorMap *map, int x, int y, int z,
+                                                   int w) {
+  asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(z), "r"(w)
+               : "memory");
+}
+
 // Atomic add with acquire-release semantics at GPU scope (returns the old
 // value).  Issued by one thread after a CTA barrier it publishes the CTA's
 // prior writes to other CTAs and, if it observes their releases, makes

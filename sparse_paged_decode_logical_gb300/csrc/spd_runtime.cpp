@@ -234,15 +234,18 @@ spd_status encode_map(spd_ctx *c, CUtensorMap *m, void *base, uint64_t rows_per_
       return c->fail(SPD_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
     encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   }
+  // {64 channels, rows, channel halves, planes}: one box is a 16-row tile of
+  // every channel, laid out in shared memory half after half (each half 16
+  // rows of 128 bytes, swizzled), i.e. one copy per tile of K or of V
   const uint64_t d = (uint64_t)c->cfg.head_dim;
-  cuuint64_t dims[3] = {d, rows_per_plane, planes};
-  cuuint64_t strides[2] = {d * 2, rows_per_plane * d * 2};
-  cuuint32_t box[3] = {64, (cuuint32_t)kTileRows, 1};
-  cuuint32_t estr[3] = {1, 1, 1};
+  cuuint64_t dims[4] = {64, rows_per_plane, d / 64, planes};
+  cuuint64_t strides[3] = {d * 2, 128, rows_per_plane * d * 2};
+  cuuint32_t box[4] = {64, (cuuint32_t)kTileRows, (cuuint32_t)(d / 64), 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = encode(m,
                       c->cfg.dtype == SPD_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                      3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      4, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                       CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return c->fail(SPD_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
