@@ -626,7 +626,7 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
         if (s_iss[st] > 0) mbar_wait(&bars[st], (s_iss[st] - 1) & 1, kWaitLimit);
     __syncthreads();
   }
-  float *o_w = reinterpret_cast<float *>(stages);  // [W][D][G]
+  float *o_w = reinterpret_cast<float *>(stages);  // [W][G][D]
   if (g8 == 0) {
     if (2 * t4 < G) {
       m_w[warp * G + 2 * t4] = m0;
@@ -637,21 +637,17 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
       l_w[warp * G + 2 * t4 + 1] = l1;
     }
   }
-  // a lane's two heads are adjacent: one 8-byte store per channel, and a
-  // half-warp's stores cover 32 distinct banks
+  // channels contiguous per (warp, head): the push below reads 4 at a time
 #pragma unroll
   for (int m = 0; m < MT; ++m) {
     const int ch = 16 * m + g8;
     if (2 * t4 < G) {
-      if constexpr (G >= 2) {
-        *reinterpret_cast<float2 *>(&o_w[(warp * D + ch) * G + 2 * t4]) =
-            make_float2(oacc[m][0], oacc[m][1]);
-        *reinterpret_cast<float2 *>(&o_w[(warp * D + ch + 8) * G + 2 * t4]) =
-            make_float2(oacc[m][2], oacc[m][3]);
-      } else {
-        o_w[warp * D + ch] = oacc[m][0];
-        o_w[warp * D + ch + 8] = oacc[m][2];
-      }
+      o_w[(warp * G + 2 * t4) * D + ch] = oacc[m][0];
+      o_w[(warp * G + 2 * t4) * D + ch + 8] = oacc[m][2];
+    }
+    if (2 * t4 + 1 < G) {
+      o_w[(warp * G + 2 * t4 + 1) * D + ch] = oacc[m][1];
+      o_w[(warp * G + 2 * t4 + 1) * D + ch + 8] = oacc[m][3];
     }
   }
   __syncthreads();
@@ -663,22 +659,30 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
   const int lcs = __ffs(CS) - 1;
   const int slice = D >> lcs, lsl = __ffs(slice) - 1;
   const uint32_t aM = smem_u32(in_M), aL = smem_u32(in_L), aO = smem_u32(in_O);
-  for (int x = tid; x < G * D; x += kThreads) {
-    const int c = x / G, g = x % G;
+  // a thread takes 4 adjacent channels of one head: the warp weights are
+  // computed once for them, read and pushed 16 bytes at a time (a slice
+  // holds a multiple of 4 channels, so the 4 share an owner)
+  for (int x = tid; x < G * D / 4; x += kThreads) {
+    const int g = x / (D / 4), c = 4 * (x % (D / 4));
     float M = m_w[g];
 #pragma unroll
     for (int w = 1; w < kWarps; ++w) M = fmaxf(M, m_w[w * G + g]);
-    float O = 0.f, Ls = 0.f;
+    float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+    float Ls = 0.f;
     if (M != -CUDART_INF_F) {
 #pragma unroll
       for (int w = 0; w < kWarps; ++w) {
         const float f = exp2f(m_w[w * G + g] - M);
-        O += f * o_w[(w * D + c) * G + g];
-        Ls += f * l_w[w * G + g];
+        const float4 o = *reinterpret_cast<const float4 *>(&o_w[(w * G + g) * D + c]);
+        O.x = fmaf(f, o.x, O.x);
+        O.y = fmaf(f, o.y, O.y);
+        O.z = fmaf(f, o.z, O.z);
+        O.w = fmaf(f, o.w, O.w);
+        Ls = fmaf(f, l_w[w * G + g], Ls);
       }
     }
     const int owner = c >> lsl, cs_ = c & (slice - 1);
-    st_dsmem_f32(map_rank(aO + 4 * ((rank * G + g) * slice + cs_), owner), O);
+    st_dsmem_v4_f32(map_rank(aO + 4 * ((rank * G + g) * slice + cs_), owner), O);
     if (cs_ == 0) {
       st_dsmem_f32(map_rank(aM + 4 * (rank * G + g), owner), M);
       st_dsmem_f32(map_rank(aL + 4 * (rank * G + g), owner), Ls);
