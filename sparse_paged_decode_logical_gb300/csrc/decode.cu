@@ -507,7 +507,8 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
       }
 
       // q.K^T for 16 rows x 8 (padded) heads
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      // two accumulators (even and odd k-steps) halve the chain of dependent MMAs
+      float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
       {
         const int row = (lane & 7) + ((lane >> 3) & 1) * 8;
         const int chalf = lane >> 4;
@@ -518,8 +519,13 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
           const int chunk = 2 * (kk & 3) + chalf;
           uint32_t a[4];
           ldmatrix_x4(kbase + box * Gm::kBoxBytes + swz128(row, chunk), a[0], a[1], a[2], a[3]);
-          mma_16816<IsBF16<T>::v>(acc, a, qb[kk][0], qb[kk][1]);
+          if (kk & 1)
+            mma_16816<IsBF16<T>::v>(acc2, a, qb[kk][0], qb[kk][1]);
+          else
+            mma_16816<IsBF16<T>::v>(acc, a, qb[kk][0], qb[kk][1]);
         }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[e] += acc2[e];
       }
       // acc: [0] row g8 head 2t4, [1] row g8 head 2t4+1, [2] row g8+8 head 2t4, [3] row g8+8 head 2t4+1
       const bool v_lo = g8 < nv, v_hi = g8 + 8 < nv;

@@ -258,14 +258,17 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_consta
 
   // ---- score 16 pages per warp ----
   if (j0 < n) {
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    // two accumulators halve the chain of dependent MMAs
+    float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int s2 = 0; s2 < PAIRS; ++s2) {
       const uint32_t a0[4] = {ra[s2].x, rb[s2].x, ra[s2].y, rb[s2].y};
       mma_16816<IsBf<T>::v>(acc, a0, qb[2 * s2][0], qb[2 * s2][1]);
       const uint32_t a1[4] = {ra[s2].z, rb[s2].z, ra[s2].w, rb[s2].w};
-      mma_16816<IsBf<T>::v>(acc, a1, qb[2 * s2 + 1][0], qb[2 * s2 + 1][1]);
+      mma_16816<IsBf<T>::v>(acc2, a1, qb[2 * s2 + 1][0], qb[2 * s2 + 1][1]);
     }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[e] += acc2[e];
     // acc: [0],[1] page g8 heads 2t4, 2t4+1; [2],[3] page g8+8
     float s0 = -CUDART_INF_F, s1 = -CUDART_INF_F;
     if (2 * t4 < G) {
