@@ -8,7 +8,8 @@ Two layers:
 
 * ``liboracle.so`` (``spd_oracle.c``): the arithmetic, written out from the
   definitions (page min/max, page score, top-k under a budget, attended
-  token sets, two-pass fp64 softmax attention).  Thin ctypes wrappers below.
+  token sets, two-pass fp64 softmax attention, the softmax row max / row
+  sum and the per-page attention mass).  Thin ctypes wrappers below.
 * ``OracleLayer``: the per-sequence decode state on logical positions --
   length, the step counter that drives selection reuse every C steps, the
   page count at the last selection and the stored selection.  Plain Python
@@ -83,6 +84,8 @@ def lib():
         L.orc_attention.restype = ci
         L.orc_softmax_stats.argtypes = [u16p, u16p, ci, ci, ci, i32p, ci, f64p, f64p]
         L.orc_softmax_stats.restype = ci
+        L.orc_page_mass.argtypes = [u16p, u16p, ci, ci, ci, i32p, ci, ci, i32p, ci, f64p]
+        L.orc_page_mass.restype = ci
         _lib = L
     return _lib
 
@@ -193,6 +196,21 @@ def softmax_stats(q, K, dtype, tokens):
     if lib().orc_softmax_stats(q, K, dtype_code(dtype), G, d, tokens, tokens.size, rm, rs) != 0:
         raise ValueError("orc_softmax_stats: empty token set")
     return rm, rs
+
+
+def page_mass(q, K, dtype, tokens, ell, pages):
+    """fp64 [G][len(pages)]: the softmax weight of the logits q . k_t / sqrt(d)
+    over rows `tokens` of K [L][d] that falls on each logical page in `pages`
+    (tokens t with t // ell == page)."""
+    q, K = _u16(q), _u16(K)
+    tokens = np.ascontiguousarray(tokens, dtype=np.int32)
+    pages = np.ascontiguousarray(pages, dtype=np.int32)
+    G, d = q.shape
+    mass = np.empty((G, pages.size), np.float64)
+    if lib().orc_page_mass(q, K, dtype_code(dtype), G, d, tokens, tokens.size, int(ell),
+                           pages, pages.size, mass) != 0:
+        raise ValueError("orc_page_mass: empty token set")
+    return mass
 
 
 # ---- decode state on logical positions ------------------------------------
@@ -339,6 +357,26 @@ class OracleLayer:
             rm[h * self.G:(h + 1) * self.G] = a
             rs[h * self.G:(h + 1) * self.G] = b
         return rm, rs
+
+    def attended_pages(self, sid, h):
+        """Logical pages a dynamic kv head attends, ascending: the stored
+        selection plus every page created since it was made."""
+        s = self.seqs[sid]
+        nL = -(-s.L // self.ell)
+        return np.union1d(s.sel[h], np.arange(s.nL0[h] - 1, nL)).astype(np.int32)
+
+    def page_mass(self, sid, q):
+        """{dynamic kv head: (pages [n] ascending, mass [G][n] fp64)}: each
+        query head's softmax weight per attended logical page (does not
+        advance the step counter)."""
+        s = self.seqs[sid]
+        q = _u16(q)
+        res = {}
+        for h in self.dyn_heads():
+            pages = self.attended_pages(sid, h)
+            res[h] = (pages, page_mass(q[h * self.G:(h + 1) * self.G], s.K[h, :s.L], self.dtype,
+                                       self.tokens(sid, h), self.ell, pages))
+        return res
 
     def step(self, sid, q, k, v, threads=1):
         """One decode step: append one token, select if due, attend."""

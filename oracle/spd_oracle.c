@@ -352,3 +352,48 @@ int orc_softmax_stats(const uint16_t *q, const uint16_t *K, int dtype, int G, in
   return 0;
 }
 
+
+/*
+ * Per-page attention mass (the third statistic of the same export: how much
+ * of each head's softmax weight falls on each attended logical page -- the
+ * eviction-style importance a modified FlashAttention can report; Novita
+ * KV-sparsity article, "attention mechanism modifications").  Same logits as
+ * orc_attention:
+ *   z_i = q_g . k_{t_i} / sqrt(d),  w_i = exp(z_i - max z) / sum exp(z - max z),
+ *   mass[g][k] = sum of w_i over the tokens t_i of logical page pages[k]
+ *                (t_i / ell == pages[k]).
+ * A token on a page missing from `pages` counts in no entry.  fp64, two
+ * passes.  Returns 0, or -1 if n <= 0 or out of memory.
+ */
+int orc_page_mass(const uint16_t *q, const uint16_t *K, int dtype, int G, int d,
+                  const int *tokens, int n, int ell, const int *pages, int n_pages,
+                  double *mass) {
+  if (n <= 0) return -1;
+  double *w = (double *)malloc(sizeof(double) * (size_t)n);
+  if (!w) return -1;
+  const double scale = 1.0 / sqrt((double)d);
+  for (int g = 0; g < G; ++g) {
+    double m = -INFINITY;
+    for (int i = 0; i < n; ++i) {
+      const uint16_t *k = K + (long)tokens[i] * d;
+      double dot = 0.0;
+      for (int c = 0; c < d; ++c)
+        dot += orc_value(q[(long)g * d + c], dtype) * orc_value(k[c], dtype);
+      w[i] = dot * scale;
+      if (w[i] > m) m = w[i];
+    }
+    double den = 0.0;
+    for (int i = 0; i < n; ++i) {
+      w[i] = exp(w[i] - m);
+      den += w[i];
+    }
+    for (int k = 0; k < n_pages; ++k) {
+      double acc = 0.0;
+      for (int i = 0; i < n; ++i)
+        if (tokens[i] / ell == pages[k]) acc += w[i];
+      mass[(long)g * n_pages + k] = acc / den;
+    }
+  }
+  free(w);
+  return 0;
+}

@@ -480,3 +480,82 @@ def test_softmax_stats_match_a_library_logsumexp(dtype):
          torch.from_numpy(oracle.decode(K, dtype))[T].T) / math.sqrt(d)
     assert np.allclose(rm, z.max(dim=1).values.numpy(), rtol=0, atol=1e-12)
     assert np.allclose(np.log(rs) + rm, torch.logsumexp(z, dim=1).numpy(), rtol=0, atol=1e-12)
+
+
+def test_page_mass_closed_forms():
+    # z = q.k / sqrt(4) over tokens 0..5 with ell = 2 (pages 0, 1, 2):
+    # logits (0, 1, -1, 0, 1, 1); every page's mass is its share of exp(z)
+    q = f16([[2, 0, 0, 0]])
+    K = f16([[0, 0, 0, 0], [1, 0, 0, 0], [-1, 0, 0, 0], [0, 0, 0, 0], [1, 0, 0, 0],
+             [1, 0, 0, 0]])
+    e = [math.exp(z) for z in (0, 1, -1, 0, 1, 1)]
+    den = sum(e)
+    m = oracle.page_mass(q, K, "f16", list(range(6)), 2, [0, 1, 2])
+    assert m[0] == pytest.approx([(e[0] + e[1]) / den, (e[2] + e[3]) / den,
+                                  (e[4] + e[5]) / den], rel=1e-14)
+    # a page outside the attended tokens has no mass; a page missing from the
+    # list takes its tokens' weight with it
+    m = oracle.page_mass(q, K, "f16", [0, 1, 4, 5], 2, [0, 1, 2])
+    assert m[0][1] == 0.0 and m[0][0] + m[0][2] == pytest.approx(1.0, abs=1e-15)
+    m = oracle.page_mass(q, K, "f16", list(range(6)), 2, [2])
+    assert m[0][0] == pytest.approx((e[4] + e[5]) / den, rel=1e-14)
+    # one token: all the mass on its page
+    assert oracle.page_mass(q, K, "f16", [3], 2, [1]).tolist() == [[1.0]]
+
+
+def test_page_mass_equal_keys_count_tokens():
+    # identical keys: every attended token has weight 1/|T|, so a page's mass
+    # is its attended token count over |T| (a partial last page included)
+    ell, L = 16, 100
+    K = f16([[0.25, -1, 2, 0.5]] * L)
+    q = f16([[1, 2, -0.5, 3], [-2, 0, 1, 1]])
+    T = np.concatenate([np.arange(0, 20), np.arange(40, 48), np.arange(90, 100)])
+    pages = [0, 1, 2, 5, 6]
+    m = oracle.page_mass(q, K, "f16", T, ell, pages)
+    want = np.array([np.sum(T // ell == j) for j in pages]) / T.size
+    assert np.allclose(m, want[None, :], rtol=0, atol=1e-15)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_page_mass_matches_a_library_softmax(dtype):
+    # every page attended: the masses are torch.softmax over all L logits
+    # (fp64 matmul), summed over each page's ell columns
+    r = np.random.default_rng(29)
+    L, d, G, ell = 300, 64, 4, 16
+    K = W.to_bits(r.standard_normal((L, d)).astype(np.float32), dtype)
+    q = W.to_bits(r.standard_normal((G, d)).astype(np.float32), dtype)
+    nL = -(-L // ell)
+    m = oracle.page_mass(q, K, dtype, np.arange(L), ell, np.arange(nL))
+    z = (torch.from_numpy(oracle.decode(q, dtype)) @
+         torch.from_numpy(oracle.decode(K, dtype)).T) / math.sqrt(d)
+    w = torch.nn.functional.pad(torch.softmax(z, dim=1), (0, nL * ell - L))
+    assert np.allclose(m, w.reshape(G, nL, ell).sum(-1).numpy(), rtol=0, atol=1e-14)
+    assert np.allclose(m.sum(1), 1.0, rtol=0, atol=1e-13)
+
+
+def test_page_mass_of_a_decode_layer():
+    # the decode state's attended pages are the selection plus the pages
+    # created since; a planted needle page takes nearly all the mass
+    cfg = dict(num_q_heads=2, num_kv_heads=1, head_dim=64, dtype="bf16", logical_page=16,
+               streaming=[False], sink=0, window=0, token_budget=64, reuse_interval=4,
+               max_context=4096)
+    r = np.random.default_rng(31)
+    orc = oracle.OracleLayer(cfg)
+    sid = orc.new_seq()
+    L = 1000
+    Kf = r.standard_normal((L, 1, 64)).astype(np.float32) * 0.1
+    u = r.standard_normal(64).astype(np.float32)
+    Kf[320:336, 0] = 8 * u / np.linalg.norm(u)          # page 20
+    K = W.to_bits(Kf, "bf16")
+    V = W.to_bits(r.standard_normal((L, 1, 64)).astype(np.float32), "bf16")
+    orc.append(sid, K, V)
+    q = W.to_bits(np.stack([u, u]), "bf16")
+    orc.select(sid, q)
+    orc.append(sid, K[:20], V[:20])                      # 20 more tokens: a new page
+    pages, mass = orc.page_mass(sid, q)[0]
+    sel = orc.seqs[sid].sel[0]
+    assert 20 in sel and sel[-1] == 62
+    assert pages.tolist() == sorted(set(sel.tolist()) | {62, 63})
+    assert mass.shape == (2, pages.size)
+    assert np.allclose(mass.sum(1), 1.0, atol=1e-13)
+    assert np.all(mass[:, pages.tolist().index(20)] > 0.9)
