@@ -257,6 +257,42 @@ spd_status spd_sparse_decode_attention_stats(spd_ctx *ctx, const void *q,
                                              float *row_sum, spd_stream stream);
 
 /*
+ * Sparse decode attention that also exports, per dynamic kv head, the share
+ * of each query head's softmax weight that falls on each attended logical
+ * page -- the per-page attention mass that completes the statistics of the
+ * Novita KV-sparsity article's modified FlashAttention ("attention mechanism
+ * modifications"; an eviction-style importance score, and a recall
+ * diagnostic for the page selection).  Same outputs and step-counter effect
+ * as spd_sparse_decode_attention (and as spd_sparse_decode_attention_stats
+ * when row_max / row_sum are given), plus, for sequence b, dynamic kv head
+ * index hd (kv heads that are not streaming, in increasing order), query
+ * head g of its group and attended page index a:
+ *   pages[b][hd][a]        the a-th attended logical page, ascending: the
+ *                          stored selection, then every page created since
+ *                          it was taken; -1 for a >= the attended count;
+ *   page_mass[b][hd][g][a] sum over that page's attended tokens t of
+ *                          exp(z_t - m) / sum_{t' in T} exp(z_t' - m), z_t =
+ *                          q . k_t / sqrt(d); 0 for a >= the attended count.
+ * The masses of one query head sum to 1.
+ *   row_max, row_sum  device [n_seqs][Hq] fp32, or both NULL.
+ *   pages      device int32 [n_seqs][Hd][max_pages] (caller-owned).
+ *   page_mass  device fp32 [n_seqs][Hd][G][max_pages] (caller-owned).
+ *   max_pages  capacity per (sequence, dynamic head), >= 1.
+ * Pointers 4-byte aligned; with no dynamic head, pages and page_mass are not
+ * touched and may be NULL.  SPD_ERR_CAPACITY (nothing enqueued) when a
+ * sequence attends more than max_pages pages per dynamic head, or more than
+ * the library's per-head limit: the pages a selection keeps plus 64 created
+ * since it was taken.  The per-tile partial sums live in the context's
+ * scratch, so calls on one context must not overlap on different streams.
+ */
+spd_status spd_sparse_decode_attention_page_mass(spd_ctx *ctx, const void *q,
+                                                 const int *seq_ids, int n_seqs,
+                                                 float *out, float *row_max,
+                                                 float *row_sum, int *pages,
+                                                 float *page_mass, int max_pages,
+                                                 spd_stream stream);
+
+/*
  * One decode step for each listed sequence: append one token (k, v device
  * [n_seqs][Hkv][d]), select if due, attend.  Same results as calling the
  * three entry points above in that order; enqueues fewer launches.

@@ -83,6 +83,7 @@ def lib():
         "spd_sparse_decode_attention": [vp, vp, ip, i, vp, vp],
         "spd_sparse_decode_attention_static": [vp, vp, ip, i, vp, vp],
         "spd_sparse_decode_attention_stats": [vp, vp, ip, i, vp, vp, vp, vp],
+        "spd_sparse_decode_attention_page_mass": [vp, vp, ip, i, vp, vp, vp, vp, vp, i, vp],
         "spd_decode_step": [vp, vp, vp, vp, ip, i, vp, vp],
         "spd_get_selection": [vp, i, i, ip, i, ip, vp],
         "spd_check_status": [vp, vp],
@@ -230,6 +231,16 @@ def spd_sparse_decode_attention_stats(ctx, q_ptr, seq_ids, out_ptr, row_max_ptr,
            "spd_sparse_decode_attention_stats", ctx)
 
 
+def spd_sparse_decode_attention_page_mass(ctx, q_ptr, seq_ids, out_ptr, row_max_ptr, row_sum_ptr,
+                                          pages_ptr, mass_ptr, max_pages, stream=0):
+    ids, n = _ids(seq_ids)
+    _check(lib().spd_sparse_decode_attention_page_mass(ctx, q_ptr, ids, n, out_ptr,
+                                                       row_max_ptr or None, row_sum_ptr or None,
+                                                       pages_ptr or None, mass_ptr or None,
+                                                       max_pages, stream or None),
+           "spd_sparse_decode_attention_page_mass", ctx)
+
+
 def spd_decode_step(ctx, q_ptr, k_ptr, v_ptr, seq_ids, out_ptr, stream=0):
     ids, n = _ids(seq_ids)
     _check(lib().spd_decode_step(ctx, q_ptr, k_ptr, v_ptr, ids, n, out_ptr, stream or None),
@@ -364,6 +375,38 @@ class SparsePagedKVCache:
                                           self._ptr(rs, (n, self.Hq), self.torch.float32),
                                           self._stream(stream))
         return out, rm, rs
+
+    def attended_page_count(self, seq_id):
+        """Logical pages each dynamic head of the sequence attends now: the
+        stored selection plus the pages created since it was taken."""
+        info = self.seq_info(seq_id)
+        ell = self.cfg_dict["logical_page"]
+        return info["pages_kept"] + -(-info["length"] // ell) - info["pages_at_selection"]
+
+    def sparse_decode_attention_page_mass(self, q, seq_ids, max_pages=None, stream=None):
+        """Attention, the softmax statistics and the per-page attention mass of
+        the dynamic heads: returns (out [n][Hq][d], row_max [n][Hq], row_sum
+        [n][Hq], pages [n][Hd][max_pages] int32 (-1 padded), mass
+        [n][Hd][G][max_pages] fp32).  max_pages defaults to the largest
+        attended page count among the sequences."""
+        n = len(seq_ids)
+        Hd = sum(1 for x in (self.cfg_dict.get("streaming") or [False] * self.Hkv) if not x)
+        G = self.Hq // self.Hkv
+        if max_pages is None:
+            max_pages = max([self.attended_page_count(s) for s in seq_ids] + [1]) if Hd else 1
+        qp = self._ptr(q, (n, self.Hq, self.d), self.dtype)
+        t, f32 = self.torch, self.torch.float32
+        out = t.empty((n, self.Hq, self.d), dtype=f32, device=self.device)
+        rm = t.empty((n, self.Hq), dtype=f32, device=self.device)
+        rs = t.empty((n, self.Hq), dtype=f32, device=self.device)
+        pages = t.empty((n, Hd, max_pages), dtype=t.int32, device=self.device)
+        mass = t.empty((n, Hd, G, max_pages), dtype=f32, device=self.device)
+        spd_sparse_decode_attention_page_mass(
+            self.ctx, qp, seq_ids, self._ptr(out, (n, self.Hq, self.d), f32),
+            self._ptr(rm, (n, self.Hq), f32), self._ptr(rs, (n, self.Hq), f32),
+            pages.data_ptr() if Hd else 0, mass.data_ptr() if Hd else 0, max_pages,
+            self._stream(stream))
+        return out, rm, rs, pages, mass
 
     def decode_step(self, q, k, v, seq_ids, out=None, stream=None):
         n = len(seq_ids)

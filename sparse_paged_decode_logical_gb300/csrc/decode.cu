@@ -1,881 +1,34 @@
-// Split-K sparse decode attention for sm_103a ("LServe long-sequence LLM
-// serving system", section 2.1: one unified kernel for streaming and dynamic
-// heads; section 3.2: streaming heads read their recent tokens through
-// shared memory).
-//
-// Work list.  A unit is (sequence, kv head).  Its attended tokens are cut
-// into tiles of 16 rows:
-//   dynamic head   the selected logical pages plus the pages created since the
-//                  selection, each page ell/16 tiles (the newest page only as
-//                  many as it holds tokens);
-//   streaming head three runs of ring-buffer slots -- sink [0, min(S, L)),
-//                  the window's slots up to the ring's end, and its wrapped
-//                  remainder -- each run tiled from its start.
-// A unit is split over nc clusters of CS CTAs (a thread-block cluster; CS and
-// the CTAs' tile ranges are chosen by the host so the launch fills the GPU);
-// a CTA ("item") takes a contiguous range of the unit's tiles.
-//
-// Data movement.  The CTA's tiles stream through a ring of kStages shared-
-// memory stages: tile t lives in stage t mod kStages, filled by TMA tensor
-// loads (one per tile of K and of V: boxes of 64 channels x 16 rows x the
-// channel halves, 128-byte swizzle; one mbarrier per stage, its phase
-// counting the stage's uses).  The first kStages tiles are
-// requested at kernel start, the later ones are prefetched into L2 then, and
-// the warp that finishes tile t refills its stage with tile t + kStages.
-// Warps take tiles from a shared counter, so a CTA with more tiles than warps
-// spreads the extra ones over whichever warps are free.  K/V bytes are read
-// from HBM once.
-//
-// Math (per warp and tile, all G query heads of the kv head at once):
-//   q.K^T   mma.sync m16n8k16, A = K tile rows (ldmatrix from the swizzled
-//           tile), B = q^T in registers (heads padded to 8 columns), fp32
-//           accumulate -- the products of 16-bit inputs are exact;
-//   softmax online, in fp32, base 2 with log2(e)/sqrt(d) folded in;
-//   P.V     mma.sync m16n8k16 as O^T = V^T P^T: A = V tile (ldmatrix.trans),
-//           B = P^T with the 16 tokens as k and the heads as the 8 columns;
-//           P is split into a 16-bit high part and the 16-bit rounding of
-//           the rest, two mma each, so the weights carry ~2^-16 relative
-//           error instead of 2^-9 (fp32 accumulate).
-// Merge.  The 8 warps merge in shared memory into the CTA's (m, l, o).  The
-// CTAs of a cluster then merge over distributed shared memory: every CTA
-// pushes each channel slice of its (m, l, o) into the inbox of the CTA that
-// owns that slice (remote shared-memory stores), and after one cluster
-// barrier each CTA combines its slice locally -- the row max / row sum export
-// of the Novita KV-sparsity article's modified FlashAttention ("attention
-// mechanism modifications").  When a
-// unit has several clusters (nc > 1), their results meet in global memory:
-// the last cluster to finish (atomic ticket, no waiting) merges them.
-//
-// Fused append (decode step).  The CTA that owns a unit's newest token also
-// appends it: the row is written to the pool / ring, patched into the
-// staged tile, and folded into the logical page's key min/max.
-#include <cuda_bf16.h>
-#include <cuda_fp16.h>
-#include <math_constants.h>
-
-#include "ptx.cuh"
-#include "spd_internal.h"
-#include "topk.cuh"
+// Split-K sparse decode attention: the plain kernel's instances, the cluster
+// sizes they can be launched with, and the launch entry (the kernel itself is
+// in decode_kernel.cuh).
+#include "decode_kernel.cuh"
 
 namespace spd {
 namespace {
-
-constexpr int kRows = 16;                  // rows per tile (one mma M tile)
-constexpr int kWarps = 8;                  // 256 threads
-constexpr int kThreads = kWarps * 32;
-constexpr int kStages = 12;                // shared-memory stage ring
-constexpr int kMaxDesc = 256;              // tiles one CTA may take
-constexpr uint32_t kWaitLimit = 1u << 24;  // bounded mbarrier polls
-
-template <int D>
-struct Geo {
-  static constexpr int kBoxes = D / 64;                      // 64-channel boxes per row
-  static constexpr int kBoxBytes = kRows * 128;              // one box: 16 rows x 128 B
-  static constexpr int kTileBytes = 2 * kBoxes * kBoxBytes;  // K boxes then V boxes
-  static constexpr int kCPL = D / 32;                        // channels per lane in P.V
-};
-
-template <int G>
-struct GP {
-  static constexpr int v = G < 4 ? 4 : G;  // padded head stride of the P buffer
-};
-
-struct TileDesc {
-  int y, z;      // TMA coordinates (row, plane) of the tile's first row
-  int n_valid;   // rows holding attended tokens (0: skip)
-  int pad;
-};
-
-// Shared memory: a fixed region (stage barriers, tile descriptors, P and
-// rescale buffers, per-warp and per-CTA row max / sum / output, flags), then
-// the stages at a 1024-byte aligned offset.  After the tile loop the stage
-// region holds the warp-merge buffer and later the global-merge buffers.
-template <int D, int G>
-struct Smem {
-  static constexpr int kBars = 0;                                      // uint64 [kStages]
-  static constexpr int kDesc = kBars + kStages * 8;                    // TileDesc [kMaxDesc]
-  static constexpr int kP = kDesc + kMaxDesc * (int)sizeof(TileDesc);  // float [W][16][GP]
-  static constexpr int kC = kP + kWarps * kRows * GP<G>::v * 4;        // float [W][GP]
-  static constexpr int kML = kC + kWarps * GP<G>::v * 4;               // float [2][W][G]
-  // inbox: what the cluster's CTAs send this CTA: M[16][G], L[16][G] and
-  // O[16 ranks][G][D / CS] (= G * D floats for any CS)
-  static constexpr int kInbox = (kML + 2 * kWarps * G * 4 + 15) / 16 * 16;
-  static constexpr int kFlag = kInbox + (32 * G + G * D) * 4;          // int [4 + kStages]
-  static constexpr int kTopkBar = (kFlag + (4 + kStages) * 4 + 7) / 8 * 8;  // uint64
-  static constexpr int kTiles = (kTopkBar + 8 + 1023) / 1024 * 1024;
-  static constexpr int kStageRegion = kStages * Geo<D>::kTileBytes;
-  static constexpr int kMergeRegion = kWarps * G * D * 4;              // o of every warp
-  static constexpr int kCombineRegion = 256 * G * 12 + 64;             // (m, l), weights
-  // before the tiles of a fused selection step: the top-k buffers, then the
-  // unit's selected pages
-  static constexpr int kTopkRegion = kTopkSmemBytes + kFusedMaxSel * 4;
-  static constexpr int kPtCache = 2048;                  // page-table entries cached with it
-  static constexpr int kPtCacheOff = kTopkRegion;        // bytes into the stage region
-  static constexpr int kR1 = kStageRegion > kMergeRegion ? kStageRegion : kMergeRegion;
-  static constexpr int kR2 = kCombineRegion > kTopkRegion + kPtCache * 4
-                                 ? kCombineRegion
-                                 : kTopkRegion + kPtCache * 4;
-  static constexpr int kRegion = kR1 > kR2 ? kR1 : kR2;
-  static constexpr int kAlloc = kTiles + kRegion + 1024;  // + alignment slack
-};
-
-template <typename T> struct IsBF16 { static constexpr bool v = false; };
-template <> struct IsBF16<__nv_bfloat16> { static constexpr bool v = true; };
-
-template <typename T>
-__device__ __forceinline__ float tof(T x);
-template <> __device__ __forceinline__ float tof(__half x) { return __half2float(x); }
-template <> __device__ __forceinline__ float tof(__nv_bfloat16 x) { return __bfloat162float(x); }
-
-template <typename T> struct Cvt;
-template <> struct Cvt<__half> {
-  static __device__ __forceinline__ __half from(float x) { return __float2half_rn(x); }
-};
-template <> struct Cvt<__nv_bfloat16> {
-  static __device__ __forceinline__ __nv_bfloat16 from(float x) { return __float2bfloat16_rn(x); }
-};
-
-__device__ __forceinline__ void set_err(int *err, int code, int a, int b, int c) {
-  if (atomicCAS(err, 0, code) == 0) {
-    err[1] = a;
-    err[2] = b;
-    err[3] = c;
-  }
-}
-
-// Bounded wait until another warp of the CTA has counted more than `u` uses
-// of a stage (its load for use u is issued).
-__device__ __forceinline__ bool wait_issued(const int *count, int u, uint32_t limit) {
-  for (uint32_t i = 0; i < limit; ++i)
-    if (*reinterpret_cast<const volatile int *>(count) > u) return true;
-  return false;
-}
-
-// Byte offset, inside a tile half (K or V), of channel `ch` of row `r`.
-template <int D>
-__device__ __forceinline__ uint32_t chan_off(int r, int ch) {
-  return (uint32_t)((ch >> 6) * Geo<D>::kBoxBytes) + swz128(r, (ch & 63) >> 3) +
-         (uint32_t)((ch & 7) * 2);
-}
-
-template <typename T, int D, int G>
-__global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_constant__ TileDecodeParams p) {
-  using Gm = Geo<D>;
-  using Sm = Smem<D, G>;
-  constexpr int CPL = Gm::kCPL;  // channels per lane of the fused append
-  constexpr int GPAD = GP<G>::v;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t *smem = reinterpret_cast<uint8_t *>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t *stages = smem + Sm::kTiles;
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Sm::kBars);
-  TileDesc *tdesc = reinterpret_cast<TileDesc *>(smem + Sm::kDesc);
-  float *P_all = reinterpret_cast<float *>(smem + Sm::kP);
-  float *m_w = reinterpret_cast<float *>(smem + Sm::kML);
-  float *l_w = m_w + kWarps * G;
-  float *in_M = reinterpret_cast<float *>(smem + Sm::kInbox);  // [rank][G]
-  float *in_L = in_M + 16 * G;                                   // [rank][G]
-  float *in_O = in_L + 16 * G;                                   // [rank][G][slice]
-  int *s_flag = reinterpret_cast<int *>(smem + Sm::kFlag);  // [1] a wait gave up, [2] next tile
-  int *s_iss = s_flag + 4;                                   // loads issued per stage
-
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  cluster_arrive_relaxed();  // paired with the wait before the first remote store
-  if (tid == 0) {
-    prefetch_tmap(&p.tm_k);
-    prefetch_tmap(&p.tm_v);
-    prefetch_tmap(&p.tm_sk);
-    prefetch_tmap(&p.tm_sv);
-    s_flag[1] = 0;  // set if a bounded wait gives up
-    s_flag[2] = kWarps;  // tiles 0..kWarps-1 go to warps 0..kWarps-1
-  }
-  const int item = blockIdx.x;
-  int i = 0;
-  while (i + 1 < p.n_seqs && p.seqs[i + 1].item_off <= item) ++i;
-  const TileSeq s = p.seqs[i];
-  int local = item - s.item_off;
-  const bool dyn = local < p.Hd * s.ns_dyn;
-  int sub, split, ns, tpi, unit_item0;
-  if (dyn) {
-    sub = local / s.ns_dyn;
-    split = local % s.ns_dyn;
-    ns = s.ns_dyn;
-    tpi = s.tpi_dyn;
-    unit_item0 = s.item_off + sub * s.ns_dyn;
-  } else {
-    local -= p.Hd * s.ns_dyn;
-    sub = local / s.ns_str;
-    split = local % s.ns_str;
-    ns = s.ns_str;
-    tpi = s.tpi_str;
-    unit_item0 = s.item_off + p.Hd * s.ns_dyn + sub * s.ns_str;
-  }
-  const int CS = p.cluster;        // CTAs per cluster (units' item counts are multiples)
-  const int rank = split % CS;     // == %cluster_ctarank: clusters start at multiples of CS
-  const int ci = split / CS;       // cluster index within the unit
-  const int nc = ns / CS;          // clusters of this unit
-  const int h = dyn ? p.dyn_kv[sub] : p.str_kv[sub];
-  const int L = s.L;
-
-  // ---- unit geometry ----
-  int n_tiles, nL = 0, n_att = 0, tpp = 0;
-  int run_start[3] = {0, 0, 0}, run_len[3] = {0, 0, 0}, run_tiles[3] = {0, 0, 0};
-  if (dyn) {
-    nL = (L + p.ell - 1) / p.ell;
-    n_att = s.sel_count + nL - s.nL0;
-    tpp = p.ell / kRows;
-    const int last_rows = (L - 1) % p.ell + 1;
-    n_tiles = (n_att - 1) * tpp + (last_rows + kRows - 1) / kRows;
-  } else {
-    run_len[0] = min(p.S, L);
-    if (L > p.S) {
-      const int w0 = max(p.S, L - p.W);
-      const int n_win = L - w0;
-      const int a0 = (w0 - p.S) % p.W;
-      run_start[1] = p.S + a0;
-      run_len[1] = min(n_win, p.W - a0);
-      run_start[2] = p.S;
-      run_len[2] = n_win - run_len[1];
-    }
-    for (int r = 0; r < 3; ++r) run_tiles[r] = (run_len[r] + kRows - 1) / kRows;
-    n_tiles = run_tiles[0] + run_tiles[1] + run_tiles[2];
-  }
-  const int tile0 = split * tpi;
-  const int nt = min(kMaxDesc, max(0, min(n_tiles, tile0 + tpi) - tile0));
-  const bool owns_newest = nt > 0 && tile0 + nt == n_tiles;
-  const bool do_append = p.k_new != nullptr && owns_newest;
-  // (a unit that selects its pages here reads this step's scores: never early)
-  const bool early = ((p.early >> (dyn ? 0 : 1)) & 1) && !(dyn && s.topk_n > 0);
-  // bit 2: the previous kernel is this context's own selection or page-table
-  // kernel, which writes nothing a streaming unit reads; q is final once that
-  // kernel runs (it waited for its own predecessor before releasing this one)
-  const bool skip_wait = !dyn && ((p.early >> 2) & 1);
-  if (tid == 0) {
-    // q (and the new token) start their way into L2 now; they are read only
-    // after the wait, and L2 is coherent, so this is a hint and nothing more
-    prefetch_l2_bulk(static_cast<const uint16_t *>(p.q) + ((size_t)i * p.Hq + h * G) * D,
-                     G * D * 2);
-    if (do_append) {
-      const size_t row = ((size_t)i * p.Hkv + h) * D;
-      prefetch_l2_bulk(static_cast<const uint16_t *>(p.k_new) + row, D * 2);
-      prefetch_l2_bulk(static_cast<const uint16_t *>(p.v_new) + row, D * 2);
-    }
-  }
-
-  // Everything above used only the parameter block.  The KV cache (page
-  // table, selection, pools) is read next: before the wait for the previous
-  // kernel on the stream when the host knows that kernel cannot have written
-  // the KV this unit reads (bit 0 of p.early for dynamic units, bit 1 for
-  // streaming ones), after it otherwise.  q, the new token and every write
-  // come after the wait.  Dependents are released only after the wait, so when
-  // this kernel runs, every kernel before its immediate predecessor has
-  // finished.
-  // stage barriers: set up before any wait (the cluster-scope fence that
-  // publishes them to the TMA unit stays off the path after it); they live
-  // outside the stage region, and every use follows a CTA barrier below
-  if (tid < kStages) {
-    mbar_init(&bars[tid], 1);
-    fence_mbar_init();
-    s_iss[tid] = 0;
-  }
-
-  // A unit that selects its pages here follows this context's own selection
-  // kernel, after the page-table flush had finished: the sequence's page
-  // table is final, so it is copied to shared memory before the wait.
-  int *pt_s = nullptr;
-  if (dyn && s.topk_n > 0 && p.max_pp <= Sm::kPtCache) {
-    pt_s = reinterpret_cast<int *>(stages + Sm::kPtCacheOff);
-    const int *row = p.page_table + (size_t)s.slot * p.max_pp;
-    for (int x = tid; x < p.max_pp; x += kThreads) pt_s[x] = row[x];
-  }
-  if (!early) {
-    if (!skip_wait) pdl_wait();
-    pdl_launch_dependents();
-  }
-
-  // ---- a fused selection step: this CTA selects the unit's pages ----
-  // (every CTA of the unit computes the same selection from the same scores;
-  // the stage region holds the work and the result until the tiles arrive)
-  const int *sel_s = nullptr;
-  if (dyn && s.topk_n > 0) {
-    TopkSmem tm = carve_topk_smem(stages);
-    tm.bar = reinterpret_cast<uint64_t *>(smem + Sm::kTopkBar);  // never repurposed
-    int *list = reinterpret_cast<int *>(stages + kTopkSmemBytes);
-    const int k = s.sel_count - 1;
-    const float *scr = p.scores + ((size_t)s.topk_row * p.Hd + sub) * p.score_stride;
-    const int got =
-        cta_topk(scr, s.topk_n, k, p.bounds + ((size_t)s.topk_row * p.Hd + sub) * p.bound_stride,
-                 s.topk_bounds, list, p.err, tm);
-    __syncthreads();
-    if (tid == 0) {
-      list[k] = s.nL0 - 1;  // the newest page is always kept
-      if (got != k) set_err(p.err, kDevTopkCount, s.slot, sub, got);
-    }
-    __syncthreads();
-    if (split == 0) {  // one CTA of the unit stores it for the steps that reuse it
-      int *gsel = const_cast<int *>(p.selection) + ((size_t)s.slot * p.Hd + sub) * p.ksel_max;
-      for (int t = tid; t < s.sel_count; t += kThreads) gsel[t] = list[t];
-    }
-    sel_s = list;
-  }
-
-  // ---- tile descriptors (threads in parallel), stage barriers ----
-  for (int t = tid; t < nt; t += kThreads) {
-    const int tau = tile0 + t;
-    TileDesc td{0, 0, 0, 0};
-    if (dyn) {
-      const int pi = tau / tpp, st = tau % tpp;
-      const int *sel = sel_s ? sel_s : p.selection + ((size_t)s.slot * p.Hd + sub) * p.ksel_max;
-      const int j = pi < s.sel_count ? sel[pi] : s.nL0 + (pi - s.sel_count);
-      const int blk = j / p.R;
-      if (j < 0 || j >= nL || blk >= p.max_pp) {
-        set_err(p.err, kDevBadSelection, s.slot, sub, j);
-      } else {
-        const int phys = pt_s ? pt_s[blk] : p.page_table[(size_t)s.slot * p.max_pp + blk];
-        if (phys < 0 || phys >= p.num_phys) {
-          set_err(p.err, kDevBadPhys, s.slot, blk, phys);
-        } else {
-          td.y = (j % p.R) * p.ell + st * kRows;
-          td.z = phys * p.Hd + sub;
-          td.n_valid = min(kRows, L - (j * p.ell + st * kRows));
-        }
-      }
-    } else {
-      int r = 0, k = tau;
-      while (r < 2 && k >= run_tiles[r]) k -= run_tiles[r++];
-      td.y = ((s.slot * p.Hs + sub) * (p.S + p.W)) + run_start[r] + k * kRows;
-      td.z = 0;
-      td.n_valid = min(kRows, run_len[r] - k * kRows);
-    }
-    tdesc[t] = td;
-  }
-  __syncthreads();  // descriptors written; the stage barriers set up at the start
-
-  const CUtensorMap *mk = dyn ? &p.tm_k : &p.tm_sk;
-  const CUtensorMap *mv = dyn ? &p.tm_v : &p.tm_sv;
-  // stage s: K boxes, then V boxes; tile t uses stage t % kStages, and its
-  // use number t / kStages is the phase its waiter checks
-  auto issue = [&](int t) {
-    const int st = t % kStages;
-    const TileDesc td = tdesc[t];
-    atomicAdd(&s_iss[st], 1);
-    if (td.n_valid <= 0) {  // nothing to load: complete the phase anyway
-      mbar_arrive_expect_tx(&bars[st], 0);
-      return;
-    }
-    uint8_t *kd = stages + st * Gm::kTileBytes;
-    uint8_t *vd = kd + Gm::kBoxes * Gm::kBoxBytes;
-    mbar_arrive_expect_tx(&bars[st], Gm::kTileBytes);
-    // one copy per tile of K and one of V: the map's third dimension walks
-    // the 64-channel halves, which land box after box
-    tma_load_4d(kd, mk, 0, td.y, 0, td.z, &bars[st]);
-    tma_load_4d(vd, mv, 0, td.y, 0, td.z, &bars[st]);
-  };
-  if (lane == 0) {
-    // the stage region was read and written through the generic proxy (the
-    // selection above): order that before the TMA writes
-    if (sel_s) fence_proxy_async_smem();
-    for (int t = warp; t < min(nt, kStages); t += kWarps) issue(t);
-    // the later tiles start their way from HBM into L2 now; their stage
-    // refills then read L2
-    for (int t = kStages + warp; t < nt; t += kWarps) {
-      const TileDesc td = tdesc[t];
-      if (td.n_valid <= 0) continue;
-      tma_prefetch_l2_4d(mk, 0, td.y, 0, td.z);
-      tma_prefetch_l2_4d(mv, 0, td.y, 0, td.z);
-    }
-  }
-
-  if (early) {
-    if (!skip_wait) pdl_wait();
-    pdl_launch_dependents();
-  }
-
-  // ---- q^T fragments (B operand), heads padded to 8 columns ----
-  const int g8 = lane >> 2, t4 = lane & 3;
-  uint32_t qb[D / 16][2];
-  {
-    const uint32_t *qp = reinterpret_cast<const uint32_t *>(
-        reinterpret_cast<const uint16_t *>(p.q) + ((size_t)i * p.Hq + h * G) * D);
-#pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-      if (g8 < G) {
-        qb[kk][0] = qp[(g8 * D + kk * 16 + 2 * t4) / 2];
-        qb[kk][1] = qp[(g8 * D + kk * 16 + 2 * t4 + 8) / 2];
-      } else {
-        qb[kk][0] = qb[kk][1] = 0u;
-      }
-    }
-  }
-
-  // ---- per-warp online softmax over its tiles ----
-  float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F, l0 = 0.f, l1 = 0.f;  // heads 2t4, 2t4+1
-  // O^T accumulators: m-tile m holds channels 16m + g8 (and + 8) x heads
-  // 2t4, 2t4 + 1 -- the two heads whose running max this lane tracks
-  constexpr int MT = D / 16;
-  float oacc[MT][4];
-#pragma unroll
-  for (int m = 0; m < MT; ++m)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) oacc[m][e] = 0.f;
-  float *Pw = P_all + warp * kRows * GPAD;
-  const float sc = p.scale_log2;
-
-  for (int t = warp; t < nt;) {
-    const TileDesc td = tdesc[t];
-    const int st = t % kStages, u = t / kStages;  // stage and its use number
-    uint8_t *kt = stages + st * Gm::kTileBytes;
-    uint8_t *vt = kt + Gm::kBoxes * Gm::kBoxBytes;
-    // Use u of the stage is loaded only after use u-1 was consumed, so the
-    // barrier's parity identifies it once the load is known to be issued
-    // (a wait on the parity alone could match use u-2).  Every tile is waited
-    // for, empty ones too, so no copy is in flight when the loop ends.
-    if (!wait_issued(&s_iss[st], u, kWaitLimit) || !mbar_wait(&bars[st], u & 1, kWaitLimit)) {
-      if (lane == 0) {
-        set_err(p.err, kDevTimeout, s.slot, h, t);
-        s_flag[1] = 1;
-      }
-      break;
-    }
-    if (td.n_valid > 0) {
-      const int nv = td.n_valid;
-
-      if (do_append && t == nt - 1) {
-        // the newest token is row nv-1 of the unit's last tile
-        const int r = nv - 1;
-        const int cb = lane * CPL;
-        const size_t src = ((size_t)i * p.Hkv + h) * D + cb;
-        const uint16_t *kn = reinterpret_cast<const uint16_t *>(p.k_new) + src;
-        const uint16_t *vn = reinterpret_cast<const uint16_t *>(p.v_new) + src;
-        uint16_t kx[CPL], vx[CPL];
-#pragma unroll
-        for (int e = 0; e < CPL; ++e) {
-          kx[e] = kn[e];
-          vx[e] = vn[e];
-        }
-#pragma unroll
-        for (int e = 0; e < CPL; ++e) {
-          *reinterpret_cast<uint16_t *>(kt + chan_off<D>(r, cb + e)) = kx[e];
-          *reinterpret_cast<uint16_t *>(vt + chan_off<D>(r, cb + e)) = vx[e];
-        }
-        size_t grow;
-        uint16_t *kg, *vg;
-        if (dyn) {
-          grow = ((size_t)td.z * p.P + td.y + r) * D + cb;
-          kg = static_cast<uint16_t *>(p.k_pool) + grow;
-          vg = static_cast<uint16_t *>(p.v_pool) + grow;
-        } else {
-          grow = ((size_t)td.y + r) * D + cb;
-          kg = static_cast<uint16_t *>(p.stream_k) + grow;
-          vg = static_cast<uint16_t *>(p.stream_v) + grow;
-        }
-#pragma unroll
-        for (int e = 0; e < CPL; ++e) {
-          kg[e] = kx[e];
-          vg[e] = vx[e];
-        }
-        if (dyn) {
-          const int j = nL - 1;
-          uint16_t *mrow = static_cast<uint16_t *>(p.meta) +
-                           ((size_t)td.z * p.R + (j % p.R)) * 2 * D + cb;
-          const bool fresh = (L - 1) % p.ell == 0;
-#pragma unroll
-          for (int e = 0; e < CPL; ++e) {
-            uint16_t bmin = kx[e], bmax = kx[e];
-            if (!fresh) {
-              const uint16_t omin = mrow[e], omax = mrow[D + e];
-              const float x = tof(*reinterpret_cast<const T *>(&kx[e]));
-              bmin = x < tof(*reinterpret_cast<const T *>(&omin)) ? kx[e] : omin;
-              bmax = x > tof(*reinterpret_cast<const T *>(&omax)) ? kx[e] : omax;
-            }
-            mrow[e] = bmin;
-            mrow[D + e] = bmax;
-          }
-        }
-        __syncwarp();
-      }
-      if (nv < kRows) {
-        // rows past the tile's attended tokens: zero V so the unrolled P.V
-        // below adds exactly 0 for them (their weights are 0 as well)
-        for (int x = lane; x < (kRows - nv) * 8 * Gm::kBoxes; x += 32) {
-          const int box = x / ((kRows - nv) * 8), rem = x % ((kRows - nv) * 8);
-          const int r = nv + rem / 8, ch = rem % 8;
-          *reinterpret_cast<uint4 *>(vt + box * Gm::kBoxBytes + r * 128 + ch * 16) =
-              make_uint4(0, 0, 0, 0);
-        }
-        __syncwarp();
-      }
-
-      // q.K^T for 16 rows x 8 (padded) heads
-      // two accumulators (even and odd k-steps) halve the chain of dependent MMAs
-      float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
-      {
-        const int row = (lane & 7) + ((lane >> 3) & 1) * 8;
-        const int chalf = lane >> 4;
-        const uint32_t kbase = smem_u32(kt);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const int box = kk >> 2;
-          const int chunk = 2 * (kk & 3) + chalf;
-          uint32_t a[4];
-          ldmatrix_x4(kbase + box * Gm::kBoxBytes + swz128(row, chunk), a[0], a[1], a[2], a[3]);
-          if (kk & 1)
-            mma_16816<IsBF16<T>::v>(acc2, a, qb[kk][0], qb[kk][1]);
-          else
-            mma_16816<IsBF16<T>::v>(acc, a, qb[kk][0], qb[kk][1]);
-        }
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc[e] += acc2[e];
-      }
-      // acc: [0] row g8 head 2t4, [1] row g8 head 2t4+1, [2] row g8+8 head 2t4, [3] row g8+8 head 2t4+1
-      const bool v_lo = g8 < nv, v_hi = g8 + 8 < nv;
-      const float z0 = v_lo ? acc[0] * sc : -CUDART_INF_F;
-      const float z1 = v_lo ? acc[1] * sc : -CUDART_INF_F;
-      const float z2 = v_hi ? acc[2] * sc : -CUDART_INF_F;
-      const float z3 = v_hi ? acc[3] * sc : -CUDART_INF_F;
-      float mx0 = fmaxf(z0, z2), mx1 = fmaxf(z1, z3);
-#pragma unroll
-      for (int off = 4; off < 32; off <<= 1) {
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-      }
-      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-      const float c0 = exp2f(m0 - mn0), c1 = exp2f(m1 - mn1);
-      const float p0 = exp2f(z0 - mn0), p1 = exp2f(z1 - mn1);
-      const float p2 = exp2f(z2 - mn0), p3 = exp2f(z3 - mn1);
-      l0 = l0 * c0 + p0 + p2;
-      l1 = l1 * c1 + p1 + p3;
-      m0 = mn0;
-      m1 = mn1;
-      const int h0 = 2 * t4, h1 = 2 * t4 + 1;
-      if (h0 < G) {
-        Pw[g8 * GPAD + h0] = p0;
-        Pw[(g8 + 8) * GPAD + h0] = p2;
-      }
-      if (h1 < G) {
-        Pw[g8 * GPAD + h1] = p1;
-        Pw[(g8 + 8) * GPAD + h1] = p3;
-      }
-      __syncwarp();
-
-      // P.V on tensor cores: rescale, then O^T += V^T (P_hi + P_lo)^T
-#pragma unroll
-      for (int m = 0; m < MT; ++m) {
-        oacc[m][0] *= c0;
-        oacc[m][1] *= c1;
-        oacc[m][2] *= c0;
-        oacc[m][3] *= c1;
-      }
-      uint32_t bh0, bh1, bl0, bl1;  // B = P^T: k = tokens 2t4.. / 2t4+8.., n = head g8
-      {
-        float pv[4] = {0.f, 0.f, 0.f, 0.f};
-        if (g8 < G) {
-          pv[0] = Pw[(2 * t4) * GPAD + g8];
-          pv[1] = Pw[(2 * t4 + 1) * GPAD + g8];
-          pv[2] = Pw[(2 * t4 + 8) * GPAD + g8];
-          pv[3] = Pw[(2 * t4 + 9) * GPAD + g8];
-        }
-        uint16_t hi[4], lo[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const T th = Cvt<T>::from(pv[e]);
-          hi[e] = *reinterpret_cast<const uint16_t *>(&th);
-          const T tl = Cvt<T>::from(pv[e] - tof(th));
-          lo[e] = *reinterpret_cast<const uint16_t *>(&tl);
-        }
-        bh0 = (uint32_t)hi[0] | ((uint32_t)hi[1] << 16);
-        bh1 = (uint32_t)hi[2] | ((uint32_t)hi[3] << 16);
-        bl0 = (uint32_t)lo[0] | ((uint32_t)lo[1] << 16);
-        bl1 = (uint32_t)lo[2] | ((uint32_t)lo[3] << 16);
-      }
-      {
-        // A = V^T for m-tile m: matrix j of ldmatrix.x4.trans takes token rows
-        // (lane & 7) + 8 * (j >> 1) and channel chunk 2m + (j & 1)
-        const int j = lane >> 3;
-        const int row = (lane & 7) + 8 * (j >> 1);
-        const uint32_t vbase = smem_u32(vt);
-#pragma unroll
-        for (int m = 0; m < MT; ++m) {
-          const int box = m >> 2;
-          const int chunk = 2 * (m & 3) + (j & 1);
-          uint32_t a[4];
-          ldmatrix_x4_trans(vbase + box * Gm::kBoxBytes + swz128(row, chunk), a[0], a[1], a[2],
-                            a[3]);
-          mma_16816<IsBF16<T>::v>(oacc[m], a, bh0, bh1);
-          mma_16816<IsBF16<T>::v>(oacc[m], a, bl0, bl1);
-        }
-      }
-      __syncwarp();
-    }
-    // refill the stage with the tile kStages further on, then take the next tile
-    if (t + kStages < nt) {
-      fence_proxy_async_smem();  // the warp's reads of the stage precede the TMA write
-      if (lane == 0) issue(t + kStages);
-    }
-    int nx = 0;
-    if (lane == 0) nx = atomicAdd(&s_flag[2], 1);
-    t = __shfl_sync(0xffffffffu, nx, 0);
-  }
-
-  // ---- merge the warps into this CTA's (M, L, O) ----
-#pragma unroll
-  for (int off = 4; off < 32; off <<= 1) {
-    l0 += __shfl_xor_sync(0xffffffffu, l0, off);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, off);
-  }
-  __syncthreads();  // every warp is done with its stage: reuse the region for o
-  if (s_flag[1]) {
-    // a wait gave up: give the last load issued to each stage one more
-    // bounded wait before the stage region is reused
-    if (lane == 0)
-      for (int st = warp; st < kStages; st += kWarps)
-        if (s_iss[st] > 0) mbar_wait(&bars[st], (s_iss[st] - 1) & 1, kWaitLimit);
-    __syncthreads();
-  }
-  float *o_w = reinterpret_cast<float *>(stages);  // [W][G][D]
-  if (g8 == 0) {
-    if (2 * t4 < G) {
-      m_w[warp * G + 2 * t4] = m0;
-      l_w[warp * G + 2 * t4] = l0;
-    }
-    if (2 * t4 + 1 < G) {
-      m_w[warp * G + 2 * t4 + 1] = m1;
-      l_w[warp * G + 2 * t4 + 1] = l1;
-    }
-  }
-  // channels contiguous per (warp, head): the push below reads 4 at a time
-#pragma unroll
-  for (int m = 0; m < MT; ++m) {
-    const int ch = 16 * m + g8;
-    if (2 * t4 < G) {
-      o_w[(warp * G + 2 * t4) * D + ch] = oacc[m][0];
-      o_w[(warp * G + 2 * t4) * D + ch + 8] = oacc[m][2];
-    }
-    if (2 * t4 + 1 < G) {
-      o_w[(warp * G + 2 * t4 + 1) * D + ch] = oacc[m][1];
-      o_w[(warp * G + 2 * t4 + 1) * D + ch + 8] = oacc[m][3];
-    }
-  }
-  __syncthreads();
-  cluster_wait();  // every CTA of the cluster has started: its inbox may be written
-  // this CTA's (M, L, O), pushed straight into the inbox of the cluster CTA
-  // that owns each channel slice (remote shared-memory stores)
-  // CS, the slice and TPE below are powers of two: shifts and masks, not
-  // run-time integer division
-  const int lcs = __ffs(CS) - 1;
-  const int slice = D >> lcs, lsl = __ffs(slice) - 1;
-  const uint32_t aM = smem_u32(in_M), aL = smem_u32(in_L), aO = smem_u32(in_O);
-  // a thread takes 4 adjacent channels of one head: the warp weights are
-  // computed once for them, read and pushed 16 bytes at a time (a slice
-  // holds a multiple of 4 channels, so the 4 share an owner)
-  for (int x = tid; x < G * D / 4; x += kThreads) {
-    const int g = x / (D / 4), c = 4 * (x % (D / 4));
-    float M = m_w[g];
-#pragma unroll
-    for (int w = 1; w < kWarps; ++w) M = fmaxf(M, m_w[w * G + g]);
-    float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
-    float Ls = 0.f;
-    if (M != -CUDART_INF_F) {
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
-        const float f = exp2f(m_w[w * G + g] - M);
-        const float4 o = *reinterpret_cast<const float4 *>(&o_w[(w * G + g) * D + c]);
-        O.x = fmaf(f, o.x, O.x);
-        O.y = fmaf(f, o.y, O.y);
-        O.z = fmaf(f, o.z, O.z);
-        O.w = fmaf(f, o.w, O.w);
-        Ls = fmaf(f, l_w[w * G + g], Ls);
-      }
-    }
-    const int owner = c >> lsl, cs_ = c & (slice - 1);
-    st_dsmem_v4_f32(map_rank(aO + 4 * ((rank * G + g) * slice + cs_), owner), O);
-    if (cs_ == 0) {
-      st_dsmem_f32(map_rank(aM + 4 * (rank * G + g), owner), M);
-      st_dsmem_f32(map_rank(aL + 4 * (rank * G + g), owner), Ls);
-    }
-  }
-
-  // ---- merge the cluster: this CTA combines channels [rank*slice, +slice) ----
-  cluster_sync();  // every push has landed; nothing remote is touched after this
-  const int unit = i * p.Hkv + h;
-  float *out = p.out + ((size_t)i * p.Hq + h * G) * D;
-  const size_t cpart = (size_t)unit_item0 + (size_t)ci * CS;  // global slot of this cluster
-  // TPE adjacent lanes share one output element and split the CS ranks
-  // between them (fewer serial steps than one lane walking all ranks)
-  const int E = G * slice;
-  int TPE = 1;
-  while (TPE * 2 <= CS && E * TPE * 2 <= kThreads) TPE *= 2;
-  const int ltpe = __ffs(TPE) - 1;
-  for (int base = 0; base < E * TPE; base += kThreads) {
-    const int xt = base + tid, x = xt >> ltpe, r0 = xt & (TPE - 1);
-    const bool valid = x < E;
-    const int g = valid ? x >> lsl : 0, cl = valid ? x & (slice - 1) : 0, c = rank * slice + cl;
-    float M = -CUDART_INF_F;
-    if (valid)
-      for (int r = r0; r < CS; r += TPE) M = fmaxf(M, in_M[r * G + g]);
-    for (int o = 1; o < TPE; o <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    float O = 0.f, Ls = 0.f;
-    if (valid && M != -CUDART_INF_F)
-      for (int r = r0; r < CS; r += TPE) {
-        const float mr = in_M[r * G + g];
-        if (mr != -CUDART_INF_F) {
-          const float f = exp2f(mr - M);
-          Ls = fmaf(f, in_L[r * G + g], Ls);
-          O = fmaf(f, in_O[(r * G + g) * slice + cl], O);
-        }
-      }
-    for (int o = 1; o < TPE; o <<= 1) {
-      O += __shfl_xor_sync(0xffffffffu, O, o);
-      Ls += __shfl_xor_sync(0xffffffffu, Ls, o);
-    }
-    if (valid && r0 == 0) {
-      if (nc == 1) {
-        out[g * D + c] = O / Ls;
-        if (p.row_max && rank == 0 && cl == 0) {
-          // the logits' max in natural units (M is base 2, scale folded in)
-          // and the sum of exp(z - max) over the attended tokens
-          const size_t hq = (size_t)i * p.Hq + h * G + g;
-          p.row_max[hq] = M * 0.6931471805599453f;
-          p.row_sum[hq] = Ls;
-        }
-      } else {
-        p.part_o[(cpart * G + g) * D + c] = O;
-        if (rank == 0 && cl == 0) p.part_ml[cpart * G + g] = make_float2(M, Ls);
-      }
-    }
-  }
-  if (nc == 1) return;
-  cluster_sync();  // every rank's slice is written before rank 0 releases it
-  if (rank != 0) return;
-
-  // ---- several clusters: the last one to finish merges their results ----
-  if (tid == 0) {
-    const int prev = atom_add_acq_rel_gpu(&p.tickets[unit], 1);
-    *s_flag = prev == nc - 1;
-  }
-  __syncthreads();  // ... and the acquire above precedes every read below
-  if (!*s_flag) return;
-  // (1) every (m, l) pair into shared memory, (2) per-head max, weights and
-  // row sum, (3) the weighted sum of the o partials, kU at a time.
-  constexpr int kChunk = 256;                       // clusters per pass
-  constexpr int OPT4 = (G * D / 4 + kThreads - 1) / kThreads;
-  constexpr int kU = 8;
-  float *Mh = m_w;                                  // [G]
-  float *Lh = l_w;                                  // [G]
-  float2 *mlk = reinterpret_cast<float2 *>(stages); // [kChunk][G]
-  float *wk = reinterpret_cast<float *>(mlk + kChunk * G);  // [kChunk][G] + [G]
-  float4 acc_o[OPT4];
-#pragma unroll
-  for (int j = 0; j < OPT4; ++j) acc_o[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (tid < G) {
-    Mh[tid] = -CUDART_INF_F;
-    Lh[tid] = 0.f;
-  }
-  for (int base = 0; base < nc; base += kChunk) {
-    const int cnt = min(kChunk, nc - base);
-    for (int x = tid; x < cnt * G; x += kThreads) {
-      const int k = x / G, g = x % G;
-      mlk[x] = __ldcg(&p.part_ml[((size_t)unit_item0 + (size_t)(base + k) * CS) * G + g]);
-    }
-    __syncthreads();
-    if (tid < G) {
-      const int g = tid;
-      float M = Mh[g];
-      for (int k = 0; k < cnt; ++k) M = fmaxf(M, mlk[k * G + g].x);
-      const float resc = Mh[g] == -CUDART_INF_F ? 0.f : exp2f(Mh[g] - M);
-      float Ls = Lh[g] * resc;
-      for (int k = 0; k < cnt; ++k) {
-        const float2 ml = mlk[k * G + g];
-        const float w = ml.x == -CUDART_INF_F ? 0.f : exp2f(ml.x - M);
-        wk[k * G + g] = w;
-        Ls = fmaf(w, ml.y, Ls);
-      }
-      wk[kChunk * G + g] = resc;
-      Mh[g] = M;
-      Lh[g] = Ls;
-    }
-    __syncthreads();
-#pragma unroll
-    for (int j = 0; j < OPT4; ++j) {
-      const int x4 = tid + kThreads * j;
-      if (x4 < G * D / 4) {
-        const float r = wk[kChunk * G + (4 * x4) / D];
-        acc_o[j].x *= r;
-        acc_o[j].y *= r;
-        acc_o[j].z *= r;
-        acc_o[j].w *= r;
-      }
-    }
-    for (int k = 0; k < cnt; k += kU) {
-      float4 v[kU][OPT4];
-#pragma unroll
-      for (int u = 0; u < kU; ++u)
-#pragma unroll
-        for (int j = 0; j < OPT4; ++j) {
-          const int x4 = tid + kThreads * j;
-          const float4 *src = reinterpret_cast<const float4 *>(
-              p.part_o + ((size_t)unit_item0 + (size_t)(base + k + u) * CS) * G * D);
-          v[u][j] = (k + u < cnt && x4 < G * D / 4) ? __ldcg(src + x4)
-                                                     : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-#pragma unroll
-      for (int u = 0; u < kU; ++u)
-#pragma unroll
-        for (int j = 0; j < OPT4; ++j) {
-          const int x4 = tid + kThreads * j;
-          if (k + u < cnt && x4 < G * D / 4) {
-            const float w = wk[(k + u) * G + (4 * x4) / D];
-            acc_o[j].x = fmaf(w, v[u][j].x, acc_o[j].x);
-            acc_o[j].y = fmaf(w, v[u][j].y, acc_o[j].y);
-            acc_o[j].z = fmaf(w, v[u][j].z, acc_o[j].z);
-            acc_o[j].w = fmaf(w, v[u][j].w, acc_o[j].w);
-          }
-        }
-    }
-    __syncthreads();
-  }
-#pragma unroll
-  for (int j = 0; j < OPT4; ++j) {
-    const int x4 = tid + kThreads * j;
-    if (x4 < G * D / 4) {
-      const float inv = 1.f / Lh[(4 * x4) / D];
-      reinterpret_cast<float4 *>(out)[x4] =
-          make_float4(acc_o[j].x * inv, acc_o[j].y * inv, acc_o[j].z * inv, acc_o[j].w * inv);
-    }
-  }
-  if (p.row_max && tid < G) {
-    const size_t hq = (size_t)i * p.Hq + h * G + tid;
-    p.row_max[hq] = Mh[tid] * 0.6931471805599453f;
-    p.row_sum[hq] = Lh[tid];
-  }
-  if (tid == 0) p.tickets[unit] = 0;
-}
 
 int g_max_cluster[2][2][4];  // [dtype][d == 128][log2 G]: co-schedulable cluster size
 
 template <typename T, int D, int G>
 cudaError_t prep_one(int *max_cluster) {
-  auto k = decode_tiles_kernel<T, D, G>;
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       Smem<D, G>::kAlloc);
+  cudaError_t e = set_smem_attrs<T, D, G, false>();
   if (e != cudaSuccess) return e;
   int cs = 8;  // portable cluster size
-  if (cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
-      cudaSuccess) {
-    cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(16);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = Smem<D, G>::kAlloc;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 16;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int q = 0;
-    if (cudaOccupancyMaxPotentialClusterSize(&q, k, &cfg) == cudaSuccess && q >= 1) cs = q;
-  }
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(16);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Smem<D, G>::kAlloc;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 16;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int q = 0;
+  if (cudaOccupancyMaxPotentialClusterSize(&q, decode_tiles_kernel<T, D, G, false>, &cfg) ==
+          cudaSuccess &&
+      q >= 1)
+    cs = q;
   (void)cudaGetLastError();
   *max_cluster = cs;
   return cudaSuccess;
@@ -891,24 +44,6 @@ cudaError_t prep_g(int dt) {
   return prep_one<T, D, 8>(&g_max_cluster[dt][di][3]);
 }
 
-template <typename T, int D, int G>
-cudaError_t launch_one(const TileDecodeParams &p, cudaStream_t st) {
-  cudaError_t e = launch_pdl_cluster(decode_tiles_kernel<T, D, G>, p.total_items, kThreads,
-                                     (size_t)Smem<D, G>::kAlloc, p.cluster, st, p);
-  return e != cudaSuccess ? e : cudaGetLastError();
-}
-
-template <typename T, int D>
-cudaError_t launch_g(const TileDecodeParams &p, int G, cudaStream_t st) {
-  switch (G) {
-    case 1: return launch_one<T, D, 1>(p, st);
-    case 2: return launch_one<T, D, 2>(p, st);
-    case 4: return launch_one<T, D, 4>(p, st);
-    case 8: return launch_one<T, D, 8>(p, st);
-    default: return cudaErrorInvalidValue;
-  }
-}
-
 }  // namespace
 
 cudaError_t prepare_decode_kernels() {
@@ -916,7 +51,9 @@ cudaError_t prepare_decode_kernels() {
   if ((e = prep_g<__half, 64>(0)) != cudaSuccess) return e;
   if ((e = prep_g<__half, 128>(0)) != cudaSuccess) return e;
   if ((e = prep_g<__nv_bfloat16, 64>(1)) != cudaSuccess) return e;
-  return prep_g<__nv_bfloat16, 128>(1);
+  if ((e = prep_g<__nv_bfloat16, 128>(1)) != cudaSuccess) return e;
+  // the mass-exporting instances: same shared memory and block, same clusters
+  return prepare_decode_mass_kernels();
 }
 
 // Largest power-of-two cluster (<= 16) the decode kernel can be launched with.
@@ -934,8 +71,8 @@ cudaError_t launch_decode_tiles(const TileDecodeParams &p, int dtype, int d, int
                                 cudaStream_t s, long long *n) {
   if (p.n_seqs == 0 || p.total_items == 0) return cudaSuccess;
   *n += 1;
-  if (dtype == 0) return d == 64 ? launch_g<__half, 64>(p, G, s) : launch_g<__half, 128>(p, G, s);
-  return d == 64 ? launch_g<__nv_bfloat16, 64>(p, G, s) : launch_g<__nv_bfloat16, 128>(p, G, s);
+  if (p.page_part != nullptr) return launch_decode_tiles_mass(p, dtype, d, G, s);
+  return launch_variant<false>(p, dtype, d, G, s);
 }
 
 }  // namespace spd

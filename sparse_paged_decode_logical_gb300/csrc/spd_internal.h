@@ -35,6 +35,7 @@ struct ScratchLayout {
   size_t part_ml;      // float2 [kMaxItems * G]   (row max in log2 units, sum)
   size_t part_o;       // float  [kMaxItems * G * d]
   size_t scores;       // float  [kSeqsPerLaunch * Hd * score_stride]
+  size_t page_part;    // float2 [kSeqsPerLaunch * Hd * mass_tiles * G] per-tile (max, sum)
   size_t total;
 };
 
@@ -122,6 +123,12 @@ struct TileDecodeParams {
   const void *k_new, *v_new; // [n_seqs][Hkv][d] for a fused append, else null
   float *out;                // [n_seqs][Hq][d]
   float *row_max, *row_sum;  // [n_seqs][Hq] softmax statistics, or null
+  // per-page attention mass of the dynamic units (all null when not asked for)
+  float2 *page_part;         // [n_seqs][Hd][page_tile_cap][G] each tile's (max, sum), base 2
+  int page_tile_cap;
+  int *pages;                // [n_seqs][Hd][max_pages] attended logical pages, -1 after
+  float *page_mass;          // [n_seqs][Hd][G][max_pages] softmax weight per attended page
+  int max_pages;
   void *k_pool, *v_pool, *meta, *stream_k, *stream_v;
   const int *page_table, *selection;
   float *part_o;
@@ -155,8 +162,14 @@ constexpr int kMaxBoundRank = 8;
 
 constexpr int kTileRows = 16;
 constexpr int kMaxTilesPerItem = 8;
+// The per-page attention mass covers a selection's pages plus this many
+// logical pages created after it was taken.
+constexpr int kMassExtraPages = 64;
 
 cudaError_t prepare_decode_kernels();
+cudaError_t prepare_decode_mass_kernels();  // called by prepare_decode_kernels()
+cudaError_t launch_decode_tiles_mass(const TileDecodeParams &p, int dtype, int d, int G,
+                                     cudaStream_t s);
 int decode_max_cluster(int dtype, int d, int G);  // after prepare_decode_kernels()
 int decode_max_tiles_per_cta();
 cudaError_t launch_decode_tiles(const TileDecodeParams &p, int dtype, int d, int G,

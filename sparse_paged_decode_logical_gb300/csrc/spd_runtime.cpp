@@ -56,6 +56,7 @@ uint64_t splitmix64(uint64_t &s) {
 struct Derived {
   int G = 0, Hd = 0, Hs = 0, R = 0, max_pp = 0, ksel_max = 0, max_nL = 0,
       seqs_per_launch = 0;
+  int mass_pages = 0, mass_tiles = 0;  // per-page mass: attended pages / tiles per unit
   unsigned char kv_kind[kMaxKvHeads] = {}, kv_sub[kMaxKvHeads] = {},
                 dyn_kv[kMaxKvHeads] = {}, str_kv[kMaxKvHeads] = {};
   ScratchLayout sl{};
@@ -144,6 +145,10 @@ const char *derive(const spd_config *c, Derived *d) {
   off = round_up(off + (size_t)kMaxItems * d->G * dim * 4, 256);
   sl.scores = off;
   off = round_up(off + (size_t)d->seqs_per_launch * d->Hd * round_up((size_t)d->max_nL, 4) * 4, 256);
+  d->mass_pages = std::min(d->ksel_max + kMassExtraPages, d->max_nL);
+  d->mass_tiles = d->mass_pages * (c->logical_page / kTileRows);
+  sl.page_part = off;
+  off = round_up(off + (size_t)d->seqs_per_launch * d->Hd * d->mass_tiles * d->G * 8, 256);
   sl.total = off;
   z.scratch = off;
   return nullptr;
@@ -561,10 +566,19 @@ int plan_tiles(const spd_ctx *c, TileDecodeParams &p, const int *ids, int n) {
 // tickets; a launch then holds at most scr->max_items items.
 // fused_topk: the selection launched just before wrote only scores for the
 // sequences marked topk_pending; this launch selects their pages.
+// Optional exports of an attention call: the softmax row max / row sum and the
+// per-page attention mass of the dynamic heads.
+struct StatsOut {
+  float *row_max = nullptr, *row_sum = nullptr;
+  int *pages = nullptr;
+  float *page_mass = nullptr;
+  int max_pages = 0;
+};
+
 spd_status attention_impl(spd_ctx *c, const void *q, const int *ids, int n, float *out,
                           const void *k_new, const void *v_new, cudaStream_t st,
                           const DecodeScratch *scr = nullptr, bool fused_topk = false,
-                          float *row_max = nullptr, float *row_sum = nullptr) {
+                          const StatsOut &so = StatsOut()) {
   spd_status r = ensure_device(c, st);
   if (r != SPD_OK) return r;
   const Derived &dv = c->dv;
@@ -592,8 +606,14 @@ spd_status attention_impl(spd_ctx *c, const void *q, const int *ids, int n, floa
     p.k_new = k_new ? static_cast<const char *>(k_new) + (size_t)b * kvrow * 2 : nullptr;
     p.v_new = v_new ? static_cast<const char *>(v_new) + (size_t)b * kvrow * 2 : nullptr;
     p.out = out + (size_t)b * qrow;
-    p.row_max = row_max ? row_max + (size_t)b * c->cfg.num_q_heads : nullptr;
-    p.row_sum = row_sum ? row_sum + (size_t)b * c->cfg.num_q_heads : nullptr;
+    p.row_max = so.row_max ? so.row_max + (size_t)b * c->cfg.num_q_heads : nullptr;
+    p.row_sum = so.row_sum ? so.row_sum + (size_t)b * c->cfg.num_q_heads : nullptr;
+    const bool mass = so.page_mass != nullptr && dv.Hd > 0;
+    p.page_part = mass ? reinterpret_cast<float2 *>(c->scratch(dv.sl.page_part)) : nullptr;
+    p.page_tile_cap = dv.mass_tiles;
+    p.pages = mass ? so.pages + (size_t)b * dv.Hd * so.max_pages : nullptr;
+    p.page_mass = mass ? so.page_mass + (size_t)b * dv.Hd * dv.G * so.max_pages : nullptr;
+    p.max_pages = so.max_pages;
     p.k_pool = c->buf.k_pool;
     p.v_pool = c->buf.v_pool;
     p.meta = c->buf.meta;
@@ -878,8 +898,49 @@ spd_status spd_sparse_decode_attention_stats(spd_ctx *c, const void *q, const in
     return c->fail(SPD_ERR_INVALID_ARG, "row_max and row_sum must be 4-byte aligned pointers");
   spd_status r = check_attention_call(c, q, seq_ids, n_seqs, out);
   if (r != SPD_OK) return r;
+  StatsOut so;
+  so.row_max = row_max;
+  so.row_sum = row_sum;
   return attention_impl(c, q, seq_ids, n_seqs, out, nullptr, nullptr, (cudaStream_t)stream,
-                        nullptr, false, row_max, row_sum);
+                        nullptr, false, so);
+}
+
+spd_status spd_sparse_decode_attention_page_mass(spd_ctx *c, const void *q, const int *seq_ids,
+                                                 int n_seqs, float *out, float *row_max,
+                                                 float *row_sum, int *pages, float *page_mass,
+                                                 int max_pages, spd_stream stream) {
+  if (!c) return SPD_ERR_INVALID_ARG;
+  if ((row_max == nullptr) != (row_sum == nullptr) ||
+      (row_max && (!aligned4(row_max) || !aligned4(row_sum))))
+    return c->fail(SPD_ERR_INVALID_ARG,
+                   "row_max and row_sum must both be NULL or both 4-byte aligned pointers");
+  const Derived &dv = c->dv;
+  if (dv.Hd > 0 && (!pages || !page_mass || !aligned4(pages) || !aligned4(page_mass)))
+    return c->fail(SPD_ERR_INVALID_ARG, "pages and page_mass must be 4-byte aligned pointers");
+  if (dv.Hd > 0 && max_pages < 1) return c->fail(SPD_ERR_INVALID_ARG, "max_pages must be >= 1");
+  spd_status r = check_attention_call(c, q, seq_ids, n_seqs, out);
+  if (r != SPD_OK) return r;
+  if (dv.Hd > 0) {
+    for (int i = 0; i < n_seqs; ++i) {
+      const Seq &s = c->seqs[seq_ids[i]];
+      const int n_att = s.sel_count + nL_of(s.L, c->cfg.logical_page) - s.nL0;
+      if (n_att > max_pages)
+        return c->fail(SPD_ERR_CAPACITY, "sequence %d attends %d pages per dynamic head, "
+                       "max_pages is %d", seq_ids[i], n_att, max_pages);
+      if (n_att > dv.mass_pages)
+        return c->fail(SPD_ERR_CAPACITY, "sequence %d attends %d pages per dynamic head; the "
+                       "per-page mass covers at most %d (select its pages again)", seq_ids[i],
+                       n_att, dv.mass_pages);
+    }
+  }
+  StatsOut so;
+  so.row_max = row_max;
+  so.row_sum = row_sum;
+  so.pages = pages;
+  so.page_mass = page_mass;
+  so.max_pages = max_pages;
+  return attention_impl(c, q, seq_ids, n_seqs, out, nullptr, nullptr, (cudaStream_t)stream,
+                        nullptr, false, so);
 }
 
 spd_status spd_decode_step(spd_ctx *c, const void *q, const void *k, const void *v,

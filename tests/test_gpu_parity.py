@@ -9,6 +9,7 @@ import torch
 import oracle
 import workloads as W
 from harness import Pair, tdev
+import sparse_paged_decode_logical_gb300 as spd
 
 pytestmark = pytest.mark.gpu
 
@@ -301,3 +302,83 @@ def test_softmax_statistics_export(which):
         pr.step(s)
     q, _, _ = W.step_tokens(wl, 2)
     _check_stats(pr, q)
+
+
+# ---- per-page attention mass ---------------------------------------------------
+# a page's mass is a sum of fp32 exp2 weights over its <= 64 rows (logits of
+# exact 16-bit products, relative error < 1e-5) over the fp32 row sum: well
+# inside 1e-4 absolute for a quantity in [0, 1]
+TOL_MASS = 1e-4
+
+
+def _check_page_mass(pr, q, max_pages=None):
+    out, rm, rs, pages, mass = pr.cache.sparse_decode_attention_page_mass(
+        tdev(q, pr.dt), pr.gids, max_pages=max_pages)
+    pr.cache.check_status()
+    out, rm, rs, mass = (t.cpu().numpy().astype(np.float64) for t in (out, rm, rs, mass))
+    pages = pages.cpu().numpy()
+    assert pages.shape[:2] == (pr.wl.batch, len(pr.dyn))
+    for b in range(pr.wl.batch):
+        oid, s = pr.oids[b], pr.orc.seqs[pr.oids[b]]
+        own = {h: s.sel[h] for h in pr.dyn}
+        for h in pr.dyn:  # the oracle on the GPU's own selection
+            s.sel[h] = np.array(pr.cache.selection(pr.gids[b], h), np.int32)
+        ref_mass = pr.orc.page_mass(oid, q[b])
+        m_o, l_o = pr.orc.softmax_stats(oid, q[b])
+        ref = pr.orc.attend(oid, q[b])
+        for h in pr.dyn:
+            s.sel[h] = own[h]
+        for hd, h in enumerate(pr.dyn):
+            pg, ms = ref_mass[h]
+            n = pg.size
+            assert np.array_equal(pages[b, hd, :n], pg), (b, h)
+            assert np.all(pages[b, hd, n:] == -1), (b, h)
+            err = np.abs(mass[b, hd, :, :n] - ms)
+            assert err.max() <= TOL_MASS, (b, h, err.max())
+            assert np.all(mass[b, hd, :, n:] == 0.0), (b, h)
+            assert np.allclose(mass[b, hd].sum(-1), 1.0, rtol=0, atol=TOL_MASS), (b, h)
+        assert np.all(np.abs(rm[b] - m_o) <= TOL_STAT_M * np.maximum(1.0, np.abs(m_o))), b
+        assert np.all(np.abs(rs[b] - l_o) <= TOL_STAT_L * l_o), b
+        err = np.abs(out[b] - ref)
+        assert err.max() <= 2e-3 and err.mean() <= 2e-4, b
+
+
+PAGE_MASS_CASES = {
+    # ragged lengths, 8 kept pages of 16 tokens, streaming heads beside
+    "synthetic": lambda: synth(batch=3, lens=[40, 700, 1500], steps=3),
+    # 64-token pages: 4 tiles a page, the newest one partial
+    "ell64": lambda: synth(Hq=4, Hkv=4, streaming=[False] * 4, ell=64, P=256, token_budget=0,
+                           context=9000, batch=1, steps=3),
+    # 1024 kept pages on one dynamic head: the unit spans several clusters
+    "many_clusters": lambda: synth(Hq=4, Hkv=2, streaming=[False, True], context=30000,
+                                   token_budget=16384, batch=1, steps=3),
+    "llama3_8b_b4_32k": lambda: W.workload("llama3_8b_b4_32k"),
+}
+
+
+@needs_gpu
+@pytest.mark.parametrize("which", list(PAGE_MASS_CASES))
+def test_page_mass_export(which):
+    wl = PAGE_MASS_CASES[which]()
+    pr = Pair(wl)
+    for s in range(2):
+        pr.step(s)
+    q, _, _ = W.step_tokens(wl, 2)
+    _check_page_mass(pr, q)
+    # a roomier output: the extra entries are padding
+    q, _, _ = W.step_tokens(wl, 3)
+    _check_page_mass(pr, q, max_pages=max(pr.cache.attended_page_count(g) for g in pr.gids) + 5)
+
+
+@needs_gpu
+def test_page_mass_capacity_is_checked_before_any_work():
+    wl = synth(batch=2, lens=[700, 1500], steps=3)
+    pr = Pair(wl)
+    pr.step(0)
+    q, _, _ = W.step_tokens(wl, 1)
+    before = [pr.cache.seq_info(g) for g in pr.gids]
+    with pytest.raises(spd.SpdError) as e:
+        pr.cache.sparse_decode_attention_page_mass(tdev(q, pr.dt), pr.gids, max_pages=3)
+    assert e.value.name == "SPD_ERR_CAPACITY"
+    assert [pr.cache.seq_info(g) for g in pr.gids] == before
+    _check_page_mass(pr, q)
