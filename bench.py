@@ -27,6 +27,7 @@ Arms:
                      128K workload).
 """
 import argparse
+import dataclasses
 import json
 import os
 import subprocess
@@ -51,6 +52,9 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="llama3_8b_b1_128k")
     ap.add_argument("--layers", type=int, default=32)
+    ap.add_argument("--streaming-layers", default="",
+                    help="comma-separated layer indices whose kv heads are all streaming "
+                         "(the other layers keep the workload's head split)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-roofline", action="store_true")
@@ -178,18 +182,20 @@ class ClockSampler:
 class Layers:
     """n_layers independent caches of the workload, one sequence each."""
 
-    def __init__(self, wl, n_layers, device, extra_tokens):
+    def __init__(self, wl, n_layers, device, extra_tokens, streaming_layers=()):
         import torch
         import sparse_paged_decode_logical_gb300 as spd
         self.torch, self.wl, self.device = torch, wl, device
         L0 = wl.context
-        cfg = wl.lib_config()
-        cfg["max_context"] = L0 + extra_tokens
-        cfg["max_seqs"] = 1
-        cfg["num_physical_pages"] = -(-cfg["max_context"] // wl.P)
-        self.cfg = cfg
+        # per layer: the workload's head split, or every kv head streaming
+        self.wls = [dataclasses.replace(wl, streaming=[True] * wl.Hkv)
+                    if layer in streaming_layers else wl for layer in range(n_layers)]
         self.caches, self.seqs = [], []
         for layer in range(n_layers):
+            cfg = self.wls[layer].lib_config()
+            cfg["max_context"] = L0 + extra_tokens
+            cfg["max_seqs"] = 1
+            cfg["num_physical_pages"] = -(-cfg["max_context"] // wl.P)
             c = spd.SparsePagedKVCache(device=device, **cfg)
             # every kernel on the stream is this library's and each layer's
             # cache is written only through its own context: the next layer
@@ -231,6 +237,12 @@ class Layers:
     def launches(self):
         return sum(c.launch_count() for c in self.caches)
 
+    def layer_bytes(self, layer, selected):
+        """(dyn, str, meta) bytes of the layer's current step (see step_bytes)."""
+        inf = self.caches[layer].seq_info(self.seqs[layer])
+        n_att = inf["pages_kept"] + (-(-inf["length"] // self.wl.ell)) - inf["pages_at_selection"]
+        return step_bytes(self.wls[layer], inf["length"], n_att, selected)
+
     def step(self, row, outs=None):
         """Enqueue one decode step on every layer; returns its algorithmic bytes."""
         outs = outs or self.out
@@ -238,12 +250,10 @@ class Layers:
         for layer, c in enumerate(self.caches):
             q, k, v = row[layer]
             c.decode_step(q, k, v, [self.seqs[layer]], out=outs[layer])
-        inf = self.info()
-        dyn, strm, meta = step_bytes(self.wl, inf["length"], inf["pages_kept"] +
-                                     (-(-inf["length"] // self.wl.ell)) - inf["pages_at_selection"],
-                                     due)
-        n = len(self.caches)
-        return n * dyn, n * strm, n * meta, due
+        tot = np.zeros(3)
+        for layer in range(len(self.caches)):
+            tot += self.layer_bytes(layer, due)
+        return tot[0], tot[1], tot[2], due
 
 
 def run_ours(args, rank, world, device):
@@ -252,7 +262,7 @@ def run_ours(args, rank, world, device):
     wl = W.workload(args.workload)
     n_l = args.layers
     extra = args.warmup + args.steps + (0 if args.no_e2e else args.steps) + 64
-    layers = Layers(wl, n_l, device, extra)
+    layers = Layers(wl, n_l, device, extra, streaming_layers(args))
     stream = torch.cuda.Stream(device=device)
     dist = None
     if world > 1:
@@ -346,7 +356,8 @@ def run_ours(args, rank, world, device):
         "vs_baseline": None,
         "dtype": wl.dtype,
         "data": "synthetic (seeded N(0,1) K/V in bf16, needle pages at 10/50/90% depth)",
-        "config": arm_config(wl, n_l, n_sel, total_bytes / args.steps, world),
+        "config": arm_config(wl, n_l, n_sel, total_bytes / args.steps, world,
+                             streaming_layers(args)),
         "bytes_per_step": {"dyn": tot[0] / args.steps, "stream": tot[1] / args.steps,
                            "meta": tot[2] / args.steps},
         "gpu_launches": launches,
@@ -359,7 +370,11 @@ def run_ours(args, rank, world, device):
     return res, layers
 
 
-def arm_config(wl, n_layers, n_sel=None, bytes_per_step=None, world=1):
+def streaming_layers(args):
+    return sorted({int(x) for x in args.streaming_layers.split(",") if x.strip()})
+
+
+def arm_config(wl, n_layers, n_sel=None, bytes_per_step=None, world=1, all_streaming=()):
     c = {
         "workload": wl.name,
         "shape": "Llama-3-8B attention: 32 q / 8 kv heads, d 128, bf16",
@@ -372,6 +387,8 @@ def arm_config(wl, n_layers, n_sel=None, bytes_per_step=None, world=1):
                   "CUDA events on the launching stream; early KV staging on",
         "parallelism": "replicas" if world > 1 else "single GPU",
     }
+    if all_streaming:
+        c["all_streaming_layers"] = list(all_streaming)
     if n_sel is not None:
         c["selection_steps_in_window"] = n_sel
     return c
@@ -396,10 +413,12 @@ def roofline(layers, stream, iters):
                 c.sparse_decode_attention(q[layer], [layers.seqs[layer]], out=layers.out[layer],
                                           stream=stream)
     per_replay = layers.launches() - l0
-    inf = layers.info()
-    nL = -(-inf["length"] // wl.ell)
-    dyn, strm, _ = step_bytes(wl, inf["length"], inf["pages_kept"] + nL - inf["pages_at_selection"],
-                              False)
+    # bytes per launch, averaged over the layers (they differ when some layers
+    # are all streaming)
+    dyn = strm = 0.0
+    for layer in range(n):
+        d_, s_, _ = layers.layer_bytes(layer, False)
+        dyn, strm = dyn + d_ / n, strm + s_ / n
     times = []
     with torch.cuda.stream(stream):
         # at least 5 timed replays, and about a second of them so that the
@@ -437,7 +456,7 @@ def roofline(layers, stream, iters):
             "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
             "peak_kind": kind + " (MEASURED_PEAKS.json hbm_gbs, burst copy)" if kind == "measured" else kind,
             "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
-            "algorithmic_bytes_per_launch": dyn + strm,
+            "algorithmic_bytes_per_launch": int(round(dyn + strm)),
             "avg_launch_us": round(avg_ms * 1e3, 3), "launches_per_replay": per_replay,
             "how": "graph of %d back-to-back decode launches (%d layers x %d), median over %d "
                    "replays / launches; includes inter-launch gaps" % (per_replay, n, iters,
@@ -552,7 +571,7 @@ def run_reference(args):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
-        "config": arm_config(wl, args.layers),
+        "config": arm_config(wl, args.layers, all_streaming=streaming_layers(args)),
         "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": threads,
                          "kind": "oracle", "sample": desc},
         "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
