@@ -44,9 +44,9 @@ import numpy as np
 
 from . import build as _build
 
-F16, BF16 = 0, 1
+F16, BF16, E4M3 = 0, 1, 2
 _DTYPES = {"f16": F16, "fp16": F16, "float16": F16,
-           "bf16": BF16, "bfloat16": BF16}
+           "bf16": BF16, "bfloat16": BF16, "e4m3": E4M3}
 
 _lib = None
 
@@ -86,6 +86,26 @@ def lib():
         L.orc_softmax_stats.restype = ci
         L.orc_page_mass.argtypes = [u16p, u16p, ci, ci, ci, i32p, ci, ci, i32p, ci, f64p]
         L.orc_page_mass.restype = ci
+        f32, f64 = ctypes.c_float, ctypes.c_double
+        L.orc_e4m3_value.argtypes = [ctypes.c_uint]
+        L.orc_e4m3_value.restype = f64
+        L.orc_e4m3_from_float.argtypes = [f32]
+        L.orc_e4m3_from_float.restype = ctypes.c_uint
+        L.orc_quantize_e4m3.argtypes = [u16p, ci, cl, f32, u16p]
+        L.orc_quantize_e4m3.restype = None
+        L.orc_page_scores_f32_kv.argtypes = [u16p, ci, u16p, u16p, ci, f64, ci, ci, ci, f32p]
+        L.orc_page_scores_f32_kv.restype = None
+        L.orc_page_scores_f64_kv.argtypes = [u16p, ci, u16p, u16p, ci, f64, ci, ci, ci, f64p]
+        L.orc_page_scores_f64_kv.restype = None
+        L.orc_attention_kv.argtypes = [u16p, ci, u16p, u16p, ci, f64, f64, ci, ci, i32p, ci,
+                                       f64p]
+        L.orc_attention_kv.restype = ci
+        L.orc_softmax_stats_kv.argtypes = [u16p, ci, u16p, ci, f64, ci, ci, i32p, ci, f64p,
+                                           f64p]
+        L.orc_softmax_stats_kv.restype = ci
+        L.orc_page_mass_kv.argtypes = [u16p, ci, u16p, ci, f64, ci, ci, i32p, ci, ci, i32p, ci,
+                                       f64p]
+        L.orc_page_mass_kv.restype = ci
         _lib = L
     return _lib
 
@@ -122,23 +142,53 @@ def page_minmax(K, dtype, ell, j0=0, j1=None):
     return kmin, kmax
 
 
-def page_scores(q, kmin, kmax, dtype):
-    """fp32 kv-head score S[nL] = max over the G query heads of q [G][d]."""
+def e4m3_value(codes):
+    """Exact value (fp64) of fp8 e4m3 codes."""
+    c = np.asarray(codes).reshape(-1)
+    return np.array([lib().orc_e4m3_value(int(x) & 0xff) for x in c],
+                    np.float64).reshape(np.shape(codes))
+
+
+def e4m3_from_float(x):
+    """Codes of fp32 values, rounded to nearest even, saturating at +-448."""
+    x = np.asarray(x, np.float32)
+    return np.array([lib().orc_e4m3_from_float(float(v)) for v in x.reshape(-1)],
+                    np.uint16).reshape(x.shape)
+
+
+def quantize_e4m3(x, dtype, scale):
+    """fp8 KV codes of 16-bit values x: e4m3(fl32(x / scale)), in uint16."""
+    x = _u16(x)
+    out = np.empty(x.shape, np.uint16)
+    lib().orc_quantize_e4m3(x.reshape(-1), dtype_code(dtype), x.size, float(scale),
+                            out.reshape(-1))
+    return out
+
+
+def _kv(dtype, kv_dtype):
+    return dtype_code(dtype), dtype_code(dtype if kv_dtype is None else kv_dtype)
+
+
+def page_scores(q, kmin, kmax, dtype, kv_dtype=None, kscale=1.0):
+    """fp32 kv-head score S[nL] = max over the G query heads of q [G][d];
+    kmin/kmax are kv_dtype codes of value / kscale (default: q's dtype, 1)."""
     q, kmin, kmax = _u16(q), _u16(kmin), _u16(kmax)
     G, d = q.shape
     nL = kmin.shape[0]
     S = np.empty(nL, np.float32)
-    lib().orc_page_scores_f32(q, kmin, kmax, dtype_code(dtype), nL, G, d, S)
+    qd, kd = _kv(dtype, kv_dtype)
+    lib().orc_page_scores_f32_kv(q, qd, kmin, kmax, kd, float(kscale), nL, G, d, S)
     return S
 
 
-def page_scores_f64(q, kmin, kmax, dtype):
+def page_scores_f64(q, kmin, kmax, dtype, kv_dtype=None, kscale=1.0):
     """fp64 per-head score s[G][nL] (not reduced over the group)."""
     q, kmin, kmax = _u16(q), _u16(kmin), _u16(kmax)
     G, d = q.shape
     nL = kmin.shape[0]
     s = np.empty((G, nL), np.float64)
-    lib().orc_page_scores_f64(q, kmin, kmax, dtype_code(dtype), nL, G, d, s)
+    qd, kd = _kv(dtype, kv_dtype)
+    lib().orc_page_scores_f64_kv(q, qd, kmin, kmax, kd, float(kscale), nL, G, d, s)
     return s
 
 
@@ -173,19 +223,21 @@ def streaming_tokens(L, sink, window):
     return out[:n].copy()
 
 
-def attention(q, K, V, dtype, tokens):
-    """fp64 softmax attention of q [G][d] over rows `tokens` of K/V [L][d]."""
+def attention(q, K, V, dtype, tokens, kv_dtype=None, kscale=1.0, vscale=1.0):
+    """fp64 softmax attention of q [G][d] over rows `tokens` of K/V [L][d]
+    (kv_dtype codes of value / kscale, value / vscale; default q's dtype, 1)."""
     q, K, V = _u16(q), _u16(K), _u16(V)
     tokens = np.ascontiguousarray(tokens, dtype=np.int32)
     G, d = q.shape
     out = np.empty((G, d), np.float64)
-    if lib().orc_attention(q, K, V, dtype_code(dtype), G, d, tokens,
-                           tokens.size, out) != 0:
+    qd, kd = _kv(dtype, kv_dtype)
+    if lib().orc_attention_kv(q, qd, K, V, kd, float(kscale), float(vscale), G, d, tokens,
+                              tokens.size, out) != 0:
         raise ValueError("orc_attention: empty token set")
     return out
 
 
-def softmax_stats(q, K, dtype, tokens):
+def softmax_stats(q, K, dtype, tokens, kv_dtype=None, kscale=1.0):
     """fp64 (row_max [G], row_sum [G]) of the logits q . k_t / sqrt(d) over
     rows `tokens` of K [L][d]: the max and the sum of exp(z - max)."""
     q, K = _u16(q), _u16(K)
@@ -193,12 +245,14 @@ def softmax_stats(q, K, dtype, tokens):
     G, d = q.shape
     rm = np.empty(G, np.float64)
     rs = np.empty(G, np.float64)
-    if lib().orc_softmax_stats(q, K, dtype_code(dtype), G, d, tokens, tokens.size, rm, rs) != 0:
+    qd, kd = _kv(dtype, kv_dtype)
+    if lib().orc_softmax_stats_kv(q, qd, K, kd, float(kscale), G, d, tokens, tokens.size, rm,
+                                  rs) != 0:
         raise ValueError("orc_softmax_stats: empty token set")
     return rm, rs
 
 
-def page_mass(q, K, dtype, tokens, ell, pages):
+def page_mass(q, K, dtype, tokens, ell, pages, kv_dtype=None, kscale=1.0):
     """fp64 [G][len(pages)]: the softmax weight of the logits q . k_t / sqrt(d)
     over rows `tokens` of K [L][d] that falls on each logical page in `pages`
     (tokens t with t // ell == page)."""
@@ -207,8 +261,9 @@ def page_mass(q, K, dtype, tokens, ell, pages):
     pages = np.ascontiguousarray(pages, dtype=np.int32)
     G, d = q.shape
     mass = np.empty((G, pages.size), np.float64)
-    if lib().orc_page_mass(q, K, dtype_code(dtype), G, d, tokens, tokens.size, int(ell),
-                           pages, pages.size, mass) != 0:
+    qd, kd = _kv(dtype, kv_dtype)
+    if lib().orc_page_mass_kv(q, qd, K, kd, float(kscale), G, d, tokens, tokens.size, int(ell),
+                              pages, pages.size, mass) != 0:
         raise ValueError("orc_page_mass: empty token set")
     return mass
 
@@ -232,7 +287,9 @@ class OracleLayer:
 
     cfg keys: num_q_heads, num_kv_heads, head_dim, dtype ('f16'/'bf16'),
     logical_page, streaming (list of bool per kv head), sink, window,
-    token_budget (<=0: min(4096, L/32)), reuse_interval (C), max_context.
+    token_budget (<=0: min(4096, L/32)), reuse_interval (C), max_context;
+    optional kv_fp8 (K and V stored as fp8 e4m3 codes of value / scale) with
+    k_scale, v_scale (per kv head, fp32, default 1).
 
     Step order (LServe write-up, section 3.2): append the new token, select
     when the sequence's step counter is a multiple of C (or when forced),
@@ -253,6 +310,14 @@ class OracleLayer:
         self.budget = cfg.get("token_budget", 0)
         self.C = cfg.get("reuse_interval", 4)
         self.cap = cfg["max_context"]
+        self.kv_fp8 = bool(cfg.get("kv_fp8", False))
+        self.kvdtype = E4M3 if self.kv_fp8 else self.dtype
+        one = [1.0] * self.Hkv
+        # the scales the GPU path uses are fp32
+        self.ks = [float(np.float32(x)) for x in (cfg.get("k_scale") or one)]
+        self.vs = [float(np.float32(x)) for x in (cfg.get("v_scale") or one)]
+        if not self.kv_fp8:
+            self.ks, self.vs = one, one
         self.seqs = {}
         self._next = 0
 
@@ -278,12 +343,17 @@ class OracleLayer:
         if s.L + n > self.cap:
             raise ValueError("append beyond max_context")
         L0, L1 = s.L, s.L + n
-        s.K[:, L0:L1] = k.transpose(1, 0, 2)
-        s.V[:, L0:L1] = v.transpose(1, 0, 2)
+        if self.kv_fp8:  # stored as e4m3 codes of value / scale, per kv head
+            for h in range(self.Hkv):
+                s.K[h, L0:L1] = quantize_e4m3(k[:, h], self.dtype, self.ks[h])
+                s.V[h, L0:L1] = quantize_e4m3(v[:, h], self.dtype, self.vs[h])
+        else:
+            s.K[:, L0:L1] = k.transpose(1, 0, 2)
+            s.V[:, L0:L1] = v.transpose(1, 0, 2)
         s.L = L1
         j0, j1 = L0 // self.ell, -(-L1 // self.ell)
         for h in self.dyn_heads():
-            mn, mx = page_minmax(s.K[h, :L1], self.dtype, self.ell, j0, j1)
+            mn, mx = page_minmax(s.K[h, :L1], self.kvdtype, self.ell, j0, j1)
             old_min = s.kmin.get(h, np.zeros((0, self.d), np.uint16))[:j0]
             old_max = s.kmax.get(h, np.zeros((0, self.d), np.uint16))[:j0]
             s.kmin[h] = np.concatenate([old_min, mn])
@@ -296,7 +366,7 @@ class OracleLayer:
     def scores(self, sid, q, h):
         s = self.seqs[sid]
         qg = _u16(q)[h * self.G:(h + 1) * self.G]
-        return page_scores(qg, s.kmin[h], s.kmax[h], self.dtype)
+        return page_scores(qg, s.kmin[h], s.kmax[h], self.dtype, self.kvdtype, self.ks[h])
 
     def select(self, sid, q, force=False):
         """Run the selection if due (counter % C == 0) or forced; returns
@@ -332,7 +402,8 @@ class OracleLayer:
             T = self.tokens(sid, h)
             qg = q[h * self.G:(h + 1) * self.G]
             out[h * self.G:(h + 1) * self.G] = attention(
-                qg, s.K[h, :s.L], s.V[h, :s.L], self.dtype, T)
+                qg, s.K[h, :s.L], s.V[h, :s.L], self.dtype, T, self.kvdtype, self.ks[h],
+                self.vs[h])
 
         if threads > 1:
             with ThreadPoolExecutor(threads) as ex:
@@ -353,7 +424,8 @@ class OracleLayer:
         rs = np.empty(self.Hq, np.float64)
         for h in range(self.Hkv):
             T = self.tokens(sid, h)
-            a, b = softmax_stats(q[h * self.G:(h + 1) * self.G], s.K[h, :s.L], self.dtype, T)
+            a, b = softmax_stats(q[h * self.G:(h + 1) * self.G], s.K[h, :s.L], self.dtype, T,
+                                 self.kvdtype, self.ks[h])
             rm[h * self.G:(h + 1) * self.G] = a
             rs[h * self.G:(h + 1) * self.G] = b
         return rm, rs
@@ -375,7 +447,8 @@ class OracleLayer:
         for h in self.dyn_heads():
             pages = self.attended_pages(sid, h)
             res[h] = (pages, page_mass(q[h * self.G:(h + 1) * self.G], s.K[h, :s.L], self.dtype,
-                                       self.tokens(sid, h), self.ell, pages))
+                                       self.tokens(sid, h), self.ell, pages, self.kvdtype,
+                                       self.ks[h]))
         return res
 
     def step(self, sid, q, k, v, threads=1):

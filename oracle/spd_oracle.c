@@ -48,6 +48,7 @@
 
 #define ORC_F16 0
 #define ORC_BF16 1
+#define ORC_E4M3 2 /* fp8 KV storage: the low byte holds an e4m3 code */
 
 /* ---- exact decoding of the 16-bit storage formats --------------------- */
 
@@ -81,8 +82,67 @@ static double orc_bf16_value(uint16_t b) {
   return sign ? -v : v;
 }
 
+/* OCP fp8 E4M3 ("e4m3fn"): 1 sign, 4 exponent (bias 7), 3 fraction bits; no
+ * infinities, exponent 15 with fraction 7 is NaN, so the largest finite
+ * magnitude is 1.75 * 2^8 = 448. */
+double orc_e4m3_value(unsigned code) {
+  int sign = (code >> 7) & 1;
+  int e = (code >> 3) & 0xf;
+  int m = code & 7;
+  double v;
+  if (e == 15 && m == 7)
+    v = NAN;
+  else if (e == 0)
+    v = ldexp((double)m, -9); /* subnormal: m/8 * 2^-6 */
+  else
+    v = ldexp((double)(m | 8), e - 10); /* (1.m) * 2^(e-7) */
+  return sign ? -v : v;
+}
+
 double orc_value(uint16_t bits, int dtype) {
+  if (dtype == ORC_E4M3) return orc_e4m3_value(bits & 0xffu);
   return dtype == ORC_BF16 ? orc_bf16_value(bits) : orc_f16_value(bits);
+}
+
+/*
+ * fp32 -> e4m3 code: round to nearest, ties to even fraction, saturating:
+ * magnitudes that round beyond 448 (and infinities) become 448; NaN becomes
+ * the NaN code.  Written from the format: for |x| below the smallest normal
+ * 2^-6 the code counts multiples of 2^-9; above, (exponent + 7, fraction
+ * rounded to 3 bits), a fraction that rounds up to 8 carrying into the
+ * exponent.
+ */
+unsigned orc_e4m3_from_float(float x) {
+  unsigned sign = signbit(x) ? 0x80u : 0u;
+  double a = fabs((double)x);
+  if (isnan(x)) return sign | 0x7fu;
+  if (a >= 448.0) return sign | 0x7eu;
+  if (a < ldexp(1.0, -6)) {
+    double m = rint(a * 512.0); /* exact scaling; rint: ties to even */
+    return sign | (unsigned)m;  /* m = 8 is the smallest normal's code */
+  }
+  int e = ilogb(a);                      /* 2^e <= a < 2^(e+1), e in [-6, 8] */
+  double f = rint((ldexp(a, -e) - 1.0) * 8.0);  /* fraction, 0..8 */
+  if (f == 8.0) {
+    f = 0.0;
+    e += 1;
+  }
+  unsigned code = (unsigned)((e + 7) << 3) | (unsigned)f;
+  return sign | (code > 0x7eu ? 0x7eu : code);
+}
+
+/*
+ * fp8 KV quantisation of n 16-bit values x (dtype) with a positive scale:
+ * code_i = e4m3(fl32(x_i / scale)), the division rounded once to fp32, so
+ * that the stored value is code * scale.  Codes go to the low byte of
+ * codes[i].
+ */
+void orc_quantize_e4m3(const uint16_t *x, int dtype, long n, float scale, uint16_t *codes) {
+  for (long i = 0; i < n; ++i) {
+    float xv = (float)orc_value(x[i], dtype); /* exact: 16-bit values fit in fp32 */
+    volatile float t = xv / scale;            /* one fp32 division */
+    codes[i] = (uint16_t)orc_e4m3_from_float(t);
+  }
 }
 
 void orc_decode(const uint16_t *in, int dtype, long n, double *out) {
@@ -127,23 +187,24 @@ int orc_page_minmax(const uint16_t *K, int dtype, int L, int d, int ell, int j0,
 
 /*
  * q is [G][d]: the G query heads that share this kv head.  kmin/kmax are
- * [nL][d].  For each page j and head h
+ * [nL][d], stored as kv_dtype codes of value / kscale (kscale = 1 for 16-bit
+ * keys; fp8 keys carry their kv head's scale).  For each page j and head h
  *     s_h(j) = sum_{c=0}^{d-1} max(q_h[c]*kmax_j[c], q_h[c]*kmin_j[c])
  * summed in increasing c, in fp32; the kv-head score is the maximum over
  * the group, S(j) = max_h s_h(j).  Scores are not scaled by 1/sqrt(d): a
  * positive scale does not change the ranking.
  */
-void orc_page_scores_f32(const uint16_t *q, const uint16_t *kmin,
-                         const uint16_t *kmax, int dtype, int nL, int G, int d,
-                         float *S) {
+void orc_page_scores_f32_kv(const uint16_t *q, int q_dtype, const uint16_t *kmin,
+                            const uint16_t *kmax, int kv_dtype, double kscale, int nL, int G,
+                            int d, float *S) {
   for (int j = 0; j < nL; ++j) {
     float best = -INFINITY;
     for (int h = 0; h < G; ++h) {
       float acc = 0.0f;
       for (int c = 0; c < d; ++c) {
-        float qv = (float)orc_value(q[(long)h * d + c], dtype);
-        float a = qv * (float)orc_value(kmax[(long)j * d + c], dtype);
-        float b = qv * (float)orc_value(kmin[(long)j * d + c], dtype);
+        float qv = (float)orc_value(q[(long)h * d + c], q_dtype);
+        float a = qv * (float)(kscale * orc_value(kmax[(long)j * d + c], kv_dtype));
+        float b = qv * (float)(kscale * orc_value(kmin[(long)j * d + c], kv_dtype));
         acc = acc + (a > b ? a : b);
       }
       if (acc > best || h == 0) best = acc;
@@ -152,21 +213,34 @@ void orc_page_scores_f32(const uint16_t *q, const uint16_t *kmin,
   }
 }
 
-/* The same score in fp64 (per head, not reduced over the group): [G][nL]. */
-void orc_page_scores_f64(const uint16_t *q, const uint16_t *kmin,
+/* q and the keys in one 16-bit dtype, no scale. */
+void orc_page_scores_f32(const uint16_t *q, const uint16_t *kmin,
                          const uint16_t *kmax, int dtype, int nL, int G, int d,
-                         double *s) {
+                         float *S) {
+  orc_page_scores_f32_kv(q, dtype, kmin, kmax, dtype, 1.0, nL, G, d, S);
+}
+
+/* The same score in fp64 (per head, not reduced over the group): [G][nL]. */
+void orc_page_scores_f64_kv(const uint16_t *q, int q_dtype, const uint16_t *kmin,
+                            const uint16_t *kmax, int kv_dtype, double kscale, int nL, int G,
+                            int d, double *s) {
   for (int h = 0; h < G; ++h)
     for (int j = 0; j < nL; ++j) {
       double acc = 0.0;
       for (int c = 0; c < d; ++c) {
-        double qv = orc_value(q[(long)h * d + c], dtype);
-        double a = qv * orc_value(kmax[(long)j * d + c], dtype);
-        double b = qv * orc_value(kmin[(long)j * d + c], dtype);
+        double qv = orc_value(q[(long)h * d + c], q_dtype);
+        double a = qv * (kscale * orc_value(kmax[(long)j * d + c], kv_dtype));
+        double b = qv * (kscale * orc_value(kmin[(long)j * d + c], kv_dtype));
         acc += a > b ? a : b;
       }
       s[(long)h * nL + j] = acc;
     }
+}
+
+void orc_page_scores_f64(const uint16_t *q, const uint16_t *kmin,
+                         const uint16_t *kmax, int dtype, int nL, int G, int d,
+                         double *s) {
+  orc_page_scores_f64_kv(q, dtype, kmin, kmax, dtype, 1.0, nL, G, d, s);
 }
 
 /* ---- (budget, top-k) --------------------------------------------------- */
@@ -272,14 +346,16 @@ int orc_streaming_tokens(long L, int S, int W, int *out) {
 /* ---- attention ---------------------------------------------------------- */
 
 /*
- * q [G][d], K and V [L][d] of one kv head; tokens[n] are positions into K/V.
+ * q [G][d] (q_dtype), K and V [L][d] of one kv head as kv_dtype codes whose
+ * values are code * kscale (keys) and code * vscale (values) -- 1 for 16-bit
+ * storage; tokens[n] are positions into K/V.
  * For each head g:  z_i = (q_g . k_{t_i}) / sqrt(d);  m = max_i z_i;
  *   out_g = sum_i exp(z_i - m) v_{t_i} / sum_i exp(z_i - m)   (fp64).
  * Returns 0, or -1 if n <= 0 or scratch cannot be allocated.
  */
-int orc_attention(const uint16_t *q, const uint16_t *K, const uint16_t *V,
-                  int dtype, int G, int d, const int *tokens, int n,
-                  double *out) {
+int orc_attention_kv(const uint16_t *q, int q_dtype, const uint16_t *K, const uint16_t *V,
+                     int kv_dtype, double kscale, double vscale, int G, int d,
+                     const int *tokens, int n, double *out) {
   if (n <= 0) return -1;
   double *z = (double *)malloc(sizeof(double) * (size_t)n);
   double *qd = (double *)malloc(sizeof(double) * (size_t)d);
@@ -290,12 +366,12 @@ int orc_attention(const uint16_t *q, const uint16_t *K, const uint16_t *V,
   }
   double scale = 1.0 / sqrt((double)d);
   for (int g = 0; g < G; ++g) {
-    for (int c = 0; c < d; ++c) qd[c] = orc_value(q[(long)g * d + c], dtype);
+    for (int c = 0; c < d; ++c) qd[c] = orc_value(q[(long)g * d + c], q_dtype);
     double m = -INFINITY;
     for (int i = 0; i < n; ++i) {
       const uint16_t *k = K + (long)tokens[i] * d;
       double dot = 0.0;
-      for (int c = 0; c < d; ++c) dot += qd[c] * orc_value(k[c], dtype);
+      for (int c = 0; c < d; ++c) dot += qd[c] * (kscale * orc_value(k[c], kv_dtype));
       z[i] = dot * scale;
       if (z[i] > m) m = z[i];
     }
@@ -308,13 +384,19 @@ int orc_attention(const uint16_t *q, const uint16_t *K, const uint16_t *V,
     for (int c = 0; c < d; ++c) o[c] = 0.0;
     for (int i = 0; i < n; ++i) {
       const uint16_t *v = V + (long)tokens[i] * d;
-      for (int c = 0; c < d; ++c) o[c] += z[i] * orc_value(v[c], dtype);
+      for (int c = 0; c < d; ++c) o[c] += z[i] * (vscale * orc_value(v[c], kv_dtype));
     }
     for (int c = 0; c < d; ++c) o[c] /= den;
   }
   free(z);
   free(qd);
   return 0;
+}
+
+int orc_attention(const uint16_t *q, const uint16_t *K, const uint16_t *V,
+                  int dtype, int G, int d, const int *tokens, int n,
+                  double *out) {
+  return orc_attention_kv(q, dtype, K, V, dtype, 1.0, 1.0, G, d, tokens, n, out);
 }
 
 /*
@@ -325,8 +407,9 @@ int orc_attention(const uint16_t *q, const uint16_t *K, const uint16_t *V,
  *   row_sum_g = sum_i exp(z_i - row_max_g)          (fp64).
  * Returns 0, or -1 if n <= 0.
  */
-int orc_softmax_stats(const uint16_t *q, const uint16_t *K, int dtype, int G, int d,
-                      const int *tokens, int n, double *row_max, double *row_sum) {
+int orc_softmax_stats_kv(const uint16_t *q, int q_dtype, const uint16_t *K, int kv_dtype,
+                         double kscale, int G, int d, const int *tokens, int n,
+                         double *row_max, double *row_sum) {
   if (n <= 0) return -1;
   double scale = 1.0 / sqrt((double)d);
   for (int g = 0; g < G; ++g) {
@@ -335,7 +418,7 @@ int orc_softmax_stats(const uint16_t *q, const uint16_t *K, int dtype, int G, in
       const uint16_t *k = K + (long)tokens[i] * d;
       double dot = 0.0;
       for (int c = 0; c < d; ++c)
-        dot += orc_value(q[(long)g * d + c], dtype) * orc_value(k[c], dtype);
+        dot += orc_value(q[(long)g * d + c], q_dtype) * (kscale * orc_value(k[c], kv_dtype));
       if (dot * scale > m) m = dot * scale;
     }
     double sum = 0.0;
@@ -343,13 +426,18 @@ int orc_softmax_stats(const uint16_t *q, const uint16_t *K, int dtype, int G, in
       const uint16_t *k = K + (long)tokens[i] * d;
       double dot = 0.0;
       for (int c = 0; c < d; ++c)
-        dot += orc_value(q[(long)g * d + c], dtype) * orc_value(k[c], dtype);
+        dot += orc_value(q[(long)g * d + c], q_dtype) * (kscale * orc_value(k[c], kv_dtype));
       sum += exp(dot * scale - m);
     }
     row_max[g] = m;
     row_sum[g] = sum;
   }
   return 0;
+}
+
+int orc_softmax_stats(const uint16_t *q, const uint16_t *K, int dtype, int G, int d,
+                      const int *tokens, int n, double *row_max, double *row_sum) {
+  return orc_softmax_stats_kv(q, dtype, K, dtype, 1.0, G, d, tokens, n, row_max, row_sum);
 }
 
 
@@ -365,9 +453,9 @@ int orc_softmax_stats(const uint16_t *q, const uint16_t *K, int dtype, int G, in
  * A token on a page missing from `pages` counts in no entry.  fp64, two
  * passes.  Returns 0, or -1 if n <= 0 or out of memory.
  */
-int orc_page_mass(const uint16_t *q, const uint16_t *K, int dtype, int G, int d,
-                  const int *tokens, int n, int ell, const int *pages, int n_pages,
-                  double *mass) {
+int orc_page_mass_kv(const uint16_t *q, int q_dtype, const uint16_t *K, int kv_dtype,
+                     double kscale, int G, int d, const int *tokens, int n, int ell,
+                     const int *pages, int n_pages, double *mass) {
   if (n <= 0) return -1;
   double *w = (double *)malloc(sizeof(double) * (size_t)n);
   if (!w) return -1;
@@ -378,7 +466,7 @@ int orc_page_mass(const uint16_t *q, const uint16_t *K, int dtype, int G, int d,
       const uint16_t *k = K + (long)tokens[i] * d;
       double dot = 0.0;
       for (int c = 0; c < d; ++c)
-        dot += orc_value(q[(long)g * d + c], dtype) * orc_value(k[c], dtype);
+        dot += orc_value(q[(long)g * d + c], q_dtype) * (kscale * orc_value(k[c], kv_dtype));
       w[i] = dot * scale;
       if (w[i] > m) m = w[i];
     }
@@ -396,4 +484,10 @@ int orc_page_mass(const uint16_t *q, const uint16_t *K, int dtype, int G, int d,
   }
   free(w);
   return 0;
+}
+
+int orc_page_mass(const uint16_t *q, const uint16_t *K, int dtype, int G, int d,
+                  const int *tokens, int n, int ell, const int *pages, int n_pages,
+                  double *mass) {
+  return orc_page_mass_kv(q, dtype, K, dtype, 1.0, G, d, tokens, n, ell, pages, n_pages, mass);
 }

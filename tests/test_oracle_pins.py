@@ -559,3 +559,111 @@ def test_page_mass_of_a_decode_layer():
     assert mass.shape == (2, pages.size)
     assert np.allclose(mass.sum(1), 1.0, atol=1e-13)
     assert np.all(mass[:, pages.tolist().index(20)] > 0.9)
+
+
+# ---- fp8 (e4m3) KV storage ------------------------------------------------------
+
+def _torch_e4m3(codes):
+    """Library decode of e4m3 codes (torch's float8_e4m3fn)."""
+    c = torch.from_numpy(np.asarray(codes, np.uint8).copy())
+    return c.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def test_e4m3_decode_all_codes_match_the_library():
+    codes = np.arange(256)
+    got = oracle.e4m3_value(codes)
+    ref = _torch_e4m3(codes)
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    m = ~np.isnan(ref)
+    assert np.array_equal(got[m], ref[m])
+    # the format's landmarks
+    assert oracle.e4m3_value([0x7E, 0x08, 0x01, 0x38, 0xB8]).tolist() == \
+        [448.0, 2.0 ** -6, 2.0 ** -9, 1.0, -1.0]
+    assert np.isnan(oracle.e4m3_value([0x7F, 0xFF])).all()
+
+
+def test_e4m3_encode_rounds_like_the_library_and_saturates():
+    r = np.random.default_rng(41)
+    grid = _torch_e4m3(np.arange(0x7F))                   # every finite magnitude
+    mids = (grid[:-1] + grid[1:]) / 2                     # exact ties
+    x = np.concatenate([grid, mids, -mids, r.uniform(-448, 448, 4000),
+                        r.standard_normal(2000) * 1e-2, np.float32(2.0 ** -10) * np.arange(9)])
+    x = x.astype(np.float32)
+    got = oracle.e4m3_from_float(x)
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(got, ref)
+    # saturation (finite clamp) above the largest magnitude, and NaN
+    big = np.array([448.0, 449.0, 463.9, 464.0, 1e4, np.inf], np.float32)
+    assert oracle.e4m3_from_float(big).tolist() == [0x7E] * 6
+    assert oracle.e4m3_from_float(-big).tolist() == [0xFE] * 6
+    assert oracle.e4m3_from_float([np.nan]).tolist() == [0x7F]
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_e4m3_quantize_divides_once_in_fp32(dtype):
+    r = np.random.default_rng(43)
+    xb = W.to_bits((r.standard_normal(5000) * 3).astype(np.float32), dtype)
+    scale = np.float32(0.0371)
+    got = oracle.quantize_e4m3(xb, dtype, scale)
+    t = torch.from_numpy(oracle.decode(xb, dtype).astype(np.float32)) / float(scale)
+    ref = t.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(got, ref)
+    # a value that is exactly scale * code comes back as that code
+    assert oracle.quantize_e4m3(W.to_bits(np.float32([0.5]), dtype), dtype, 0.25).tolist() == \
+        [0x40]
+
+
+def test_fp8_scores_scale_with_the_key_scale_and_bound_the_keys():
+    r = np.random.default_rng(45)
+    L, d, G, ell = 160, 64, 2, 16
+    K = r.integers(0, 0x7F, (L, d)) | (r.integers(0, 2, (L, d)) << 7)
+    K = K.astype(np.uint16)
+    q = W.to_bits(r.standard_normal((G, d)).astype(np.float32), "bf16")
+    mn, mx = oracle.page_minmax(K, "e4m3", ell)
+    s1 = oracle.page_scores(q, mn, mx, "bf16", "e4m3", 1.0)
+    s2 = oracle.page_scores(q, mn, mx, "bf16", "e4m3", 2.0)
+    assert np.array_equal(s2, 2 * s1)
+    # upper bound: s_h(j) >= q_h . k_t for every token of page j (fp64)
+    ks = 0.75
+    s64 = oracle.page_scores_f64(q, mn, mx, "bf16", "e4m3", ks)
+    dots = oracle.decode(q, "bf16") @ (ks * oracle.e4m3_value(K)).T   # [G][L]
+    for j in range(L // ell):
+        assert np.all(s64[:, j] >= dots[:, j * ell:(j + 1) * ell].max(1) - 1e-12)
+
+
+def test_fp8_decode_layer_is_sdpa_over_dequantized_kv():
+    # budget >= L, no streaming head: the fp8 layer attends every token of
+    # the quantised cache -- torch SDPA over the dequantised values, where the
+    # codes come from the library's own fp32 division and e4m3 rounding
+    r = np.random.default_rng(47)
+    L, d, Hkv, G = 300, 64, 2, 2
+    ks, vs = [0.02, 0.5], [0.125, 3.0]
+    cfg = dict(num_q_heads=Hkv * G, num_kv_heads=Hkv, head_dim=d, dtype="bf16",
+               logical_page=16, streaming=[False] * Hkv, sink=0, window=0,
+               token_budget=10 ** 6, reuse_interval=4, max_context=1024,
+               kv_fp8=True, k_scale=ks, v_scale=vs)
+    orc = oracle.OracleLayer(cfg)
+    sid = orc.new_seq()
+    K = W.to_bits(r.standard_normal((L, Hkv, d)).astype(np.float32), "bf16")
+    V = W.to_bits(r.standard_normal((L, Hkv, d)).astype(np.float32), "bf16")
+    q = W.to_bits(r.standard_normal((Hkv * G, d)).astype(np.float32), "bf16")
+    orc.append(sid, K, V)
+    orc.select(sid, q)
+    out = orc.attend(sid, q)
+
+    def deq(bits, scale):
+        t = torch.from_numpy(oracle.decode(bits, "bf16").astype(np.float32)) / np.float32(scale)
+        return t.to(torch.float8_e4m3fn).to(torch.float64) * float(np.float32(scale))
+
+    qd = torch.from_numpy(oracle.decode(q, "bf16"))
+    for h in range(Hkv):
+        kd, vd = deq(K[:, h], ks[h]), deq(V[:, h], vs[h])
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            qd[h * G:(h + 1) * G][None, :, None, :], kd[None, None].expand(1, G, -1, -1),
+            vd[None, None].expand(1, G, -1, -1))[0, :, 0].numpy()
+        assert np.allclose(out[h * G:(h + 1) * G], ref, rtol=0, atol=1e-12), h
+    # the stored codes and the page metadata are the quantised keys
+    s = orc.seqs[sid]
+    assert np.array_equal(s.K[0, :L], oracle.quantize_e4m3(K[:, 0], "bf16", ks[0]))
+    mn, mx = oracle.page_minmax(s.K[1, :L], "e4m3", 16)
+    assert np.array_equal(s.kmin[1], mn) and np.array_equal(s.kmax[1], mx)
