@@ -55,6 +55,8 @@ def parse():
     ap.add_argument("--streaming-layers", default="",
                     help="comma-separated layer indices whose kv heads are all streaming "
                          "(the other layers keep the workload's head split)")
+    ap.add_argument("--kv-fp8", action="store_true",
+                    help="store K/V as fp8 E4M3 codes (scale 1/32 on every kv head)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-roofline", action="store_true")
@@ -84,15 +86,15 @@ def whole_job_gbs(bytes_per_rank, ms_max, world):
 
 # ---- algorithmic bytes ------------------------------------------------------
 
-def step_bytes(wl, L, n_att, selected):
+def step_bytes(wl, L, n_att, selected, e=2):
     """Bytes one layer-step must read for one sequence of length L.
 
     n_att: attended logical pages per dynamic head (selection plus pages
     created since it).  Dynamic heads read every token of those pages (the
     last one holds L - (nL-1)*ell tokens); streaming heads read
     min(L, sink + window) tokens; a selection step also scans the min/max
-    rows of the nL - 1 candidate pages."""
-    e = 2
+    rows of the nL - 1 candidate pages.  e: bytes per stored element (2, or
+    1 for fp8 storage)."""
     Hd = sum(1 for s in wl.streaming if not s)
     Hs = wl.Hkv - Hd
     nL = -(-L // wl.ell)
@@ -182,7 +184,9 @@ class ClockSampler:
 class Layers:
     """n_layers independent caches of the workload, one sequence each."""
 
-    def __init__(self, wl, n_layers, device, extra_tokens, streaming_layers=()):
+    FP8_SCALE = 1.0 / 32
+
+    def __init__(self, wl, n_layers, device, extra_tokens, streaming_layers=(), kv_fp8=False):
         import torch
         import sparse_paged_decode_logical_gb300 as spd
         self.torch, self.wl, self.device = torch, wl, device
@@ -190,12 +194,16 @@ class Layers:
         # per layer: the workload's head split, or every kv head streaming
         self.wls = [dataclasses.replace(wl, streaming=[True] * wl.Hkv)
                     if layer in streaming_layers else wl for layer in range(n_layers)]
+        self.elem = 1 if kv_fp8 else 2
         self.caches, self.seqs = [], []
         for layer in range(n_layers):
             cfg = self.wls[layer].lib_config()
             cfg["max_context"] = L0 + extra_tokens
             cfg["max_seqs"] = 1
             cfg["num_physical_pages"] = -(-cfg["max_context"] // wl.P)
+            if kv_fp8:
+                cfg.update(kv_fp8=True, k_scale=[self.FP8_SCALE] * wl.Hkv,
+                           v_scale=[self.FP8_SCALE] * wl.Hkv)
             c = spd.SparsePagedKVCache(device=device, **cfg)
             # every kernel on the stream is this library's and each layer's
             # cache is written only through its own context: the next layer
@@ -241,7 +249,7 @@ class Layers:
         """(dyn, str, meta) bytes of the layer's current step (see step_bytes)."""
         inf = self.caches[layer].seq_info(self.seqs[layer])
         n_att = inf["pages_kept"] + (-(-inf["length"] // self.wl.ell)) - inf["pages_at_selection"]
-        return step_bytes(self.wls[layer], inf["length"], n_att, selected)
+        return step_bytes(self.wls[layer], inf["length"], n_att, selected, self.elem)
 
     def step(self, row, outs=None):
         """Enqueue one decode step on every layer; returns its algorithmic bytes."""
@@ -262,7 +270,7 @@ def run_ours(args, rank, world, device):
     wl = W.workload(args.workload)
     n_l = args.layers
     extra = args.warmup + args.steps + (0 if args.no_e2e else args.steps) + 64
-    layers = Layers(wl, n_l, device, extra, streaming_layers(args))
+    layers = Layers(wl, n_l, device, extra, streaming_layers(args), args.kv_fp8)
     stream = torch.cuda.Stream(device=device)
     dist = None
     if world > 1:
@@ -318,6 +326,8 @@ def run_ours(args, rank, world, device):
     # roofline: the decode kernel alone (read-only, replayable), events around
     # every launch inside one graph
     rl = None if args.no_roofline else roofline(layers, stream, args.roofline_iters)
+    if rl is not None:
+        rl["exports"] = variant_timings(layers, stream)
     clk = clocks.stop()
 
     # end to end: pinned host inputs -> device -> step -> pinned host outputs
@@ -357,7 +367,7 @@ def run_ours(args, rank, world, device):
         "dtype": wl.dtype,
         "data": "synthetic (seeded N(0,1) K/V in bf16, needle pages at 10/50/90% depth)",
         "config": arm_config(wl, n_l, n_sel, total_bytes / args.steps, world,
-                             streaming_layers(args)),
+                             streaming_layers(args), args.kv_fp8),
         "bytes_per_step": {"dyn": tot[0] / args.steps, "stream": tot[1] / args.steps,
                            "meta": tot[2] / args.steps},
         "gpu_launches": launches,
@@ -374,7 +384,8 @@ def streaming_layers(args):
     return sorted({int(x) for x in args.streaming_layers.split(",") if x.strip()})
 
 
-def arm_config(wl, n_layers, n_sel=None, bytes_per_step=None, world=1, all_streaming=()):
+def arm_config(wl, n_layers, n_sel=None, bytes_per_step=None, world=1, all_streaming=(),
+               kv_fp8=False):
     c = {
         "workload": wl.name,
         "shape": "Llama-3-8B attention: 32 q / 8 kv heads, d 128, bf16",
@@ -389,9 +400,53 @@ def arm_config(wl, n_layers, n_sel=None, bytes_per_step=None, world=1, all_strea
     }
     if all_streaming:
         c["all_streaming_layers"] = list(all_streaming)
+    if kv_fp8:
+        c["kv_storage"] = "fp8 e4m3, scale %g per kv head" % Layers.FP8_SCALE
     if n_sel is not None:
         c["selection_steps_in_window"] = n_sel
     return c
+
+
+def variant_timings(layers, stream, iters=10):
+    """Per-launch time of the attention call with its optional exports, each
+    timed like `roofline`: a graph of `iters` x n_layers back-to-back calls,
+    median over replays.  plain: spd_sparse_decode_attention; stats: + row
+    max / row sum; page_mass: + the dynamic heads' per-page attention mass."""
+    import torch
+    n = len(layers.caches)
+    row = layers.inputs(1)[0]
+    q = [row[layer][0] for layer in range(n)]
+    calls = {
+        "plain": lambda c, l: c.sparse_decode_attention(q[l], [layers.seqs[l]],
+                                                        out=layers.out[l], stream=stream),
+        "stats": lambda c, l: c.sparse_decode_attention_stats(q[l], [layers.seqs[l]],
+                                                              stream=stream),
+        "page_mass": lambda c, l: c.sparse_decode_attention_page_mass(
+            q[l], [layers.seqs[l]], stream=stream),
+    }
+    res = {}
+    for name, call in calls.items():
+        torch.cuda.synchronize()
+        l0 = layers.launches()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(iters):
+                for layer, c in enumerate(layers.caches):
+                    call(c, layer)
+        per_replay = layers.launches() - l0
+        times = []
+        with torch.cuda.stream(stream):
+            for rep in range(12):
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                g.replay()
+                b.record(stream)
+                b.synchronize()
+                if rep:
+                    times.append(a.elapsed_time(b))
+        res[name + "_us_per_launch"] = round(float(np.median(times)) / per_replay * 1e3, 3)
+    return res
 
 
 def roofline(layers, stream, iters):

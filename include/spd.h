@@ -86,11 +86,25 @@ typedef struct {
   int reuse_interval;/* C >= 1: selection runs when step % C == 0            */
   unsigned long long free_list_seed; /* 0: pages handed out in order;
                                         else a seeded permutation of the pool */
+  /* fp8 KV storage (the LServe write-up's sparse_config, section 5.2, names
+   * an fp8 KV cache).  kv_fp8 = 1: keys, values and the key min/max metadata
+   * are stored as OCP fp8 E4M3 codes of value / scale -- each 16-bit input
+   * divided once in fp32, rounded to nearest even, saturated at +-448 --
+   * with one scale per kv head for keys and one for values (host [Hkv]
+   * positive finite fp32, copied at spd_create; NULL: all 1).  q and the
+   * K/V handed to the append calls stay `dtype`; page scores and attention
+   * read the stored values code * scale.  Needs head_dim 128.  kv_fp8 = 0
+   * (a zero-initialised config) keeps 16-bit storage and ignores the scales. */
+  int kv_fp8;
+  const float *k_scale;
+  const float *v_scale;
 } spd_config;
 
 /*
  * Bytes of every device buffer the caller must provide.  Layouts (elements
- * of `dtype` unless noted; Hd / Hs = number of dynamic / streaming kv heads,
+ * of `dtype` unless noted -- one-byte E4M3 codes for k_pool, v_pool, meta,
+ * stream_k and stream_v when kv_fp8 is set; Hd / Hs = number of dynamic /
+ * streaming kv heads,
  * R = P / l, MP = ceil(max_context / P), KS = pages kept at the largest
  * budget):
  *   k_pool, v_pool [num_physical_pages][Hd][P][d]   keys / values of dynamic

@@ -43,7 +43,9 @@ class spd_config(ctypes.Structure):
                 ("kv_head_is_streaming", ctypes.POINTER(ctypes.c_ubyte)),
                 ("sink", ctypes.c_int), ("window", ctypes.c_int),
                 ("token_budget", ctypes.c_int), ("reuse_interval", ctypes.c_int),
-                ("free_list_seed", ctypes.c_ulonglong)]
+                ("free_list_seed", ctypes.c_ulonglong), ("kv_fp8", ctypes.c_int),
+                ("k_scale", ctypes.POINTER(ctypes.c_float)),
+                ("v_scale", ctypes.POINTER(ctypes.c_float))]
 
 
 class spd_sizes(ctypes.Structure):
@@ -109,8 +111,11 @@ def lib():
 def make_config(num_q_heads, num_kv_heads, head_dim, dtype, logical_page,
                 physical_page, num_physical_pages, max_seqs, max_context,
                 streaming=None, sink=0, window=0, token_budget=0,
-                reuse_interval=4, free_list_seed=0):
-    """Build an ``spd_config`` (the streaming mask array is kept alive on it)."""
+                reuse_interval=4, free_list_seed=0, kv_fp8=False, k_scale=None,
+                v_scale=None):
+    """Build an ``spd_config`` (the streaming mask and scale arrays are kept
+    alive on it).  kv_fp8: store K/V as fp8 E4M3 codes of value / scale, with
+    per-kv-head k_scale / v_scale (default 1)."""
     c = spd_config()
     c.num_q_heads, c.num_kv_heads, c.head_dim = num_q_heads, num_kv_heads, head_dim
     c.dtype = DTYPES[dtype] if isinstance(dtype, str) else int(dtype)
@@ -122,6 +127,12 @@ def make_config(num_q_heads, num_kv_heads, head_dim, dtype, logical_page,
         c.kv_head_is_streaming = ctypes.cast(arr, ctypes.POINTER(ctypes.c_ubyte))
     c.sink, c.window, c.token_budget = sink, window, token_budget
     c.reuse_interval, c.free_list_seed = reuse_interval, free_list_seed
+    c.kv_fp8 = 1 if kv_fp8 else 0
+    for name, vals in (("k_scale", k_scale), ("v_scale", v_scale)):
+        if vals is not None:
+            arr = (ctypes.c_float * num_kv_heads)(*[float(x) for x in vals])
+            setattr(c, "_" + name, arr)
+            setattr(c, name, ctypes.cast(arr, ctypes.POINTER(ctypes.c_float)))
     return c
 
 

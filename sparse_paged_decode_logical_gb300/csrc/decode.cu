@@ -52,8 +52,10 @@ cudaError_t prepare_decode_kernels() {
   if ((e = prep_g<__half, 128>(0)) != cudaSuccess) return e;
   if ((e = prep_g<__nv_bfloat16, 64>(1)) != cudaSuccess) return e;
   if ((e = prep_g<__nv_bfloat16, 128>(1)) != cudaSuccess) return e;
-  // the mass-exporting instances: same shared memory and block, same clusters
-  return prepare_decode_mass_kernels();
+  // the mass-exporting and fp8 instances: same block; their cluster sizes are
+  // taken to be the plain kernel's (the fp8 ones need no more shared memory)
+  if ((e = prepare_decode_mass_kernels()) != cudaSuccess) return e;
+  return prepare_decode_fp8_kernels();
 }
 
 // Largest power-of-two cluster (<= 16) the decode kernel can be launched with.
@@ -71,6 +73,7 @@ cudaError_t launch_decode_tiles(const TileDecodeParams &p, int dtype, int d, int
                                 cudaStream_t s, long long *n) {
   if (p.n_seqs == 0 || p.total_items == 0) return cudaSuccess;
   *n += 1;
+  if (p.kv_fp8) return d == 128 ? launch_decode_tiles_fp8(p, dtype, G, s) : cudaErrorInvalidValue;
   if (p.page_part != nullptr) return launch_decode_tiles_mass(p, dtype, d, G, s);
   return launch_variant<false>(p, dtype, d, G, s);
 }

@@ -56,6 +56,7 @@
 // parallel).
 #pragma once
 #include <cuda_bf16.h>
+#include <type_traits>
 #include <cuda_fp16.h>
 #include <math_constants.h>
 
@@ -73,12 +74,15 @@ constexpr int kStages = 12;                // shared-memory stage ring
 constexpr int kMaxDesc = 256;              // tiles one CTA may take
 constexpr uint32_t kWaitLimit = 1u << 24;  // bounded mbarrier polls
 
-template <int D>
+// A tile row is D elements of 2 bytes, or of 1 byte with fp8 storage (F8);
+// it is stored as 128-byte "boxes" (64 16-bit channels or 128 fp8 ones).
+template <int D, bool F8 = false>
 struct Geo {
-  static constexpr int kBoxes = D / 64;                      // 64-channel boxes per row
+  static constexpr int kRowBytes = D * (F8 ? 1 : 2);
+  static constexpr int kBoxes = kRowBytes / 128;             // 128-byte boxes per row
   static constexpr int kBoxBytes = kRows * 128;              // one box: 16 rows x 128 B
   static constexpr int kTileBytes = 2 * kBoxes * kBoxBytes;  // K boxes then V boxes
-  static constexpr int kCPL = D / 32;                        // channels per lane in P.V
+  static constexpr int kCPL = D / 32;                        // channels per lane (append)
 };
 
 template <int G>
@@ -96,7 +100,7 @@ struct TileDesc {
 // rescale buffers, per-warp and per-CTA row max / sum / output, flags), then
 // the stages at a 1024-byte aligned offset.  After the tile loop the stage
 // region holds the warp-merge buffer and later the global-merge buffers.
-template <int D, int G>
+template <int D, int G, bool F8 = false>
 struct Smem {
   static constexpr int kBars = 0;                                      // uint64 [kStages]
   static constexpr int kDesc = kBars + kStages * 8;                    // TileDesc [kMaxDesc]
@@ -109,7 +113,7 @@ struct Smem {
   static constexpr int kFlag = kInbox + (32 * G + G * D) * 4;          // int [4 + kStages]
   static constexpr int kTopkBar = (kFlag + (4 + kStages) * 4 + 7) / 8 * 8;  // uint64
   static constexpr int kTiles = (kTopkBar + 8 + 1023) / 1024 * 1024;
-  static constexpr int kStageRegion = kStages * Geo<D>::kTileBytes;
+  static constexpr int kStageRegion = kStages * Geo<D, F8>::kTileBytes;
   static constexpr int kMergeRegion = kWarps * G * D * 4;              // o of every warp
   static constexpr int kCombineRegion = 256 * G * 12 + 64;             // (m, l), weights
   // before the tiles of a fused selection step: the top-k buffers, then the
@@ -201,11 +205,19 @@ __device__ void write_page_mass(const TileDecodeParams &p, int i, int sub, const
 }
 
 // kMass: the per-page attention mass is exported (its own instance, so the
-// plain kernel carries none of that work)
-template <typename T, int D, int G, bool kMass>
+// plain kernel carries none of that work).  kF8: K/V are stored as fp8 E4M3
+// codes of value / scale (head_dim 128): tiles are half the bytes, widened
+// exactly to fp16 on their way into the tensor-core fragments, and the
+// products run in fp16 (q narrowed to fp16 once, P split into fp16 halves).
+template <typename T, int D, int G, bool kMass, bool kF8 = false>
 __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_constant__ TileDecodeParams p) {
-  using Gm = Geo<D>;
-  using Sm = Smem<D, G>;
+  static_assert(!kF8 || D == 128, "fp8 storage: one 128-byte row per token");
+  // tensor-core element type: T, or fp16 with fp8 storage (an E4M3 value
+  // widens to fp16 in one instruction; q is narrowed to fp16 once)
+  using TM = typename std::conditional<kF8, __half, T>::type;
+  constexpr bool kMmaBf = IsBF16<TM>::v;
+  using Gm = Geo<D, kF8>;
+  using Sm = Smem<D, G, kF8>;
   constexpr int CPL = Gm::kCPL;  // channels per lane of the fused append
   constexpr int GPAD = GP<G>::v;
   extern __shared__ uint8_t smem_raw[];
@@ -411,9 +423,15 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
     uint8_t *vd = kd + Gm::kBoxes * Gm::kBoxBytes;
     mbar_arrive_expect_tx(&bars[st], Gm::kTileBytes);
     // one copy per tile of K and one of V: the map's third dimension walks
-    // the 64-channel halves, which land box after box
-    tma_load_4d(kd, mk, 0, td.y, 0, td.z, &bars[st]);
-    tma_load_4d(vd, mv, 0, td.y, 0, td.z, &bars[st]);
+    // the 64-channel halves, which land box after box (fp8: one 128-byte
+    // box per row, a 3-D map)
+    if constexpr (kF8) {
+      tma_load_3d(kd, mk, 0, td.y, td.z, &bars[st]);
+      tma_load_3d(vd, mv, 0, td.y, td.z, &bars[st]);
+    } else {
+      tma_load_4d(kd, mk, 0, td.y, 0, td.z, &bars[st]);
+      tma_load_4d(vd, mv, 0, td.y, 0, td.z, &bars[st]);
+    }
   };
   if (lane == 0) {
     // the stage region was read and written through the generic proxy (the
@@ -425,8 +443,13 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
     for (int t = kStages + warp; t < nt; t += kWarps) {
       const TileDesc td = tdesc[t];
       if (td.n_valid <= 0) continue;
-      tma_prefetch_l2_4d(mk, 0, td.y, 0, td.z);
-      tma_prefetch_l2_4d(mv, 0, td.y, 0, td.z);
+      if constexpr (kF8) {
+        tma_prefetch_l2_3d(mk, 0, td.y, td.z);
+        tma_prefetch_l2_3d(mv, 0, td.y, td.z);
+      } else {
+        tma_prefetch_l2_4d(mk, 0, td.y, 0, td.z);
+        tma_prefetch_l2_4d(mv, 0, td.y, 0, td.z);
+      }
     }
   }
 
@@ -444,8 +467,15 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
       if (g8 < G) {
-        qb[kk][0] = qp[(g8 * D + kk * 16 + 2 * t4) / 2];
-        qb[kk][1] = qp[(g8 * D + kk * 16 + 2 * t4 + 8) / 2];
+        if constexpr (kF8) {
+          // k slots {2t4, 2t4+1 | 2t4+8, 2t4+9} of k-step kk are channels
+          // 16kk + 4t4 + {0, 1 | 2, 3} (the order the fp8 K fragments use)
+          qb[kk][0] = to_f16x2<T>(qp[(g8 * D + kk * 16 + 4 * t4) / 2]);
+          qb[kk][1] = to_f16x2<T>(qp[(g8 * D + kk * 16 + 4 * t4 + 2) / 2]);
+        } else {
+          qb[kk][0] = qp[(g8 * D + kk * 16 + 2 * t4) / 2];
+          qb[kk][1] = qp[(g8 * D + kk * 16 + 2 * t4 + 8) / 2];
+        }
       } else {
         qb[kk][0] = qb[kk][1] = 0u;
       }
@@ -463,7 +493,8 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
 #pragma unroll
     for (int e = 0; e < 4; ++e) oacc[m][e] = 0.f;
   float *Pw = P_all + warp * kRows * GPAD;
-  const float sc = p.scale_log2;
+  // fp8: the stored keys are code * k_scale; the scale folds into the logits'
+  const float sc = kF8 ? p.scale_log2 * p.k_scale[h] : p.scale_log2;
 
   for (int t = warp; t < nt;) {
     const TileDesc td = tdesc[t];
@@ -484,7 +515,54 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
     if (td.n_valid > 0) {
       const int nv = td.n_valid;
 
-      if (do_append && t == nt - 1) {
+      if (kF8 && do_append && t == nt - 1) {
+        // the newest token, row nv-1 of the unit's last tile, as E4M3 codes:
+        // this lane's 4 channels are one 4-byte word of a 16-byte chunk
+        const int r = nv - 1;
+        const int cb = lane * CPL;
+        const size_t src = ((size_t)i * p.Hkv + h) * D + cb;
+        const T *kn = reinterpret_cast<const T *>(p.k_new) + src;
+        const T *vn = reinterpret_cast<const T *>(p.v_new) + src;
+        const float ksc = p.k_scale[h], vsc = p.v_scale[h];
+        uint32_t kc = 0u, vc = 0u;
+#pragma unroll
+        for (int e = 0; e < CPL; ++e) {
+          kc |= e4m3_code(tof(kn[e]), ksc) << (8 * e);
+          vc |= e4m3_code(tof(vn[e]), vsc) << (8 * e);
+        }
+        const uint32_t off = (uint32_t)r * 128u + ((((uint32_t)cb >> 4) ^ (uint32_t)(r & 7)) << 4) +
+                             (uint32_t)(cb & 15);
+        *reinterpret_cast<uint32_t *>(kt + off) = kc;
+        *reinterpret_cast<uint32_t *>(vt + off) = vc;
+        const size_t grow = dyn ? ((size_t)td.z * p.P + td.y + r) * D + cb
+                                : ((size_t)td.y + r) * D + cb;
+        *reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(dyn ? p.k_pool : p.stream_k) + grow) =
+            kc;
+        *reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(dyn ? p.v_pool : p.stream_v) + grow) =
+            vc;
+        if (dyn) {
+          const int j = nL - 1;
+          uint8_t *mrow = static_cast<uint8_t *>(p.meta) +
+                          ((size_t)td.z * p.R + (j % p.R)) * 2 * D + cb;
+          const bool fresh = (L - 1) % p.ell == 0;
+          uint32_t mn = kc, mx = kc;
+          if (!fresh) {
+            const uint32_t omin = *reinterpret_cast<const uint32_t *>(mrow);
+            const uint32_t omax = *reinterpret_cast<const uint32_t *>(mrow + D);
+            mn = mx = 0u;
+#pragma unroll
+            for (int e = 0; e < CPL; ++e) {
+              const uint32_t x = (kc >> (8 * e)) & 0xffu;
+              const uint32_t a = (omin >> (8 * e)) & 0xffu, b = (omax >> (8 * e)) & 0xffu;
+              mn |= (e4m3_key(x) < e4m3_key(a) ? x : a) << (8 * e);
+              mx |= (e4m3_key(x) > e4m3_key(b) ? x : b) << (8 * e);
+            }
+          }
+          *reinterpret_cast<uint32_t *>(mrow) = mn;
+          *reinterpret_cast<uint32_t *>(mrow + D) = mx;
+        }
+        __syncwarp();
+      } else if (!kF8 && do_append && t == nt - 1) {
         // the newest token is row nv-1 of the unit's last tile
         const int r = nv - 1;
         const int cb = lane * CPL;
@@ -553,7 +631,28 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
       // q.K^T for 16 rows x 8 (padded) heads
       // two accumulators (even and odd k-steps) halve the chain of dependent MMAs
       float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
-      {
+      if constexpr (kF8) {
+        // ldmatrix of byte pairs: matrices (rows 0-7 | 8-15) x (16-channel
+        // chunk 2k2 | 2k2+1); a lane gets channels 4t4..4t4+3 of rows g8 and
+        // g8+8 -- the A fragment's k slots {2t4, 2t4+1} (low half) and
+        // {2t4+8, 2t4+9} (high half) in the q fragments' channel order
+        const int row = (lane & 7) + ((lane >> 3) & 1) * 8;
+        const int chalf = lane >> 4;
+        const uint32_t kbase = smem_u32(kt);
+#pragma unroll
+        for (int k2 = 0; k2 < D / 32; ++k2) {
+          uint32_t r0, r1, r2, r3;
+          ldmatrix_x4(kbase + swz128(row, 2 * k2 + chalf), r0, r1, r2, r3);
+          const uint32_t a0[4] = {e4m3x2_to<__half>(r0), e4m3x2_to<__half>(r1), e4m3x2_to<__half>(r0 >> 16),
+                                  e4m3x2_to<__half>(r1 >> 16)};
+          mma_16816<kMmaBf>(acc, a0, qb[2 * k2][0], qb[2 * k2][1]);
+          const uint32_t a1[4] = {e4m3x2_to<__half>(r2), e4m3x2_to<__half>(r3), e4m3x2_to<__half>(r2 >> 16),
+                                  e4m3x2_to<__half>(r3 >> 16)};
+          mma_16816<kMmaBf>(acc2, a1, qb[2 * k2 + 1][0], qb[2 * k2 + 1][1]);
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[e] += acc2[e];
+      } else {
         const int row = (lane & 7) + ((lane >> 3) & 1) * 8;
         const int chalf = lane >> 4;
         const uint32_t kbase = smem_u32(kt);
@@ -564,9 +663,9 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
           uint32_t a[4];
           ldmatrix_x4(kbase + box * Gm::kBoxBytes + swz128(row, chunk), a[0], a[1], a[2], a[3]);
           if (kk & 1)
-            mma_16816<IsBF16<T>::v>(acc2, a, qb[kk][0], qb[kk][1]);
+            mma_16816<kMmaBf>(acc2, a, qb[kk][0], qb[kk][1]);
           else
-            mma_16816<IsBF16<T>::v>(acc, a, qb[kk][0], qb[kk][1]);
+            mma_16816<kMmaBf>(acc, a, qb[kk][0], qb[kk][1]);
         }
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[e] += acc2[e];
@@ -638,9 +737,9 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
         uint16_t hi[4], lo[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const T th = Cvt<T>::from(pv[e]);
+          const TM th = Cvt<TM>::from(pv[e]);
           hi[e] = *reinterpret_cast<const uint16_t *>(&th);
-          const T tl = Cvt<T>::from(pv[e] - tof(th));
+          const TM tl = Cvt<TM>::from(pv[e] - tof(th));
           lo[e] = *reinterpret_cast<const uint16_t *>(&tl);
         }
         bh0 = (uint32_t)hi[0] | ((uint32_t)hi[1] << 16);
@@ -648,7 +747,30 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
         bl0 = (uint32_t)lo[0] | ((uint32_t)lo[1] << 16);
         bl1 = (uint32_t)lo[2] | ((uint32_t)lo[3] << 16);
       }
-      {
+      if constexpr (kF8) {
+        // A = V^T, transposed ldmatrix of byte pairs: matrices (tokens 0-7 |
+        // 8-15) x (chunk 2m2 | 2m2+1); a lane gets tokens 2t4, 2t4+1 (+8) x
+        // channels 2g8, 2g8+1.  Rows of the m-tile are channel 2g8 (m = g8)
+        // and 2g8+1 (m = g8+8): a byte permute splits the word into them.
+        const int row = (lane & 7) + ((lane >> 3) & 1) * 8;
+        const int chalf = lane >> 4;
+        const uint32_t vbase = smem_u32(vt);
+#pragma unroll
+        for (int m2 = 0; m2 < D / 32; ++m2) {
+          uint32_t r0, r1, r2, r3;
+          ldmatrix_x4_trans(vbase + swz128(row, 2 * m2 + chalf), r0, r1, r2, r3);
+          const uint32_t e0 = __byte_perm(r0, 0u, 0x3120), e1 = __byte_perm(r1, 0u, 0x3120);
+          const uint32_t e2 = __byte_perm(r2, 0u, 0x3120), e3 = __byte_perm(r3, 0u, 0x3120);
+          const uint32_t a0[4] = {e4m3x2_to<__half>(e0), e4m3x2_to<__half>(e0 >> 16), e4m3x2_to<__half>(e1),
+                                  e4m3x2_to<__half>(e1 >> 16)};
+          mma_16816<kMmaBf>(oacc[2 * m2], a0, bh0, bh1);
+          mma_16816<kMmaBf>(oacc[2 * m2], a0, bl0, bl1);
+          const uint32_t a1[4] = {e4m3x2_to<__half>(e2), e4m3x2_to<__half>(e2 >> 16), e4m3x2_to<__half>(e3),
+                                  e4m3x2_to<__half>(e3 >> 16)};
+          mma_16816<kMmaBf>(oacc[2 * m2 + 1], a1, bh0, bh1);
+          mma_16816<kMmaBf>(oacc[2 * m2 + 1], a1, bl0, bl1);
+        }
+      } else {
         // A = V^T for m-tile m: matrix j of ldmatrix.x4.trans takes token rows
         // (lane & 7) + 8 * (j >> 1) and channel chunk 2m + (j & 1)
         const int j = lane >> 3;
@@ -661,8 +783,8 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
           uint32_t a[4];
           ldmatrix_x4_trans(vbase + box * Gm::kBoxBytes + swz128(row, chunk), a[0], a[1], a[2],
                             a[3]);
-          mma_16816<IsBF16<T>::v>(oacc[m], a, bh0, bh1);
-          mma_16816<IsBF16<T>::v>(oacc[m], a, bl0, bl1);
+          mma_16816<kMmaBf>(oacc[m], a, bh0, bh1);
+          mma_16816<kMmaBf>(oacc[m], a, bl0, bl1);
         }
       }
       __syncwarp();
@@ -707,16 +829,18 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
     }
   }
   // channels contiguous per (warp, head): the push below reads 4 at a time
+  // (fp8: rows g8 / g8+8 of m-tile m are channels 16m + 2g8 / + 1)
 #pragma unroll
   for (int m = 0; m < MT; ++m) {
-    const int ch = 16 * m + g8;
+    const int ch = kF8 ? 16 * m + 2 * g8 : 16 * m + g8;
+    const int ch2 = kF8 ? ch + 1 : ch + 8;
     if (2 * t4 < G) {
       o_w[(warp * G + 2 * t4) * D + ch] = oacc[m][0];
-      o_w[(warp * G + 2 * t4) * D + ch + 8] = oacc[m][2];
+      o_w[(warp * G + 2 * t4) * D + ch2] = oacc[m][2];
     }
     if (2 * t4 + 1 < G) {
       o_w[(warp * G + 2 * t4 + 1) * D + ch] = oacc[m][1];
-      o_w[(warp * G + 2 * t4 + 1) * D + ch + 8] = oacc[m][3];
+      o_w[(warp * G + 2 * t4 + 1) * D + ch2] = oacc[m][3];
     }
   }
   __syncthreads();
@@ -793,7 +917,8 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
     }
     if (valid && r0 == 0) {
       if (nc == 1) {
-        out[g * D + c] = O / Ls;
+        // (fp8: the stored values are code * v_scale)
+        out[g * D + c] = kF8 ? O / Ls * p.v_scale[h] : O / Ls;
         if (p.row_max && rank == 0 && cl == 0) {
           // the logits' max in natural units (M is base 2, scale folded in)
           // and the sum of exp(z - max) over the attended tokens
@@ -920,7 +1045,7 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
   for (int j = 0; j < OPT4; ++j) {
     const int x4 = tid + kThreads * j;
     if (x4 < G * D / 4) {
-      const float inv = 1.f / Lh[(4 * x4) / D];
+      const float inv = (kF8 ? p.v_scale[h] : 1.f) / Lh[(4 * x4) / D];
       reinterpret_cast<float4 *>(out)[x4] =
           make_float4(acc_o[j].x * inv, acc_o[j].y * inv, acc_o[j].z * inv, acc_o[j].w * inv);
     }
@@ -938,11 +1063,11 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
 }
 
 
-template <typename T, int D, int G, bool kMass>
+template <typename T, int D, int G, bool kMass, bool kF8 = false>
 cudaError_t set_smem_attrs() {
-  auto k = decode_tiles_kernel<T, D, G, kMass>;
+  auto k = decode_tiles_kernel<T, D, G, kMass, kF8>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       Smem<D, G>::kAlloc);
+                                       Smem<D, G, kF8>::kAlloc);
   if (e != cudaSuccess) return e;
   (void)cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   (void)cudaGetLastError();
@@ -967,10 +1092,10 @@ cudaError_t set_smem_attrs_all() {
   return set_smem_attrs_g<__nv_bfloat16, 128, kMass>();
 }
 
-template <typename T, int D, int G, bool kMass>
+template <typename T, int D, int G, bool kMass, bool kF8 = false>
 cudaError_t launch_one(const TileDecodeParams &p, cudaStream_t st) {
-  cudaError_t e = launch_pdl_cluster(decode_tiles_kernel<T, D, G, kMass>, p.total_items, kThreads,
-                                     (size_t)Smem<D, G>::kAlloc, p.cluster, st, p);
+  cudaError_t e = launch_pdl_cluster(decode_tiles_kernel<T, D, G, kMass, kF8>, p.total_items,
+                                     kThreads, (size_t)Smem<D, G, kF8>::kAlloc, p.cluster, st, p);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

@@ -6,7 +6,8 @@
 //                 page's channel-wise key min/max ("LServe long-sequence LLM
 //                 serving system", section 2.1, min-max pooling); used for
 //                 bulk appends (prefill) -- the one-token append of a decode
-//                 step is fused into the decode kernel
+//                 step is fused into the decode kernel; with fp8 storage the
+//                 rows are written as E4M3 codes of value / scale
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <math_constants.h>
@@ -71,8 +72,26 @@ __global__ void pt_write_kernel(const __grid_constant__ PtWriteParams p) {
 // ---- append + metadata -----------------------------------------------------
 // Dynamic part: one CTA per (sequence, touched logical page, dynamic head);
 // thread c owns channel c.  Streaming part: one CTA per (sequence, head).
-template <typename T, int D>
+// Storage element E: the input type T, or (kF8) one-byte E4M3 codes of
+// value / scale, whose min/max compare by the code's sign-magnitude order.
+template <typename T, bool kF8> struct Store;
+template <typename T> struct Store<T, false> {
+  using E = T;
+  static __device__ __forceinline__ E put(T x, float) { return x; }
+  static __device__ __forceinline__ float key(E e) { return Elem<T>::to_f(e); }
+};
+template <typename T> struct Store<T, true> {
+  using E = uint8_t;
+  static __device__ __forceinline__ E put(T x, float scale) {
+    return (E)e4m3_code(Elem<T>::to_f(x), scale);
+  }
+  static __device__ __forceinline__ float key(E e) { return (float)e4m3_key(e); }
+};
+
+template <typename T, int D, bool kF8>
 __global__ void __launch_bounds__(128) append_kernel(const __grid_constant__ AppendParams p) {
+  using St = Store<T, kF8>;
+  using E = typename St::E;
   pdl_wait();
   pdl_launch_dependents();
   const int c = threadIdx.x;
@@ -87,6 +106,7 @@ __global__ void __launch_bounds__(128) append_kernel(const __grid_constant__ App
     const int hd = local % p.Hd;
     const int j = s.L_old / p.ell + local / p.Hd;  // logical page
     const int h = p.dyn_kv[hd];
+    const float ks = kF8 ? p.k_scale[h] : 1.f, vs = kF8 ? p.v_scale[h] : 1.f;
     const int L_new = s.L_old + n;
     const int t0 = j * p.ell;
     const int t1 = min(t0 + p.ell, L_new);
@@ -101,31 +121,30 @@ __global__ void __launch_bounds__(128) append_kernel(const __grid_constant__ App
       return;
     }
     const size_t page_base = ((size_t)phys * p.Hd + hd) * p.P;  // in rows
-    T *__restrict__ kp = static_cast<T *>(p.k_pool);
-    T *__restrict__ vp = static_cast<T *>(p.v_pool);
-    T *__restrict__ meta = static_cast<T *>(p.meta) +
+    E *__restrict__ kp = static_cast<E *>(p.k_pool);
+    E *__restrict__ vp = static_cast<E *>(p.v_pool);
+    E *__restrict__ meta = static_cast<E *>(p.meta) +
               (((size_t)phys * p.Hd + hd) * p.R + (j % p.R)) * 2 * D;
     if (c >= D) return;
-    T bmin, bmax;
+    E bmin, bmax;
     float vmin, vmax;
     int t = max(t0, s.L_old);
     if (t0 < s.L_old) {  // the page already holds tokens: start from its metadata
       bmin = meta[c];
       bmax = meta[D + c];
-      vmin = Elem<T>::to_f(bmin);
-      vmax = Elem<T>::to_f(bmax);
     } else {
-      bmin = bmax = kin[(((size_t)i * n + (t - s.L_old)) * p.Hkv + h) * D + c];
-      vmin = vmax = Elem<T>::to_f(bmin);
+      bmin = bmax = St::put(kin[(((size_t)i * n + (t - s.L_old)) * p.Hkv + h) * D + c], ks);
     }
+    vmin = St::key(bmin);
+    vmax = St::key(bmax);
 #pragma unroll 8
     for (; t < t1; ++t) {
       const size_t src = (((size_t)i * n + (t - s.L_old)) * p.Hkv + h) * D + c;
-      const T kx = __ldg(kin + src);
+      const E kx = St::put(__ldg(kin + src), ks);
       const size_t dst = (page_base + (t % p.P)) * D + c;
       kp[dst] = kx;
-      vp[dst] = __ldg(vin + src);
-      const float x = Elem<T>::to_f(kx);
+      vp[dst] = St::put(__ldg(vin + src), vs);
+      const float x = St::key(kx);
       if (x < vmin) { vmin = x; bmin = kx; }
       if (x > vmax) { vmax = x; bmax = kx; }
     }
@@ -135,11 +154,12 @@ __global__ void __launch_bounds__(128) append_kernel(const __grid_constant__ App
     const int b = blockIdx.x - p.dyn_ctas;
     const int i = b / p.Hs, hs = b % p.Hs;
     const int h = p.str_kv[hs];
+    const float ks = kF8 ? p.k_scale[h] : 1.f, vs = kF8 ? p.v_scale[h] : 1.f;
     const AppendSeq s = p.seqs[i];
     const int L_new = s.L_old + n;
     const int SW = p.S + p.W;
-    T *sk = static_cast<T *>(p.stream_k) + ((size_t)s.slot * p.Hs + hs) * SW * D;
-    T *sv = static_cast<T *>(p.stream_v) + ((size_t)s.slot * p.Hs + hs) * SW * D;
+    E *sk = static_cast<E *>(p.stream_k) + ((size_t)s.slot * p.Hs + hs) * SW * D;
+    E *sv = static_cast<E *>(p.stream_v) + ((size_t)s.slot * p.Hs + hs) * SW * D;
     // positions that can still be read: sink t < S, window t >= L_new - W
     const int w0 = max(s.L_old, max(p.S, L_new - p.W));
     for (int t = s.L_old; t < L_new; ++t) {
@@ -147,8 +167,8 @@ __global__ void __launch_bounds__(128) append_kernel(const __grid_constant__ App
       const int slot = t < p.S ? t : p.S + (t - p.S) % p.W;
       const size_t src = (((size_t)i * n + (t - s.L_old)) * p.Hkv + h) * D;
       for (int cc = c; cc < D; cc += blockDim.x) {
-        sk[(size_t)slot * D + cc] = kin[src + cc];
-        sv[(size_t)slot * D + cc] = vin[src + cc];
+        sk[(size_t)slot * D + cc] = St::put(kin[src + cc], ks);
+        sv[(size_t)slot * D + cc] = St::put(vin[src + cc], vs);
       }
     }
   }
@@ -168,12 +188,17 @@ cudaError_t launch_append(const AppendParams &p, int dtype, int d, cudaStream_t 
   if (grid == 0) return cudaSuccess;
   *n += 1;
   cudaError_t e;
-  if (dtype == 0)
-    e = d == 64 ? launch_pdl(append_kernel<__half, 64>, grid, 128, 0, s, p)
-                : launch_pdl(append_kernel<__half, 128>, grid, 128, 0, s, p);
-  else
-    e = d == 64 ? launch_pdl(append_kernel<__nv_bfloat16, 64>, grid, 128, 0, s, p)
-                : launch_pdl(append_kernel<__nv_bfloat16, 128>, grid, 128, 0, s, p);
+  if (p.kv_fp8) {  // (fp8 storage needs head_dim 128)
+    if (d != 128) return cudaErrorInvalidValue;
+    e = dtype == 0 ? launch_pdl(append_kernel<__half, 128, true>, grid, 128, 0, s, p)
+                   : launch_pdl(append_kernel<__nv_bfloat16, 128, true>, grid, 128, 0, s, p);
+  } else if (dtype == 0) {
+    e = d == 64 ? launch_pdl(append_kernel<__half, 64, false>, grid, 128, 0, s, p)
+                : launch_pdl(append_kernel<__half, 128, false>, grid, 128, 0, s, p);
+  } else {
+    e = d == 64 ? launch_pdl(append_kernel<__nv_bfloat16, 64, false>, grid, 128, 0, s, p)
+                : launch_pdl(append_kernel<__nv_bfloat16, 128, false>, grid, 128, 0, s, p);
+  }
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

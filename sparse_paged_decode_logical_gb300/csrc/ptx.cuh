@@ -2,6 +2,9 @@
 // mma.sync.  Every wait is bounded: on timeout the caller gets `false` and
 // records an error instead of spinning forever.
 #pragma once
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -216,6 +219,49 @@ __device__ __forceinline__ float ld_dsmem_f32(uint32_t addr) {
 
 // 128-byte swizzle of TMA tiles: the 16-byte chunk c of row r (rows of 128
 // bytes, tile base 1024-byte aligned) sits at chunk c ^ (r & 7).
+// ---- fp8 (OCP E4M3) KV storage ----
+// Two E4M3 codes (first in the low byte) -> two 16-bit floats of type T
+// packed low half first.  Exact: every E4M3 value is an fp16 and a bf16 value.
+template <typename T>
+__device__ __forceinline__ uint32_t e4m3x2_to(uint32_t two);
+template <>
+__device__ __forceinline__ uint32_t e4m3x2_to<__half>(uint32_t two) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two & 0xffffu), __NV_E4M3);
+  return (uint32_t)h.x | ((uint32_t)h.y << 16);
+}
+template <>
+__device__ __forceinline__ uint32_t e4m3x2_to<__nv_bfloat16>(uint32_t two) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two & 0xffffu), __NV_E4M3);
+  const float2 f = __half22float2(__half2(h));
+  const __nv_bfloat162 b = __float22bfloat162_rn(f);
+  return *reinterpret_cast<const uint32_t *>(&b);
+}
+// Two 16-bit floats of type T -> fp16x2, for the fp16 tensor-core products
+// of the fp8 path.  Exact for every value fp16 holds: a bf16 input is exact
+// unless its magnitude is at least 65520 (then inf) or below 2^-14 with
+// nonzero bits under the fp16 subnormal step 2^-24.
+template <typename T>
+__device__ __forceinline__ uint32_t to_f16x2(uint32_t two);
+template <>
+__device__ __forceinline__ uint32_t to_f16x2<__half>(uint32_t two) {
+  return two;
+}
+template <>
+__device__ __forceinline__ uint32_t to_f16x2<__nv_bfloat16>(uint32_t two) {
+  const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&two));
+  const __half2 h = __float22half2_rn(f);
+  return *reinterpret_cast<const uint32_t *>(&h);
+}
+// Code of x / scale: the quotient rounded once to fp32, then to the nearest
+// E4M3 value (ties to even), saturating at +-448.
+__device__ __forceinline__ uint32_t e4m3_code(float x, float scale) {
+  return (uint32_t)__nv_cvt_float_to_fp8(__fdiv_rn(x, scale), __NV_SATFINITE, __NV_E4M3);
+}
+// Order key of a finite E4M3 code (sign and magnitude; +0 and -0 tie).
+__device__ __forceinline__ int e4m3_key(uint32_t c) {
+  return (c & 0x80u) ? -(int)(c & 0x7fu) : (int)(c & 0x7fu);
+}
+
 __device__ __forceinline__ uint32_t swz128(int row, int chunk) {
   return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
 }

@@ -16,7 +16,9 @@
 // Fragments are loaded straight from global memory: the k order inside each
 // pair of k-steps is permuted (both operands alike, which leaves the sum
 // unchanged) so that every thread reads 16 contiguous bytes of a metadata
-// row per load.
+// row per load (8 with fp8 E4M3 metadata, widened exactly to fp16, q then
+// narrowed to fp16 for fp16 products; the per-head key scale is positive and
+// leaves the ranking unchanged).
 //
 // Top-k.  Each scoring CTA writes its pages' scores, then takes a ticket;
 // the last CTA of a (sequence, head) runs an exact radix select for the
@@ -139,7 +141,8 @@ __device__ int cta_topk_global(const float *sc, int n, int k, int *out) {
   return taken;
 }
 
-template <typename T, int D, int G>
+// kF8: the metadata rows hold fp8 E4M3 codes, widened exactly to T as they load
+template <typename T, int D, int G, bool kF8>
 __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_constant__ SelectParams p) {
   __shared__ int s_last;
   // the group's [q- ; q+] rows (2D elements each), padded by 32 bytes so that a
@@ -192,8 +195,10 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_consta
   bool ok[2] = {false, false};
   uint4 ra[PAIRS], rb[PAIRS];
   if (j0 < n) {
-    const uint16_t *meta = static_cast<const uint16_t *>(p.meta);
-    const uint4 *rowp[2] = {nullptr, nullptr};
+    // a metadata row is 2D elements of 2 bytes, or of 1 byte (fp8)
+    const uint8_t *meta = static_cast<const uint8_t *>(p.meta);
+    constexpr int kRowBytes = 2 * D * (kF8 ? 1 : 2);
+    const uint8_t *rowp[2] = {nullptr, nullptr};
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
       const int j = j0 + g8 + 8 * hh;
@@ -204,15 +209,28 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_consta
           set_err(p.err, kDevBadPhys, s.slot, blk, phys);
         } else {
           ok[hh] = true;
-          rowp[hh] = reinterpret_cast<const uint4 *>(
-              meta + (((size_t)phys * p.Hd + hd) * p.R + (j % p.R)) * 2 * D);
+          rowp[hh] = meta + (((size_t)phys * p.Hd + hd) * p.R + (j % p.R)) * kRowBytes;
         }
       }
     }
 #pragma unroll
     for (int s2 = 0; s2 < PAIRS; ++s2) {
-      ra[s2] = ok[0] ? __ldg(rowp[0] + 4 * s2 + t4) : make_uint4(0, 0, 0, 0);
-      rb[s2] = ok[1] ? __ldg(rowp[1] + 4 * s2 + t4) : make_uint4(0, 0, 0, 0);
+      if constexpr (kF8) {
+        // the same 8 elements: 8 bytes, widened pair by pair
+        const uint2 a8 = ok[0] ? __ldg(reinterpret_cast<const uint2 *>(rowp[0]) + 4 * s2 + t4)
+                               : make_uint2(0, 0);
+        const uint2 b8 = ok[1] ? __ldg(reinterpret_cast<const uint2 *>(rowp[1]) + 4 * s2 + t4)
+                               : make_uint2(0, 0);
+        ra[s2] = make_uint4(e4m3x2_to<__half>(a8.x), e4m3x2_to<__half>(a8.x >> 16), e4m3x2_to<__half>(a8.y),
+                            e4m3x2_to<__half>(a8.y >> 16));
+        rb[s2] = make_uint4(e4m3x2_to<__half>(b8.x), e4m3x2_to<__half>(b8.x >> 16), e4m3x2_to<__half>(b8.y),
+                            e4m3x2_to<__half>(b8.y >> 16));
+      } else {
+        ra[s2] = ok[0] ? __ldg(reinterpret_cast<const uint4 *>(rowp[0]) + 4 * s2 + t4)
+                       : make_uint4(0, 0, 0, 0);
+        rb[s2] = ok[1] ? __ldg(reinterpret_cast<const uint4 *>(rowp[1]) + 4 * s2 + t4)
+                       : make_uint4(0, 0, 0, 0);
+      }
     }
   }
   if (early) {
@@ -238,6 +256,10 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_consta
         const bool nl = Neg<T>::neg(lo), nh = Neg<T>::neg(hi);
         neg[y] = (nl ? lo : 0u) | ((nh ? (uint32_t)hi : 0u) << 16);
         pos[y] = (nl ? 0u : lo) | ((nh ? 0u : (uint32_t)hi) << 16);
+        if constexpr (kF8) {  // fp16 products with the widened fp8 metadata
+          neg[y] = to_f16x2<T>(neg[y]);
+          pos[y] = to_f16x2<T>(pos[y]);
+        }
       }
       uint16_t *row = &q_s[(x / (D / 8)) * QS + (x % (D / 8)) * 8];
       *reinterpret_cast<uint4 *>(row) = make_uint4(neg[0], neg[1], neg[2], neg[3]);
@@ -263,9 +285,9 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_consta
 #pragma unroll
     for (int s2 = 0; s2 < PAIRS; ++s2) {
       const uint32_t a0[4] = {ra[s2].x, rb[s2].x, ra[s2].y, rb[s2].y};
-      mma_16816<IsBf<T>::v>(acc, a0, qb[2 * s2][0], qb[2 * s2][1]);
+      mma_16816<(kF8 ? false : IsBf<T>::v)>(acc, a0, qb[2 * s2][0], qb[2 * s2][1]);
       const uint32_t a1[4] = {ra[s2].z, rb[s2].z, ra[s2].w, rb[s2].w};
-      mma_16816<IsBf<T>::v>(acc2, a1, qb[2 * s2 + 1][0], qb[2 * s2 + 1][1]);
+      mma_16816<(kF8 ? false : IsBf<T>::v)>(acc2, a1, qb[2 * s2 + 1][0], qb[2 * s2 + 1][1]);
     }
 #pragma unroll
     for (int e = 0; e < 4; ++e) acc[e] += acc2[e];
@@ -351,15 +373,15 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_consta
   }
 }
 
-template <typename T, int D>
+template <typename T, int D, bool kF8>
 cudaError_t launch_g(const SelectParams &p, int G, cudaStream_t st) {
   const int grid = p.score_ctas;
   cudaError_t e;
   switch (G) {
-    case 1: e = launch_pdl(select_kernel<T, D, 1>, grid, kSelThreads, 0, st, p); break;
-    case 2: e = launch_pdl(select_kernel<T, D, 2>, grid, kSelThreads, 0, st, p); break;
-    case 4: e = launch_pdl(select_kernel<T, D, 4>, grid, kSelThreads, 0, st, p); break;
-    case 8: e = launch_pdl(select_kernel<T, D, 8>, grid, kSelThreads, 0, st, p); break;
+    case 1: e = launch_pdl(select_kernel<T, D, 1, kF8>, grid, kSelThreads, 0, st, p); break;
+    case 2: e = launch_pdl(select_kernel<T, D, 2, kF8>, grid, kSelThreads, 0, st, p); break;
+    case 4: e = launch_pdl(select_kernel<T, D, 4, kF8>, grid, kSelThreads, 0, st, p); break;
+    case 8: e = launch_pdl(select_kernel<T, D, 8, kF8>, grid, kSelThreads, 0, st, p); break;
     default: return cudaErrorInvalidValue;
   }
   return e != cudaSuccess ? e : cudaGetLastError();
@@ -373,8 +395,15 @@ cudaError_t launch_select_fused(const SelectParams &p, int dtype, int d, int G, 
                                 long long *n) {
   if (p.n_seqs == 0 || p.Hd == 0 || p.score_ctas == 0) return cudaSuccess;
   *n += 1;
-  if (dtype == 0) return d == 64 ? launch_g<__half, 64>(p, G, s) : launch_g<__half, 128>(p, G, s);
-  return d == 64 ? launch_g<__nv_bfloat16, 64>(p, G, s) : launch_g<__nv_bfloat16, 128>(p, G, s);
+  if (p.kv_fp8) {  // (fp8 storage needs head_dim 128)
+    if (d != 128) return cudaErrorInvalidValue;
+    return dtype == 0 ? launch_g<__half, 128, true>(p, G, s)
+                      : launch_g<__nv_bfloat16, 128, true>(p, G, s);
+  }
+  if (dtype == 0)
+    return d == 64 ? launch_g<__half, 64, false>(p, G, s) : launch_g<__half, 128, false>(p, G, s);
+  return d == 64 ? launch_g<__nv_bfloat16, 64, false>(p, G, s)
+                 : launch_g<__nv_bfloat16, 128, false>(p, G, s);
 }
 
 }  // namespace spd

@@ -53,6 +53,8 @@ struct AppendParams {
   int *err;
   int n_seqs, n_tokens, Hkv, Hd, Hs, ell, P, R, max_pp, S, W, num_phys;
   int dyn_ctas;                // sum over seqs of touched logical pages * Hd
+  int kv_fp8;                  // store fp8 E4M3 codes of value / scale
+  float k_scale[kMaxKvHeads], v_scale[kMaxKvHeads];
   unsigned char dyn_kv[kMaxKvHeads];  // dynamic index -> kv head
   unsigned char str_kv[kMaxKvHeads];  // streaming index -> kv head
   AppendSeq seqs[kSeqsPerLaunch];
@@ -95,6 +97,7 @@ struct SelectParams {
   int score_ctas;       // total scoring CTAs
   int score_only;       // 1: write the scores and stop (the decode kernel selects)
   int early;            // 1: read metadata before waiting for the previous kernel
+  int kv_fp8;           // metadata rows are fp8 E4M3 codes (one byte each)
   unsigned char dyn_kv[kMaxKvHeads];
   SelectSeq seqs[kSeqsPerLaunch];
 };
@@ -146,10 +149,15 @@ struct TileDecodeParams {
                       // bit 0 dynamic units, bit 1 streaming units; bit 2:
                       // streaming units do not wait at all
   float scale_log2;
+  int kv_fp8;                // K/V stored as fp8 E4M3 codes of value / scale
+  float k_scale[kMaxKvHeads], v_scale[kMaxKvHeads];  // per kv head (fp8 only)
   unsigned char dyn_kv[kMaxKvHeads];
   unsigned char str_kv[kMaxKvHeads];
   TileSeq seqs[kSeqsPerLaunch];
 };
+
+// kernel parameter blocks are passed by value: at most 32764 bytes
+static_assert(sizeof(TileDecodeParams) <= 32764, "decode parameter block too large");
 
 // A fused decode step (selection inside the decode kernel) holds at most this
 // many candidate scores and kept pages in shared memory; larger ones use the
@@ -170,6 +178,9 @@ cudaError_t prepare_decode_kernels();
 cudaError_t prepare_decode_mass_kernels();  // called by prepare_decode_kernels()
 cudaError_t launch_decode_tiles_mass(const TileDecodeParams &p, int dtype, int d, int G,
                                      cudaStream_t s);
+cudaError_t prepare_decode_fp8_kernels();  // called by prepare_decode_kernels()
+cudaError_t launch_decode_tiles_fp8(const TileDecodeParams &p, int dtype, int G,
+                                    cudaStream_t s);
 int decode_max_cluster(int dtype, int d, int G);  // after prepare_decode_kernels()
 int decode_max_tiles_per_cta();
 cudaError_t launch_decode_tiles(const TileDecodeParams &p, int dtype, int d, int G,

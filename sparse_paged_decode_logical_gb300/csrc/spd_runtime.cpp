@@ -10,6 +10,7 @@
 // changes nothing (the free-list pager of "Long-context inference
 // optimization for LLMs", section 3.4, raises on an empty list).
 #include <algorithm>
+#include <cfloat>
 #include <cmath>
 #include <mutex>
 #include <unordered_map>
@@ -57,6 +58,8 @@ struct Derived {
   int G = 0, Hd = 0, Hs = 0, R = 0, max_pp = 0, ksel_max = 0, max_nL = 0,
       seqs_per_launch = 0;
   int mass_pages = 0, mass_tiles = 0;  // per-page mass: attended pages / tiles per unit
+  int kv_fp8 = 0;                       // K/V stored as E4M3 codes of value / scale
+  float k_scale[kMaxKvHeads] = {}, v_scale[kMaxKvHeads] = {};
   unsigned char kv_kind[kMaxKvHeads] = {}, kv_sub[kMaxKvHeads] = {},
                 dyn_kv[kMaxKvHeads] = {}, str_kv[kMaxKvHeads] = {};
   ScratchLayout sl{};
@@ -91,6 +94,16 @@ const char *derive(const spd_config *c, Derived *d) {
   if (c->max_seqs < 1) return "max_seqs must be >= 1";
   if (c->max_context < 1 || c->max_context > (1 << 28)) return "max_context must be in [1, 2^28]";
   if (c->reuse_interval < 1) return "reuse_interval must be >= 1";
+  if (c->kv_fp8 != 0 && c->kv_fp8 != 1) return "kv_fp8 must be 0 or 1";
+  d->kv_fp8 = c->kv_fp8;
+  if (d->kv_fp8 && c->head_dim != 128) return "fp8 KV storage needs head_dim 128";
+  for (int h = 0; h < c->num_kv_heads; ++h) {
+    d->k_scale[h] = d->kv_fp8 && c->k_scale ? c->k_scale[h] : 1.f;
+    d->v_scale[h] = d->kv_fp8 && c->v_scale ? c->v_scale[h] : 1.f;
+    if (!(d->k_scale[h] > 0.f && d->k_scale[h] <= FLT_MAX) ||
+        !(d->v_scale[h] > 0.f && d->v_scale[h] <= FLT_MAX))
+      return "k_scale and v_scale must be positive and finite";
+  }
   d->Hd = d->Hs = 0;
   for (int h = 0; h < c->num_kv_heads; ++h) {
     const bool str = c->kv_head_is_streaming && c->kv_head_is_streaming[h];
@@ -123,7 +136,7 @@ const char *derive(const spd_config *c, Derived *d) {
   if (d->Hs > 0 && (long long)c->max_seqs * d->Hs * (c->sink + c->window) >= (1LL << 31))
     return "streaming buffers exceed 2^31 rows";
 
-  const size_t e = 2, dim = (size_t)c->head_dim;
+  const size_t e = d->kv_fp8 ? 1 : 2, dim = (size_t)c->head_dim;
   const int S = d->Hs ? c->sink : 0, W = d->Hs ? c->window : 0;
   spd_sizes &z = d->sizes;
   z.k_pool = z.v_pool = (size_t)c->num_physical_pages * d->Hd * c->physical_page * dim * e;
@@ -225,8 +238,8 @@ spd_status cuda_fail(spd_ctx *c, cudaError_t e, const char *what) {
   return c->fail(SPD_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
-// TMA descriptors over the paged pool and the streaming buffers: 3-D tiled
-// maps, boxes of 64 channels x 16 rows, 128-byte swizzle.
+// TMA descriptors over the paged pool and the streaming buffers: tiled maps
+// whose box is a 16-row tile of a whole row (128-byte swizzle).
 spd_status encode_map(spd_ctx *c, CUtensorMap *m, void *base, uint64_t rows_per_plane,
                       uint64_t planes) {
   static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
@@ -239,10 +252,24 @@ spd_status encode_map(spd_ctx *c, CUtensorMap *m, void *base, uint64_t rows_per_
       return c->fail(SPD_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
     encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   }
+  const uint64_t d = (uint64_t)c->cfg.head_dim;
+  if (c->dv.kv_fp8) {
+    // fp8 rows are 128 bytes (head_dim 128): {channels, rows, planes}, one
+    // box of 16 rows x 128 bytes per tile of K or of V, swizzled
+    cuuint64_t dims[3] = {d, rows_per_plane, planes};
+    cuuint64_t strides[2] = {d, rows_per_plane * d};
+    cuuint32_t box[3] = {(cuuint32_t)d, (cuuint32_t)kTileRows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base, dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+      return c->fail(SPD_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return SPD_OK;
+  }
   // {64 channels, rows, channel halves, planes}: one box is a 16-row tile of
   // every channel, laid out in shared memory half after half (each half 16
   // rows of 128 bytes, swizzled), i.e. one copy per tile of K or of V
-  const uint64_t d = (uint64_t)c->cfg.head_dim;
   cuuint64_t dims[4] = {64, rows_per_plane, d / 64, planes};
   cuuint64_t strides[3] = {d * 2, 128, rows_per_plane * d * 2};
   cuuint32_t box[4] = {64, (cuuint32_t)kTileRows, (cuuint32_t)(d / 64), 1};
@@ -383,6 +410,9 @@ spd_status append_impl(spd_ctx *c, const int *ids, int n, int n_tokens, const vo
     p.S = dv.Hs ? c->cfg.sink : 0;
     p.W = dv.Hs ? c->cfg.window : 0;
     p.num_phys = c->cfg.num_physical_pages;
+    p.kv_fp8 = dv.kv_fp8;
+    memcpy(p.k_scale, dv.k_scale, sizeof p.k_scale);
+    memcpy(p.v_scale, dv.v_scale, sizeof p.v_scale);
     memcpy(p.dyn_kv, dv.dyn_kv, sizeof p.dyn_kv);
     memcpy(p.str_kv, dv.str_kv, sizeof p.str_kv);
     long long ctas = 0;
@@ -452,6 +482,7 @@ spd_status select_impl(spd_ctx *c, const void *q, const int *ids, int n, bool fo
       p.ksel_max = dv.ksel_max;
       p.score_stride = (int)round_up((size_t)dv.max_nL, 4);  // 16-byte aligned rows
       p.pages_per_chunk = ppc;
+      p.kv_fp8 = dv.kv_fp8;
       p.num_phys = c->cfg.num_physical_pages;
       memcpy(p.dyn_kv, dv.dyn_kv, sizeof p.dyn_kv);
       int off = 0;
@@ -648,6 +679,9 @@ spd_status attention_impl(spd_ctx *c, const void *q, const int *ids, int n, floa
     p.W = dv.Hs ? c->cfg.window : 0;
     p.num_phys = c->cfg.num_physical_pages;
     p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)c->cfg.head_dim));
+    p.kv_fp8 = dv.kv_fp8;
+    memcpy(p.k_scale, dv.k_scale, sizeof p.k_scale);
+    memcpy(p.v_scale, dv.v_scale, sizeof p.v_scale);
     memcpy(p.dyn_kv, dv.dyn_kv, sizeof p.dyn_kv);
     memcpy(p.str_kv, dv.str_kv, sizeof p.str_kv);
     // bit 0: dynamic units may stage before the wait, bit 1: streaming units;
@@ -746,6 +780,7 @@ spd_status spd_create(const spd_config *cfg, const spd_buffers *bufs, spd_ctx **
   if (cfg->kv_head_is_streaming)
     c->streaming.assign(cfg->kv_head_is_streaming, cfg->kv_head_is_streaming + cfg->num_kv_heads);
   c->cfg.kv_head_is_streaming = c->streaming.empty() ? nullptr : c->streaming.data();
+  c->cfg.k_scale = c->cfg.v_scale = nullptr;  // copied into c->dv
   c->buf = *bufs;
   const int N = d.Hd ? cfg->num_physical_pages : 0;
   c->free_pages.resize(N);

@@ -2,7 +2,8 @@
 the same seeded inputs and compares them.  Test infrastructure.
 
 Acceptance (restating the target's tolerances):
-  * page table, K/V placement and min/max metadata: bit-exact (+0 == -0);
+  * page table, K/V placement and min/max metadata: bit-exact (+0 == -0),
+    fp8 storage included (the codes of value / scale);
   * selected page sets: identical, except pages whose oracle score lies
     within 1e-4 * max(|S_cut|, 1e-30) of the cut score S_cut;
   * attention: max |gpu - oracle| <= 2e-3 and mean <= 2e-4, the oracle run
@@ -26,11 +27,13 @@ def tdev(bits, dtype, device="cuda"):
     return t.view(torch.bfloat16 if dtype == "bf16" else torch.float16).to(device)
 
 
-def bits_equal(a, b):
+def bits_equal(a, b, magnitude=0x7FFF):
+    """Equal bit patterns, +0 and -0 counted equal (magnitude: the bits below
+    the sign: 0x7FFF for 16-bit floats, 0x7F for fp8 codes)."""
     a = np.asarray(a, np.uint16)
     b = np.asarray(b, np.uint16)
     same = a == b
-    zero = ((a & 0x7FFF) == 0) & ((b & 0x7FFF) == 0)
+    zero = ((a & magnitude) == 0) & ((b & magnitude) == 0)
     return bool(np.all(same | zero))
 
 
@@ -40,7 +43,8 @@ def oracle_cfg(cfg):
                 logical_page=cfg["logical_page"], streaming=cfg["streaming"],
                 sink=cfg["sink"], window=cfg["window"],
                 token_budget=cfg["token_budget"], reuse_interval=cfg["reuse_interval"],
-                max_context=cfg["max_context"])
+                max_context=cfg["max_context"], kv_fp8=cfg.get("kv_fp8", False),
+                k_scale=cfg.get("k_scale"), v_scale=cfg.get("v_scale"))
 
 
 class Pair:
@@ -86,15 +90,19 @@ class Pair:
         Hd, Hs = len(self.dyn), len(self.strm)
         N = cfg["num_physical_pages"]
         S, Wn = cfg["sink"], cfg["window"]
+        fp8 = bool(cfg.get("kv_fp8"))
+        mag = 0x7F if fp8 else 0x7FFF
+
+        def elems(name):  # stored elements: fp8 codes (bytes) or 16-bit patterns
+            t = c.buffers[name]
+            return t.cpu().numpy() if fp8 else t.view(torch.int16).cpu().numpy().view(np.uint16)
+
         if Hd:
-            kp = c.buffers["k_pool"].view(torch.int16).cpu().numpy().view(np.uint16)
-            vp = c.buffers["v_pool"].view(torch.int16).cpu().numpy().view(np.uint16)
+            kp, vp = elems("k_pool"), elems("v_pool")
             kp, vp = kp.reshape(N, Hd, P, d), vp.reshape(N, Hd, P, d)
-            meta = c.buffers["meta"].view(torch.int16).cpu().numpy().view(np.uint16)
-            meta = meta.reshape(N, Hd, R, 2, d)
+            meta = elems("meta").reshape(N, Hd, R, 2, d)
         if Hs:
-            sk = c.buffers["stream_k"].view(torch.int16).cpu().numpy().view(np.uint16)
-            sv = c.buffers["stream_v"].view(torch.int16).cpu().numpy().view(np.uint16)
+            sk, sv = elems("stream_k"), elems("stream_v")
             sk = sk.reshape(cfg["max_seqs"], Hs, S + Wn, d)
             sv = sv.reshape(cfg["max_seqs"], Hs, S + Wn, d)
         for b in range(self.wl.batch):
@@ -113,8 +121,8 @@ class Pair:
                     assert np.array_equal(kp[phys, hd, row], s.K[h, :L]), ("k_pool", b, h)
                     assert np.array_equal(vp[phys, hd, row], s.V[h, :L]), ("v_pool", b, h)
                     m = meta[pt[j // R], hd, j % R]
-                    assert bits_equal(m[:, 0], s.kmin[h]), ("kmin", b, h)
-                    assert bits_equal(m[:, 1], s.kmax[h]), ("kmax", b, h)
+                    assert bits_equal(m[:, 0], s.kmin[h], mag), ("kmin", b, h)
+                    assert bits_equal(m[:, 1], s.kmax[h], mag), ("kmax", b, h)
             for hs, h in enumerate(self.strm):
                 T = oracle.streaming_tokens(L, S, Wn)
                 slot = np.where(T < S, T, S + (T - S) % Wn)

@@ -382,3 +382,52 @@ def test_page_mass_capacity_is_checked_before_any_work():
     assert e.value.name == "SPD_ERR_CAPACITY"
     assert [pr.cache.seq_info(g) for g in pr.gids] == before
     _check_page_mass(pr, q)
+
+
+# ---- fp8 (E4M3) KV storage -------------------------------------------------------
+# Codes and metadata bit-exact against the oracle's quantisation (fp32 division,
+# round to nearest even, saturation); attention against the oracle over the
+# dequantised values (code * scale), same tolerances.  One key scale is small
+# enough that large keys saturate at 448.
+FP8 = dict(kv_fp8=True, k_scale=[0.05, 0.004, 1.0, 0.5], v_scale=[0.1, 2.0, 0.03, 1.0])
+FP8_SHAPES = [
+    dict(),
+    dict(dtype="f16"),
+    dict(Hq=4, Hkv=4, streaming=[False] * 4, ell=64, P=256, token_budget=0, context=9000),
+    dict(Hq=32, Hkv=4, streaming=[True, False, False, True], sink=0, window=1),
+    dict(context=1, steps=5, batch=3),
+    dict(batch=5, lens=[1, 17, 64, 640, 1000], steps=6, permute_pages=True),
+]
+
+
+def _fp8_cfg(wl):
+    return {k: (v[:wl.Hkv] if isinstance(v, list) else v) for k, v in FP8.items()}
+
+
+@needs_gpu
+@pytest.mark.parametrize("shape", range(len(FP8_SHAPES)))
+def test_fp8_kv_shapes_and_edges(shape):
+    kw = FP8_SHAPES[shape]
+    if "lens" in kw:
+        kw = dict(kw, batch=len(kw["lens"]))
+    wl = synth(**kw)
+    run(wl, layout_every=2, cfg_overrides=_fp8_cfg(wl))
+
+
+@needs_gpu
+def test_fp8_kv_full_size_workload():
+    wl = W.workload("llama3_8b_b1_128k")
+    cfg = dict(kv_fp8=True, k_scale=[0.02 * (1 + h) for h in range(wl.Hkv)],
+               v_scale=[0.05] * wl.Hkv)
+    run(wl, steps=5, layout_every=4, cfg_overrides=cfg)
+
+
+@needs_gpu
+@pytest.mark.parametrize("which", ["synthetic", "many_clusters"])
+def test_fp8_kv_statistics_and_page_mass(which):
+    wl = PAGE_MASS_CASES[which]()
+    pr = Pair(wl, cfg_overrides=_fp8_cfg(wl))
+    for s in range(2):
+        pr.step(s)
+    q, _, _ = W.step_tokens(wl, 2)
+    _check_page_mass(pr, q)
