@@ -50,10 +50,15 @@
 // appends it: the row is written to the pool / ring, patched into the
 // staged tile, and folded into the logical page's key min/max.
 //
+// fp8 storage (kF8).  K/V rows are E4M3 codes of value / scale, one 128-byte
+// row per token (head_dim 128): a tile of K or V is one 16 x 128-byte box
+// (3-D map), the ring has 16 stages, and the tensor-core fragments are built
+// from byte pairs (ldmatrix, byte permutes) widened to fp16 in registers.
+//
 // Files.  This header holds the kernel template and its launch helpers;
 // decode.cu instantiates the plain kernel, decode_mass.cu the one that also
-// exports the per-page attention mass (two translation units, built in
-// parallel).
+// exports the per-page attention mass, decode_fp8.cu the fp8-storage ones
+// (separate translation units, built in parallel).
 #pragma once
 #include <cuda_bf16.h>
 #include <type_traits>
@@ -70,7 +75,13 @@ namespace {
 constexpr int kRows = 16;                  // rows per tile (one mma M tile)
 constexpr int kWarps = 8;                  // 256 threads
 constexpr int kThreads = kWarps * 32;
-constexpr int kStages = 12;                // shared-memory stage ring
+// shared-memory stage ring: 12 stages of 16-bit tiles keep a CTA within half
+// an SM (the next launch's CTAs stage beside it); fp8 tiles are half the
+// size, and 16 of them fit in the space the selection buffers take anyway
+template <bool F8>
+struct Ring {
+  static constexpr int n = F8 ? 16 : 12;
+};
 constexpr int kMaxDesc = 256;              // tiles one CTA may take
 constexpr uint32_t kWaitLimit = 1u << 24;  // bounded mbarrier polls
 
@@ -102,6 +113,7 @@ struct TileDesc {
 // region holds the warp-merge buffer and later the global-merge buffers.
 template <int D, int G, bool F8 = false>
 struct Smem {
+  static constexpr int kStages = Ring<F8>::n;
   static constexpr int kBars = 0;                                      // uint64 [kStages]
   static constexpr int kDesc = kBars + kStages * 8;                    // TileDesc [kMaxDesc]
   static constexpr int kP = kDesc + kMaxDesc * (int)sizeof(TileDesc);  // float [W][16][GP]
@@ -218,6 +230,7 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
   constexpr bool kMmaBf = IsBF16<TM>::v;
   using Gm = Geo<D, kF8>;
   using Sm = Smem<D, G, kF8>;
+  constexpr int kStages = Sm::kStages;
   constexpr int CPL = Gm::kCPL;  // channels per lane of the fused append
   constexpr int GPAD = GP<G>::v;
   extern __shared__ uint8_t smem_raw[];
