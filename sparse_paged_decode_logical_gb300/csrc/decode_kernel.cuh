@@ -53,7 +53,8 @@
 // fp8 storage (kF8).  K/V rows are E4M3 codes of value / scale, one 128-byte
 // row per token (head_dim 128): a tile of K or V is one 16 x 128-byte box
 // (3-D map), the ring has 16 stages, and the tensor-core fragments are built
-// from byte pairs (ldmatrix, byte permutes) widened to fp16 in registers.
+// from byte pairs (ldmatrix, byte permutes) widened in registers (keys to
+// fp16, values to T).
 //
 // Files.  This header holds the kernel template and its launch helpers;
 // decode.cu instantiates the plain kernel, decode_mass.cu the one that also
@@ -219,15 +220,16 @@ __device__ void write_page_mass(const TileDecodeParams &p, int i, int sub, const
 // kMass: the per-page attention mass is exported (its own instance, so the
 // plain kernel carries none of that work).  kF8: K/V are stored as fp8 E4M3
 // codes of value / scale (head_dim 128): tiles are half the bytes, widened
-// exactly to fp16 on their way into the tensor-core fragments, and the
-// products run in fp16 (q narrowed to fp16 once, P split into fp16 halves).
+// exactly on their way into the tensor-core fragments: keys to fp16 for fp16
+// q.K products (q narrowed to fp16 once), values to T for the P.V products.
 template <typename T, int D, int G, bool kMass, bool kF8 = false>
 __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_constant__ TileDecodeParams p) {
   static_assert(!kF8 || D == 128, "fp8 storage: one 128-byte row per token");
-  // tensor-core element type: T, or fp16 with fp8 storage (an E4M3 value
-  // widens to fp16 in one instruction; q is narrowed to fp16 once)
-  using TM = typename std::conditional<kF8, __half, T>::type;
-  constexpr bool kMmaBf = IsBF16<TM>::v;
+  // tensor-core element types.  q.K: T, or fp16 with fp8 storage (an E4M3
+  // value widens to fp16 in one instruction; q is narrowed to fp16 once).
+  // P.V: T, so that the softmax weights keep T's exponent range.
+  constexpr bool kQkBf = kF8 ? false : IsBF16<T>::v;
+  constexpr bool kPvBf = IsBF16<T>::v;
   using Gm = Geo<D, kF8>;
   using Sm = Smem<D, G, kF8>;
   constexpr int kStages = Sm::kStages;
@@ -656,12 +658,12 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
         for (int k2 = 0; k2 < D / 32; ++k2) {
           uint32_t r0, r1, r2, r3;
           ldmatrix_x4(kbase + swz128(row, 2 * k2 + chalf), r0, r1, r2, r3);
-          const uint32_t a0[4] = {e4m3x2_to<__half>(r0), e4m3x2_to<__half>(r1), e4m3x2_to<__half>(r0 >> 16),
-                                  e4m3x2_to<__half>(r1 >> 16)};
-          mma_16816<kMmaBf>(acc, a0, qb[2 * k2][0], qb[2 * k2][1]);
-          const uint32_t a1[4] = {e4m3x2_to<__half>(r2), e4m3x2_to<__half>(r3), e4m3x2_to<__half>(r2 >> 16),
-                                  e4m3x2_to<__half>(r3 >> 16)};
-          mma_16816<kMmaBf>(acc2, a1, qb[2 * k2 + 1][0], qb[2 * k2 + 1][1]);
+          const uint32_t a0[4] = {e4m3x2_to<__half>(r0), e4m3x2_to<__half>(r1),
+                                  e4m3x2_to<__half>(r0 >> 16), e4m3x2_to<__half>(r1 >> 16)};
+          mma_16816<kQkBf>(acc, a0, qb[2 * k2][0], qb[2 * k2][1]);
+          const uint32_t a1[4] = {e4m3x2_to<__half>(r2), e4m3x2_to<__half>(r3),
+                                  e4m3x2_to<__half>(r2 >> 16), e4m3x2_to<__half>(r3 >> 16)};
+          mma_16816<kQkBf>(acc2, a1, qb[2 * k2 + 1][0], qb[2 * k2 + 1][1]);
         }
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[e] += acc2[e];
@@ -676,9 +678,9 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
           uint32_t a[4];
           ldmatrix_x4(kbase + box * Gm::kBoxBytes + swz128(row, chunk), a[0], a[1], a[2], a[3]);
           if (kk & 1)
-            mma_16816<kMmaBf>(acc2, a, qb[kk][0], qb[kk][1]);
+            mma_16816<kQkBf>(acc2, a, qb[kk][0], qb[kk][1]);
           else
-            mma_16816<kMmaBf>(acc, a, qb[kk][0], qb[kk][1]);
+            mma_16816<kQkBf>(acc, a, qb[kk][0], qb[kk][1]);
         }
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[e] += acc2[e];
@@ -750,9 +752,9 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
         uint16_t hi[4], lo[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const TM th = Cvt<TM>::from(pv[e]);
+          const T th = Cvt<T>::from(pv[e]);
           hi[e] = *reinterpret_cast<const uint16_t *>(&th);
-          const TM tl = Cvt<TM>::from(pv[e] - tof(th));
+          const T tl = Cvt<T>::from(pv[e] - tof(th));
           lo[e] = *reinterpret_cast<const uint16_t *>(&tl);
         }
         bh0 = (uint32_t)hi[0] | ((uint32_t)hi[1] << 16);
@@ -774,14 +776,14 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
           ldmatrix_x4_trans(vbase + swz128(row, 2 * m2 + chalf), r0, r1, r2, r3);
           const uint32_t e0 = __byte_perm(r0, 0u, 0x3120), e1 = __byte_perm(r1, 0u, 0x3120);
           const uint32_t e2 = __byte_perm(r2, 0u, 0x3120), e3 = __byte_perm(r3, 0u, 0x3120);
-          const uint32_t a0[4] = {e4m3x2_to<__half>(e0), e4m3x2_to<__half>(e0 >> 16), e4m3x2_to<__half>(e1),
-                                  e4m3x2_to<__half>(e1 >> 16)};
-          mma_16816<kMmaBf>(oacc[2 * m2], a0, bh0, bh1);
-          mma_16816<kMmaBf>(oacc[2 * m2], a0, bl0, bl1);
-          const uint32_t a1[4] = {e4m3x2_to<__half>(e2), e4m3x2_to<__half>(e2 >> 16), e4m3x2_to<__half>(e3),
-                                  e4m3x2_to<__half>(e3 >> 16)};
-          mma_16816<kMmaBf>(oacc[2 * m2 + 1], a1, bh0, bh1);
-          mma_16816<kMmaBf>(oacc[2 * m2 + 1], a1, bl0, bl1);
+          const uint32_t a0[4] = {e4m3x2_to<T>(e0), e4m3x2_to<T>(e0 >> 16), e4m3x2_to<T>(e1),
+                                  e4m3x2_to<T>(e1 >> 16)};
+          mma_16816<kPvBf>(oacc[2 * m2], a0, bh0, bh1);
+          mma_16816<kPvBf>(oacc[2 * m2], a0, bl0, bl1);
+          const uint32_t a1[4] = {e4m3x2_to<T>(e2), e4m3x2_to<T>(e2 >> 16), e4m3x2_to<T>(e3),
+                                  e4m3x2_to<T>(e3 >> 16)};
+          mma_16816<kPvBf>(oacc[2 * m2 + 1], a1, bh0, bh1);
+          mma_16816<kPvBf>(oacc[2 * m2 + 1], a1, bl0, bl1);
         }
       } else {
         // A = V^T for m-tile m: matrix j of ldmatrix.x4.trans takes token rows
@@ -796,8 +798,8 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
           uint32_t a[4];
           ldmatrix_x4_trans(vbase + box * Gm::kBoxBytes + swz128(row, chunk), a[0], a[1], a[2],
                             a[3]);
-          mma_16816<kMmaBf>(oacc[m], a, bh0, bh1);
-          mma_16816<kMmaBf>(oacc[m], a, bl0, bl1);
+          mma_16816<kPvBf>(oacc[m], a, bh0, bh1);
+          mma_16816<kPvBf>(oacc[m], a, bl0, bl1);
         }
       }
       __syncwarp();
