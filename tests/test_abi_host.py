@@ -188,3 +188,46 @@ def test_status_strings():
     L = spd.lib()
     for code in range(8):
         assert L.spd_status_string(code)
+
+
+def test_fp8_storage_halves_the_kv_buffers():
+    z16 = spd.spd_query_sizes(cfg(head_dim=128))
+    z8 = spd.spd_query_sizes(cfg(head_dim=128, kv_fp8=True, k_scale=[0.5, 2.0],
+                                 v_scale=[1.0, 0.25]))
+    for f in ("k_pool", "v_pool", "meta", "stream_k", "stream_v"):
+        assert z8[f] * 2 == z16[f], f
+    assert z8["page_table"] == z16["page_table"] and z8["selection"] == z16["selection"]
+
+
+@pytest.mark.parametrize("bad", [
+    dict(kv_fp8=True),                                   # head_dim 64
+    dict(head_dim=128, kv_fp8=True, k_scale=[0.0, 1.0]),
+    dict(head_dim=128, kv_fp8=True, v_scale=[1.0, -2.0]),
+    dict(head_dim=128, kv_fp8=True, k_scale=[float("inf"), 1.0]),
+    dict(head_dim=128, kv_fp8=True, v_scale=[float("nan"), 1.0]),
+])
+def test_fp8_configs_checked(bad):
+    with pytest.raises(spd.SpdError) as e:
+        spd.spd_query_sizes(cfg(**bad))
+    assert e.value.name == "SPD_ERR_INVALID_ARG"
+
+
+def test_scales_are_ignored_without_fp8_storage():
+    z = spd.spd_query_sizes(cfg(k_scale=[0.0, -1.0]))
+    assert z["k_pool"] == 8 * 1 * 64 * 64 * 2
+
+
+def test_page_mass_arguments_checked_before_any_work():
+    _, ctx = new_ctx()
+    s = spd.spd_seq_create(ctx)
+    fake = 1 << 41
+    # no selection yet, then bad output pointers / capacity: nothing moves
+    with pytest.raises(spd.SpdError) as e:
+        spd.spd_sparse_decode_attention_page_mass(ctx, fake, [s], fake, 0, 0, fake, fake, 4)
+    assert e.value.name == "SPD_ERR_STATE"
+    for args in ((fake, 0, fake, fake, 4), (0, 0, 0, fake, 4), (0, 0, fake, fake, 0),
+                 (0, 0, fake + 2, fake, 4)):
+        with pytest.raises(spd.SpdError) as e:
+            spd.spd_sparse_decode_attention_page_mass(ctx, fake, [s], fake, *args)
+        assert e.value.name == "SPD_ERR_INVALID_ARG", args
+    assert spd.spd_seq_info(ctx, s)["step_counter"] == 0
