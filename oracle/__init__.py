@@ -106,6 +106,9 @@ def lib():
         L.orc_page_mass_kv.argtypes = [u16p, ci, u16p, ci, f64, ci, ci, i32p, ci, ci, i32p, ci,
                                        f64p]
         L.orc_page_mass_kv.restype = ci
+        L.orc_prefill_block_scores.argtypes = [u16p, ci, u16p, ci, f64, f32p, f32p, ci, ci, ci,
+                                               ci, ci, f64p]
+        L.orc_prefill_block_scores.restype = ci
         _lib = L
     return _lib
 
@@ -266,6 +269,54 @@ def page_mass(q, K, dtype, tokens, ell, pages, kv_dtype=None, kscale=1.0):
                               pages, pages.size, mass) != 0:
         raise ValueError("orc_page_mass: empty token set")
     return mass
+
+
+# ---- prefill: low-rank block importance and block-sparse causal attention ----
+
+def prefill_block_scores(Q, K, dtype, Wq, Wk, blk, kv_dtype=None, kscale=1.0):
+    """fp64 [nb][nb] block importance of one kv head (see
+    orc_prefill_block_scores): Q [G][L][d], K [L][d], Wq/Wk [d][r] fp32."""
+    Q, K = _u16(Q), _u16(K)
+    G, L, d = Q.shape
+    Wq = np.ascontiguousarray(Wq, np.float32)
+    Wk = np.ascontiguousarray(Wk, np.float32)
+    r = Wq.shape[1]
+    nb = -(-L // blk)
+    S = np.empty((nb, nb), np.float64)
+    qd, kd = _kv(dtype, kv_dtype)
+    if lib().orc_prefill_block_scores(Q, qd, K, kd, float(kscale), Wq, Wk, G, d, r, L, int(blk),
+                                      S) != 0:
+        raise ValueError("orc_prefill_block_scores: bad arguments")
+    return S
+
+
+def prefill_select(S, blk, L, token_budget, dense_below):
+    """Key blocks each query block attends, ascending (LServe write-up,
+    section 3.1): below `dense_below` tokens every causal block; otherwise the
+    query block's own (diagonal) block plus the best of the earlier ones by
+    (score desc, index asc), max(1, token_budget // blk) blocks in all --
+    the decode selection rule with the diagonal block in the newest page's
+    place."""
+    nb = S.shape[0]
+    if L < dense_below:
+        return [np.arange(b + 1, dtype=np.int32) for b in range(nb)]
+    k = max(1, int(token_budget) // int(blk))
+    return [select(np.asarray(S[b, :b + 1], np.float32), b + 1, k) for b in range(nb)]
+
+
+def prefill_attention(Q, K, V, dtype, blocks, blk, kv_dtype=None, kscale=1.0, vscale=1.0):
+    """fp64 [G][L][d] causal attention of every query token t over the keys
+    s <= t of its query block's chosen key blocks (two-pass softmax per
+    token, as in `attention`)."""
+    Q = _u16(Q)
+    G, L, d = Q.shape
+    out = np.empty((G, L, d), np.float64)
+    for b, sel in enumerate(blocks):
+        base = np.concatenate([np.arange(i * blk, min((i + 1) * blk, L)) for i in sel])
+        for t in range(b * blk, min((b + 1) * blk, L)):
+            toks = base[base <= t]
+            out[:, t] = attention(Q[:, t], K, V, dtype, toks, kv_dtype, kscale, vscale)
+    return out
 
 
 # ---- decode state on logical positions ------------------------------------

@@ -491,3 +491,68 @@ int orc_page_mass(const uint16_t *q, const uint16_t *K, int dtype, int G, int d,
                   double *mass) {
   return orc_page_mass_kv(q, dtype, K, dtype, 1.0, G, d, tokens, n, ell, pages, n_pages, mass);
 }
+
+/* ---- (prefill) low-rank block importance ------------------------------- */
+
+/*
+ * Block importance for prefill ("LServe long-sequence LLM serving system",
+ * section 3.1): Score(Q, K_i) ~ (Q W_q)(K_i W_k)^T / sqrt(d), with low-rank
+ * projections W_q, W_k of d x r (r = d/8), estimated for every (query
+ * block b, key block i) before exact attention runs on the chosen blocks.
+ * Reading: the score of a block pair is the mean of the approximate logits
+ * over its token pairs, and a kv head's score the maximum over its G query
+ * heads.  The mean of a bilinear form over all pairs (t in b, u in i) is the
+ * form of the two means, so the score is computed as
+ *   s_g(b, i) = (mean_{t in b} q_{g,t} W_q) . (mean_{u in i} k_u W_k) / sqrt(d)
+ * (the test-suite checks it against the pairwise mean on small inputs).
+ * Q [G][L][d] (q_dtype), K [L][d] (kv_dtype codes, value = code * kscale),
+ * W_q, W_k [d][r] fp32 row-major; blocks of `blk` tokens (the last may be
+ * shorter).  Output S [nb][nb] (nb = ceil(L / blk)), S[b][i] for i <= b,
+ * -inf above the diagonal (causal: a query block sees earlier blocks only).
+ * fp64.  Returns 0, or -1 on a bad argument or out of memory.
+ */
+int orc_prefill_block_scores(const uint16_t *Q, int q_dtype, const uint16_t *K, int kv_dtype,
+                             double kscale, const float *Wq, const float *Wk, int G, int d,
+                             int r, int L, int blk, double *S) {
+  if (L <= 0 || d <= 0 || r <= 0 || blk <= 0 || G <= 0) return -1;
+  int nb = (L + blk - 1) / blk;
+  double *qbar = (double *)calloc((size_t)G * nb * r, sizeof(double)); /* [G][nb][r] */
+  double *kbar = (double *)calloc((size_t)nb * r, sizeof(double));     /* [nb][r] */
+  if (!qbar || !kbar) {
+    free(qbar);
+    free(kbar);
+    return -1;
+  }
+  for (int b = 0; b < nb; ++b) {
+    int t0 = b * blk, t1 = t0 + blk < L ? t0 + blk : L;
+    for (int t = t0; t < t1; ++t)
+      for (int j = 0; j < r; ++j) {
+        double kp = 0.0;
+        for (int c = 0; c < d; ++c)
+          kp += kscale * orc_value(K[(long)t * d + c], kv_dtype) * (double)Wk[(long)c * r + j];
+        kbar[(long)b * r + j] += kp / (t1 - t0);
+        for (int g = 0; g < G; ++g) {
+          double qp = 0.0;
+          for (int c = 0; c < d; ++c)
+            qp += orc_value(Q[((long)g * L + t) * d + c], q_dtype) * (double)Wq[(long)c * r + j];
+          qbar[((long)g * nb + b) * r + j] += qp / (t1 - t0);
+        }
+      }
+  }
+  double scale = 1.0 / sqrt((double)d);
+  for (int b = 0; b < nb; ++b)
+    for (int i = 0; i < nb; ++i) {
+      double best = -INFINITY;
+      if (i <= b)
+        for (int g = 0; g < G; ++g) {
+          double acc = 0.0;
+          for (int j = 0; j < r; ++j) acc += qbar[((long)g * nb + b) * r + j] * kbar[(long)i * r + j];
+          acc *= scale;
+          if (acc > best) best = acc;
+        }
+      S[(long)b * nb + i] = best;
+    }
+  free(qbar);
+  free(kbar);
+  return 0;
+}

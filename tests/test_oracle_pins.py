@@ -667,3 +667,109 @@ def test_fp8_decode_layer_is_sdpa_over_dequantized_kv():
     assert np.array_equal(s.K[0, :L], oracle.quantize_e4m3(K[:, 0], "bf16", ks[0]))
     mn, mx = oracle.page_minmax(s.K[1, :L], "e4m3", 16)
     assert np.array_equal(s.kmin[1], mn) and np.array_equal(s.kmax[1], mx)
+
+
+# ---- prefill: low-rank block importance, block-sparse causal attention ----------
+
+def _prefill_inputs(seed, L, d, G, r, dtype="bf16"):
+    rg = np.random.default_rng(seed)
+    Q = W.to_bits(rg.standard_normal((G, L, d)).astype(np.float32), dtype)
+    K = W.to_bits(rg.standard_normal((L, d)).astype(np.float32), dtype)
+    V = W.to_bits(rg.standard_normal((L, d)).astype(np.float32), dtype)
+    Wq = (rg.standard_normal((d, r)) / math.sqrt(d)).astype(np.float32)
+    Wk = (rg.standard_normal((d, r)) / math.sqrt(d)).astype(np.float32)
+    return Q, K, V, Wq, Wk
+
+
+def test_prefill_block_scores_equal_the_pairwise_mean():
+    # the definition: mean over the block pair's token pairs of the low-rank
+    # logits, max over the group -- brute force with torch, partial last block
+    L, d, G, r, blk = 150, 64, 2, 8, 32
+    Q, K, _, Wq, Wk = _prefill_inputs(51, L, d, G, r)
+    S = oracle.prefill_block_scores(Q, K, "bf16", Wq, Wk, blk)
+    qt = torch.from_numpy(oracle.decode(Q, "bf16")) @ torch.from_numpy(Wq).double()
+    kt = torch.from_numpy(oracle.decode(K, "bf16")) @ torch.from_numpy(Wk).double()
+    z = qt @ kt.T / math.sqrt(d)                                  # [G][L][L]
+    nb = -(-L // blk)
+    for b in range(nb):
+        for i in range(nb):
+            if i > b:
+                assert S[b, i] == -np.inf
+                continue
+            m = z[:, b * blk:(b + 1) * blk, i * blk:(i + 1) * blk].mean(dim=(1, 2))
+            assert abs(S[b, i] - float(m.max())) <= 1e-12, (b, i)
+
+
+def test_prefill_identity_projection_scores_mean_exact_logits():
+    L, d, G, blk = 96, 16, 1, 32
+    Q, K, _, _, _ = _prefill_inputs(53, L, d, G, 2, "f16")
+    eye = np.eye(d, dtype=np.float32)
+    S = oracle.prefill_block_scores(Q, K, "f16", eye, eye, blk)
+    z = (torch.from_numpy(oracle.decode(Q, "f16"))[0] @
+         torch.from_numpy(oracle.decode(K, "f16")).T) / math.sqrt(d)
+    assert abs(S[2, 1] - float(z[64:96, 32:64].mean())) <= 1e-12
+
+
+def _block_mask(blocks, blk, L):
+    M = np.zeros((L, L), bool)
+    for b, sel in enumerate(blocks):
+        for t in range(b * blk, min((b + 1) * blk, L)):
+            for i in sel:
+                s0, s1 = i * blk, min((i + 1) * blk, t + 1)
+                if s1 > s0:
+                    M[t, s0:s1] = True
+    return M
+
+
+def _sdpa_masked(Q, K, V, dtype, M):
+    q = torch.from_numpy(oracle.decode(Q, dtype))[None]            # [1][G][L][d]
+    k = torch.from_numpy(oracle.decode(K, dtype))[None, None].expand(1, Q.shape[0], -1, -1)
+    v = torch.from_numpy(oracle.decode(V, dtype))[None, None].expand(1, Q.shape[0], -1, -1)
+    return torch.nn.functional.scaled_dot_product_attention(
+        q, k, v, attn_mask=torch.from_numpy(M)[None, None])[0].numpy()
+
+
+def test_prefill_below_the_dense_threshold_is_causal_attention():
+    L, d, G, r, blk = 200, 32, 2, 4, 32
+    Q, K, V, Wq, Wk = _prefill_inputs(55, L, d, G, r)
+    S = oracle.prefill_block_scores(Q, K, "bf16", Wq, Wk, blk)
+    blocks = oracle.prefill_select(S, blk, L, token_budget=32, dense_below=32768)
+    assert [b.tolist() for b in blocks] == [list(range(b + 1)) for b in range(len(blocks))]
+    out = oracle.prefill_attention(Q, K, V, "bf16", blocks, blk)
+    q = torch.from_numpy(oracle.decode(Q, "bf16"))[None]
+    k = torch.from_numpy(oracle.decode(K, "bf16"))[None, None].expand(1, G, -1, -1)
+    v = torch.from_numpy(oracle.decode(V, "bf16"))[None, None].expand(1, G, -1, -1)
+    ref = torch.nn.functional.scaled_dot_product_attention(q, k, v, is_causal=True)[0].numpy()
+    assert np.allclose(out, ref, rtol=0, atol=1e-12)
+
+
+def test_prefill_sparse_blocks_are_block_masked_attention():
+    L, d, G, r, blk = 480, 32, 2, 4, 32
+    Q, K, V, Wq, Wk = _prefill_inputs(57, L, d, G, r)
+    S = oracle.prefill_block_scores(Q, K, "bf16", Wq, Wk, blk)
+    blocks = oracle.prefill_select(S, blk, L, token_budget=4 * blk, dense_below=256)
+    for b, sel in enumerate(blocks):
+        assert b in sel and np.all(np.diff(sel) > 0) and len(sel) == min(b + 1, 4)
+        if b >= 4:   # the best three earlier blocks by (score desc, index asc)
+            order = np.lexsort((np.arange(b), -S[b, :b].astype(np.float32)))
+            assert sorted(order[:3].tolist()) == [i for i in sel.tolist() if i != b]
+    out = oracle.prefill_attention(Q, K, V, "bf16", blocks, blk)
+    ref = _sdpa_masked(Q, K, V, "bf16", _block_mask(blocks, blk, L))
+    assert np.allclose(out, ref, rtol=0, atol=1e-12)
+
+
+def test_prefill_planted_block_is_chosen():
+    # a key block aligned with every query's projected direction outranks
+    # the rest for all later query blocks
+    L, d, G, r, blk = 640, 32, 1, 4, 32
+    _, K, _, Wq, Wk = _prefill_inputs(59, L, d, G, r)
+    rg = np.random.default_rng(60)
+    c = rg.standard_normal(d).astype(np.float32)                 # queries share a direction
+    Q = W.to_bits((c + 0.5 * rg.standard_normal((G, L, d))).astype(np.float32), "bf16")
+    Kf = oracle.decode(K, "bf16").astype(np.float32)
+    u = c @ Wq @ Wk.T                                            # the key the scores reward
+    Kf[96:128] = 6 * u / np.linalg.norm(u)
+    K2 = W.to_bits(Kf, "bf16")
+    S = oracle.prefill_block_scores(Q, K2, "bf16", Wq, Wk, blk)
+    blocks = oracle.prefill_select(S, blk, L, token_budget=2 * blk, dense_below=0)
+    assert all(3 in sel for sel in blocks[4:])
