@@ -55,6 +55,9 @@ def parse():
     ap.add_argument("--streaming-layers", default="",
                     help="comma-separated layer indices whose kv heads are all streaming "
                          "(the other layers keep the workload's head split)")
+    ap.add_argument("--prefill", type=int, default=0, metavar="L",
+                    help="time only the prefill block-sparse attention of one L-token prompt "
+                         "(Llama-3-8B shapes, budget 4096, dense below 32K) and print its line")
     ap.add_argument("--kv-fp8", action="store_true",
                     help="store K/V as fp8 E4M3 codes (scale 1/32 on every kv head)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -638,8 +641,66 @@ def run_reference(args):
     }
 
 
+def run_prefill(L, steps, warmup, device):
+    """Prefill block-sparse attention of one L-token prompt with Llama-3-8B
+    attention shapes (32 q / 8 kv heads, d 128, bf16, rank d/8): per step the
+    three kernels (block means, selection, attention).  FLOP/s counts the
+    attention actually computed: per query and head, 4 d flops for each key of
+    its chosen blocks it may see (causal)."""
+    import torch
+    import sparse_paged_decode_logical_gb300 as spd
+    Hq, Hkv, d, r, blk, budget, dense_below = 32, 8, 128, 16, 64, 4096, 32768
+    g = torch.Generator(device=device)
+    g.manual_seed(20262)
+    q = torch.randn((L, Hq, d), generator=g, device=device).to(torch.bfloat16)
+    k = torch.randn((L, Hkv, d), generator=g, device=device).to(torch.bfloat16)
+    v = torch.randn((L, Hkv, d), generator=g, device=device).to(torch.bfloat16)
+    wq = torch.randn((Hkv, d, r), generator=g, device=device) / d ** 0.5
+    wk = torch.randn((Hkv, d, r), generator=g, device=device) / d ** 0.5
+    for _ in range(warmup):
+        spd.prefill_block_sparse_attention(q, k, v, wq, wk, blk, budget, dense_below, check=False)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        out, blocks = spd.prefill_block_sparse_attention(q, k, v, wq, wk, blk, budget,
+                                                         dense_below, check=False)
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    nb = -(-L // blk)
+    keys = 0
+    for bq in range(nb):
+        n_sel = bq + 1 if L < dense_below else min(bq + 1, budget // blk)
+        rows = min(blk, L - bq * blk)
+        keys += (n_sel - 1) * blk * rows + rows * (rows + 1) // 2  # earlier blocks + causal own
+    flops = keys * Hq * 4 * d
+    peak = None
+    pk = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(pk):
+        peak = json.load(open(pk)).get("bf16_tflops")
+    tf = flops / (ms * 1e-3) / 1e12
+    return {"metric": "prefill block-sparse attention ms per prompt", "value": round(ms, 3),
+            "unit": "ms", "higher_is_better": False, "steps": steps, "warmup": warmup,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "prefill of one %d-token prompt, Llama-3-8B attention "
+                                   "shapes, blocks of 64, budget 4096, rank 16" % L,
+                       "dense": L < dense_below},
+            "attention_tflops": round(tf, 2),
+            "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": peak,
+                         "unit": "TFLOP/s", "frac": round(tf / peak, 4) if peak else None,
+                         "traffic": None,
+                         "note": "attention FLOPs computed / time of the three kernels"}}
+
+
 def main():
     args = parse()
+    if args.prefill:
+        import torch
+        res = run_prefill(args.prefill, max(1, min(args.steps, 5)), max(1, min(args.warmup, 2)),
+                          torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0"))))
+        print(json.dumps(res), flush=True)
+        return
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))

@@ -351,6 +351,69 @@ spd_status spd_launch_count(spd_ctx *ctx, long long *n);
 /* Human-readable detail of the last error on this context ("" if none). */
 const char *spd_last_error(spd_ctx *ctx);
 
+/* ---- prefill: block-sparse attention of a prompt ------------------------ */
+/*
+ * The phase before decode ("LServe long-sequence LLM serving system",
+ * section 3.1): every text block's importance to every query block is
+ * estimated with low-rank projections, Score(Q, K_i) ~ (Q W_q)(K_i W_k)^T /
+ * sqrt(d), and exact attention runs only on the most important blocks;
+ * prompts shorter than a threshold (32K in the write-up) fall back to dense
+ * attention.  Readings fixed here (the write-up gives none of them): blocks
+ * of `block` tokens; the score of a (query block b, key block i <= b) pair
+ * is the mean of the low-rank logits over the pair's tokens, and a kv head's
+ * the maximum over its query heads; query block b attends its own block and
+ * the best earlier blocks (ties to the lower block), token_budget / block
+ * blocks in all, or every block 0..b when the prompt is shorter than
+ * dense_below; within them, causal softmax attention (key t' <= query t)
+ * with scale 1 / sqrt(head_dim).  No paged cache is involved: K and V are
+ * the prompt's own rows (spd_kv_append stores them in a context).
+ */
+typedef struct {
+  int num_q_heads, num_kv_heads, head_dim; /* as spd_config: Hq % Hkv == 0,
+                                               Hq / Hkv in {1,2,4,8}, d in {64,128} */
+  spd_dtype dtype;                         /* of q, k and v                     */
+  int rank;          /* r: columns of W_q and W_k, 1..64 (d / 8 in the write-up) */
+  int block;         /* tokens per block; 64 is the size built                  */
+  int token_budget;  /* key tokens a query block keeps (>= block)                */
+  int dense_below;   /* prompts shorter than this attend every causal block     */
+} spd_prefill_config;
+
+/*
+ * Sizes for a prompt of seq_len tokens: KB, the length of each query block's
+ * list in `blocks` (nb = ceil(seq_len / block) when dense, else
+ * min(nb, token_budget / block)), and the workspace bytes.  Host only.
+ * SPD_ERR_INVALID_ARG on a bad configuration or seq_len < 1;
+ * SPD_ERR_CAPACITY beyond 8192 blocks.
+ */
+spd_status spd_prefill_sizes(const spd_prefill_config *cfg, int seq_len,
+                             int *blocks_per_query_block, size_t *workspace_bytes);
+
+/*
+ * Block-sparse causal attention of one prompt, enqueued on `stream` (three
+ * kernels: block means, block selection, attention).
+ *   q          device [seq_len][Hq][d] of dtype, 16-byte aligned.
+ *   k, v       device [seq_len][Hkv][d] of dtype, 16-byte aligned.
+ *   w_q, w_k   device fp32 [Hkv][d][rank]: the low-rank projections of each
+ *              kv head (its query heads share w_q).
+ *   out        device fp32 [seq_len][Hq][d].
+ *   blocks     device int32 [Hkv][nb][KB] or NULL: the key blocks each query
+ *              block attended, ascending, -1 after the last.
+ *   workspace  device, 256-byte aligned, at least the spd_prefill_sizes bytes
+ *              (owned by the caller; holds the block means, the lists and a
+ *              device error word; one call at a time per workspace).
+ * SPD_ERR_INVALID_ARG / SPD_ERR_CAPACITY on bad arguments (nothing
+ * enqueued); SPD_ERR_CUDA if a launch fails.
+ */
+spd_status spd_prefill_block_sparse_attention(const spd_prefill_config *cfg, int seq_len,
+                                              const void *q, const void *k, const void *v,
+                                              const float *w_q, const float *w_k, float *out,
+                                              int *blocks, void *workspace,
+                                              size_t workspace_bytes, spd_stream stream);
+
+/* Waits for `stream` and reads the workspace's device error word:
+ * SPD_ERR_DEVICE_CHECK if a kernel's own check tripped, else SPD_OK. */
+spd_status spd_prefill_check(const void *workspace, spd_stream stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -48,6 +48,13 @@ class spd_config(ctypes.Structure):
                 ("v_scale", ctypes.POINTER(ctypes.c_float))]
 
 
+class spd_prefill_config(ctypes.Structure):
+    _fields_ = [("num_q_heads", ctypes.c_int), ("num_kv_heads", ctypes.c_int),
+                ("head_dim", ctypes.c_int), ("dtype", ctypes.c_int), ("rank", ctypes.c_int),
+                ("block", ctypes.c_int), ("token_budget", ctypes.c_int),
+                ("dense_below", ctypes.c_int)]
+
+
 class spd_sizes(ctypes.Structure):
     _fields_ = [(f, ctypes.c_size_t) for f in BUFFER_FIELDS]
 
@@ -91,6 +98,11 @@ def lib():
         "spd_check_status": [vp, vp],
         "spd_launch_count": [vp, ll],
         "spd_set_early_kv_staging": [vp, i],
+        "spd_prefill_sizes": [ctypes.POINTER(spd_prefill_config), i, ip,
+                              ctypes.POINTER(ctypes.c_size_t)],
+        "spd_prefill_block_sparse_attention": [ctypes.POINTER(spd_prefill_config), i, vp, vp, vp,
+                                               vp, vp, vp, vp, vp, ctypes.c_size_t, vp],
+        "spd_prefill_check": [vp, vp],
     }
     for name, args in sig.items():
         f = getattr(L, name)
@@ -442,3 +454,45 @@ class SparsePagedKVCache:
 
     def set_early_kv_staging(self, enable=True):
         spd_set_early_kv_staging(self.ctx, enable)
+
+
+# ---- prefill: block-sparse attention of one prompt ----------------------------
+
+def prefill_block_sparse_attention(q, k, v, w_q, w_k, block=64, token_budget=4096,
+                                   dense_below=32768, stream=None, check=True):
+    """Block-sparse causal attention of a prompt (spd_prefill_block_sparse_attention).
+
+    q [L][Hq][d], k, v [L][Hkv][d] (fp16 or bf16, one CUDA device), w_q, w_k
+    fp32 [Hkv][d][r].  Returns (out fp32 [L][Hq][d], blocks int32
+    [Hkv][nb][KB]: the key blocks each query block attended, -1 padded)."""
+    import torch
+    L, Hq, d = q.shape
+    Hkv = k.shape[1]
+    r = w_q.shape[2]
+    dt = q.dtype
+    if dt not in (torch.float16, torch.bfloat16) or k.dtype != dt or v.dtype != dt:
+        raise ValueError("q, k, v must share one dtype, fp16 or bf16")
+    for t, shape in ((k, (L, Hkv, d)), (v, (L, Hkv, d)), (w_q, (Hkv, d, r)), (w_k, (Hkv, d, r))):
+        if tuple(t.shape) != shape or not t.is_contiguous() or t.device != q.device:
+            raise ValueError("expected a contiguous tensor %s on %s" % (shape, q.device))
+    if w_q.dtype != torch.float32 or w_k.dtype != torch.float32 or not q.is_contiguous():
+        raise ValueError("w_q, w_k must be fp32 and q contiguous")
+    cfg = spd_prefill_config(Hq, Hkv, d, 1 if dt == torch.bfloat16 else 0, r, block,
+                             token_budget, dense_below)
+    kb, ws = ctypes.c_int(), ctypes.c_size_t()
+    _check(lib().spd_prefill_sizes(ctypes.byref(cfg), L, ctypes.byref(kb), ctypes.byref(ws)),
+           "spd_prefill_sizes")
+    nb = -(-L // block)
+    out = torch.empty((L, Hq, d), dtype=torch.float32, device=q.device)
+    blocks = torch.empty((Hkv, nb, kb.value), dtype=torch.int32, device=q.device)
+    work = torch.empty(ws.value, dtype=torch.uint8, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    st = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    _check(lib().spd_prefill_block_sparse_attention(
+        ctypes.byref(cfg), L, q.data_ptr(), k.data_ptr(), v.data_ptr(), w_q.data_ptr(),
+        w_k.data_ptr(), out.data_ptr(), blocks.data_ptr(), work.data_ptr(), ws.value,
+        st or None), "spd_prefill_block_sparse_attention")
+    if check:
+        _check(lib().spd_prefill_check(work.data_ptr(), st or None), "spd_prefill_check")
+    return out, blocks

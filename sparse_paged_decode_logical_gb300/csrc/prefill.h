@@ -1,0 +1,33 @@
+// Internal interface of the prefill kernels (prefill.cu): block importance,
+// block selection and block-sparse causal attention of one prompt.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace spd {
+
+constexpr int kPrefillBlock = 64;       // tokens per block (query and key)
+constexpr int kPrefillMaxBlocks = 8192;  // blocks of a prompt (the top-k holds this many)
+constexpr int kPrefillMaxRank = 64;
+
+struct PrefillParams {
+  const void *q;         // [L][Hq][d]
+  const void *k, *v;     // [L][Hkv][d]
+  const float *wq, *wk;  // [Hkv][d][r]
+  float *out;            // [L][Hq][d]
+  int *blocks_out;       // [Hkv][nb][KB] or null
+  float *qbar;           // [Hkv][G][nb][r] block means of q, projected
+  float *kbar;           // [Hkv][nb][r]    block means of k, projected
+  int *lists;            // [Hkv][nb][KB]   key blocks of every query block, ascending, -1 after
+  int *err;              // device error word (4 ints)
+  int L, Hq, Hkv, G, r, nb, KB;
+  int kblocks;           // key blocks a query block keeps in sparse mode (own block included)
+  int dense;             // 1: every causal block
+  float score_scale;     // 1 / sqrt(d)
+  float scale_log2;      // log2(e) / sqrt(d)
+};
+
+// dtype: 0 fp16, 1 bf16; d: 64 or 128.  Each returns cudaGetLastError().
+cudaError_t launch_prefill(const PrefillParams &p, int dtype, int d, cudaStream_t st);
+
+}  // namespace spd

@@ -231,3 +231,48 @@ def test_page_mass_arguments_checked_before_any_work():
             spd.spd_sparse_decode_attention_page_mass(ctx, fake, [s], fake, *args)
         assert e.value.name == "SPD_ERR_INVALID_ARG", args
     assert spd.spd_seq_info(ctx, s)["step_counter"] == 0
+
+
+def pcfg(**kw):
+    base = dict(num_q_heads=8, num_kv_heads=2, head_dim=128, dtype=1, rank=16, block=64,
+                token_budget=256, dense_below=32768)
+    base.update(kw)
+    return spd.spd_prefill_config(**base)
+
+
+def prefill_sizes(c, L):
+    kb, ws = ctypes.c_int(), ctypes.c_size_t()
+    st = spd.lib().spd_prefill_sizes(ctypes.byref(c), L, ctypes.byref(kb), ctypes.byref(ws))
+    return st, kb.value, ws.value
+
+
+def test_prefill_sizes_dense_and_sparse():
+    st, kb, ws = prefill_sizes(pcfg(), 1000)            # below 32K: dense, 16 blocks
+    assert st == 0 and kb == 16 and ws > 0
+    st, kb, _ = prefill_sizes(pcfg(dense_below=0), 1000)  # sparse: 256 / 64 blocks
+    assert st == 0 and kb == 4
+    st, kb, _ = prefill_sizes(pcfg(dense_below=0, token_budget=10 ** 6), 1000)
+    assert st == 0 and kb == 16
+    st, _, _ = prefill_sizes(pcfg(dense_below=0), 64 * 8192 + 1)
+    assert spd.STATUS[st] == "SPD_ERR_CAPACITY"
+
+
+@pytest.mark.parametrize("bad", [dict(block=32), dict(rank=0), dict(rank=65), dict(head_dim=96),
+                                 dict(token_budget=63), dict(num_q_heads=6), dict(dtype=3),
+                                 dict(dense_below=-1)])
+def test_prefill_configs_checked(bad):
+    st, _, _ = prefill_sizes(pcfg(**bad), 1000)
+    assert spd.STATUS[st] == "SPD_ERR_INVALID_ARG"
+    assert spd.STATUS[prefill_sizes(pcfg(), 0)[0]] == "SPD_ERR_INVALID_ARG"
+
+
+def test_prefill_arguments_checked_before_any_work():
+    c = pcfg()
+    _, _, ws = prefill_sizes(c, 1000)
+    L = spd.lib()
+    a = 1 << 41
+    run = lambda q, w, n: L.spd_prefill_block_sparse_attention(
+        ctypes.byref(c), 1000, q, a, a, a, a, a, None, w, n, None)
+    assert spd.STATUS[run(a + 8, a, ws)] == "SPD_ERR_INVALID_ARG"   # q not 16-byte aligned
+    assert spd.STATUS[run(a, a + 16, ws)] == "SPD_ERR_INVALID_ARG"  # workspace not 256-aligned
+    assert spd.STATUS[run(a, a, ws - 1)] == "SPD_ERR_CAPACITY"      # workspace too small

@@ -1,0 +1,89 @@
+"""GPU parity of the prefill-side block-sparse attention ("LServe long-sequence
+LLM serving system", section 3.1) against the CPU oracle, through the C ABI.
+
+Block selection: the GPU's lists equal the oracle's, except blocks whose
+oracle score lies within 1e-4 of the row's largest score magnitude of the
+cut (the GPU pools then projects in fp32, the oracle projects then pools in
+fp64).  Attention: the oracle run on the GPU's own lists, max-abs <= 2e-3
+and mean-abs <= 2e-4 (the decode tolerances)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from harness import TOL_MAX, TOL_MEAN, tdev
+import sparse_paged_decode_logical_gb300 as spd
+
+pytestmark = pytest.mark.gpu
+
+needs_gpu = pytest.mark.skipif(not torch.cuda.is_available(), reason="no CUDA device")
+BLK = 64
+BAND = 1e-4
+
+
+def _inputs(seed, L, Hq, Hkv, d, r, dtype):
+    rg = np.random.default_rng([20260, 77, seed])
+    Q = W.to_bits(rg.standard_normal((L, Hq, d)).astype(np.float32), dtype)
+    K = W.to_bits(rg.standard_normal((L, Hkv, d)).astype(np.float32), dtype)
+    V = W.to_bits(rg.standard_normal((L, Hkv, d)).astype(np.float32), dtype)
+    # a planted key block that the low-rank scores favour for some heads
+    Wq = (rg.standard_normal((Hkv, d, r)) / np.sqrt(d)).astype(np.float32)
+    Wk = (rg.standard_normal((Hkv, d, r)) / np.sqrt(d)).astype(np.float32)
+    return Q, K, V, Wq, Wk
+
+
+def _check(L, Hq, Hkv, d, r, dtype, budget, dense_below, seed):
+    Q, K, V, Wq, Wk = _inputs(seed, L, Hq, Hkv, d, r, dtype)
+    out, blocks = spd.prefill_block_sparse_attention(
+        tdev(Q, dtype), tdev(K, dtype), tdev(V, dtype), torch.from_numpy(Wq).cuda(),
+        torch.from_numpy(Wk).cuda(), block=BLK, token_budget=budget, dense_below=dense_below)
+    torch.cuda.synchronize()
+    out = out.cpu().numpy().astype(np.float64)
+    blocks = blocks.cpu().numpy()
+    G = Hq // Hkv
+    nb = -(-L // BLK)
+    for hk in range(Hkv):
+        Qh = np.ascontiguousarray(Q[:, hk * G:(hk + 1) * G].transpose(1, 0, 2))
+        S = oracle.prefill_block_scores(Qh, K[:, hk], dtype, Wq[hk], Wk[hk], BLK)
+        own = oracle.prefill_select(S, BLK, L, budget, dense_below)
+        gpu = []
+        for b in range(nb):
+            row = blocks[hk, b]
+            g = row[row >= 0]
+            assert np.all(np.diff(g) > 0) and g[-1] == b, (hk, b, g)
+            assert np.all(row[len(g):] == -1)
+            if not np.array_equal(g, own[b]):
+                assert len(g) == len(own[b]), (hk, b)
+                cand = [i for i in own[b] if i != b]
+                cut = S[b, cand].min()
+                tol = BAND * max(np.abs(S[b, :b]).max(), 1e-30)
+                diff = np.setxor1d(g, own[b])
+                assert np.all(np.abs(S[b, diff] - cut) <= tol), (hk, b, diff, S[b, diff], cut)
+            gpu.append(g.astype(np.int32))
+        ref = oracle.prefill_attention(Qh, K[:, hk], V[:, hk], dtype, gpu, BLK)  # [G][L][d]
+        got = out[:, hk * G:(hk + 1) * G].transpose(1, 0, 2)
+        err = np.abs(got - ref)
+        assert np.isfinite(got).all()
+        assert err.max() <= TOL_MAX and err.mean() <= TOL_MEAN, (hk, err.max(), err.mean())
+    return blocks
+
+
+@needs_gpu
+def test_prefill_dense_below_the_threshold():
+    # 300 tokens: 5 blocks, the last partial; every causal block attended
+    blocks = _check(300, 4, 2, 128, 16, "bf16", budget=128, dense_below=32768, seed=1)
+    assert blocks.shape == (2, 5, 5)
+
+
+@needs_gpu
+@pytest.mark.parametrize("case", [
+    dict(L=1000, Hq=8, Hkv=2, d=128, r=16, dtype="bf16", budget=256, seed=2),
+    dict(L=777, Hq=2, Hkv=2, d=64, r=8, dtype="f16", budget=128, seed=3),
+    dict(L=500, Hq=8, Hkv=1, d=128, r=16, dtype="bf16", budget=64, seed=4),
+    dict(L=2048, Hq=4, Hkv=1, d=128, r=16, dtype="f16", budget=512, seed=5),
+])
+def test_prefill_sparse_blocks(case):
+    c = dict(case)
+    _check(c.pop("L"), c.pop("Hq"), c.pop("Hkv"), c.pop("d"), c.pop("r"), c.pop("dtype"),
+           c.pop("budget"), dense_below=0, seed=c.pop("seed"))
