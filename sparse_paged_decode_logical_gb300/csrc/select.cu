@@ -357,6 +357,9 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_consta
   }
   __syncthreads();  // ... and the acquire above precedes every read below
   if (!s_last) return;
+  // the other CTAs wrote their scores through the generic proxy; the top-k's
+  // bulk copy reads them through the async proxy
+  asm volatile("fence.proxy.async.global;" ::: "memory");
   const int k = s.K_sel - 1;
   int got;
   if (n <= kMaxKeys) {
