@@ -32,6 +32,7 @@ import json
 import os
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -141,7 +142,7 @@ class ClockSampler:
             if vis:
                 self.index = vis.split(",")[index]
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", "clocks_%d.csv" % os.getpid())
+        self.path = os.path.join(tempfile.gettempdir(), "spd_clocks_%d.csv" % os.getpid())
 
     def start(self):
         try:

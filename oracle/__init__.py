@@ -26,7 +26,7 @@ Sources ("LServe long-sequence LLM serving system" write-up unless noted):
                query-aware block importance) and section 2.3 (GQA head
                sharing, 1/sqrt(head_dim) scale).
 
-Readings where the pages are silent (each also listed in the design doc):
+Readings where the pages are silent:
   the group score is the max over the G query heads sharing a kv head; the
   page holding the newest token is always kept; pages created during a
   reuse window are attended; the window includes the newest token and sink
