@@ -87,3 +87,16 @@ def test_prefill_sparse_blocks(case):
     c = dict(case)
     _check(c.pop("L"), c.pop("Hq"), c.pop("Hkv"), c.pop("d"), c.pop("r"), c.pop("dtype"),
            c.pop("budget"), dense_below=0, seed=c.pop("seed"))
+
+
+@needs_gpu
+@pytest.mark.parametrize("case", [
+    dict(L=1, Hq=4, Hkv=2, d=128, r=16, dtype="bf16", budget=64, dense_below=0, seed=6),
+    dict(L=64, Hq=2, Hkv=1, d=64, r=8, dtype="f16", budget=64, dense_below=0, seed=7),
+    dict(L=320, Hq=4, Hkv=4, d=128, r=16, dtype="bf16", budget=10 ** 6, dense_below=0, seed=8),
+])
+def test_prefill_edges(case):
+    # one token; exactly one full block; a budget above the prompt (every block kept)
+    c = dict(case)
+    _check(c.pop("L"), c.pop("Hq"), c.pop("Hkv"), c.pop("d"), c.pop("r"), c.pop("dtype"),
+           c.pop("budget"), c.pop("dense_below"), seed=c.pop("seed"))
