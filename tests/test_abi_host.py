@@ -276,3 +276,19 @@ def test_prefill_arguments_checked_before_any_work():
     assert spd.STATUS[run(a + 8, a, ws)] == "SPD_ERR_INVALID_ARG"   # q not 16-byte aligned
     assert spd.STATUS[run(a, a + 16, ws)] == "SPD_ERR_INVALID_ARG"  # workspace not 256-aligned
     assert spd.STATUS[run(a, a, ws - 1)] == "SPD_ERR_CAPACITY"      # workspace too small
+
+
+def test_prefill_binding_checks_tensors_before_the_library():
+    torch = pytest.importorskip("torch")
+    L, Hq, Hkv, d, r = 70, 4, 2, 64, 8
+    q = torch.zeros((L, Hq, d), dtype=torch.bfloat16)
+    k = torch.zeros((L, Hkv, d), dtype=torch.bfloat16)
+    w = torch.zeros((Hkv, d, r), dtype=torch.float32)
+    with pytest.raises(ValueError):   # k and v must share q's dtype
+        spd.prefill_block_sparse_attention(q, k, k.half(), w, w)
+    with pytest.raises(ValueError):   # k's shape must follow q's
+        spd.prefill_block_sparse_attention(q, k[:-1], k, w, w)
+    with pytest.raises(ValueError):   # projections are fp32 [Hkv][d][r]
+        spd.prefill_block_sparse_attention(q, k, k, w.half(), w)
+    with pytest.raises(ValueError):   # fp16 / bf16 only
+        spd.prefill_block_sparse_attention(q.float(), k.float(), k.float(), w, w)
