@@ -109,6 +109,9 @@ def lib():
         L.orc_prefill_block_scores.argtypes = [u16p, ci, u16p, ci, f64, f32p, f32p, ci, ci, ci,
                                                ci, ci, f64p]
         L.orc_prefill_block_scores.restype = ci
+        L.orc_prefill_attention.argtypes = [u16p, ci, u16p, u16p, ci, f64, f64, ci, ci, ci, ci,
+                                            i32p, i32p, f64p]
+        L.orc_prefill_attention.restype = ci
         _lib = L
     return _lib
 
@@ -306,16 +309,18 @@ def prefill_select(S, blk, L, token_budget, dense_below):
 
 def prefill_attention(Q, K, V, dtype, blocks, blk, kv_dtype=None, kscale=1.0, vscale=1.0):
     """fp64 [G][L][d] causal attention of every query token t over the keys
-    s <= t of its query block's chosen key blocks (two-pass softmax per
-    token, as in `attention`)."""
-    Q = _u16(Q)
+    s <= t of its query block's chosen key blocks (see orc_prefill_attention;
+    per token the two-pass softmax of `attention`)."""
+    Q, K, V = _u16(Q), _u16(K), _u16(V)
     G, L, d = Q.shape
+    flat = np.ascontiguousarray(np.concatenate([np.asarray(b, np.int32) for b in blocks]),
+                                np.int32)
+    offs = np.ascontiguousarray(np.cumsum([0] + [len(b) for b in blocks]), np.int32)
     out = np.empty((G, L, d), np.float64)
-    for b, sel in enumerate(blocks):
-        base = np.concatenate([np.arange(i * blk, min((i + 1) * blk, L)) for i in sel])
-        for t in range(b * blk, min((b + 1) * blk, L)):
-            toks = base[base <= t]
-            out[:, t] = attention(Q[:, t], K, V, dtype, toks, kv_dtype, kscale, vscale)
+    qd, kd = _kv(dtype, kv_dtype)
+    if lib().orc_prefill_attention(Q, qd, K, V, kd, float(kscale), float(vscale), G, d, L,
+                                   int(blk), flat, offs, out) != 0:
+        raise ValueError("orc_prefill_attention: bad arguments")
     return out
 
 

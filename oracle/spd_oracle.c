@@ -556,3 +556,71 @@ int orc_prefill_block_scores(const uint16_t *Q, int q_dtype, const uint16_t *K, 
   free(kbar);
   return 0;
 }
+
+/*
+ * Block-sparse causal attention of a prompt for one kv head (LServe write-up,
+ * section 3.1): query token t of each of the G heads attends the keys u <= t
+ * of the key blocks chosen for its query block t / blk, blocks[offsets[b] ..
+ * offsets[b+1]).  Per query token the two-pass fp64 softmax of
+ * orc_attention_kv (same products, same order).  Q [G][L][d] (q_dtype), K
+ * and V [L][d] (kv_dtype codes, values code * kscale / code * vscale), out
+ * [G][L][d].  Returns 0, or -1 on a bad argument or out of memory.
+ */
+int orc_prefill_attention(const uint16_t *Q, int q_dtype, const uint16_t *K, const uint16_t *V,
+                          int kv_dtype, double kscale, double vscale, int G, int d, int L,
+                          int blk, const int *blocks, const int *offsets, double *out) {
+  if (L <= 0 || d <= 0 || G <= 0 || blk <= 0) return -1;
+  int nb = (L + blk - 1) / blk;
+  double *kd = (double *)malloc(sizeof(double) * (size_t)L * d);
+  double *vd = (double *)malloc(sizeof(double) * (size_t)L * d);
+  double *qd = (double *)malloc(sizeof(double) * (size_t)d);
+  double *z = (double *)malloc(sizeof(double) * (size_t)L);
+  int *keys = (int *)malloc(sizeof(int) * (size_t)L);
+  if (!kd || !vd || !qd || !z || !keys) {
+    free(kd); free(vd); free(qd); free(z); free(keys);
+    return -1;
+  }
+  for (long x = 0; x < (long)L * d; ++x) {
+    kd[x] = kscale * orc_value(K[x], kv_dtype);
+    vd[x] = vscale * orc_value(V[x], kv_dtype);
+  }
+  double scale = 1.0 / sqrt((double)d);
+  for (int b = 0; b < nb; ++b) {
+    for (int t = b * blk; t < L && t < (b + 1) * blk; ++t) {
+      int n = 0;
+      for (int e = offsets[b]; e < offsets[b + 1]; ++e) {
+        int i = blocks[e];
+        if (i < 0 || i >= nb) {
+          free(kd); free(vd); free(qd); free(z); free(keys);
+          return -1;
+        }
+        for (int u = i * blk; u < L && u < (i + 1) * blk && u <= t; ++u) keys[n++] = u;
+      }
+      for (int g = 0; g < G; ++g) {
+        double *o = out + ((long)g * L + t) * d;
+        for (int c = 0; c < d; ++c) qd[c] = orc_value(Q[((long)g * L + t) * d + c], q_dtype);
+        double m = -INFINITY;
+        for (int j = 0; j < n; ++j) {
+          const double *k = kd + (long)keys[j] * d;
+          double dot = 0.0;
+          for (int c = 0; c < d; ++c) dot += qd[c] * k[c];
+          z[j] = dot * scale;
+          if (z[j] > m) m = z[j];
+        }
+        double den = 0.0;
+        for (int j = 0; j < n; ++j) {
+          z[j] = exp(z[j] - m);
+          den += z[j];
+        }
+        for (int c = 0; c < d; ++c) o[c] = 0.0;
+        for (int j = 0; j < n; ++j) {
+          const double *v = vd + (long)keys[j] * d;
+          for (int c = 0; c < d; ++c) o[c] += z[j] * v[c];
+        }
+        for (int c = 0; c < d; ++c) o[c] = n > 0 ? o[c] / den : 0.0;
+      }
+    }
+  }
+  free(kd); free(vd); free(qd); free(z); free(keys);
+  return 0;
+}

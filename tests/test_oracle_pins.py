@@ -773,3 +773,18 @@ def test_prefill_planted_block_is_chosen():
     S = oracle.prefill_block_scores(Q, K2, "bf16", Wq, Wk, blk)
     blocks = oracle.prefill_select(S, blk, L, token_budget=2 * blk, dense_below=0)
     assert all(3 in sel for sel in blocks[4:])
+
+
+def test_prefill_attention_is_the_per_token_attention():
+    # the prompt routine equals `attention` called once per query token on
+    # its allowed keys, bit for bit (same products in the same order)
+    L, d, G, blk = 200, 32, 2, 32
+    Q, K, V, Wq, Wk = _prefill_inputs(61, L, d, G, 4, "f16")
+    S = oracle.prefill_block_scores(Q, K, "f16", Wq, Wk, blk)
+    blocks = oracle.prefill_select(S, blk, L, token_budget=2 * blk, dense_below=0)
+    out = oracle.prefill_attention(Q, K, V, "f16", blocks, blk)
+    for t in (0, 31, 32, 100, 199):
+        sel = blocks[t // blk]
+        toks = np.concatenate([np.arange(i * blk, min((i + 1) * blk, L)) for i in sel])
+        ref = oracle.attention(Q[:, t], K, V, "f16", toks[toks <= t])
+        assert np.array_equal(out[:, t], ref), t
