@@ -237,11 +237,18 @@ spd_status spd_sparse_decode_attention(spd_ctx *ctx, const void *q,
  * partials and tickets of the fused combine live in a library-owned
  * file-scope device array of 4,292,608 bytes, held on every GPU that loads
  * the library until the process exits, instead of the context's scratch.
- * Limits: at most 1024 split items per launch (an item is up to 128 attended
- * rows of one kv head); a sequence whose work needs more is rejected with
- * SPD_ERR_CAPACITY before anything is enqueued.  The first call on a device
+ * Limits: the array holds the partials of 1024 split items per launch.  The
+ * library cuts each (sequence, kv head) into items of at most 256 tiles of 16
+ * attended rows (4,096 tokens), in whole thread-block clusters of up to 16
+ * items, and normally plans about one item per SM per launch; a batch that
+ * needs more items is spread over several launches, and a single sequence
+ * whose items alone exceed 1024 (for example 33 kv heads each attending
+ * 131,072 tokens) makes the call fail with SPD_ERR_CAPACITY.  Every launch
+ * is planned before anything is enqueued, so a refused call writes nothing
+ * and advances no step counter.  The first call on a device
  * looks up the array's device address (cudaGetSymbolAddress with that device
- * current); make it before any stream capture.  All calls share the array
+ * current, then the caller's current device is restored); make it before any
+ * stream capture.  All calls share the array
  * and it keeps the last call's contents: tickets are cleared at each call,
  * and calls whose GPU work overlaps (other streams, other contexts) race --
  * issue them in order on one stream.  It calls no cudaMalloc, cudaFree or

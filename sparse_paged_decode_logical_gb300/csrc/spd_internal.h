@@ -199,6 +199,9 @@ struct DecodeScratch {
 spd_status check_attention_call(spd_ctx *c, const void *q, const int *ids, int n,
                                 const float *out);
 spd_status bind_device(spd_ctx *c, cudaStream_t st, int *device);
+// SPD_ERR_CAPACITY (with nothing enqueued) if some launch of the call would
+// need more than max_items split items.
+spd_status check_attention_capacity(spd_ctx *c, const int *ids, int n, int max_items);
 spd_status attention_with_scratch(spd_ctx *c, const void *q, const int *ids, int n, float *out,
                                   cudaStream_t st, const DecodeScratch &scratch);
 spd_status fail_message(spd_ctx *c, spd_status s, const char *msg);

@@ -300,8 +300,24 @@ spd_status make_tensor_maps(spd_ctx *c) {
   return SPD_OK;
 }
 
-// First GPU-side call: bind the device that owns the buffers, learn the SM
-// count, and zero the scratch header (error word) and ticket counters.
+// The set-up of ensure_device, with the buffers' device current.
+spd_status ensure_device_current(spd_ctx *c, cudaStream_t st) {
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, c->device) == cudaSuccess &&
+      sms > 0)
+    c->num_sms = sms;
+  cudaError_t e;
+  if ((e = prepare_decode_kernels()) != cudaSuccess) return cuda_fail(c, e, "kernel attributes");
+  spd_status r = make_tensor_maps(c);
+  if (r != SPD_OK) return r;
+  e = cudaMemsetAsync(c->buf.scratch, 0, c->dv.sl.part_ml, st);
+  if (e != cudaSuccess) return cuda_fail(c, e, "cudaMemsetAsync(scratch header)");
+  return SPD_OK;
+}
+
+// First GPU-side call: find the device that owns the buffers, learn its SM
+// count, set the kernels' attributes and zero the scratch header (error word)
+// and ticket counters.  The caller's current device is left as it was.
 spd_status ensure_device(spd_ctx *c, cudaStream_t st) {
   if (c->device_ready) return SPD_OK;
   cudaPointerAttributes a{};
@@ -310,18 +326,19 @@ spd_status ensure_device(spd_ctx *c, cudaStream_t st) {
   if (a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeManaged)
     return c->fail(SPD_ERR_INVALID_ARG, "scratch is not device memory");
   c->device = a.device;
-  if ((e = cudaSetDevice(c->device)) != cudaSuccess) return cuda_fail(c, e, "cudaSetDevice");
-  int sms = 0;
-  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, c->device) == cudaSuccess &&
-      sms > 0)
-    c->num_sms = sms;
-  if ((e = prepare_decode_kernels()) != cudaSuccess) return cuda_fail(c, e, "kernel attributes");
-  spd_status r = make_tensor_maps(c);
-  if (r != SPD_OK) return r;
-  e = cudaMemsetAsync(c->buf.scratch, 0, c->dv.sl.part_ml, st);
-  if (e != cudaSuccess) return cuda_fail(c, e, "cudaMemsetAsync(scratch header)");
-  c->device_ready = true;
-  return SPD_OK;
+  // kernel attributes are per device: set them with the buffers' device
+  // current, then give the caller back the device it had
+  int prev = -1;
+  const bool had = cudaGetDevice(&prev) == cudaSuccess;
+  if (!had || prev != c->device)
+    if ((e = cudaSetDevice(c->device)) != cudaSuccess) return cuda_fail(c, e, "cudaSetDevice");
+  spd_status r = ensure_device_current(c, st);
+  if (had && prev != c->device) {
+    const cudaError_t e2 = cudaSetDevice(prev);
+    if (r == SPD_OK && e2 != cudaSuccess) return cuda_fail(c, e2, "cudaSetDevice(restore)");
+  }
+  if (r == SPD_OK) c->device_ready = true;
+  return r;
 }
 
 spd_status check_seqs(spd_ctx *c, const int *ids, int n) {
@@ -593,6 +610,31 @@ int plan_tiles(const spd_ctx *c, TileDecodeParams &p, const int *ids, int n) {
   return items;
 }
 
+// The sequences [b, b + m) of a call that one decode launch takes: as many as
+// fit one parameter block and max_items, halving until they do (down to one
+// sequence).  Leaves p planned for them and returns m.
+int next_batch(const spd_ctx *c, TileDecodeParams &p, const int *ids, int b, int n,
+               int max_items) {
+  int m = std::min(c->dv.seqs_per_launch, n - b);
+  while (plan_tiles(c, p, ids + b, m) > max_items && m > 1) m = (m + 1) / 2;
+  return m;
+}
+
+// Plans every launch of an attention call without enqueuing anything; fails
+// with SPD_ERR_CAPACITY if a launch would need more than max_items items
+// (a single sequence whose split items alone exceed it).
+spd_status check_capacity(spd_ctx *c, const int *ids, int n, int max_items) {
+  static thread_local TileDecodeParams p;
+  for (int b = 0; b < n;) {
+    const int m = next_batch(c, p, ids, b, n, max_items);
+    if (p.total_items > max_items)
+      return c->fail(SPD_ERR_CAPACITY, "sequence %d needs %d split items, the library-owned "
+                     "scratch holds %d", ids[b], p.total_items, max_items);
+    b += m;
+  }
+  return SPD_OK;
+}
+
 // `scr` (optional) replaces the context's scratch for the split partials and
 // tickets; a launch then holds at most scr->max_items items.
 // fused_topk: the selection launched just before wrote only scores for the
@@ -616,18 +658,12 @@ spd_status attention_impl(spd_ctx *c, const void *q, const int *ids, int n, floa
   const size_t qrow = (size_t)c->cfg.num_q_heads * c->cfg.head_dim;
   const size_t kvrow = (size_t)c->cfg.num_kv_heads * c->cfg.head_dim;
   const int max_items = scr ? scr->max_items : kMaxItems;
+  // a bounded scratch: every launch is planned before the first is enqueued
+  if (scr && (r = check_capacity(c, ids, n, max_items)) != SPD_OK) return r;
   int b = 0;
   while (b < n) {
-    // grow the batch while it fits one parameter block and max_items
-    int m = std::min(dv.seqs_per_launch, n - b);
     static thread_local TileDecodeParams p;
-    for (;;) {
-      if (plan_tiles(c, p, ids + b, m) <= max_items || m == 1) break;
-      m = (m + 1) / 2;
-    }
-    if (scr && p.total_items > max_items)
-      return c->fail(SPD_ERR_CAPACITY, "sequence %d needs %d split items, the library-owned "
-                     "scratch holds %d", ids[b], p.total_items, max_items);
+    const int m = next_batch(c, p, ids, b, n, max_items);
     p.n_seqs = m;
     p.tm_k = c->tm_k;
     p.tm_v = c->tm_v;
@@ -730,6 +766,10 @@ spd_status check_attention_call(spd_ctx *c, const void *q, const int *ids, int n
   spd_status r = check_seqs(c, ids, n);
   if (r != SPD_OK) return r;
   return check_attend_state(c, ids, n, false);
+}
+
+spd_status check_attention_capacity(spd_ctx *c, const int *ids, int n, int max_items) {
+  return check_capacity(c, ids, n, max_items);
 }
 
 spd_status bind_device(spd_ctx *c, cudaStream_t st, int *device) {

@@ -29,7 +29,7 @@
 
 namespace {
 
-constexpr int kStaticItems = 1024;   // split items per launch (<= 128 rows each)
+constexpr int kStaticItems = 1024;   // split items per launch (<= 256 tiles of 16 rows each)
 constexpr int kStaticMaxG = 8;       // query heads per kv head
 constexpr int kStaticMaxD = 128;     // head_dim
 constexpr size_t kTicketBytes = (size_t)spd::kSeqsPerLaunch * spd::kMaxKvHeads * sizeof(int);
@@ -63,20 +63,28 @@ extern "C" spd_status spd_sparse_decode_attention_static(spd_ctx *ctx, const voi
   {
     std::lock_guard<std::mutex> lock(g_setup_mu);
     if (!g_scratch_addr[dev]) {
-      // set-up, once per device, with that device current
+      // set-up, once per device, with that device current; the caller's
+      // current device is restored afterwards, on success and on failure
       int cur = -1;
-      if (cudaGetDevice(&cur) != cudaSuccess || cur != dev) {
+      const bool had = cudaGetDevice(&cur) == cudaSuccess;
+      if (!had || cur != dev) {
         if (cudaSetDevice(dev) != cudaSuccess)
           return spd::fail_message(ctx, SPD_ERR_CUDA, "cudaSetDevice failed");
       }
       void *p = nullptr;
       const cudaError_t e = cudaGetSymbolAddress(&p, g_decode_scratch);
+      const bool restored = !(had && cur != dev) || cudaSetDevice(cur) == cudaSuccess;
       if (e != cudaSuccess || !p)
         return spd::fail_message(ctx, SPD_ERR_CUDA, "cudaGetSymbolAddress(static scratch) failed");
+      if (!restored)
+        return spd::fail_message(ctx, SPD_ERR_CUDA, "cudaSetDevice(restore) failed");
       g_scratch_addr[dev] = p;
     }
     base = g_scratch_addr[dev];
   }
+  // every launch of the call is planned against the array's capacity before
+  // anything (the ticket clear included) is enqueued
+  if ((r = spd::check_attention_capacity(ctx, seq_ids, n_seqs, kStaticItems)) != SPD_OK) return r;
   // the per-unit tickets must start at zero
   cudaError_t e = cudaMemsetAsync(base, 0, kTicketBytes, st);
   if (e != cudaSuccess) return spd::fail_message(ctx, SPD_ERR_CUDA, "cudaMemsetAsync(tickets) failed");
