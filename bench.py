@@ -45,14 +45,25 @@ import workloads as W  # noqa: E402
 METRIC = "sparse decode attn us/step and KV GB/s (frac of ~8 TB/s HBM) at 128K context"
 
 
+def metric_of(workload):
+    """The headline metric on its workload; the same quantity on the others."""
+    if workload == "llama3_8b_b1_128k":
+        return METRIC
+    return "sparse decode attn us/step and KV GB/s (frac of ~8 TB/s HBM) on " + workload
+
+
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=64)
     ap.add_argument("--warmup", type=int, default=8)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="llama3_8b_b1_128k")
-    ap.add_argument("--layers", type=int, default=32)
+    ap.add_argument("--workload", default="llama3_8b_b1_128k", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--layers", type=int, default=0,
+                    help="layer instances (default: the workload's, at least 4x L2 touched "
+                         "per step)")
+    ap.add_argument("--replays", type=int, default=10,
+                    help="timed replays of the K-step window (median, p10, p90 reported)")
     ap.add_argument("--streaming-layers", default="",
                     help="comma-separated layer indices whose kv heads are all streaming "
                          "(the other layers keep the workload's head split)")
@@ -64,10 +75,28 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-roofline", action="store_true")
+    ap.add_argument("--no-dyn-only", action="store_true")
     ap.add_argument("--no-eager", action="store_true")
     ap.add_argument("--roofline-iters", type=int, default=40)
-    ap.add_argument("--cpu-sample-steps", type=int, default=16)
+    ap.add_argument("--cpu-sample-steps", type=int, default=0,
+                    help="oracle steps per CPU-baseline sample (default: the workload's)")
     return ap.parse_args()
+
+
+# Layer instances per workload: enough that one step touches at least 4x the
+# 129 MB L2 (KV bytes per layer-step x layers), so every step streams from HBM.
+LAYERS = {"llama3_8b_b1_128k": 32, "llama3_8b_b4_32k": 16, "llama2_7b_mha_256k": 16,
+          "cont_batch_16": 8, "tiny": 4}
+# Oracle decode steps per CPU-baseline sample (about 10-30 s of host work at
+# one thread on the slowest of them).
+CPU_STEPS = {"llama3_8b_b1_128k": 8, "llama3_8b_b4_32k": 4, "llama2_7b_mha_256k": 2,
+             "cont_batch_16": 2, "tiny": 8}
+L2_BYTES = 129e6
+
+
+def model_name(wl):
+    return {(32, 8): "Llama-3-8B attention", (32, 32): "Llama-2-7B attention (MHA)"}.get(
+        (wl.Hq, wl.Hkv), "synthetic attention")
 
 
 # ---- multi-rank aggregation (replicas: no data-path collective) -------------
@@ -121,6 +150,12 @@ def measured_peaks():
             j = json.load(f)
         return float(j["hbm_gbs"]), "measured"
     return 6800.0, "fallback"
+
+
+def pct(xs):
+    """(median, p10, p90) of a list."""
+    a = np.asarray(xs, dtype=np.float64)
+    return float(np.median(a)), float(np.percentile(a, 10)), float(np.percentile(a, 90))
 
 
 # ---- clocks ------------------------------------------------------------------
@@ -186,7 +221,8 @@ class ClockSampler:
 # ---- the CUDA arm ----------------------------------------------------------------
 
 class Layers:
-    """n_layers independent caches of the workload, one sequence each."""
+    """n_layers independent caches of the workload, each holding the
+    workload's batch of sequences at their context lengths."""
 
     FP8_SCALE = 1.0 / 32
 
@@ -194,7 +230,8 @@ class Layers:
         import torch
         import sparse_paged_decode_logical_gb300 as spd
         self.torch, self.wl, self.device = torch, wl, device
-        L0 = wl.context
+        lens = wl.seq_lens()
+        self.lens = lens
         # per layer: the workload's head split, or every kv head streaming
         self.wls = [dataclasses.replace(wl, streaming=[True] * wl.Hkv)
                     if layer in streaming_layers else wl for layer in range(n_layers)]
@@ -202,9 +239,8 @@ class Layers:
         self.caches, self.seqs = [], []
         for layer in range(n_layers):
             cfg = self.wls[layer].lib_config()
-            cfg["max_context"] = L0 + extra_tokens
-            cfg["max_seqs"] = 1
-            cfg["num_physical_pages"] = -(-cfg["max_context"] // wl.P)
+            cfg["max_context"] = max(lens) + extra_tokens
+            cfg["num_physical_pages"] = sum(-(-(L + extra_tokens) // wl.P) for L in lens)
             if kv_fp8:
                 cfg.update(kv_fp8=True, k_scale=[self.FP8_SCALE] * wl.Hkv,
                            v_scale=[self.FP8_SCALE] * wl.Hkv)
@@ -213,16 +249,17 @@ class Layers:
             # cache is written only through its own context: the next layer
             # may stage its K/V tiles while the previous layer finishes
             c.set_early_kv_staging(True)
-            s = c.seq_create()
-            K, V = W.device_context(wl, 0, L0, layer, device)
-            c.kv_append([s], K[None], V[None])
-            del K, V
+            ids = [c.seq_create() for _ in range(wl.batch)]
+            for b, L in enumerate(lens):
+                K, V = W.device_context(wl, b, L, layer, device)
+                c.kv_append([ids[b]], K[None], V[None])
+                del K, V
             self.caches.append(c)
-            self.seqs.append(s)
+            self.seqs.append(ids)
         torch.cuda.synchronize()
         tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float16
         self.tdt = tdt
-        self.out = [torch.empty((1, wl.Hq, wl.d), dtype=torch.float32, device=device)
+        self.out = [torch.empty((wl.batch, wl.Hq, wl.d), dtype=torch.float32, device=device)
                     for _ in range(n_layers)]
         self.u = [torch.from_numpy(W.query_base(wl, layer)).to(device) for layer in range(n_layers)]
         self.gen = torch.Generator(device=device)
@@ -237,23 +274,30 @@ class Layers:
             for layer in range(len(self.caches)):
                 q = (self.u[layer] + 0.25 * torch.randn(self.u[layer].shape, generator=self.gen,
                                                         device=self.device)).to(self.tdt)
-                k = torch.randn((1, wl.Hkv, wl.d), generator=self.gen, device=self.device).to(self.tdt)
-                v = torch.randn((1, wl.Hkv, wl.d), generator=self.gen, device=self.device).to(self.tdt)
+                k = torch.randn((wl.batch, wl.Hkv, wl.d), generator=self.gen,
+                                device=self.device).to(self.tdt)
+                v = torch.randn((wl.batch, wl.Hkv, wl.d), generator=self.gen,
+                                device=self.device).to(self.tdt)
                 row.append((q.contiguous(), k, v))
             res.append(row)
         return res
 
     def info(self):
-        return self.caches[0].seq_info(self.seqs[0])
+        return self.caches[0].seq_info(self.seqs[0][0])
 
     def launches(self):
         return sum(c.launch_count() for c in self.caches)
 
     def layer_bytes(self, layer, selected):
-        """(dyn, str, meta) bytes of the layer's current step (see step_bytes)."""
-        inf = self.caches[layer].seq_info(self.seqs[layer])
-        n_att = inf["pages_kept"] + (-(-inf["length"] // self.wl.ell)) - inf["pages_at_selection"]
-        return step_bytes(self.wls[layer], inf["length"], n_att, selected, self.elem)
+        """(dyn, str, meta) bytes of the layer's current step, summed over its
+        sequences (see step_bytes)."""
+        tot = np.zeros(3)
+        for sid in self.seqs[layer]:
+            inf = self.caches[layer].seq_info(sid)
+            n_att = (inf["pages_kept"] + (-(-inf["length"] // self.wl.ell))
+                     - inf["pages_at_selection"])
+            tot += step_bytes(self.wls[layer], inf["length"], n_att, selected, self.elem)
+        return tot
 
     def step(self, row, outs=None):
         """Enqueue one decode step on every layer; returns its algorithmic bytes."""
@@ -261,19 +305,24 @@ class Layers:
         due = self.info()["step_counter"] % self.wl.C == 0
         for layer, c in enumerate(self.caches):
             q, k, v = row[layer]
-            c.decode_step(q, k, v, [self.seqs[layer]], out=outs[layer])
+            c.decode_step(q, k, v, self.seqs[layer], out=outs[layer])
         tot = np.zeros(3)
         for layer in range(len(self.caches)):
             tot += self.layer_bytes(layer, due)
         return tot[0], tot[1], tot[2], due
 
 
+def n_layers_of(args):
+    return args.layers if args.layers > 0 else LAYERS.get(args.workload, 32)
+
+
 def run_ours(args, rank, world, device):
     import torch
     torch.cuda.set_device(device)
     wl = W.workload(args.workload)
-    n_l = args.layers
-    extra = args.warmup + args.steps + (0 if args.no_e2e else args.steps) + 64
+    n_l = n_layers_of(args)
+    host_steps = 0 if args.no_eager else 4
+    extra = args.warmup + args.steps + (0 if args.no_e2e else args.steps) + host_steps + 64
     layers = Layers(wl, n_l, device, extra, streaming_layers(args), args.kv_fp8)
     stream = torch.cuda.Stream(device=device)
     dist = None
@@ -296,7 +345,11 @@ def run_ours(args, rank, world, device):
     for c in layers.caches:
         c.check_status(stream)
 
-    # timed window: K steps captured into one graph, then run once
+    # timed window: K steps captured into one graph.  The first replay runs
+    # the K new steps; the window is then replayed again (each replay repeats
+    # the same steps on the same inputs: appends rewrite the same slots, the
+    # same pages are selected and attended, the same bytes are read) for the
+    # spread over replays.
     rows = layers.inputs(args.steps)
     torch.cuda.synchronize()
     l0 = layers.launches()
@@ -311,27 +364,34 @@ def run_ours(args, rank, world, device):
     launches = layers.launches() - l0
     clocks = ClockSampler(device.index if device.index is not None else 0)
     clocks.start()
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
+    reps = max(1, args.replays)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
     barrier()
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
-        t_start.record(stream)
-        g.replay()
-        t_end.record(stream)
+        evs[0].record(stream)
+        for r in range(reps):
+            g.replay()
+            evs[r + 1].record(stream)
     torch.cuda.synchronize()
     barrier()
-    ms = max_over_ranks(t_start.elapsed_time(t_end))
+    rep_ms = [max_over_ranks(evs[r].elapsed_time(evs[r + 1])) for r in range(reps)]
+    ms, ms_p10, ms_p90 = pct(rep_ms)
     for c in layers.caches:
         c.check_status(stream)
     total_bytes = float(tot.sum())
     gbs = whole_job_gbs(total_bytes, ms, world)
 
     # roofline: the decode kernel alone (read-only, replayable), events around
-    # every launch inside one graph
+    # every launch inside one graph; then the same for a context of the
+    # workload's dynamic heads only (the selected-page bytes)
     rl = None if args.no_roofline else roofline(layers, stream, args.roofline_iters)
     if rl is not None:
         rl["exports"] = variant_timings(layers, stream)
+        if not args.no_dyn_only and any(not s for s in wl.streaming) and \
+                any(wl.streaming) and not streaming_layers(args):
+            rl["dyn_only"] = dyn_only_roofline(wl, device, stream, args.roofline_iters,
+                                               args.kv_fp8)
     clk = clocks.stop()
 
     # end to end: pinned host inputs -> device -> step -> pinned host outputs
@@ -339,21 +399,15 @@ def run_ours(args, rank, world, device):
     if not args.no_e2e:
         e2e = run_e2e(layers, stream, args.steps, barrier, max_over_ranks, world)
 
-    # eager launches (no graph), for context
-    eager_us = float("nan")
+    # eager launches (no graph): the host cost of the C-ABI decode step, and
+    # the eager step time, for context
+    host = None
     if not args.no_eager:
-        eager_rows = layers.inputs(4)
-        torch.cuda.synchronize()
-        te0 = time.perf_counter()
-        with torch.cuda.stream(stream):
-            for row in eager_rows:
-                layers.step(row)
-        stream.synchronize()
-        eager_us = (time.perf_counter() - te0) / len(eager_rows) * 1e6
+        host = host_cost(layers, stream, host_steps)
 
     peak, peak_kind = measured_peaks()
     res = {
-        "metric": METRIC,
+        "metric": metric_of(args.workload),
         "value": round(gbs, 2),
         "unit": "GB/s",
         "n_gpus": world,
@@ -362,6 +416,11 @@ def run_ours(args, rank, world, device):
         "ms_per_step": ms / args.steps,
         "us_per_step": ms / args.steps * 1e3,
         "us_per_layer_step": ms / args.steps / n_l * 1e3,
+        "replays": {"n": reps, "ms_per_window_median": round(ms, 4),
+                    "p10": round(ms_p10, 4), "p90": round(ms_p90, 4),
+                    "first": round(rep_ms[0], 4),
+                    "us_per_layer_step_p10_p90": [round(ms_p10 / args.steps / n_l * 1e3, 3),
+                                                  round(ms_p90 / args.steps / n_l * 1e3, 3)]},
         "frac_of_hbm": round(gbs / world / peak, 4),
         "hbm_peak_gbs": peak,
         "hbm_peak_kind": peak_kind,
@@ -369,7 +428,7 @@ def run_ours(args, rank, world, device):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": wl.dtype,
-        "data": "synthetic (seeded N(0,1) K/V in bf16, needle pages at 10/50/90% depth)",
+        "data": data_desc(wl),
         "config": arm_config(wl, n_l, n_sel, total_bytes / args.steps, world,
                              streaming_layers(args), args.kv_fp8),
         "bytes_per_step": {"dyn": tot[0] / args.steps, "stream": tot[1] / args.steps,
@@ -377,11 +436,30 @@ def run_ours(args, rank, world, device):
         "gpu_launches": launches,
         "roofline": rl,
         "clocks": clk,
-        "eager_us_per_step": round(eager_us, 1),
     }
+    if host:
+        res["host_us_per_layer_step"] = host["c_abi_us"]
+        res["host"] = host
     if e2e:
         res["e2e"] = e2e
     return res, layers
+
+
+def data_desc(wl):
+    parts = ["seeded N(0,1) K/V in %s" % wl.dtype]
+    if wl.outliers:
+        parts.append("2 outlier key channels x50")
+    if wl.needle == "pages":
+        parts.append("needle pages at %s depth" % "/".join("%d%%" % (100 * f)
+                                                           for f in wl.needle_depths))
+    elif wl.needle == "tokens":
+        parts.append("%.1f%% planted needle tokens" % (100 * wl.needle_frac))
+    if wl.log_uniform_lens:
+        parts.append("lengths log-uniform in [%dK, %dK]" % (wl.log_uniform_lens[0] // 1024,
+                                                            wl.log_uniform_lens[1] // 1024))
+    if wl.permute_pages:
+        parts.append("physical pages in random order")
+    return "synthetic (" + ", ".join(parts) + ")"
 
 
 def streaming_layers(args):
@@ -390,16 +468,23 @@ def streaming_layers(args):
 
 def arm_config(wl, n_layers, n_sel=None, bytes_per_step=None, world=1, all_streaming=(),
                kv_fp8=False):
+    lens = wl.seq_lens()
     c = {
         "workload": wl.name,
-        "shape": "Llama-3-8B attention: 32 q / 8 kv heads, d 128, bf16",
-        "context": wl.context, "batch": wl.batch, "layers": n_layers,
+        "shape": "%s: %d q / %d kv heads, d %d, %s" % (model_name(wl), wl.Hq, wl.Hkv, wl.d,
+                                                      wl.dtype),
+        "context": wl.context if not wl.log_uniform_lens else
+        "%d sequences, %d..%d tokens (sum %d)" % (len(lens), min(lens), max(lens), sum(lens)),
+        "batch": wl.batch, "layers": n_layers,
         "logical_page": wl.ell, "physical_page": wl.P,
         "streaming_kv_heads": sum(wl.streaming), "sink": wl.sink, "window": wl.window,
-        "token_budget": "min(4096, L/32)", "reuse_interval": wl.C,
-        "l2": "inputs larger than L2: %d layers x ~19 MB touched per step" % n_layers,
-        "timing": "timed window captured once into a CUDA graph and run once; "
-                  "CUDA events on the launching stream; early KV staging on",
+        "token_budget": wl.token_budget if wl.token_budget > 0 else "min(4096, L/32)",
+        "reuse_interval": wl.C,
+        "l2": "inputs larger than L2: %d layers x %.0f MB touched per step" % (
+            n_layers, (bytes_per_step or 0) / max(1, n_layers) / 1e6) if bytes_per_step else
+        "inputs larger than L2",
+        "timing": "timed window captured once into a CUDA graph and replayed (median over "
+                  "replays); CUDA events on the launching stream; early KV staging on",
         "parallelism": "replicas" if world > 1 else "single GPU",
     }
     if all_streaming:
@@ -421,12 +506,12 @@ def variant_timings(layers, stream, iters=10):
     row = layers.inputs(1)[0]
     q = [row[layer][0] for layer in range(n)]
     calls = {
-        "plain": lambda c, l: c.sparse_decode_attention(q[l], [layers.seqs[l]],
+        "plain": lambda c, l: c.sparse_decode_attention(q[l], layers.seqs[l],
                                                         out=layers.out[l], stream=stream),
-        "stats": lambda c, l: c.sparse_decode_attention_stats(q[l], [layers.seqs[l]],
+        "stats": lambda c, l: c.sparse_decode_attention_stats(q[l], layers.seqs[l],
                                                               stream=stream),
         "page_mass": lambda c, l: c.sparse_decode_attention_page_mass(
-            q[l], [layers.seqs[l]], stream=stream),
+            q[l], layers.seqs[l], stream=stream),
     }
     res = {}
     for name, call in calls.items():
@@ -453,13 +538,15 @@ def variant_timings(layers, stream, iters=10):
     return res
 
 
-def roofline(layers, stream, iters):
-    """Average duration of the decode kernel: a graph of `iters` x n_layers
-    back-to-back spd_sparse_decode_attention launches (one kernel each, the
-    split combine is fused), replayed on the launching stream between CUDA
-    events.  Read-only on the KV cache, so replays repeat identical work."""
+def time_attention_graph(layers, stream, iters):
+    """Median per-launch time (ms) of a graph of iters x n_layers back-to-back
+    spd_sparse_decode_attention calls (one kernel each, the split combine is
+    fused), replayed between CUDA events on the launching stream (read-only
+    on the KV cache, so replays repeat identical work); at least 5 timed
+    replays and about a second of them, so that the clock sampler sees the
+    kernel under load.  Returns (ms per launch, launches per replay, replays,
+    p10, p90)."""
     import torch
-    wl = layers.wl
     n = len(layers.caches)
     row = layers.inputs(1)[0]
     q = [row[layer][0] for layer in range(n)]
@@ -469,19 +556,11 @@ def roofline(layers, stream, iters):
     with torch.cuda.graph(g, stream=stream):
         for _ in range(iters):
             for layer, c in enumerate(layers.caches):
-                c.sparse_decode_attention(q[layer], [layers.seqs[layer]], out=layers.out[layer],
+                c.sparse_decode_attention(q[layer], layers.seqs[layer], out=layers.out[layer],
                                           stream=stream)
     per_replay = layers.launches() - l0
-    # bytes per launch, averaged over the layers (they differ when some layers
-    # are all streaming)
-    dyn = strm = 0.0
-    for layer in range(n):
-        d_, s_, _ = layers.layer_bytes(layer, False)
-        dyn, strm = dyn + d_ / n, strm + s_ / n
     times = []
     with torch.cuda.stream(stream):
-        # at least 5 timed replays, and about a second of them so that the
-        # clock sampler sees the kernel under load
         for rep in range(2000):
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
@@ -493,20 +572,36 @@ def roofline(layers, stream, iters):
                 times.append(a.elapsed_time(b))
             if len(times) >= 5 and sum(times) > 1000.0:
                 break
-    avg_ms = float(np.median(times)) / per_replay
+    med, p10, p90 = pct(times)
+    return med / per_replay, per_replay, len(times), p10 / per_replay, p90 / per_replay
+
+
+def roofline(layers, stream, iters):
+    """Average duration of the decode kernel (time_attention_graph) against
+    the algorithmic bytes of one launch: the dynamic and streaming KV of one
+    layer-step, averaged over the layers (they differ when some layers are
+    all streaming)."""
+    n = len(layers.caches)
+    dyn = strm = 0.0
+    for layer in range(n):
+        d_, s_, _ = layers.layer_bytes(layer, False)
+        dyn, strm = dyn + d_ / n, strm + s_ / n
+    avg_ms, per_replay, n_rep, p10, p90 = time_attention_graph(layers, stream, iters)
     achieved = (dyn + strm) / (avg_ms * 1e-3) / 1e9
     peak, kind = measured_peaks()
     traffic = None
     tp = os.path.join(ROOT, "profiles", "decode_traffic.txt")
     if os.path.exists(tp):
         # "key: value" lines written from an ncu capture of this kernel; the
-        # figure is used only while the kernel sources are unchanged
+        # figure is used only while the kernel sources are unchanged and the
+        # workload is the one it was captured on
         kv = {}
         for ln in open(tp):
             if ":" in ln and not ln.startswith("#"):
                 k, v = ln.split(":", 1)
                 kv[k.strip()] = v.strip()
-        if kv.get("kernel_source_hash") == kernel_hash():
+        if kv.get("kernel_source_hash") == kernel_hash() and \
+                kv.get("workload", "llama3_8b_b1_128k") == layers.wl.name:
             try:
                 traffic = float(kv["traffic_bytes_per_launch"])
             except (KeyError, ValueError):
@@ -516,10 +611,100 @@ def roofline(layers, stream, iters):
             "peak_kind": kind + " (MEASURED_PEAKS.json hbm_gbs, burst copy)" if kind == "measured" else kind,
             "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
             "algorithmic_bytes_per_launch": int(round(dyn + strm)),
-            "avg_launch_us": round(avg_ms * 1e3, 3), "launches_per_replay": per_replay,
+            "avg_launch_us": round(avg_ms * 1e3, 3),
+            "launch_us_p10_p90": [round(p10 * 1e3, 3), round(p90 * 1e3, 3)],
+            "launches_per_replay": per_replay,
             "how": "graph of %d back-to-back decode launches (%d layers x %d), median over %d "
-                   "replays / launches; includes inter-launch gaps" % (per_replay, n, iters,
-                                                                        len(times))}
+                   "replays / launches; includes inter-launch gaps" % (per_replay, n, iters, n_rep)}
+
+
+def dyn_only_roofline(wl, device, stream, iters, kv_fp8=False, n_layers=48):
+    """The decode kernel on the selected pages alone: contexts holding only
+    the workload's dynamic kv heads (same shapes, budget and data
+    distribution), n_layers of them (a round of launches reads more than 3x
+    L2), timed like `roofline`; bytes per launch = the dynamic heads' |T| x d
+    x 2 x element bytes."""
+    import torch
+    Hd = sum(1 for s in wl.streaming if not s)
+    wd = dataclasses.replace(wl, Hkv=Hd, Hq=Hd * wl.G, streaming=[False] * Hd)
+    lay = Layers(wd, n_layers, device, 64, kv_fp8=kv_fp8)
+    with torch.cuda.stream(stream):
+        for row in lay.inputs(2):
+            lay.step(row)
+    stream.synchronize()
+    dyn = 0.0
+    for layer in range(n_layers):
+        dyn += lay.layer_bytes(layer, False)[0] / n_layers
+    avg_ms, per_replay, n_rep, p10, p90 = time_attention_graph(lay, stream, iters)
+    for c in lay.caches:
+        c.check_status(stream)
+    achieved = dyn / (avg_ms * 1e-3) / 1e9
+    peak, kind = measured_peaks()
+    del lay
+    torch.cuda.empty_cache()
+    return {"kernel": "decode_tiles_kernel on the dynamic heads only (selected pages)",
+            "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "algorithmic_bytes_per_launch": int(round(dyn)),
+            "avg_launch_us": round(avg_ms * 1e3, 3),
+            "launch_us_p10_p90": [round(p10 * 1e3, 3), round(p90 * 1e3, 3)],
+            "how": "%d contexts of %d dynamic kv heads (%d q heads), graph of %d back-to-back "
+                   "launches, median over %d replays" % (n_layers, Hd, Hd * wl.G, per_replay,
+                                                         n_rep)}
+
+
+def host_cost(layers, stream, n_steps):
+    """Host time of the decode step's C-ABI call, eager (no graph): every
+    layer's spd_decode_step called through ctypes with pre-marshalled
+    arguments for n_steps steps, timed on the host around the calls (the
+    GPU keeps up: the device time per layer-step is shorter), then the
+    same through the Python binding, and the eager step time with the GPU
+    work included."""
+    import ctypes
+    import torch
+    import sparse_paged_decode_logical_gb300 as spd
+    L = spd.lib()
+    n = len(layers.caches)
+    rows = layers.inputs(2 * n_steps)
+    st = ctypes.c_void_p(stream.cuda_stream)
+    args = []
+    for s_ in range(n_steps):
+        row = []
+        for layer, c in enumerate(layers.caches):
+            q, k, v = rows[s_][layer]
+            ids = (ctypes.c_int * len(layers.seqs[layer]))(*layers.seqs[layer])
+            row.append((c.ctx, ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()),
+                        ctypes.c_void_p(v.data_ptr()), ids, len(layers.seqs[layer]),
+                        ctypes.c_void_p(layers.out[layer].data_ptr())))
+        args.append(row)
+    torch.cuda.synchronize()
+    t_call = 0.0
+    for row in args:
+        for a in row:
+            t0 = time.perf_counter()
+            r = L.spd_decode_step(a[0], a[1], a[2], a[3], a[4], a[5], a[6], st)
+            t_call += time.perf_counter() - t0
+            assert r == 0
+    stream.synchronize()
+    # the Python binding (argument checks and marshalling included), and the
+    # eager step time (host and GPU)
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for s_ in range(n_steps, 2 * n_steps):
+            for layer, c in enumerate(layers.caches):
+                q, k, v = rows[s_][layer]
+                c.decode_step(q, k, v, layers.seqs[layer], out=layers.out[layer])
+    t_bind = time.perf_counter() - t0
+    stream.synchronize()
+    t_eager = time.perf_counter() - t0
+    for c in layers.caches:
+        c.check_status(stream)
+    k = n_steps * n
+    return {"c_abi_us": round(t_call / k * 1e6, 2),
+            "binding_us": round(t_bind / k * 1e6, 2),
+            "eager_us_per_layer_step": round(t_eager / k * 1e6, 2),
+            "how": "host time of %d eager spd_decode_step calls (%d layers x %d steps) through "
+                   "ctypes, then the same through the Python binding; eager = host enqueue "
+                   "plus GPU, synchronized at the end" % (k, n, n_steps)}
 
 
 # the sources the decode kernel is compiled from (its traffic figure is valid
@@ -543,8 +728,9 @@ def run_e2e(layers, stream, n_steps, barrier, max_over_ranks, world):
     import torch
     wl = layers.wl
     n = len(layers.caches)
+    B = wl.batch
     rows = layers.inputs(n_steps)
-    qn, kn = wl.Hq * wl.d, wl.Hkv * wl.d
+    qn, kn = B * wl.Hq * wl.d, B * wl.Hkv * wl.d
     per_layer = qn + 2 * kn
     host_in = torch.empty((n_steps, n, per_layer), dtype=layers.tdt).pin_memory()
     for s_, row in enumerate(rows):
@@ -552,11 +738,12 @@ def run_e2e(layers, stream, n_steps, barrier, max_over_ranks, world):
             q, k, v = row[layer]
             host_in[s_, layer] = torch.cat([q.reshape(-1), k.reshape(-1), v.reshape(-1)]).cpu()
     dev_in = torch.empty((n, per_layer), dtype=layers.tdt, device=layers.device)
-    views = [(dev_in[layer, :qn].view(1, wl.Hq, wl.d), dev_in[layer, qn:qn + kn].view(1, wl.Hkv, wl.d),
-              dev_in[layer, qn + kn:].view(1, wl.Hkv, wl.d)) for layer in range(n)]
-    dev_out = torch.empty((n, 1, wl.Hq, wl.d), dtype=torch.float32, device=layers.device)
+    views = [(dev_in[layer, :qn].view(B, wl.Hq, wl.d),
+              dev_in[layer, qn:qn + kn].view(B, wl.Hkv, wl.d),
+              dev_in[layer, qn + kn:].view(B, wl.Hkv, wl.d)) for layer in range(n)]
+    dev_out = torch.empty((n, B, wl.Hq, wl.d), dtype=torch.float32, device=layers.device)
     outs = [dev_out[layer] for layer in range(n)]
-    host_out = torch.empty((n_steps, n, 1, wl.Hq, wl.d), dtype=torch.float32).pin_memory()
+    host_out = torch.empty((n_steps, n, B, wl.Hq, wl.d), dtype=torch.float32).pin_memory()
     h2d = host_in[0].numel() * host_in.element_size()
     d2h = host_out[0].numel() * 4
     torch.cuda.synchronize()
@@ -590,53 +777,89 @@ def run_e2e(layers, stream, n_steps, barrier, max_over_ranks, world):
 
 # ---- the CPU oracle arm ------------------------------------------------------------
 
-def oracle_sample(wl, n_steps, warmup=0):
-    """Time the oracle's decode steps (one layer, one sequence) on host cores.
-    Returns (GB/s, seconds per step, threads, description)."""
+def core_counts():
+    """(threads available to this process (what nproc prints), online CPUs
+    (the count std::thread::hardware_concurrency reports))."""
+    avail = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    try:
+        nproc = int(subprocess.run(["nproc"], capture_output=True, text=True).stdout.strip())
+    except Exception:
+        nproc = avail
+    return nproc, os.cpu_count()
+
+
+def oracle_sample(wl, n_steps, threads, warmup=0):
+    """Time the oracle's decode steps (one layer, the workload's batch) on
+    host cores, threads over kv heads.  Returns (GB/s, seconds per step,
+    description)."""
     import oracle
-    threads = oracle.cpu_threads()
-    cfg = wl.lib_config()
+    lens = wl.seq_lens()
     lay = oracle.OracleLayer(dict(
         num_q_heads=wl.Hq, num_kv_heads=wl.Hkv, head_dim=wl.d, dtype=wl.dtype,
         logical_page=wl.ell, streaming=wl.streaming, sink=wl.sink, window=wl.window,
         token_budget=wl.token_budget, reuse_interval=wl.C,
-        max_context=wl.context + warmup + n_steps + 8))
-    sid = lay.new_seq()
-    K, V = W.context(wl, 0, wl.context)
-    lay.append(sid, K, V)
-    del K, V
+        max_context=max(lens) + warmup + n_steps + 8))
+    sids = []
+    for b, L in enumerate(lens):
+        sid = lay.new_seq()
+        K, V = W.context(wl, b, L)
+        lay.append(sid, K, V)
+        del K, V
+        sids.append(sid)
     for s in range(warmup):
         q, k, v = W.step_tokens(wl, s)
-        lay.step(sid, q[0], k[0], v[0], threads=threads)
+        for b, sid in enumerate(sids):
+            lay.step(sid, q[b], k[b], v[b], threads=threads)
     tot, t = 0.0, 0.0
+    dh = [h for h in range(wl.Hkv) if not wl.streaming[h]]
     for s in range(warmup, warmup + n_steps):
         q, k, v = W.step_tokens(wl, s)
-        due = lay.selection_due(sid)
+        dues = [lay.selection_due(sid) for sid in sids]
         t0 = time.perf_counter()
-        lay.step(sid, q[0], k[0], v[0], threads=threads)
+        for b, sid in enumerate(sids):
+            lay.step(sid, q[b], k[b], v[b], threads=threads)
         t += time.perf_counter() - t0
-        st = lay.seqs[sid]
-        dh = [h for h in range(wl.Hkv) if not wl.streaming[h]]
-        nL = -(-st.L // wl.ell)
-        n_att = len(st.sel[dh[0]]) + nL - st.nL0[dh[0]] if dh else 0
-        tot += sum(step_bytes(wl, st.L, n_att, due))
-    desc = ("oracle decode steps (append + select when due + fp64 attention) of one "
-            "layer of %s at %d tokens, %d steps, threads over kv heads"
-            % (wl.name, wl.context, n_steps))
-    return tot / t / 1e9, t / n_steps, threads, desc
+        for b, sid in enumerate(sids):
+            st = lay.seqs[sid]
+            nL = -(-st.L // wl.ell)
+            n_att = len(st.sel[dh[0]]) + nL - st.nL0[dh[0]] if dh else 0
+            tot += sum(step_bytes(wl, st.L, n_att, dues[b]))
+    desc = ("oracle decode steps (append + select when due + fp64 attention) of one layer "
+            "of %s (%d sequence%s), %d steps, %d thread%s over kv heads"
+            % (wl.name, len(lens), "s" if len(lens) > 1 else "", n_steps, threads,
+               "s" if threads > 1 else ""))
+    return tot / t / 1e9, t / n_steps, desc
+
+
+def cpu_baseline(wl, n_steps):
+    """The oracle at every available core and at one thread, same sample."""
+    import oracle
+    nproc, online = core_counts()
+    threads = oracle.cpu_threads()
+    gbs, sec, desc = oracle_sample(wl, n_steps, threads)
+    gbs1, sec1, _ = oracle_sample(wl, n_steps, 1)
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": desc, "ms_per_layer_step": round(sec * 1e3, 2),
+            "value_1_thread": round(gbs1, 4), "ms_per_layer_step_1_thread": round(sec1 * 1e3, 2),
+            "nproc": nproc, "hardware_concurrency": online}
 
 
 def run_reference(args):
+    import oracle
     wl = W.workload(args.workload)
-    gbs, sec, threads, desc = oracle_sample(wl, args.steps, args.warmup)
+    threads = oracle.cpu_threads()
+    nproc, online = core_counts()
+    gbs, sec, desc = oracle_sample(wl, args.steps, threads, args.warmup)
     return {
-        "metric": METRIC, "impl": "reference", "value": round(gbs, 4), "unit": "GB/s",
+        "metric": metric_of(args.workload), "impl": "reference", "value": round(gbs, 4),
+        "unit": "GB/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
-        "config": arm_config(wl, args.layers, all_streaming=streaming_layers(args)),
+        "config": arm_config(wl, n_layers_of(args), all_streaming=streaming_layers(args)),
         "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": threads,
-                         "kind": "oracle", "sample": desc},
+                         "kind": "oracle", "sample": desc, "nproc": nproc,
+                         "hardware_concurrency": online},
         "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -661,14 +884,19 @@ def run_prefill(L, steps, warmup, device):
     for _ in range(warmup):
         spd.prefill_block_sparse_attention(q, k, v, wq, wk, blk, budget, dense_below, check=False)
     torch.cuda.synchronize()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record()
+    clocks = ClockSampler(device.index if device.index is not None else 0)
+    clocks.start()
+    times = []
     for _ in range(steps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
         out, blocks = spd.prefill_block_sparse_attention(q, k, v, wq, wk, blk, budget,
                                                          dense_below, check=False)
-    b.record()
-    torch.cuda.synchronize()
-    ms = a.elapsed_time(b) / steps
+        b.record()
+        b.synchronize()
+        times.append(a.elapsed_time(b))
+    clk = clocks.stop()
+    ms, ms_p10, ms_p90 = pct(times)
     nb = -(-L // blk)
     keys = 0
     for bq in range(nb):
@@ -688,6 +916,7 @@ def run_prefill(L, steps, warmup, device):
                                    "shapes, blocks of 64, budget 4096, rank 16" % L,
                        "dense": L < dense_below},
             "attention_tflops": round(tf, 2),
+            "ms_p10_p90": [round(ms_p10, 3), round(ms_p90, 3)], "clocks": clk,
             "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": peak,
                          "unit": "TFLOP/s", "frac": round(tf / peak, 4) if peak else None,
                          "traffic": None,
@@ -698,7 +927,7 @@ def main():
     args = parse()
     if args.prefill:
         import torch
-        res = run_prefill(args.prefill, max(1, min(args.steps, 5)), max(1, min(args.warmup, 2)),
+        res = run_prefill(args.prefill, max(3, min(args.steps, 10)), max(1, min(args.warmup, 2)),
                           torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0"))))
         print(json.dumps(res), flush=True)
         return
@@ -714,14 +943,14 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     device = torch.device("cuda", local)
-    res, _ = run_ours(args, rank, world, device)
+    res, layers = run_ours(args, rank, world, device)
+    del layers
+    torch.cuda.empty_cache()
     if rank == 0:
         if not args.no_cpu_baseline:
             wl = W.workload(args.workload)
-            gbs, sec, threads, desc = oracle_sample(wl, args.cpu_sample_steps)
-            res["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": threads,
-                                   "kind": "oracle", "sample": desc,
-                                   "ms_per_layer_step": round(sec * 1e3, 2)}
+            res["cpu_baseline"] = cpu_baseline(
+                wl, args.cpu_sample_steps or CPU_STEPS.get(args.workload, 8))
         print(json.dumps(res), flush=True)
     if world > 1:
         import torch.distributed as dist
