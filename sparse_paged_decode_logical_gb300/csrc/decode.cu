@@ -6,17 +6,18 @@
 namespace spd {
 namespace {
 
-int g_max_cluster[2][2][4];  // [dtype][d == 128][log2 G]: co-schedulable cluster size
+// [deep][dtype][d == 128][log2 G]: co-schedulable cluster size
+int g_max_cluster[2][2][2][4];
 
-template <typename T, int D, int G>
+template <typename T, int D, int G, bool kDeep>
 cudaError_t prep_one(int *max_cluster) {
-  cudaError_t e = set_smem_attrs<T, D, G, false>();
+  cudaError_t e = set_smem_attrs<T, D, G, false, false, kDeep>();
   if (e != cudaSuccess) return e;
   int cs = 8;  // portable cluster size
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(16);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = Smem<D, G>::kAlloc;
+  cfg.dynamicSmemBytes = Smem<D, G, false, kDeep>::kAlloc;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 16;
@@ -25,7 +26,8 @@ cudaError_t prep_one(int *max_cluster) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int q = 0;
-  if (cudaOccupancyMaxPotentialClusterSize(&q, decode_tiles_kernel<T, D, G, false>, &cfg) ==
+  if (cudaOccupancyMaxPotentialClusterSize(&q, decode_tiles_kernel<T, D, G, false, false, kDeep>,
+                                          &cfg) ==
           cudaSuccess &&
       q >= 1)
     cs = q;
@@ -34,24 +36,31 @@ cudaError_t prep_one(int *max_cluster) {
   return cudaSuccess;
 }
 
-template <typename T, int D>
+template <typename T, int D, bool kDeep>
 cudaError_t prep_g(int dt) {
   cudaError_t e;
-  const int di = D == 128;
-  if ((e = prep_one<T, D, 1>(&g_max_cluster[dt][di][0])) != cudaSuccess) return e;
-  if ((e = prep_one<T, D, 2>(&g_max_cluster[dt][di][1])) != cudaSuccess) return e;
-  if ((e = prep_one<T, D, 4>(&g_max_cluster[dt][di][2])) != cudaSuccess) return e;
-  return prep_one<T, D, 8>(&g_max_cluster[dt][di][3]);
+  int *mc = g_max_cluster[kDeep][dt][D == 128];
+  if ((e = prep_one<T, D, 1, kDeep>(&mc[0])) != cudaSuccess) return e;
+  if ((e = prep_one<T, D, 2, kDeep>(&mc[1])) != cudaSuccess) return e;
+  if ((e = prep_one<T, D, 4, kDeep>(&mc[2])) != cudaSuccess) return e;
+  return prep_one<T, D, 8, kDeep>(&mc[3]);
+}
+
+template <bool kDeep>
+cudaError_t prep_shape() {
+  cudaError_t e;
+  if ((e = prep_g<__half, 64, kDeep>(0)) != cudaSuccess) return e;
+  if ((e = prep_g<__half, 128, kDeep>(0)) != cudaSuccess) return e;
+  if ((e = prep_g<__nv_bfloat16, 64, kDeep>(1)) != cudaSuccess) return e;
+  return prep_g<__nv_bfloat16, 128, kDeep>(1);
 }
 
 }  // namespace
 
 cudaError_t prepare_decode_kernels() {
   cudaError_t e;
-  if ((e = prep_g<__half, 64>(0)) != cudaSuccess) return e;
-  if ((e = prep_g<__half, 128>(0)) != cudaSuccess) return e;
-  if ((e = prep_g<__nv_bfloat16, 64>(1)) != cudaSuccess) return e;
-  if ((e = prep_g<__nv_bfloat16, 128>(1)) != cudaSuccess) return e;
+  if ((e = prep_shape<false>()) != cudaSuccess) return e;
+  if ((e = prep_shape<true>()) != cudaSuccess) return e;
   // the mass-exporting and fp8 instances: same block; their cluster sizes are
   // taken to be the plain kernel's (the fp8 ones need no more shared memory)
   if ((e = prepare_decode_mass_kernels()) != cudaSuccess) return e;
@@ -59,9 +68,9 @@ cudaError_t prepare_decode_kernels() {
 }
 
 // Largest power-of-two cluster (<= 16) the decode kernel can be launched with.
-int decode_max_cluster(int dtype, int d, int G) {
+int decode_max_cluster(int dtype, int d, int G, bool deep) {
   const int gi = G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : 3;
-  const int cs = g_max_cluster[dtype ? 1 : 0][d == 128][gi];
+  const int cs = g_max_cluster[deep ? 1 : 0][dtype ? 1 : 0][d == 128][gi];
   int p2 = 1;
   while (p2 * 2 <= cs && p2 < 16) p2 *= 2;
   return p2;
@@ -69,12 +78,15 @@ int decode_max_cluster(int dtype, int d, int G) {
 
 int decode_max_tiles_per_cta() { return kMaxDesc; }
 
+int decode_ring_stages(bool deep) { return deep ? Ring<false, true>::n : Ring<false>::n; }
+
 cudaError_t launch_decode_tiles(const TileDecodeParams &p, int dtype, int d, int G,
                                 cudaStream_t s, long long *n) {
   if (p.n_seqs == 0 || p.total_items == 0) return cudaSuccess;
   *n += 1;
   if (p.kv_fp8) return d == 128 ? launch_decode_tiles_fp8(p, dtype, G, s) : cudaErrorInvalidValue;
   if (p.page_part != nullptr) return launch_decode_tiles_mass(p, dtype, d, G, s);
+  if (p.deep) return launch_variant<false, true>(p, dtype, d, G, s);
   return launch_variant<false>(p, dtype, d, G, s);
 }
 

@@ -76,12 +76,18 @@ namespace {
 constexpr int kRows = 16;                  // rows per tile (one mma M tile)
 constexpr int kWarps = 8;                  // 256 threads
 constexpr int kThreads = kWarps * 32;
-// shared-memory stage ring: 12 stages of 16-bit tiles keep a CTA within half
-// an SM (the next launch's CTAs stage beside it); fp8 tiles are half the
-// size, and 16 of them fit in the space the selection buffers take anyway
-template <bool F8>
+// Shared-memory stage ring.  Two launch shapes:
+//   shared  12 stages of 16-bit tiles keep a CTA within half an SM, so a CTA
+//           of the next launch stages its tiles beside it while it computes;
+//           fp8 tiles are half the size, and 16 of them fit in the space the
+//           selection buffers take anyway;
+//   deep    (Deep, for launches whose tiles far exceed what two such rings
+//           hold) 24 stages of 16-bit tiles, one CTA per SM: while the
+//           eight warps each hold the stage they compute on, the others stay
+//           in flight, and the ring keeps streaming at the HBM rate.
+template <bool F8, bool Deep = false>
 struct Ring {
-  static constexpr int n = F8 ? 16 : 12;
+  static constexpr int n = Deep ? 24 : (F8 ? 16 : 12);
 };
 constexpr int kMaxDesc = 256;              // tiles one CTA may take
 constexpr uint32_t kWaitLimit = 1u << 24;  // bounded mbarrier polls
@@ -112,9 +118,9 @@ struct TileDesc {
 // rescale buffers, per-warp and per-CTA row max / sum / output, flags), then
 // the stages at a 1024-byte aligned offset.  After the tile loop the stage
 // region holds the warp-merge buffer and later the global-merge buffers.
-template <int D, int G, bool F8 = false>
+template <int D, int G, bool F8 = false, bool Deep = false>
 struct Smem {
-  static constexpr int kStages = Ring<F8>::n;
+  static constexpr int kStages = Ring<F8, Deep>::n;
   static constexpr int kBars = 0;                                      // uint64 [kStages]
   static constexpr int kDesc = kBars + kStages * 8;                    // TileDesc [kMaxDesc]
   static constexpr int kP = kDesc + kMaxDesc * (int)sizeof(TileDesc);  // float [W][16][GP]
@@ -140,6 +146,7 @@ struct Smem {
                                  : kTopkRegion + kPtCache * 4;
   static constexpr int kRegion = kR1 > kR2 ? kR1 : kR2;
   static constexpr int kAlloc = kTiles + kRegion + 1024;  // + alignment slack
+  static_assert(kAlloc <= 232448, "more shared memory than a CTA may have");
 };
 
 template <typename T> struct IsBF16 { static constexpr bool v = false; };
@@ -222,7 +229,7 @@ __device__ void write_page_mass(const TileDecodeParams &p, int i, int sub, const
 // codes of value / scale (head_dim 128): tiles are half the bytes, widened
 // exactly on their way into the tensor-core fragments: keys to fp16 for fp16
 // q.K products (q narrowed to fp16 once), values to T for the P.V products.
-template <typename T, int D, int G, bool kMass, bool kF8 = false>
+template <typename T, int D, int G, bool kMass, bool kF8 = false, bool kDeep = false>
 __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_constant__ TileDecodeParams p) {
   static_assert(!kF8 || D == 128, "fp8 storage: one 128-byte row per token");
   // tensor-core element types.  q.K: T, or fp16 with fp8 storage (an E4M3
@@ -231,7 +238,7 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
   constexpr bool kQkBf = kF8 ? false : IsBF16<T>::v;
   constexpr bool kPvBf = IsBF16<T>::v;
   using Gm = Geo<D, kF8>;
-  using Sm = Smem<D, G, kF8>;
+  using Sm = Smem<D, G, kF8, kDeep>;
   constexpr int kStages = Sm::kStages;
   constexpr int CPL = Gm::kCPL;  // channels per lane of the fused append
   constexpr int GPAD = GP<G>::v;
@@ -1078,11 +1085,11 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
 }
 
 
-template <typename T, int D, int G, bool kMass, bool kF8 = false>
+template <typename T, int D, int G, bool kMass, bool kF8 = false, bool kDeep = false>
 cudaError_t set_smem_attrs() {
-  auto k = decode_tiles_kernel<T, D, G, kMass, kF8>;
+  auto k = decode_tiles_kernel<T, D, G, kMass, kF8, kDeep>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       Smem<D, G, kF8>::kAlloc);
+                                       Smem<D, G, kF8, kDeep>::kAlloc);
   if (e != cudaSuccess) return e;
   (void)cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   (void)cudaGetLastError();
@@ -1107,30 +1114,32 @@ cudaError_t set_smem_attrs_all() {
   return set_smem_attrs_g<__nv_bfloat16, 128, kMass>();
 }
 
-template <typename T, int D, int G, bool kMass, bool kF8 = false>
+template <typename T, int D, int G, bool kMass, bool kF8 = false, bool kDeep = false>
 cudaError_t launch_one(const TileDecodeParams &p, cudaStream_t st) {
-  cudaError_t e = launch_pdl_cluster(decode_tiles_kernel<T, D, G, kMass, kF8>, p.total_items,
-                                     kThreads, (size_t)Smem<D, G, kF8>::kAlloc, p.cluster, st, p);
+  cudaError_t e = launch_pdl_cluster(decode_tiles_kernel<T, D, G, kMass, kF8, kDeep>,
+                                     p.total_items, kThreads,
+                                     (size_t)Smem<D, G, kF8, kDeep>::kAlloc, p.cluster, st, p);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-template <typename T, int D, bool kMass>
+template <typename T, int D, bool kMass, bool kDeep = false>
 cudaError_t launch_g(const TileDecodeParams &p, int G, cudaStream_t st) {
   switch (G) {
-    case 1: return launch_one<T, D, 1, kMass>(p, st);
-    case 2: return launch_one<T, D, 2, kMass>(p, st);
-    case 4: return launch_one<T, D, 4, kMass>(p, st);
-    case 8: return launch_one<T, D, 8, kMass>(p, st);
+    case 1: return launch_one<T, D, 1, kMass, false, kDeep>(p, st);
+    case 2: return launch_one<T, D, 2, kMass, false, kDeep>(p, st);
+    case 4: return launch_one<T, D, 4, kMass, false, kDeep>(p, st);
+    case 8: return launch_one<T, D, 8, kMass, false, kDeep>(p, st);
     default: return cudaErrorInvalidValue;
   }
 }
 
-template <bool kMass>
+template <bool kMass, bool kDeep = false>
 cudaError_t launch_variant(const TileDecodeParams &p, int dtype, int d, int G, cudaStream_t s) {
   if (dtype == 0)
-    return d == 64 ? launch_g<__half, 64, kMass>(p, G, s) : launch_g<__half, 128, kMass>(p, G, s);
-  return d == 64 ? launch_g<__nv_bfloat16, 64, kMass>(p, G, s)
-                 : launch_g<__nv_bfloat16, 128, kMass>(p, G, s);
+    return d == 64 ? launch_g<__half, 64, kMass, kDeep>(p, G, s)
+                   : launch_g<__half, 128, kMass, kDeep>(p, G, s);
+  return d == 64 ? launch_g<__nv_bfloat16, 64, kMass, kDeep>(p, G, s)
+                 : launch_g<__nv_bfloat16, 128, kMass, kDeep>(p, G, s);
 }
 
 }  // namespace

@@ -145,6 +145,7 @@ struct TileDecodeParams {
   int n_seqs, Hq, Hkv, Hd, Hs, ell, P, R, max_pp, ksel_max, S, W, num_phys;
   int total_items;
   int cluster;        // CTAs per thread-block cluster; every unit's item count is a multiple
+  int deep;           // the deep-ring launch shape (one CTA per SM, 24 stages)
   int early;          // stage K/V tiles before waiting for the previous kernel:
                       // bit 0 dynamic units, bit 1 streaming units; bit 2:
                       // streaming units do not wait at all
@@ -181,8 +182,10 @@ cudaError_t launch_decode_tiles_mass(const TileDecodeParams &p, int dtype, int d
 cudaError_t prepare_decode_fp8_kernels();  // called by prepare_decode_kernels()
 cudaError_t launch_decode_tiles_fp8(const TileDecodeParams &p, int dtype, int G,
                                     cudaStream_t s);
-int decode_max_cluster(int dtype, int d, int G);  // after prepare_decode_kernels()
+// after prepare_decode_kernels(); deep: the deep-ring launch shape
+int decode_max_cluster(int dtype, int d, int G, bool deep = false);
 int decode_max_tiles_per_cta();
+int decode_ring_stages(bool deep);  // 16-bit tiles the ring of a launch shape holds
 cudaError_t launch_decode_tiles(const TileDecodeParams &p, int dtype, int d, int G,
                                 cudaStream_t s, long long *launches);
 

@@ -567,10 +567,25 @@ int unit_tiles_str(const spd_ctx *c, const Seq &s) {
 // Split policy.  Every unit (sequence, kv head) gets nc clusters of CS CTAs;
 // CS, the same for the whole launch, is the largest power of two (up to the
 // size the kernel can be co-scheduled with) that keeps units x CS within one
-// CTA per SM; nc is 1 unless a unit holds much more than its share of the
-// launch's tiles (uneven batches), in which case its clusters are merged in
-// global memory.  Tiles are then spread evenly over the unit's CTAs.
-int plan_tiles(const spd_ctx *c, TileDecodeParams &p, const int *ids, int n) {
+// CTA per SM.  Tiles are then spread evenly over the unit's CTAs.
+//
+// Launch shape.  The shared shape (two CTAs per SM: this launch's and the
+// next one's, which stages its tiles early) is planned first.  Its nc is 1
+// while a unit's tiles fit kPreferTiles per CTA (merging several clusters
+// goes through global memory and costs more than the longer tile loop),
+// else the unit's share of the launch's tiles over CS CTAs (rounded).  When
+// that plan needs more CTAs than SMs (some SMs would run two CTAs of the
+// launch) or merges clusters in global memory, and the launch holds more
+// than kDeepTilesPerSm tiles per SM, the deep-ring shape (one CTA per SM, 24
+// stages) is planned instead when allow_deep: the SMs are shared out in
+// proportion to the tiles, one cluster per unit first and then, cluster by
+// cluster, to the (sequence, head kind) whose units hold the most tiles per
+// CTA, never more CTAs than SMs.  Either way a CTA takes at most
+// decode_max_tiles_per_cta() tiles.
+constexpr int kPreferTiles = 24;
+constexpr int kDeepTilesPerSm = 16;
+
+int plan_tiles(const spd_ctx *c, TileDecodeParams &p, const int *ids, int n, bool allow_deep) {
   const Derived &dv = c->dv;
   long long total = 0;
   for (int i = 0; i < n; ++i) {
@@ -579,54 +594,122 @@ int plan_tiles(const spd_ctx *c, TileDecodeParams &p, const int *ids, int n) {
     if (dv.Hs) total += (long long)dv.Hs * unit_tiles_str(c, s);
   }
   const long long units = (long long)n * (dv.Hd + dv.Hs);
-  int cs = 1;
-  const int cs_max = decode_max_cluster(c->cfg.dtype, c->cfg.head_dim, dv.G);
-  while (cs * 2 <= cs_max && units * cs * 2 <= c->num_sms) cs *= 2;
-  const long long tpc = std::max<long long>(1, (total + c->num_sms - 1) / c->num_sms);
   const int max_tiles = decode_max_tiles_per_cta();
-  auto split = [&](int nt, int *ns, int *tpi) {
-    long long nc = std::max<long long>(1, (nt + cs * tpc / 2) / (cs * tpc));  // rounded
-    nc = std::max<long long>(nc, (nt + (long long)cs * max_tiles - 1) / ((long long)cs * max_tiles));
-    *ns = (int)(nc * cs);
-    *tpi = std::max(1, (nt + *ns - 1) / *ns);
-  };
-  int items = 0;
-  for (int i = 0; i < n; ++i) {
+  auto fill = [&](int i, int ns_dyn, int ns_str, int *items) {
     const Seq &s = c->seqs[ids[i]];
     TileSeq &d = p.seqs[i];
     d.slot = ids[i];
     d.L = (int)s.L;
     d.nL0 = s.nL0;
     d.sel_count = s.sel_count;
-    d.item_off = items;
-    d.ns_dyn = d.ns_str = 0;
-    d.tpi_dyn = d.tpi_str = 1;
-    if (dv.Hd) split(unit_tiles_dyn(c, s), &d.ns_dyn, &d.tpi_dyn);
-    if (dv.Hs) split(unit_tiles_str(c, s), &d.ns_str, &d.tpi_str);
-    items += dv.Hd * d.ns_dyn + dv.Hs * d.ns_str;
+    d.item_off = *items;
+    d.ns_dyn = dv.Hd ? ns_dyn : 0;
+    d.ns_str = dv.Hs ? ns_str : 0;
+    d.tpi_dyn = dv.Hd ? std::max(1, (unit_tiles_dyn(c, s) + ns_dyn - 1) / ns_dyn) : 1;
+    d.tpi_str = dv.Hs ? std::max(1, (unit_tiles_str(c, s) + ns_str - 1) / ns_str) : 1;
+    *items += dv.Hd * d.ns_dyn + dv.Hs * d.ns_str;
+  };
+
+  int cs = 1;
+  const int cs_max = decode_max_cluster(c->cfg.dtype, c->cfg.head_dim, dv.G);
+  while (cs * 2 <= cs_max && units * cs * 2 <= c->num_sms) cs *= 2;
+  const long long tpc = std::max<long long>(1, (total + c->num_sms - 1) / c->num_sms);
+  bool merges = false;  // some unit has several clusters
+  auto split = [&](int nt) {
+    long long nc = nt <= (long long)cs * kPreferTiles
+                       ? 1
+                       : std::max<long long>(1, (nt + cs * tpc / 2) / (cs * tpc));  // rounded
+    nc = std::max<long long>(nc, (nt + (long long)cs * max_tiles - 1) / ((long long)cs * max_tiles));
+    merges = merges || nc > 1;
+    return (int)(nc * cs);
+  };
+  int items = 0;
+  for (int i = 0; i < n; ++i) {
+    const Seq &s = c->seqs[ids[i]];
+    fill(i, dv.Hd ? split(unit_tiles_dyn(c, s)) : 0, dv.Hs ? split(unit_tiles_str(c, s)) : 0,
+         &items);
   }
   p.cluster = cs;
   p.total_items = items;
-  return items;
+  p.deep = 0;
+  if (!allow_deep || (items <= c->num_sms && !merges) ||
+      total <= (long long)c->num_sms * kDeepTilesPerSm)
+    return items;
+  {
+    int cs = 1;
+    const int cs_max = decode_max_cluster(c->cfg.dtype, c->cfg.head_dim, dv.G, true);
+    while (cs * 2 <= cs_max && units * cs * 2 <= c->num_sms) cs *= 2;
+    if (units * cs <= c->num_sms) {
+      // groups: (sequence, head kind); a step gives each unit of a group one
+      // more cluster
+      struct Grp {
+        int seq, kind, units, ns;
+        long long nt;
+      };
+      std::vector<Grp> gs;
+      for (int i = 0; i < n; ++i) {
+        const Seq &s = c->seqs[ids[i]];
+        if (dv.Hd) gs.push_back(Grp{i, 0, dv.Hd, cs, unit_tiles_dyn(c, s)});
+        if (dv.Hs) gs.push_back(Grp{i, 1, dv.Hs, cs, unit_tiles_str(c, s)});
+      }
+      long long free_ctas = c->num_sms - units * cs;
+      auto load = [](const Grp &g) { return (double)g.nt / g.ns; };
+      auto cmp = [&](int a, int b) { return load(gs[a]) < load(gs[b]); };
+      std::vector<int> heap(gs.size());
+      for (size_t k = 0; k < gs.size(); ++k) heap[k] = (int)k;
+      std::make_heap(heap.begin(), heap.end(), cmp);
+      while (!heap.empty()) {
+        std::pop_heap(heap.begin(), heap.end(), cmp);
+        Grp &g = gs[heap.back()];
+        const long long cost = (long long)g.units * cs;
+        if (cost > free_ctas || g.ns + cs > g.nt) {
+          heap.pop_back();  // no room for this group's next cluster
+          continue;
+        }
+        g.ns += cs;
+        free_ctas -= cost;
+        std::push_heap(heap.begin(), heap.end(), cmp);
+      }
+      bool ok = true;
+      for (const Grp &g : gs) ok = ok && (g.nt + g.ns - 1) / g.ns <= max_tiles;
+      if (ok) {
+        int items = 0;
+        std::vector<int> nsd(n, cs), nss(n, cs);
+        for (const Grp &g : gs) (g.kind ? nss : nsd)[g.seq] = g.ns;
+        for (int i = 0; i < n; ++i) fill(i, nsd[i], nss[i], &items);
+        p.cluster = cs;
+        p.total_items = items;
+        p.deep = 1;
+        return items;
+      }
+    }
+  }
+
+  // (the deep plan did not fit: the shared one again)
+  return plan_tiles(c, p, ids, n, false);
 }
+
+// The deep-ring shape serves the plain 16-bit kernel (no per-page mass
+// export, no fp8 storage).
+bool deep_allowed(const spd_ctx *c, bool mass) { return !c->dv.kv_fp8 && !mass; }
 
 // The sequences [b, b + m) of a call that one decode launch takes: as many as
 // fit one parameter block and max_items, halving until they do (down to one
 // sequence).  Leaves p planned for them and returns m.
 int next_batch(const spd_ctx *c, TileDecodeParams &p, const int *ids, int b, int n,
-               int max_items) {
+               int max_items, bool allow_deep) {
   int m = std::min(c->dv.seqs_per_launch, n - b);
-  while (plan_tiles(c, p, ids + b, m) > max_items && m > 1) m = (m + 1) / 2;
+  while (plan_tiles(c, p, ids + b, m, allow_deep) > max_items && m > 1) m = (m + 1) / 2;
   return m;
 }
 
 // Plans every launch of an attention call without enqueuing anything; fails
 // with SPD_ERR_CAPACITY if a launch would need more than max_items items
 // (a single sequence whose split items alone exceed it).
-spd_status check_capacity(spd_ctx *c, const int *ids, int n, int max_items) {
+spd_status check_capacity(spd_ctx *c, const int *ids, int n, int max_items, bool allow_deep) {
   static thread_local TileDecodeParams p;
   for (int b = 0; b < n;) {
-    const int m = next_batch(c, p, ids, b, n, max_items);
+    const int m = next_batch(c, p, ids, b, n, max_items, allow_deep);
     if (p.total_items > max_items)
       return c->fail(SPD_ERR_CAPACITY, "sequence %d needs %d split items, the library-owned "
                      "scratch holds %d", ids[b], p.total_items, max_items);
@@ -658,12 +741,13 @@ spd_status attention_impl(spd_ctx *c, const void *q, const int *ids, int n, floa
   const size_t qrow = (size_t)c->cfg.num_q_heads * c->cfg.head_dim;
   const size_t kvrow = (size_t)c->cfg.num_kv_heads * c->cfg.head_dim;
   const int max_items = scr ? scr->max_items : kMaxItems;
+  const bool allow_deep = deep_allowed(c, so.page_mass != nullptr && dv.Hd > 0);
   // a bounded scratch: every launch is planned before the first is enqueued
-  if (scr && (r = check_capacity(c, ids, n, max_items)) != SPD_OK) return r;
+  if (scr && (r = check_capacity(c, ids, n, max_items, allow_deep)) != SPD_OK) return r;
   int b = 0;
   while (b < n) {
     static thread_local TileDecodeParams p;
-    const int m = next_batch(c, p, ids, b, n, max_items);
+    const int m = next_batch(c, p, ids, b, n, max_items, allow_deep);
     p.n_seqs = m;
     p.tm_k = c->tm_k;
     p.tm_v = c->tm_v;
@@ -769,7 +853,7 @@ spd_status check_attention_call(spd_ctx *c, const void *q, const int *ids, int n
 }
 
 spd_status check_attention_capacity(spd_ctx *c, const int *ids, int n, int max_items) {
-  return check_capacity(c, ids, n, max_items);
+  return check_capacity(c, ids, n, max_items, deep_allowed(c, false));
 }
 
 spd_status bind_device(spd_ctx *c, cudaStream_t st, int *device) {
