@@ -127,13 +127,13 @@ struct Smem {
   static constexpr int kC = kP + kWarps * kRows * GP<G>::v * 4;        // float [W][GP]
   static constexpr int kML = kC + kWarps * GP<G>::v * 4;               // float [2][W][G]
   // inbox: what the cluster's CTAs send this CTA: M[16][G], L[16][G] and
-  // O[16 ranks][G][D / CS] (= G * D floats for any CS)
+  // O[CS ranks][G][D / CS + pad 4] (<= G * D + 64 floats for any CS <= 16)
   static constexpr int kInbox = (kML + 2 * kWarps * G * 4 + 15) / 16 * 16;
-  static constexpr int kFlag = kInbox + (32 * G + G * D) * 4;          // int [4 + kStages]
+  static constexpr int kFlag = kInbox + (32 * G + G * D + 64) * 4;     // int [4 + kStages]
   static constexpr int kTopkBar = (kFlag + (4 + kStages) * 4 + 7) / 8 * 8;  // uint64
   static constexpr int kTiles = (kTopkBar + 8 + 1023) / 1024 * 1024;
   static constexpr int kStageRegion = kStages * Geo<D, F8>::kTileBytes;
-  static constexpr int kMergeRegion = kWarps * G * D * 4;              // o of every warp
+  static constexpr int kMergeRegion = kWarps * G * (D + 4) * 4;        // o of every warp
   static constexpr int kCombineRegion = 256 * G * 12 + 64;             // (m, l), weights
   // before the tiles of a fused selection step: the top-k buffers, then the
   // unit's selected pages
@@ -839,7 +839,10 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
         if (s_iss[st] > 0) mbar_wait(&bars[st], (s_iss[st] - 1) & 1, kWaitLimit);
     __syncthreads();
   }
-  float *o_w = reinterpret_cast<float *>(stages);  // [W][G][D]
+  // [W][G][D + 4]: the 4 padding words per row put the heads of a lane
+  // group's stores in different banks
+  constexpr int OS = D + 4;
+  float *o_w = reinterpret_cast<float *>(stages);
   if (g8 == 0) {
     if (2 * t4 < G) {
       m_w[warp * G + 2 * t4] = m0;
@@ -857,12 +860,12 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
     const int ch = kF8 ? 16 * m + 2 * g8 : 16 * m + g8;
     const int ch2 = kF8 ? ch + 1 : ch + 8;
     if (2 * t4 < G) {
-      o_w[(warp * G + 2 * t4) * D + ch] = oacc[m][0];
-      o_w[(warp * G + 2 * t4) * D + ch2] = oacc[m][2];
+      o_w[(warp * G + 2 * t4) * OS + ch] = oacc[m][0];
+      o_w[(warp * G + 2 * t4) * OS + ch2] = oacc[m][2];
     }
     if (2 * t4 + 1 < G) {
-      o_w[(warp * G + 2 * t4 + 1) * D + ch] = oacc[m][1];
-      o_w[(warp * G + 2 * t4 + 1) * D + ch2] = oacc[m][3];
+      o_w[(warp * G + 2 * t4 + 1) * OS + ch] = oacc[m][1];
+      o_w[(warp * G + 2 * t4 + 1) * OS + ch2] = oacc[m][3];
     }
   }
   __syncthreads();
@@ -888,7 +891,7 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
 #pragma unroll
       for (int w = 0; w < kWarps; ++w) {
         const float f = exp2f(m_w[w * G + g] - M);
-        const float4 o = *reinterpret_cast<const float4 *>(&o_w[(w * G + g) * D + c]);
+        const float4 o = *reinterpret_cast<const float4 *>(&o_w[(w * G + g) * OS + c]);
         O.x = fmaf(f, o.x, O.x);
         O.y = fmaf(f, o.y, O.y);
         O.z = fmaf(f, o.z, O.z);
@@ -897,7 +900,9 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
       }
     }
     const int owner = c >> lsl, cs_ = c & (slice - 1);
-    st_dsmem_v4_f32(map_rank(aO + 4 * ((rank * G + g) * slice + cs_), owner), O);
+    // an owner's inbox row per sending rank is G * slice + 4 words: the
+    // ranks of one element fall in different banks when it is read back
+    st_dsmem_v4_f32(map_rank(aO + 4 * (rank * (G * slice + 4) + g * slice + cs_), owner), O);
     if (cs_ == 0) {
       st_dsmem_f32(map_rank(aM + 4 * (rank * G + g), owner), M);
       st_dsmem_f32(map_rank(aL + 4 * (rank * G + g), owner), Ls);
@@ -930,7 +935,7 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
         if (mr != -CUDART_INF_F) {
           const float f = exp2f(mr - M);
           Ls = fmaf(f, in_L[r * G + g], Ls);
-          O = fmaf(f, in_O[(r * G + g) * slice + cl], O);
+          O = fmaf(f, in_O[r * (E + 4) + g * slice + cl], O);
         }
       }
     for (int o = 1; o < TPE; o <<= 1) {
