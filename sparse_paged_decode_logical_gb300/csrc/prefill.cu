@@ -14,7 +14,9 @@
 //           exact top-k (ties to the lower block) of them; the list is the
 //           chosen blocks plus b itself, ascending.  Dense mode, or b below
 //           the budget: every block 0..b.
-//   attn    one CTA per (query block, query head), 4 warps of 16 queries:
+//   attn    (prefill_tc.cu on the 5th-generation tensor cores when G >= 2;
+//           this kernel otherwise)
+//           one CTA per (query block, query head), 4 warps of 16 queries:
 //           the chosen key blocks are staged in shared memory 64 rows at a
 //           time and each warp runs the decode kernel's tile math with its
 //           16 queries as two 8-column tiles -- S^T = K Q^T and O^T += V^T
@@ -365,6 +367,7 @@ cudaError_t launch_t(const PrefillParams &p, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   e = launch_pdl(prefill_select_kernel, grid_kv, kSelThreads, (size_t)kTopkSmemBytes, st, p);
   if (e != cudaSuccess) return e;
+  if (prefill_tc_supported(p.G)) return launch_prefill_attn_tc(p, PF<T>::bf ? 1 : 0, D, st);
   e = launch_pdl(prefill_attn_kernel<T, D>, grid_q, kAttnThreads, (size_t)PfSmem<D>::kBytes, st,
                  p);
   return e != cudaSuccess ? e : cudaGetLastError();

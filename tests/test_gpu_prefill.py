@@ -84,6 +84,8 @@ def test_prefill_dense_below_the_threshold():
     dict(L=777, Hq=2, Hkv=2, d=64, r=8, dtype="f16", budget=128, seed=3),
     dict(L=500, Hq=8, Hkv=1, d=128, r=16, dtype="bf16", budget=64, seed=4),
     dict(L=2048, Hq=4, Hkv=1, d=128, r=16, dtype="f16", budget=512, seed=5),
+    dict(L=1500, Hq=16, Hkv=2, d=64, r=8, dtype="bf16", budget=384, seed=9),
+    dict(L=1100, Hq=8, Hkv=4, d=64, r=8, dtype="f16", budget=256, seed=10),
 ])
 def test_prefill_sparse_blocks(case):
     c = dict(case)
