@@ -12,9 +12,9 @@ constexpr int kPrefillMaxBlocks = 8192;  // blocks of a prompt (the top-k holds 
 constexpr int kPrefillMaxRank = 64;
 
 struct PrefillParams {
-  // K and V for the tensor-core attention: 4-D maps {64 channels, d / 64,
-  // Hkv, L}, boxes of 64 channels x 64 tokens, 128-byte swizzle
-  CUtensorMap tm_k, tm_v;
+  // Q, K and V for the tensor-core attention: 4-D maps {64 channels, d / 64,
+  // heads, L}, boxes of 64 channels x 64 tokens, 128-byte swizzle
+  CUtensorMap tm_q, tm_k, tm_v;
   const void *q;         // [L][Hq][d]
   const void *k, *v;     // [L][Hkv][d]
   const float *wq, *wk;  // [Hkv][d][r]
@@ -34,7 +34,7 @@ struct PrefillParams {
 // dtype: 0 fp16, 1 bf16; d: 64 or 128.  Each returns cudaGetLastError().
 // launch_prefill runs the block means, the selection and the attention, the
 // latter on the 5th-generation tensor cores when prefill_tc_supported(G)
-// (tm_k / tm_v set), else with mma.sync tiles.
+// (tm_q / tm_k / tm_v set), else with mma.sync tiles.
 cudaError_t launch_prefill(const PrefillParams &p, int dtype, int d, cudaStream_t st);
 bool prefill_tc_supported(int G);
 cudaError_t launch_prefill_attn_tc(const PrefillParams &p, int dtype, int d, cudaStream_t st);

@@ -57,11 +57,11 @@ spd_status layout(const spd_prefill_config *c, int L, PrefillLayout *z) {
 
 bool aligned(const void *p, uintptr_t a) { return p && reinterpret_cast<uintptr_t>(p) % a == 0; }
 
-// TMA map over K or V ([L][Hkv][d], 16-bit) for the tensor-core attention:
-// {64 channels, d / 64, Hkv, L}; one box is 64 tokens x 64 channels, stored
-// in shared memory as 64 rows of 128 bytes with the 128-byte swizzle.
-// Tokens past L read as zero.
-bool encode_kv_map(CUtensorMap *m, const void *base, const spd_prefill_config *c, int L) {
+// TMA map over Q, K or V ([L][heads][d], 16-bit) for the tensor-core
+// attention: {64 channels, d / 64, heads, L}; one box is 64 tokens x 64
+// channels of one head, stored in shared memory as 64 rows of 128 bytes with
+// the 128-byte swizzle.  Tokens past L read as zero.
+bool encode_map(CUtensorMap *m, const void *base, const spd_prefill_config *c, int heads, int L) {
   static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   if (!encode) {
     void *fn = nullptr;
@@ -72,9 +72,9 @@ bool encode_kv_map(CUtensorMap *m, const void *base, const spd_prefill_config *c
       return false;
     encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   }
-  const cuuint64_t d = (cuuint64_t)c->head_dim, hkv = (cuuint64_t)c->num_kv_heads;
-  cuuint64_t dims[4] = {64, d / 64, hkv, (cuuint64_t)L};
-  cuuint64_t strides[3] = {128, d * 2, hkv * d * 2};
+  const cuuint64_t d = (cuuint64_t)c->head_dim, h = (cuuint64_t)heads;
+  cuuint64_t dims[4] = {64, d / 64, h, (cuuint64_t)L};
+  cuuint64_t strides[3] = {128, d * 2, h * d * 2};
   cuuint32_t box[4] = {64, 1, 1, (cuuint32_t)spd::kPrefillBlock};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   return encode(m, c->dtype == SPD_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
@@ -146,7 +146,8 @@ spd_status spd_prefill_block_sparse_attention(const spd_prefill_config *cfg, int
   p.score_scale = (float)(1.0 / std::sqrt((double)cfg->head_dim));
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)cfg->head_dim));
   if (spd::prefill_tc_supported(p.G) &&
-      (!encode_kv_map(&p.tm_k, k, cfg, seq_len) || !encode_kv_map(&p.tm_v, v, cfg, seq_len)))
+      (!encode_map(&p.tm_q, q, cfg, p.Hq, seq_len) || !encode_map(&p.tm_k, k, cfg, p.Hkv, seq_len) ||
+       !encode_map(&p.tm_v, v, cfg, p.Hkv, seq_len)))
     return SPD_ERR_CUDA;
   return spd::launch_prefill(p, cfg->dtype, cfg->head_dim, st) == cudaSuccess ? SPD_OK
                                                                               : SPD_ERR_CUDA;

@@ -4,21 +4,29 @@
 //
 // One CTA per (query block b, kv head, group of HC query heads), HC = 2 or 4:
 // its HC x 64 query rows are MT = HC / 2 matrices of 128 rows (two heads x
-// the block's 64 tokens each).  Per chosen key block i (ascending):
-//   S_m  = Q_m . K_i^T         tcgen05.mma, M 128 x N 64 x K d, fp32 in TMEM
-//   softmax, one row per thread: tcgen05.ld of its 64 logits, the causal mask
-//        on the diagonal block (and keys past the prompt), an online max and
-//        sum in fp32 (base 2), P written to shared memory as a 16-bit high
-//        part and the 16-bit rounding of the rest (like the decode kernel's
-//        P.V), and O's row rescaled in tensor memory when its max moved;
-//   O_m += (P_hi + P_lo)_m . V_i  tcgen05.mma, M 128 x N 64 (per half of d)
-//        x K 64 keys, fp32 in TMEM.
-// Q is staged once in shared memory (128-byte swizzled rows of 64 channels);
-// K and V blocks come by TMA (4-D maps over [L][Hkv][d], 64 x 64 boxes,
-// 128-byte swizzle) into two buffers, the next block loading while the
-// current one is in use.  One thread issues the MMAs and commits them to an
-// mbarrier; every wait is bounded, and a CTA that gives up records the error,
-// waits (bounded) for what it has in flight and frees its tensor memory.
+// the block's 64 tokens each).  Per chosen key block j (ascending):
+//   S_m  = Q_m . K_j^T          tcgen05.mma, M 128 x N 64 x K d, fp32 in
+//                               tensor memory (two buffers per matrix)
+//   softmax, one row per thread: its 64 logits from tensor memory, the
+//        causal mask on the diagonal block (and keys past the prompt), an
+//        online max and sum in fp32 (base 2), and P written back over S in
+//        tensor memory as a 16-bit high part and the 16-bit rounding of the
+//        rest (so P . V keeps about 16 bits of each weight);
+//   O_m += (P_hi + P_lo)_m . V_j  tcgen05.mma with A = P from tensor memory,
+//                               M 128 x N 64 (per 64 channels) x K 64 keys.
+// The running max only moves when a row's block max exceeds it by more than
+// 2^8 (log2 units), so O is rescaled rarely; weights then stay below 2^8,
+// and the final O / l is the same quotient (every term of O and of l carries
+// the same factor).
+//
+// Warp roles: warps 0 .. 4 MT - 1 run the softmax (matrix warp / 4, tensor
+// memory lanes 32 (warp % 4) ..), warp 4 MT issues the MMAs from one thread,
+// warp 4 MT + 1 loads Q once and K / V into a ring of stages by TMA (4-D maps
+// over [L][heads][d], 64 x 64 boxes, 128-byte swizzle).  S_m(j + 1) runs on
+// the tensor cores while the softmax of block j runs, and the two matrices'
+// work interleaves.  Every wait is bounded: a CTA that gives up records the
+// error, lets the other roles leave, waits (bounded) for its copies and MMAs
+// in flight and frees its tensor memory.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <math_constants.h>
@@ -31,46 +39,45 @@ namespace spd {
 namespace {
 
 constexpr uint32_t kTcWait = 1u << 22;  // bounded mbarrier polls
-
-template <typename T> struct TcT;
-template <> struct TcT<__half> {
-  static constexpr bool bf = false;
-  static __device__ __forceinline__ uint16_t bits(float x) {
-    const __half h = __float2half_rn(x);
-    return *reinterpret_cast<const uint16_t *>(&h);
-  }
-  static __device__ __forceinline__ float val(uint16_t b) {
-    return __half2float(*reinterpret_cast<const __half *>(&b));
-  }
-};
-template <> struct TcT<__nv_bfloat16> {
-  static constexpr bool bf = true;
-  static __device__ __forceinline__ uint16_t bits(float x) {
-    const __nv_bfloat16 h = __float2bfloat16_rn(x);
-    return *reinterpret_cast<const uint16_t *>(&h);
-  }
-  static __device__ __forceinline__ float val(uint16_t b) {
-    return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(&b));
-  }
-};
+constexpr float kRescaleAbove = 8.f;    // log2 growth of a row max that moves it
 
 // Shared memory (offsets from a 1024-byte aligned base).  Every matrix is a
 // stack of 64-column sub-tiles of rows x 128 bytes, 128-byte swizzled.
 template <int D, int HC>
 struct TcSmem {
-  static constexpr int MT = HC / 2;            // 128-row matrices of the CTA
-  static constexpr int KB = D / 64;            // 64-column sub-tiles of a row
-  static constexpr int kQ = 0;                 // [MT][KB][128 x 128 B]
-  static constexpr int kKV = kQ + MT * KB * 16384;  // [2 buffers][K, V][KB][64 x 128 B]
-  static constexpr int kKVBuf = 2 * KB * 8192;
-  static constexpr int kP = kKV + 2 * kKVBuf;  // [MT][hi, lo][128 x 128 B]
-  static constexpr int kBars = kP + MT * 2 * 16384;  // uint64 [4]: kv[2], s, pv
-  static constexpr int kMisc = kBars + 32;           // tmem base, fail flag
-  static constexpr int kBytes = kMisc + 16 + 1024;   // + alignment slack
-  // tensor-memory columns: S_m at 64m, O_m at 64 MT + D m
-  static constexpr int kCols = MT * (64 + D);
-  static constexpr int kAlloc = kCols <= 128 ? 128 : kCols <= 256 ? 256 : 512;
+  static constexpr int MT = HC / 2;                 // 128-row matrices of the CTA
+  static constexpr int KB = D / 64;                 // 64-column sub-tiles of a row
+  static constexpr int kStages = 4;                 // K / V ring
+  static constexpr int kQ = 0;                      // [MT][KB][128 x 128 B]
+  static constexpr int kK = kQ + MT * KB * 16384;   // [stage][KB][64 x 128 B]
+  static constexpr int kV = kK + kStages * KB * 8192;
+  static constexpr int kBars = kV + kStages * KB * 8192;
+  // mbarriers: Q, K full, V full, K/V empty (per stage), S full and P full
+  // (per matrix and buffer), O done (per matrix and block), O final (per
+  // matrix, once), drain.  A parity wait only tells apart phases one apart:
+  // every waiter below is at most one completion behind the barrier, which
+  // is why the end of O has a barrier of its own (the softmax can finish its
+  // last block while O done is still two completions short).
+  static constexpr int kBarQ = 0;
+  static constexpr int kBarKF = 1;
+  static constexpr int kBarVF = kBarKF + kStages;
+  static constexpr int kBarKE = kBarVF + kStages;
+  static constexpr int kBarSF = kBarKE + kStages;
+  static constexpr int kBarPF = kBarSF + 2 * MT;
+  static constexpr int kBarOD = kBarPF + 2 * MT;
+  static constexpr int kBarOF = kBarOD + MT;
+  static constexpr int kBarDR = kBarOF + MT;
+  static constexpr int kNumBars = kBarDR + 1;
+  static constexpr int kMisc = kBars + 8 * kNumBars;  // tmem base, fail flag
+  static constexpr int kBytes = kMisc + 16 + 1024;    // + alignment slack
+  // tensor-memory columns: S / P of matrix m, buffer u at 128 m + 64 u;
+  // O_m at 128 MT + D m
+  static constexpr int kCols = MT * (128 + D);
+  static constexpr int kAlloc = kCols <= 256 ? 256 : 512;
+  static constexpr int kThreads = MT * 128 + 64;
+  static constexpr int kMmaWarp = MT * 4, kLoadWarp = MT * 4 + 1;
   static_assert(kBytes <= 232448, "shared memory");
+  static_assert(kCols <= 512, "tensor memory");
 };
 
 __device__ __forceinline__ void pf_set_err(int *err, int code, int a, int b, int c) {
@@ -81,253 +88,288 @@ __device__ __forceinline__ void pf_set_err(int *err, int code, int a, int b, int
   }
 }
 
-__device__ __forceinline__ bool tc_wait(uint64_t *bar, uint32_t parity) {
+// Bounded wait for the phase of `parity` to complete; gives up early once
+// another role of the CTA has raised the fail flag.
+__device__ __forceinline__ bool tc_wait(uint64_t *bar, uint32_t parity, volatile int *fail) {
+  for (uint32_t i = 0; i < kTcWait; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 255u) == 255u && *fail) return false;
+  }
+  *fail = 1;
+  return false;
+}
+
+// A pair of softmax weights split into 16-bit high parts (packed) and the
+// 16-bit rounding of what is left (packed), element 0 in the low half.
+template <typename T> struct PSplit;
+template <> struct PSplit<__nv_bfloat16> {
+  static constexpr bool bf16 = true;
+  static __device__ __forceinline__ void run(float p0, float p1, uint32_t &hi, uint32_t &lo) {
+    // bf16 high parts by truncation: p - hi is then exact in fp32
+    const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
+    hi = __byte_perm(b0, b1, 0x7632);
+    const float r0 = p0 - __uint_as_float(b0 & 0xffff0000u);
+    const float r1 = p1 - __uint_as_float(b1 & 0xffff0000u);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(r0, r1);
+    lo = *reinterpret_cast<const uint32_t *>(&l);
+  }
+};
+template <> struct PSplit<__half> {
+  static constexpr bool bf16 = false;
+  static __device__ __forceinline__ void run(float p0, float p1, uint32_t &hi, uint32_t &lo) {
+    const __half2 h = __floats2half2_rn(p0, p1);
+    const float2 hf = __half22float2(h);
+    const __half2 l = __floats2half2_rn(p0 - hf.x, p1 - hf.y);
+    hi = *reinterpret_cast<const uint32_t *>(&h);
+    lo = *reinterpret_cast<const uint32_t *>(&l);
+  }
+};
+
+// Bounded wait that the fail flag does not cut short (copies and MMAs in
+// flight before the CTA frees its memory).
+__device__ __forceinline__ bool tc_drain(uint64_t *bar, uint32_t parity) {
   for (uint32_t i = 0; i < kTcWait; ++i)
     if (mbar_try_wait(bar, parity)) return true;
   return false;
 }
 
 template <typename T, int D, int HC>
-__global__ void __launch_bounds__(HC / 2 * 128) prefill_attn_tc_kernel(const __grid_constant__ PrefillParams p) {
+__global__ void __launch_bounds__(TcSmem<D, HC>::kThreads, 1)
+    prefill_attn_tc_kernel(const __grid_constant__ PrefillParams p) {
   using Sm = TcSmem<D, HC>;
-  constexpr int MT = Sm::MT, KB = Sm::KB;
-  constexpr int kThreads = MT * 128;
+  constexpr int MT = Sm::MT, KB = Sm::KB, S = Sm::kStages;
   extern __shared__ uint8_t tc_smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Sm::kBars);  // kv[0], kv[1], s, pv
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Sm::kBars);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Sm::kMisc);
+  volatile int *fail = reinterpret_cast<volatile int *>(smem + Sm::kMisc + 4);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int m = warp >> 2;                      // this thread's 128-row matrix
-  const int row = 32 * (warp & 3) + lane;       // its row there = tensor-memory lane
-  const int b = blockIdx.x % p.nb, rest = blockIdx.x / p.nb;
+  // the heaviest query blocks (most causal key blocks) first
+  const int b = p.nb - 1 - (int)(blockIdx.x % p.nb), rest = blockIdx.x / p.nb;
   const int hk = rest % p.Hkv, hg = rest / p.Hkv;
   const int t0 = b * kPrefillBlock;
-  // the thread's query: head (of the kv head's group) and token
-  const int h_row = hk * p.G + hg * HC + 2 * m + (row >> 6);
-  const int t_row = t0 + (row & 63);
+  const int h0 = hk * p.G + hg * HC;  // the CTA's first query head
 
-  pdl_wait();
-  pdl_launch_dependents();
-  if (warp == 0) tmem_alloc(tmem_slot, Sm::kAlloc);
-  if (tid == 0) {
-    for (int x = 0; x < 4; ++x) mbar_init(&bars[x], 1);
+  if (warp == Sm::kMmaWarp) tmem_alloc(tmem_slot, Sm::kAlloc);
+  if (tid == Sm::kLoadWarp * 32) {
+    for (int x = 0; x < Sm::kNumBars; ++x)
+      mbar_init(&bars[x], (x >= Sm::kBarPF && x < Sm::kBarOD) ? 4 : 1);  // P: one per warp
+    *fail = 0;
     fence_mbar_init();
+    prefetch_tmap(&p.tm_q);
     prefetch_tmap(&p.tm_k);
     prefetch_tmap(&p.tm_v);
   }
-  // ---- Q: the CTA's rows, 16 bytes per thread and step ----
-  {
-    const uint16_t *q = static_cast<const uint16_t *>(p.q);
-    for (int x = tid; x < MT * 128 * (D / 8); x += kThreads) {
-      const int mm = x / (128 * (D / 8)), rem = x % (128 * (D / 8));
-      const int r = rem / (D / 8), c16 = rem % (D / 8);
-      const int t = t0 + (r & 63), h = hk * p.G + hg * HC + 2 * mm + (r >> 6);
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (t < p.L) v = *reinterpret_cast<const uint4 *>(q + ((size_t)t * p.Hq + h) * D + c16 * 8);
-      uint8_t *sub = smem + Sm::kQ + (mm * KB + (c16 >> 3)) * 16384;
-      *reinterpret_cast<uint4 *>(sub + swz128(r, c16 & 7)) = v;
-    }
-  }
-  fence_proxy_async_smem();  // the MMAs read Q through the async proxy
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-
+  pdl_wait();  // the block lists come from the selection kernel
+  pdl_launch_dependents();
   const int *list = p.lists + ((size_t)hk * p.nb + b) * p.KB;
-  const int nsel = p.dense ? b + 1 : min(b + 1, p.kblocks);
-  // TMA of key block i into buffer buf: K then V, KB boxes each
-  auto load_kv = [&](int i, int buf) {
-    uint8_t *kv = smem + Sm::kKV + buf * Sm::kKVBuf;
-    mbar_arrive_expect_tx(&bars[buf], 2 * KB * 8192);
-    for (int kb = 0; kb < KB; ++kb) {
-      tma_load_4d(kv + kb * 8192, &p.tm_k, 0, kb, hk, i * kPrefillBlock, &bars[buf]);
-      tma_load_4d(kv + (KB + kb) * 8192, &p.tm_v, 0, kb, hk, i * kPrefillBlock, &bars[buf]);
-    }
-  };
-  int issued[2] = {0, 0};  // (thread 0) loads issued per buffer
-  if (tid == 0) {
-    for (int li = 0; li < min(2, nsel); ++li) {
-      const int i = list[li];
-      if (i >= 0 && i <= b) {
-        load_kv(i, li);
-        ++issued[li];
+  const int n = p.dense ? b + 1 : min(b + 1, p.kblocks);
+
+  if (warp == Sm::kLoadWarp) {
+    // ---- TMA: Q once, then K and V of every chosen block through the ring ----
+    if (lane == 0) {
+      int issued = 0;
+      bool ok = true;
+      mbar_arrive_expect_tx(&bars[Sm::kBarQ], MT * KB * 16384);
+      for (int mm = 0; mm < MT; ++mm)
+        for (int kb = 0; kb < KB; ++kb)
+          for (int hh = 0; hh < 2; ++hh)  // rows 0-63: head 2 mm, rows 64-127: head 2 mm + 1
+            tma_load_4d(smem + Sm::kQ + (mm * KB + kb) * 16384 + hh * 8192, &p.tm_q, 0, kb,
+                        h0 + 2 * mm + hh, t0, &bars[Sm::kBarQ]);
+      for (int j = 0; j < n; ++j) {
+        const int s = j % S;
+        if (j >= S && !(ok = tc_wait(&bars[Sm::kBarKE + s], ((j / S) - 1) & 1, fail))) break;
+        const int i = list[j];
+        if (i < 0 || i > b) {  // (the selection never yields one: record it and leave)
+          pf_set_err(p.err, kDevBadSelection, hk, b, i);
+          *fail = 1;
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&bars[Sm::kBarKF + s], KB * 8192);
+        for (int kb = 0; kb < KB; ++kb)
+          tma_load_4d(smem + Sm::kK + (s * KB + kb) * 8192, &p.tm_k, 0, kb, hk,
+                      i * kPrefillBlock, &bars[Sm::kBarKF + s]);
+        mbar_arrive_expect_tx(&bars[Sm::kBarVF + s], KB * 8192);
+        for (int kb = 0; kb < KB; ++kb)
+          tma_load_4d(smem + Sm::kV + (s * KB + kb) * 8192, &p.tm_v, 0, kb, hk,
+                      i * kPrefillBlock, &bars[Sm::kBarVF + s]);
+        ++issued;
+      }
+      if (!ok) {  // the copies still in flight land before the CTA leaves
+        tc_drain(&bars[Sm::kBarQ], 0);
+        for (int j = issued > S ? issued - S : 0; j < issued; ++j) {
+          tc_drain(&bars[Sm::kBarKF + j % S], (j / S) & 1);
+          tc_drain(&bars[Sm::kBarVF + j % S], (j / S) & 1);
+        }
       }
     }
-  }
-
-  const bool bf = TcT<T>::bf;
-  const uint32_t idesc_s = umma_idesc_f16(bf, 128, 64, 0, 0);  // Q . K^T: both K-major
-  const uint32_t idesc_o = umma_idesc_f16(bf, 128, 64, 0, 1);  // P . V: V MN-major
-  const float sc = p.scale_log2;
-  float m_run = -CUDART_INF_F, l_run = 0.f;
-  int commits = 0;       // (thread 0) MMA commits issued; alternately s and pv
-  bool fail = false;
-  for (int li = 0; li < nsel && !fail; ++li) {
-    const int i = list[li];
-    if (i < 0 || i > b) {  // (the selection never yields one: record it and drain)
-      if (tid == 0) pf_set_err(p.err, kDevBadSelection, hk, b, i);
-      fail = true;
-      break;
-    }
-    const int buf = li & 1;
-    uint8_t *kv = smem + Sm::kKV + buf * Sm::kKVBuf;
-    // ---- S = Q . K^T ----
-    bool ok = true;
-    if (tid == 0) {
-      ok = tc_wait(&bars[buf], (li >> 1) & 1);
+  } else if (warp == Sm::kMmaWarp) {
+    // ---- MMA issue: S of block j + 1 ahead of P . V of block j ----
+    if (lane == 0) {
+      const bool bf = PSplit<T>::bf16;
+      const uint32_t idesc_s = umma_idesc_f16(bf, 128, 64, 0, 0);  // Q . K^T: both K-major
+      const uint32_t idesc_o = umma_idesc_f16(bf, 128, 64, 0, 1);  // P . V: V MN-major
+      // S_m(j) = Q_m . K_j^T into buffer j & 1 of matrix m
+      auto issue_s = [&](int j, int m) {
+        const uint8_t *kt = smem + Sm::kK + (j % S) * KB * 8192;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t a = umma_desc_sw128(
+              smem_u32(smem + Sm::kQ + (m * KB + (kk >> 2)) * 16384) + (kk & 3) * 32, 16, 1024);
+          const uint64_t bd =
+              umma_desc_sw128(smem_u32(kt + (kk >> 2) * 8192) + (kk & 3) * 32, 16, 1024);
+          umma_f16(tmem + 128 * m + 64 * (j & 1), a, bd, idesc_s, kk > 0);
+        }
+        umma_commit(&bars[Sm::kBarSF + 2 * m + (j & 1)]);
+      };
+      bool ok = tc_wait(&bars[Sm::kBarQ], 0, fail) && tc_wait(&bars[Sm::kBarKF], 0, fail);
+      const bool any = ok;
       if (ok) {
         tc_fence_after();
-#pragma unroll
-        for (int mm = 0; mm < MT; ++mm)
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t a = umma_desc_sw128(
-                smem_u32(smem + Sm::kQ + (mm * KB + (kk >> 2)) * 16384) + (kk & 3) * 32, 16, 1024);
-            const uint64_t bd =
-                umma_desc_sw128(smem_u32(kv + (kk >> 2) * 8192) + (kk & 3) * 32, 16, 1024);
-            umma_f16(tmem + 64 * mm, a, bd, idesc_s, kk > 0);
-          }
-        umma_commit(&bars[2]);
-        ++commits;
+        for (int m = 0; m < MT; ++m) issue_s(0, m);
       }
-    }
-    ok = tc_wait(&bars[2], li & 1) && ok;
-    ok = __all_sync(0xffffffffu, ok);  // the tensor-memory loads below are warp-wide
-    tc_fence_after();
-    // ---- softmax of this thread's row ----
-    float alpha = 1.f;
-    if (ok) {
-      const uint32_t ta = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 64 * m;
-      uint32_t s[64];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t r16[16];
-        tmem_ld16(ta + 16 * c, r16);
-        tmem_wait_ld();
-#pragma unroll
-        for (int j = 0; j < 16; ++j) s[16 * c + j] = r16[j];
-      }
-      const int key0 = i * kPrefillBlock;
-      const int lim = min(i == b ? (row & 63) : 63, p.L - 1 - key0);  // last allowed key
-      float mx = -CUDART_INF_F;
-#pragma unroll
-      for (int j = 0; j < 64; ++j)
-        if (j <= lim) mx = fmaxf(mx, __uint_as_float(s[j]) * sc);
-      const float m_new = fmaxf(m_run, mx);
-      alpha = m_run == -CUDART_INF_F ? 0.f : exp2f(m_run - m_new);
-      float lsum = 0.f;
-      uint8_t *phi = smem + Sm::kP + (2 * m) * 16384, *plo = phi + 16384;
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {  // 16-byte chunks: keys 8c .. 8c+7
-        uint32_t hw[4], lw[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          uint16_t hb[2], lb[2];
-#pragma unroll
-          for (int f = 0; f < 2; ++f) {
-            const int j = 8 * c + 2 * e + f;
-            const float pj =
-                (j <= lim && m_new != -CUDART_INF_F) ? exp2f(__uint_as_float(s[j]) * sc - m_new)
-                                                     : 0.f;
-            lsum += pj;
-            hb[f] = TcT<T>::bits(pj);
-            lb[f] = TcT<T>::bits(pj - TcT<T>::val(hb[f]));
-          }
-          hw[e] = (uint32_t)hb[0] | ((uint32_t)hb[1] << 16);
-          lw[e] = (uint32_t)lb[0] | ((uint32_t)lb[1] << 16);
-        }
-        *reinterpret_cast<uint4 *>(phi + swz128(row, c)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-        *reinterpret_cast<uint4 *>(plo + swz128(row, c)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-      }
-      l_run = l_run * alpha + lsum;
-      m_run = m_new;
-    }
-    // O's row follows the new max (the previous block's P.V has finished)
-    if (li > 0 && __any_sync(0xffffffffu, ok && alpha != 1.f)) {
-      const uint32_t to = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 64 * MT + D * m;
-#pragma unroll 1
-      for (int c = 0; c < D / 16; ++c) {
-        uint32_t r16[16];
-        tmem_ld16(to + 16 * c, r16);
-        tmem_wait_ld();
-#pragma unroll
-        for (int j = 0; j < 16; ++j) r16[j] = __float_as_uint(__uint_as_float(r16[j]) * alpha);
-        tmem_st16(to + 16 * c, r16);
-      }
-      tmem_wait_st();
-    }
-    fence_proxy_async_smem();  // P was written through the generic proxy
-    tc_fence_before();
-    fail = __syncthreads_or(!ok);
-    tc_fence_after();
-    if (fail) break;
-    // ---- O += P . V ----
-    if (tid == 0) {
-#pragma unroll
-      for (int mm = 0; mm < MT; ++mm)
-#pragma unroll
-        for (int half = 0; half < KB; ++half)
-#pragma unroll
-          for (int part = 0; part < 2; ++part)
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t a = umma_desc_sw128(
-                  smem_u32(smem + Sm::kP + (2 * mm + part) * 16384) + kk * 32, 16, 1024);
-              const uint64_t bd =
-                  umma_desc_sw128(smem_u32(kv + (KB + half) * 8192) + kk * 2048, 16, 1024);
-              umma_f16(tmem + 64 * MT + D * mm + 64 * half, a, bd, idesc_o,
-                       li > 0 || part > 0 || kk > 0);
+      for (int j = 0; j < n && ok; ++j) {
+        const int s = j % S;
+        if (j + 1 < n) {
+          const int j1 = j + 1;
+          if (!(ok = tc_wait(&bars[Sm::kBarKF + j1 % S], (j1 / S) & 1, fail))) break;
+          for (int m = 0; m < MT && ok; ++m) {
+            // buffer j1 & 1 held P_m(j - 1): its P . V has to be done
+            if (j >= 1) ok = tc_wait(&bars[Sm::kBarOD + m], (j - 1) & 1, fail);
+            if (ok) {
+              tc_fence_after();
+              issue_s(j1, m);
             }
-      umma_commit(&bars[3]);
-      ++commits;
-    }
-    ok = tc_wait(&bars[3], li & 1);
-    tc_fence_after();
-    fail = __syncthreads_or(!ok);
-    if (fail) break;
-    // the buffer's MMAs are done: it takes block li + 2
-    if (tid == 0 && li + 2 < nsel) {
-      const int i2 = list[li + 2];
-      if (i2 >= 0 && i2 <= b) {
-        load_kv(i2, buf);
-        ++issued[buf];
+          }
+          if (!ok) break;
+        }
+        if (!(ok = tc_wait(&bars[Sm::kBarVF + s], (j / S) & 1, fail))) break;
+        const uint8_t *vt = smem + Sm::kV + s * KB * 8192;
+        for (int m = 0; m < MT && ok; ++m) {
+          if (!(ok = tc_wait(&bars[Sm::kBarPF + 2 * m + (j & 1)], (j >> 1) & 1, fail))) break;
+          tc_fence_after();
+          const uint32_t pa = tmem + 128 * m + 64 * (j & 1);
+#pragma unroll
+          for (int half = 0; half < KB; ++half)
+#pragma unroll
+            for (int part = 0; part < 2; ++part)  // P_hi, then P_lo
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t bd =
+                    umma_desc_sw128(smem_u32(vt + half * 8192) + kk * 2048, 16, 1024);
+                umma_f16_ts(tmem + 128 * MT + D * m + 64 * half, pa + 32 * part + 8 * kk, bd,
+                            idesc_o, j > 0 || part > 0 || kk > 0);
+              }
+          umma_commit(&bars[Sm::kBarOD + m]);
+          if (j == n - 1) umma_commit(&bars[Sm::kBarOF + m]);
+        }
+        if (!ok) break;
+        umma_commit(&bars[Sm::kBarKE + s]);  // the stage is free once these MMAs are done
       }
-    }
-  }
-  if (fail) {
-    // record it (the first error stays), and give what is still in flight one
-    // more bounded wait
-    if (tid == 0) {
-      pf_set_err(p.err, kDevTimeout, hk, b, 0);
-      for (int x = 0; x < 2; ++x)
-        if (issued[x] > 0) tc_wait(&bars[x], (issued[x] - 1) & 1);
-      if (commits > 0) tc_wait(&bars[2 + ((commits - 1) & 1)], ((commits - 1) >> 1) & 1);
+      if (any) {  // every MMA done before the CTA frees its memory
+        umma_commit(&bars[Sm::kBarDR]);
+        tc_drain(&bars[Sm::kBarDR], 0);
+      }
     }
   } else {
-    // ---- out = O / l (the loads are warp-wide; rows past the prompt store nothing) ----
-    const uint32_t to = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 64 * MT + D * m;
-    float *o = p.out + ((size_t)t_row * p.Hq + h_row) * D;
-    const float inv = 1.f / l_run;
-#pragma unroll 1
-    for (int c = 0; c < D / 16; ++c) {
-      uint32_t r16[16];
-      tmem_ld16(to + 16 * c, r16);
-      tmem_wait_ld();
-      if (t_row < p.L) {
+    // ---- softmax: one query row per thread ----
+    const int m = warp >> 2, row = 32 * (warp & 3) + lane;
+    const int h_row = h0 + 2 * m + (row >> 6), t_row = t0 + (row & 63);
+    const uint32_t lanes = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+    const uint32_t t_o = lanes + 128 * MT + D * m;
+    const float sc = p.scale_log2;
+    float m_run = -CUDART_INF_F, l_run = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n; ++j) {
+      const int u = j & 1;
+      const uint32_t t_s = lanes + 128 * m + 64 * u;
+      ok = tc_wait(&bars[Sm::kBarSF + 2 * m + u], (j >> 1) & 1, fail);
+      if (!(ok = __all_sync(0xffffffffu, ok))) break;  // the tensor-memory accesses are warp-wide
+      tc_fence_after();
+      uint32_t s[64];
+      tmem_ld32_sync(t_s, *reinterpret_cast<uint32_t(*)[32]>(s));
+      tmem_ld32_sync(t_s + 32, *reinterpret_cast<uint32_t(*)[32]>(s + 32));
+      const int i = list[j];
+      // last key of the block this row may see: the causal diagonal, the prompt's end
+      const int lim = i == b ? min(row & 63, p.L - 1 - i * kPrefillBlock) : kPrefillBlock - 1;
+      float mx = -CUDART_INF_F;
 #pragma unroll
-        for (int j = 0; j < 16; j += 4)
-          *reinterpret_cast<float4 *>(o + 16 * c + j) =
-              make_float4(__uint_as_float(r16[j]) * inv, __uint_as_float(r16[j + 1]) * inv,
-                          __uint_as_float(r16[j + 2]) * inv, __uint_as_float(r16[j + 3]) * inv);
+      for (int c = 0; c < 64; ++c)
+        if (c <= lim) mx = fmaxf(mx, __uint_as_float(s[c]));
+      mx *= sc;
+      const bool need = mx > m_run + kRescaleAbove;
+      if (__any_sync(0xffffffffu, need)) {
+        const float m_new = need ? mx : m_run;
+        const float alpha = m_run == -CUDART_INF_F ? 0.f : exp2f(m_run - m_new);
+        if (j > 0) {  // O_m follows the new max once P_m(j - 1) . V has landed
+          ok = tc_wait(&bars[Sm::kBarOD + m], (j - 1) & 1, fail);
+          if (!(ok = __all_sync(0xffffffffu, ok))) break;
+          tc_fence_after();
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32_sync(t_o + 32 * c, o);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st32(t_o + 32 * c, o);
+          }
+          tmem_wait_st();
+        }
+        l_run *= alpha;
+        m_run = m_new;
+      }
+      // weights exp2(s sc - m), split into high and low 16-bit parts, over S
+      uint32_t hi[32], lo[32];
+      float lsum = 0.f;
+      const float nm = -m_run;
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        const float p0 = 2 * c <= lim ? exp2f(fmaf(__uint_as_float(s[2 * c]), sc, nm)) : 0.f;
+        const float p1 = 2 * c + 1 <= lim ? exp2f(fmaf(__uint_as_float(s[2 * c + 1]), sc, nm)) : 0.f;
+        lsum += p0 + p1;
+        PSplit<T>::run(p0, p1, hi[c], lo[c]);
+      }
+      l_run += lsum;
+      tmem_st32(t_s, hi);
+      tmem_st32(t_s + 32, lo);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[Sm::kBarPF + 2 * m + u]);
+    }
+    if (ok) {
+      ok = tc_wait(&bars[Sm::kBarOF + m], 0, fail);
+      if ((ok = __all_sync(0xffffffffu, ok))) {
+        // ---- out = O / l (rows past the prompt store nothing) ----
+        tc_fence_after();
+        float *o = p.out + ((size_t)t_row * p.Hq + h_row) * D;
+        const float inv = 1.f / l_run;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32_sync(t_o + 32 * c, r);
+          if (t_row < p.L) {
+#pragma unroll
+            for (int e = 0; e < 32; e += 4)
+              *reinterpret_cast<float4 *>(o + 32 * c + e) =
+                  make_float4(__uint_as_float(r[e]) * inv, __uint_as_float(r[e + 1]) * inv,
+                              __uint_as_float(r[e + 2]) * inv, __uint_as_float(r[e + 3]) * inv);
+          }
+        }
       }
     }
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 0) tmem_dealloc(tmem, Sm::kAlloc);
+  if (tid == 0 && *fail) pf_set_err(p.err, kDevTimeout, hk, b, 0);  // (a selection error stays)
+  if (warp == Sm::kMmaWarp) tmem_dealloc(tmem, Sm::kAlloc);
 }
 
 template <typename T, int D, int HC>
@@ -337,7 +379,7 @@ cudaError_t launch_tc(const PrefillParams &p, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Sm::kBytes);
   if (e != cudaSuccess) return e;
   const int grid = p.nb * p.Hkv * (p.G / HC);
-  return launch_pdl(k, grid, Sm::MT * 128, (size_t)Sm::kBytes, st, p);
+  return launch_pdl(k, grid, Sm::kThreads, (size_t)Sm::kBytes, st, p);
 }
 
 template <typename T, int D>
