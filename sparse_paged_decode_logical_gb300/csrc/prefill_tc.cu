@@ -20,7 +20,8 @@
 // the same factor).
 //
 // Warp roles: warps 0 .. 4 MT - 1 run the softmax (matrix warp / 4, tensor
-// memory lanes 32 (warp % 4) ..), warp 4 MT issues the MMAs from one thread,
+// memory lanes 32 (warp % 4) ..), warp 4 MT issues the MMAs (the whole warp
+// runs the issue loop with warp-uniform operands, one elected lane issues),
 // warp 4 MT + 1 loads Q once and K / V into a ring of stages by TMA (4-D maps
 // over [L][heads][d], 64 x 64 boxes, 128-byte swizzle).  S_m(j + 1) runs on
 // the tensor cores while the softmax of block j runs, and the two matrices'
@@ -104,22 +105,24 @@ __device__ __forceinline__ bool tc_wait(uint64_t *bar, uint32_t parity, volatile
 template <typename T> struct PSplit;
 template <> struct PSplit<__nv_bfloat16> {
   static constexpr bool bf16 = true;
-  static __device__ __forceinline__ void run(float p0, float p1, uint32_t &hi, uint32_t &lo) {
-    // bf16 high parts by truncation: p - hi is then exact in fp32
-    const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
+  static __device__ __forceinline__ void run(float2 pp, uint32_t &hi, uint32_t &lo) {
+    // bf16 high parts by truncation (the top 16 bits of each fp32 pattern),
+    // so p - hi is exact in fp32; the rest is rounded to bf16
+    const uint32_t b0 = __float_as_uint(pp.x), b1 = __float_as_uint(pp.y);
     hi = __byte_perm(b0, b1, 0x7632);
-    const float r0 = p0 - __uint_as_float(b0 & 0xffff0000u);
-    const float r1 = p1 - __uint_as_float(b1 & 0xffff0000u);
-    const __nv_bfloat162 l = __floats2bfloat162_rn(r0, r1);
+    const float2 r = f2_sub(pp, make_float2(__uint_as_float(b0 & 0xffff0000u),
+                                            __uint_as_float(b1 & 0xffff0000u)));
+    const __nv_bfloat162 l = __floats2bfloat162_rn(r.x, r.y);
     lo = *reinterpret_cast<const uint32_t *>(&l);
   }
 };
+
 template <> struct PSplit<__half> {
   static constexpr bool bf16 = false;
-  static __device__ __forceinline__ void run(float p0, float p1, uint32_t &hi, uint32_t &lo) {
-    const __half2 h = __floats2half2_rn(p0, p1);
-    const float2 hf = __half22float2(h);
-    const __half2 l = __floats2half2_rn(p0 - hf.x, p1 - hf.y);
+  static __device__ __forceinline__ void run(float2 pp, uint32_t &hi, uint32_t &lo) {
+    const __half2 h = __floats2half2_rn(pp.x, pp.y);
+    const float2 r = f2_sub(pp, __half22float2(h));
+    const __half2 l = __floats2half2_rn(r.x, r.y);
     hi = *reinterpret_cast<const uint32_t *>(&h);
     lo = *reinterpret_cast<const uint32_t *>(&l);
   }
@@ -164,7 +167,7 @@ __global__ void __launch_bounds__(TcSmem<D, HC>::kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
+  const uint32_t tmem = __shfl_sync(0xffffffffu, *tmem_slot, 0);  // warp-uniform
   pdl_wait();  // the block lists come from the selection kernel
   pdl_launch_dependents();
   const int *list = p.lists + ((size_t)hk * p.nb + b) * p.KB;
@@ -210,72 +213,74 @@ __global__ void __launch_bounds__(TcSmem<D, HC>::kThreads, 1)
       }
     }
   } else if (warp == Sm::kMmaWarp) {
-    // ---- MMA issue: S of block j + 1 ahead of P . V of block j ----
-    if (lane == 0) {
-      const bool bf = PSplit<T>::bf16;
-      const uint32_t idesc_s = umma_idesc_f16(bf, 128, 64, 0, 0);  // Q . K^T: both K-major
-      const uint32_t idesc_o = umma_idesc_f16(bf, 128, 64, 0, 1);  // P . V: V MN-major
-      // S_m(j) = Q_m . K_j^T into buffer j & 1 of matrix m
-      auto issue_s = [&](int j, int m) {
-        const uint8_t *kt = smem + Sm::kK + (j % S) * KB * 8192;
+    // ---- MMA issue (the whole warp, one elected lane issuing): S of block
+    // j + 1 ahead of P . V of block j ----
+    const bool bf = PSplit<T>::bf16;
+    const uint32_t idesc_s = umma_idesc_f16(bf, 128, 64, 0, 0);  // Q . K^T: both K-major
+    const uint32_t idesc_o = umma_idesc_f16(bf, 128, 64, 0, 1);  // P . V: V MN-major
+    // base descriptors; a byte offset o inside the region adds o / 16
+    const uint64_t dq = umma_desc_sw128(smem_u32(smem + Sm::kQ), 16, 1024);
+    const uint64_t dk = umma_desc_sw128(smem_u32(smem + Sm::kK), 16, 1024);
+    const uint64_t dv = umma_desc_sw128(smem_u32(smem + Sm::kV), 16, 1024);
+    // every lane waits; the warp goes on only if all saw the phase
+    auto wwait = [&](uint64_t *bar, uint32_t parity) {
+      return __all_sync(0xffffffffu, tc_wait(bar, parity, fail));
+    };
+    // S_m(j) = Q_m . K_j^T into buffer j & 1 of matrix m
+    auto issue_s = [&](int j, int m) {
+      const uint64_t kt = dk + (uint64_t)(((j % S) * KB * 8192) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t a = umma_desc_sw128(
-              smem_u32(smem + Sm::kQ + (m * KB + (kk >> 2)) * 16384) + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd =
-              umma_desc_sw128(smem_u32(kt + (kk >> 2) * 8192) + (kk & 3) * 32, 16, 1024);
-          umma_f16(tmem + 128 * m + 64 * (j & 1), a, bd, idesc_s, kk > 0);
-        }
-        umma_commit(&bars[Sm::kBarSF + 2 * m + (j & 1)]);
-      };
-      bool ok = tc_wait(&bars[Sm::kBarQ], 0, fail) && tc_wait(&bars[Sm::kBarKF], 0, fail);
-      const bool any = ok;
-      if (ok) {
-        tc_fence_after();
-        for (int m = 0; m < MT; ++m) issue_s(0, m);
-      }
-      for (int j = 0; j < n && ok; ++j) {
-        const int s = j % S;
-        if (j + 1 < n) {
-          const int j1 = j + 1;
-          if (!(ok = tc_wait(&bars[Sm::kBarKF + j1 % S], (j1 / S) & 1, fail))) break;
-          for (int m = 0; m < MT && ok; ++m) {
-            // buffer j1 & 1 held P_m(j - 1): its P . V has to be done
-            if (j >= 1) ok = tc_wait(&bars[Sm::kBarOD + m], (j - 1) & 1, fail);
-            if (ok) {
-              tc_fence_after();
-              issue_s(j1, m);
-            }
-          }
-          if (!ok) break;
-        }
-        if (!(ok = tc_wait(&bars[Sm::kBarVF + s], (j / S) & 1, fail))) break;
-        const uint8_t *vt = smem + Sm::kV + s * KB * 8192;
+      for (int kk = 0; kk < D / 16; ++kk)
+        umma_f16_warp(tmem + 128 * m + 64 * (j & 1),
+                      dq + (uint64_t)(((m * KB + (kk >> 2)) * 16384 + (kk & 3) * 32) >> 4),
+                      kt + (uint64_t)(((kk >> 2) * 8192 + (kk & 3) * 32) >> 4), idesc_s, kk > 0);
+      umma_commit_warp(&bars[Sm::kBarSF + 2 * m + (j & 1)]);
+    };
+    bool ok = wwait(&bars[Sm::kBarQ], 0) && wwait(&bars[Sm::kBarKF], 0);
+    const bool any = ok;
+    if (ok) {
+      tc_fence_after();
+      for (int m = 0; m < MT; ++m) issue_s(0, m);
+    }
+    for (int j = 0; j < n && ok; ++j) {
+      const int s = j % S;
+      if (j + 1 < n) {
+        const int j1 = j + 1;
+        if (!(ok = wwait(&bars[Sm::kBarKF + j1 % S], (j1 / S) & 1))) break;
         for (int m = 0; m < MT && ok; ++m) {
-          if (!(ok = tc_wait(&bars[Sm::kBarPF + 2 * m + (j & 1)], (j >> 1) & 1, fail))) break;
-          tc_fence_after();
-          const uint32_t pa = tmem + 128 * m + 64 * (j & 1);
-#pragma unroll
-          for (int half = 0; half < KB; ++half)
-#pragma unroll
-            for (int part = 0; part < 2; ++part)  // P_hi, then P_lo
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk) {
-                const uint64_t bd =
-                    umma_desc_sw128(smem_u32(vt + half * 8192) + kk * 2048, 16, 1024);
-                umma_f16_ts(tmem + 128 * MT + D * m + 64 * half, pa + 32 * part + 8 * kk, bd,
-                            idesc_o, j > 0 || part > 0 || kk > 0);
-              }
-          umma_commit(&bars[Sm::kBarOD + m]);
-          if (j == n - 1) umma_commit(&bars[Sm::kBarOF + m]);
+          // buffer j1 & 1 held P_m(j - 1): its P . V has to be done
+          if (j >= 1) ok = wwait(&bars[Sm::kBarOD + m], (j - 1) & 1);
+          if (ok) {
+            tc_fence_after();
+            issue_s(j1, m);
+          }
         }
         if (!ok) break;
-        umma_commit(&bars[Sm::kBarKE + s]);  // the stage is free once these MMAs are done
       }
-      if (any) {  // every MMA done before the CTA frees its memory
-        umma_commit(&bars[Sm::kBarDR]);
-        tc_drain(&bars[Sm::kBarDR], 0);
+      if (!(ok = wwait(&bars[Sm::kBarVF + s], (j / S) & 1))) break;
+      const uint64_t vt = dv + (uint64_t)((s * KB * 8192) >> 4);
+      for (int m = 0; m < MT && ok; ++m) {
+        if (!(ok = wwait(&bars[Sm::kBarPF + 2 * m + (j & 1)], (j >> 1) & 1))) break;
+        tc_fence_after();
+        const uint32_t pa = tmem + 128 * m + 64 * (j & 1);
+#pragma unroll
+        for (int half = 0; half < KB; ++half)
+#pragma unroll
+          for (int part = 0; part < 2; ++part)  // P_hi, then P_lo
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              umma_f16_ts_warp(tmem + 128 * MT + D * m + 64 * half, pa + 32 * part + 8 * kk,
+                               vt + (uint64_t)((half * 8192 + kk * 2048) >> 4), idesc_o,
+                               j > 0 || part > 0 || kk > 0);
+        umma_commit_warp(&bars[Sm::kBarOD + m]);
+        if (j == n - 1) umma_commit_warp(&bars[Sm::kBarOF + m]);
       }
+      if (!ok) break;
+      umma_commit_warp(&bars[Sm::kBarKE + s]);  // the stage is free once these MMAs are done
+    }
+    if (any) {  // every MMA done before the CTA frees its memory
+      umma_commit_warp(&bars[Sm::kBarDR]);
+      if (lane == 0) tc_drain(&bars[Sm::kBarDR], 0);
     }
   } else {
     // ---- softmax: one query row per thread ----
@@ -289,20 +294,29 @@ __global__ void __launch_bounds__(TcSmem<D, HC>::kThreads, 1)
     for (int j = 0; j < n; ++j) {
       const int u = j & 1;
       const uint32_t t_s = lanes + 128 * m + 64 * u;
+      const int i = list[j];
       ok = tc_wait(&bars[Sm::kBarSF + 2 * m + u], (j >> 1) & 1, fail);
       if (!(ok = __all_sync(0xffffffffu, ok))) break;  // the tensor-memory accesses are warp-wide
       tc_fence_after();
       uint32_t s[64];
       tmem_ld32_sync(t_s, *reinterpret_cast<uint32_t(*)[32]>(s));
       tmem_ld32_sync(t_s + 32, *reinterpret_cast<uint32_t(*)[32]>(s + 32));
-      const int i = list[j];
-      // last key of the block this row may see: the causal diagonal, the prompt's end
-      const int lim = i == b ? min(row & 63, p.L - 1 - i * kPrefillBlock) : kPrefillBlock - 1;
-      float mx = -CUDART_INF_F;
+      if (i == b) {
+        // the diagonal block: keys after the row's token, or past the prompt, drop out
+        const int lim = min(row & 63, p.L - 1 - i * kPrefillBlock);
 #pragma unroll
-      for (int c = 0; c < 64; ++c)
-        if (c <= lim) mx = fmaxf(mx, __uint_as_float(s[c]));
-      mx *= sc;
+        for (int c = 0; c < 64; ++c)
+          if (c > lim) s[c] = 0xff800000u;  // -inf
+      }
+      float mq[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) mq[k] = __uint_as_float(s[k]);
+#pragma unroll
+      for (int c = 4; c < 64; c += 8)
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          mq[k] = fmax3f(mq[k], __uint_as_float(s[c + 2 * k]), __uint_as_float(s[c + 2 * k + 1]));
+      const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])) * sc;
       const bool need = mx > m_run + kRescaleAbove;
       if (__any_sync(0xffffffffu, need)) {
         const float m_new = need ? mx : m_run;
@@ -324,18 +338,20 @@ __global__ void __launch_bounds__(TcSmem<D, HC>::kThreads, 1)
         l_run *= alpha;
         m_run = m_new;
       }
-      // weights exp2(s sc - m), split into high and low 16-bit parts, over S
+      // weights 2^(s sc - m) (masked keys: 2^-inf = 0), split into high and
+      // low 16-bit parts, over S
       uint32_t hi[32], lo[32];
-      float lsum = 0.f;
-      const float nm = -m_run;
+      const float2 sc2 = make_float2(sc, sc), nm2 = make_float2(-m_run, -m_run);
+      float2 ls[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
-        const float p0 = 2 * c <= lim ? exp2f(fmaf(__uint_as_float(s[2 * c]), sc, nm)) : 0.f;
-        const float p1 = 2 * c + 1 <= lim ? exp2f(fmaf(__uint_as_float(s[2 * c + 1]), sc, nm)) : 0.f;
-        lsum += p0 + p1;
-        PSplit<T>::run(p0, p1, hi[c], lo[c]);
+        const float2 x =
+            f2_fma(make_float2(__uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1])), sc2, nm2);
+        const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+        ls[c & 1] = f2_add(ls[c & 1], pp);
+        PSplit<T>::run(pp, hi[c], lo[c]);
       }
-      l_run += lsum;
+      l_run += (ls[0].x + ls[1].x) + (ls[0].y + ls[1].y);
       tmem_st32(t_s, hi);
       tmem_st32(t_s + 32, lo);
       tmem_wait_st();
