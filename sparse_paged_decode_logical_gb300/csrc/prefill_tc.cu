@@ -20,9 +20,10 @@
 // the same factor).
 //
 // Warp roles: warps 0 .. 4 MT - 1 run the softmax (matrix warp / 4, tensor
-// memory lanes 32 (warp % 4) ..), warp 4 MT issues the MMAs (the whole warp
-// runs the issue loop with warp-uniform operands, one elected lane issues),
-// warp 4 MT + 1 loads Q once and K / V into a ring of stages by TMA (4-D maps
+// memory lanes 32 (warp % 4) ..), warps 4 MT + m issue matrix m's MMAs (the
+// whole warp runs the issue loop with warp-uniform operands, one elected lane
+// issues; the tensor pipe interleaves the matrices' two independent chains),
+// warp 5 MT loads Q once and K / V into a ring of stages by TMA (4-D maps
 // over [L][heads][d], 64 x 64 boxes, 128-byte swizzle).  S_m(j + 1) runs on
 // the tensor cores while the softmax of block j runs, and the two matrices'
 // work interleaves.  Every wait is bounded: a CTA that gives up records the
@@ -67,16 +68,18 @@ struct TcSmem {
   static constexpr int kBarPF = kBarSF + 2 * MT;
   static constexpr int kBarOD = kBarPF + 2 * MT;
   static constexpr int kBarOF = kBarOD + MT;
-  static constexpr int kBarDR = kBarOF + MT;
-  static constexpr int kNumBars = kBarDR + 1;
+  static constexpr int kBarDR = kBarOF + MT;  // per MMA warp
+  static constexpr int kNumBars = kBarDR + MT;
   static constexpr int kMisc = kBars + 8 * kNumBars;  // tmem base, fail flag
   static constexpr int kBytes = kMisc + 16 + 1024;    // + alignment slack
   // tensor-memory columns: S / P of matrix m, buffer u at 128 m + 64 u;
   // O_m at 128 MT + D m
   static constexpr int kCols = MT * (128 + D);
   static constexpr int kAlloc = kCols <= 256 ? 256 : 512;
-  static constexpr int kThreads = MT * 128 + 64;
-  static constexpr int kMmaWarp = MT * 4, kLoadWarp = MT * 4 + 1;
+  // warps: softmax 0 .. 4 MT - 1, MMA issue 4 MT .. 5 MT - 1 (one per
+  // matrix), TMA 5 MT
+  static constexpr int kMmaWarp = MT * 4, kLoadWarp = MT * 5;
+  static constexpr int kThreads = (kLoadWarp + 1) * 32;
   static_assert(kBytes <= 232448, "shared memory");
   static_assert(kCols <= 512, "tensor memory");
 };
@@ -154,10 +157,12 @@ __global__ void __launch_bounds__(TcSmem<D, HC>::kThreads, 1)
   const int t0 = b * kPrefillBlock;
   const int h0 = hk * p.G + hg * HC;  // the CTA's first query head
 
-  if (warp == Sm::kMmaWarp) tmem_alloc(tmem_slot, Sm::kAlloc);
+  if (warp == Sm::kMmaWarp) tmem_alloc(tmem_slot, Sm::kAlloc);  // (the first MMA warp)
   if (tid == Sm::kLoadWarp * 32) {
     for (int x = 0; x < Sm::kNumBars; ++x)
-      mbar_init(&bars[x], (x >= Sm::kBarPF && x < Sm::kBarOD) ? 4 : 1);  // P: one per warp
+      mbar_init(&bars[x], (x >= Sm::kBarPF && x < Sm::kBarOD)   ? 4    // P: one per softmax warp
+                          : (x >= Sm::kBarKE && x < Sm::kBarSF) ? MT   // K/V empty: one per MMA warp
+                                                                : 1);
     *fail = 0;
     fence_mbar_init();
     prefetch_tmap(&p.tm_q);
@@ -212,27 +217,29 @@ __global__ void __launch_bounds__(TcSmem<D, HC>::kThreads, 1)
         }
       }
     }
-  } else if (warp == Sm::kMmaWarp) {
-    // ---- MMA issue (the whole warp, one elected lane issuing): S of block
-    // j + 1 ahead of P . V of block j ----
+  } else if (warp >= Sm::kMmaWarp) {
+    // ---- MMA issue for matrix m (the whole warp, one elected lane issuing):
+    // S_m of block j + 1 ahead of P_m . V of block j ----
+    const int m = warp - Sm::kMmaWarp;
     const bool bf = PSplit<T>::bf16;
     const uint32_t idesc_s = umma_idesc_f16(bf, 128, 64, 0, 0);  // Q . K^T: both K-major
     const uint32_t idesc_o = umma_idesc_f16(bf, 128, 64, 0, 1);  // P . V: V MN-major
     // base descriptors; a byte offset o inside the region adds o / 16
-    const uint64_t dq = umma_desc_sw128(smem_u32(smem + Sm::kQ), 16, 1024);
+    const uint64_t dq = umma_desc_sw128(smem_u32(smem + Sm::kQ + m * KB * 16384), 16, 1024);
     const uint64_t dk = umma_desc_sw128(smem_u32(smem + Sm::kK), 16, 1024);
     const uint64_t dv = umma_desc_sw128(smem_u32(smem + Sm::kV), 16, 1024);
+    const uint32_t t_o = tmem + 128 * MT + D * m;
     // every lane waits; the warp goes on only if all saw the phase
     auto wwait = [&](uint64_t *bar, uint32_t parity) {
       return __all_sync(0xffffffffu, tc_wait(bar, parity, fail));
     };
-    // S_m(j) = Q_m . K_j^T into buffer j & 1 of matrix m
-    auto issue_s = [&](int j, int m) {
+    // S_m(j) = Q_m . K_j^T into buffer j & 1
+    auto issue_s = [&](int j) {
       const uint64_t kt = dk + (uint64_t)(((j % S) * KB * 8192) >> 4);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk)
         umma_f16_warp(tmem + 128 * m + 64 * (j & 1),
-                      dq + (uint64_t)(((m * KB + (kk >> 2)) * 16384 + (kk & 3) * 32) >> 4),
+                      dq + (uint64_t)((((kk >> 2)) * 16384 + (kk & 3) * 32) >> 4),
                       kt + (uint64_t)(((kk >> 2) * 8192 + (kk & 3) * 32) >> 4), idesc_s, kk > 0);
       umma_commit_warp(&bars[Sm::kBarSF + 2 * m + (j & 1)]);
     };
@@ -240,47 +247,39 @@ __global__ void __launch_bounds__(TcSmem<D, HC>::kThreads, 1)
     const bool any = ok;
     if (ok) {
       tc_fence_after();
-      for (int m = 0; m < MT; ++m) issue_s(0, m);
+      issue_s(0);
     }
     for (int j = 0; j < n && ok; ++j) {
       const int s = j % S;
       if (j + 1 < n) {
         const int j1 = j + 1;
+        // buffer j1 & 1 held P_m(j - 1): its P . V has to be done
         if (!(ok = wwait(&bars[Sm::kBarKF + j1 % S], (j1 / S) & 1))) break;
-        for (int m = 0; m < MT && ok; ++m) {
-          // buffer j1 & 1 held P_m(j - 1): its P . V has to be done
-          if (j >= 1) ok = wwait(&bars[Sm::kBarOD + m], (j - 1) & 1);
-          if (ok) {
-            tc_fence_after();
-            issue_s(j1, m);
-          }
-        }
-        if (!ok) break;
+        if (j >= 1 && !(ok = wwait(&bars[Sm::kBarOD + m], (j - 1) & 1))) break;
+        tc_fence_after();
+        issue_s(j1);
       }
       if (!(ok = wwait(&bars[Sm::kBarVF + s], (j / S) & 1))) break;
+      if (!(ok = wwait(&bars[Sm::kBarPF + 2 * m + (j & 1)], (j >> 1) & 1))) break;
+      tc_fence_after();
       const uint64_t vt = dv + (uint64_t)((s * KB * 8192) >> 4);
-      for (int m = 0; m < MT && ok; ++m) {
-        if (!(ok = wwait(&bars[Sm::kBarPF + 2 * m + (j & 1)], (j >> 1) & 1))) break;
-        tc_fence_after();
-        const uint32_t pa = tmem + 128 * m + 64 * (j & 1);
+      const uint32_t pa = tmem + 128 * m + 64 * (j & 1);
 #pragma unroll
-        for (int half = 0; half < KB; ++half)
+      for (int half = 0; half < KB; ++half)
 #pragma unroll
-          for (int part = 0; part < 2; ++part)  // P_hi, then P_lo
+        for (int part = 0; part < 2; ++part)  // P_hi, then P_lo
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              umma_f16_ts_warp(tmem + 128 * MT + D * m + 64 * half, pa + 32 * part + 8 * kk,
-                               vt + (uint64_t)((half * 8192 + kk * 2048) >> 4), idesc_o,
-                               j > 0 || part > 0 || kk > 0);
-        umma_commit_warp(&bars[Sm::kBarOD + m]);
-        if (j == n - 1) umma_commit_warp(&bars[Sm::kBarOF + m]);
-      }
-      if (!ok) break;
-      umma_commit_warp(&bars[Sm::kBarKE + s]);  // the stage is free once these MMAs are done
+          for (int kk = 0; kk < 4; ++kk)
+            umma_f16_ts_warp(t_o + 64 * half, pa + 32 * part + 8 * kk,
+                             vt + (uint64_t)((half * 8192 + kk * 2048) >> 4), idesc_o,
+                             j > 0 || part > 0 || kk > 0);
+      umma_commit_warp(&bars[Sm::kBarOD + m]);
+      if (j == n - 1) umma_commit_warp(&bars[Sm::kBarOF + m]);
+      umma_commit_warp(&bars[Sm::kBarKE + s]);  // the stage is free once both warps' MMAs are done
     }
-    if (any) {  // every MMA done before the CTA frees its memory
-      umma_commit_warp(&bars[Sm::kBarDR]);
-      if (lane == 0) tc_drain(&bars[Sm::kBarDR], 0);
+    if (any) {  // every MMA of this warp done before the CTA frees its memory
+      umma_commit_warp(&bars[Sm::kBarDR + m]);
+      if (lane == 0) tc_drain(&bars[Sm::kBarDR + m], 0);
     }
   } else {
     // ---- softmax: one query row per thread ----
