@@ -120,16 +120,46 @@ __global__ void __launch_bounds__(kSelThreads) prefill_select_kernel(const __gri
   } else {
     cnt = p.kblocks;
     TopkSmem m = carve_topk_smem(sel_smem);
-    for (int i = tid; i < b; i += kSelThreads) {
-      float best = -CUDART_INF_F;
-      for (int g = 0; g < p.G; ++g) {
-        const float *qb = p.qbar + (((size_t)hk * p.G + g) * p.nb + b) * p.r;
-        const float *kb = p.kbar + ((size_t)hk * p.nb + i) * p.r;
-        float acc = 0.f;
-        for (int j = 0; j < p.r; ++j) acc = fmaf(qb[j], kb[j], acc);
-        best = fmaxf(best, acc * p.score_scale);
+    if (p.r == 16 && p.G <= 8) {
+      // the common rank: the query block's G projected means in shared
+      // memory (broadcast reads), each candidate's row as four 16-byte loads
+      __shared__ float4 s_q[8 * 4];
+      if (tid < p.G * 4)
+        s_q[tid] = reinterpret_cast<const float4 *>(
+            p.qbar + (((size_t)hk * p.G + tid / 4) * p.nb + b) * 16)[tid % 4];
+      __syncthreads();
+      const float4 *kb = reinterpret_cast<const float4 *>(p.kbar + (size_t)hk * p.nb * 16);
+      for (int i = tid; i < b; i += kSelThreads) {
+        float4 kr[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) kr[c] = kb[(size_t)i * 4 + c];
+        float best = -CUDART_INF_F;
+        for (int g = 0; g < p.G; ++g) {
+          float acc = 0.f;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const float4 q = s_q[4 * g + c];
+            acc = fmaf(q.x, kr[c].x, acc);
+            acc = fmaf(q.y, kr[c].y, acc);
+            acc = fmaf(q.z, kr[c].z, acc);
+            acc = fmaf(q.w, kr[c].w, acc);
+          }
+          best = fmaxf(best, acc * p.score_scale);
+        }
+        m.skey[i] = score_key(best);
       }
-      m.skey[i] = score_key(best);
+    } else {
+      for (int i = tid; i < b; i += kSelThreads) {
+        float best = -CUDART_INF_F;
+        for (int g = 0; g < p.G; ++g) {
+          const float *qb = p.qbar + (((size_t)hk * p.G + g) * p.nb + b) * p.r;
+          const float *kb = p.kbar + ((size_t)hk * p.nb + i) * p.r;
+          float acc = 0.f;
+          for (int j = 0; j < p.r; ++j) acc = fmaf(qb[j], kb[j], acc);
+          best = fmaxf(best, acc * p.score_scale);
+        }
+        m.skey[i] = score_key(best);
+      }
     }
     __syncthreads();
     const int k = p.kblocks - 1;  // 1 <= k < b

@@ -298,8 +298,7 @@ __global__ void __launch_bounds__(TcSmem<D, HC>::kThreads, 1)
       if (!(ok = __all_sync(0xffffffffu, ok))) break;  // the tensor-memory accesses are warp-wide
       tc_fence_after();
       uint32_t s[64];
-      tmem_ld32_sync(t_s, *reinterpret_cast<uint32_t(*)[32]>(s));
-      tmem_ld32_sync(t_s + 32, *reinterpret_cast<uint32_t(*)[32]>(s + 32));
+      tmem_ld64_sync(t_s, s);
       if (i == b) {
         // the diagonal block: keys after the row's token, or past the prompt, drop out
         const int lim = min(row & 63, p.L - 1 - i * kPrefillBlock);
