@@ -709,7 +709,8 @@ def host_cost(layers, stream, n_steps):
 
 # the sources the decode kernel is compiled from (its traffic figure is valid
 # while they are unchanged)
-DECODE_SOURCES = ("decode.cu", "decode_kernel.cuh", "ptx.cuh", "spd_internal.h", "topk.cuh")
+DECODE_SOURCES = ("decode.cu", "decode_reuse.cu", "decode_kernel.cuh", "ptx.cuh", "spd_internal.h",
+                  "topk.cuh")
 
 
 def kernel_hash():

@@ -64,6 +64,7 @@ cudaError_t prepare_decode_kernels() {
   // the mass-exporting and fp8 instances: same block; their cluster sizes are
   // taken to be the plain kernel's (the fp8 ones need no more shared memory)
   if ((e = prepare_decode_mass_kernels()) != cudaSuccess) return e;
+  if ((e = prepare_decode_reuse_kernels()) != cudaSuccess) return e;
   return prepare_decode_fp8_kernels();
 }
 
@@ -86,6 +87,9 @@ cudaError_t launch_decode_tiles(const TileDecodeParams &p, int dtype, int d, int
   *n += 1;
   if (p.kv_fp8) return d == 128 ? launch_decode_tiles_fp8(p, dtype, G, s) : cudaErrorInvalidValue;
   if (p.page_part != nullptr) return launch_decode_tiles_mass(p, dtype, d, G, s);
+  bool selects = false;  // does any unit of this launch select its pages?
+  for (int i = 0; i < p.n_seqs && !selects; ++i) selects = p.seqs[i].topk_n > 0;
+  if (!selects) return launch_decode_tiles_reuse(p, dtype, d, G, s);
   if (p.deep) return launch_variant<false, true>(p, dtype, d, G, s);
   return launch_variant<false>(p, dtype, d, G, s);
 }

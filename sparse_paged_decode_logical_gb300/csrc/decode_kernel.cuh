@@ -229,7 +229,11 @@ __device__ void write_page_mass(const TileDecodeParams &p, int i, int sub, const
 // codes of value / scale (head_dim 128): tiles are half the bytes, widened
 // exactly on their way into the tensor-core fragments: keys to fp16 for fp16
 // q.K products (q narrowed to fp16 once), values to T for the P.V products.
-template <typename T, int D, int G, bool kMass, bool kF8 = false, bool kDeep = false>
+// kReuse: an instance for launches in which no unit selects its pages (the
+// steps that reuse a stored selection), built without the fused top-k code so
+// the code a launch runs once stays small.
+template <typename T, int D, int G, bool kMass, bool kF8 = false, bool kDeep = false,
+          bool kReuse = false>
 __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_constant__ TileDecodeParams p) {
   static_assert(!kF8 || D == 128, "fp8 storage: one 128-byte row per token");
   // tensor-core element types.  q.K: T, or fp16 with fp8 storage (an E4M3
@@ -323,7 +327,10 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
   const bool owns_newest = nt > 0 && tile0 + nt == n_tiles;
   const bool do_append = p.k_new != nullptr && owns_newest;
   // (a unit that selects its pages here reads this step's scores: never early)
-  const bool early = ((p.early >> (dyn ? 0 : 1)) & 1) && !(dyn && s.topk_n > 0);
+  // this unit selects its pages here (never in a reuse instance: the host
+  // launches one only when no unit of the launch selects)
+  const bool selects = !kReuse && dyn && s.topk_n > 0;
+  const bool early = ((p.early >> (dyn ? 0 : 1)) & 1) && !selects;
   // bit 2: the previous kernel is this context's own selection or page-table
   // kernel, which writes nothing a streaming unit reads; q is final once that
   // kernel runs (it waited for its own predecessor before releasing this one)
@@ -361,7 +368,7 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
   // kernel, after the page-table flush had finished: the sequence's page
   // table is final, so it is copied to shared memory before the wait.
   int *pt_s = nullptr;
-  if (dyn && s.topk_n > 0 && p.max_pp <= Sm::kPtCache) {
+  if (selects && p.max_pp <= Sm::kPtCache) {
     pt_s = reinterpret_cast<int *>(stages + Sm::kPtCacheOff);
     const int *row = p.page_table + (size_t)s.slot * p.max_pp;
     for (int x = tid; x < p.max_pp; x += kThreads) pt_s[x] = row[x];
@@ -375,7 +382,9 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
   // (every CTA of the unit computes the same selection from the same scores;
   // the stage region holds the work and the result until the tiles arrive)
   const int *sel_s = nullptr;
-  if (dyn && s.topk_n > 0) {
+  if constexpr (kReuse) {
+    if (dyn && s.topk_n > 0 && tid == 0) set_err(p.err, kDevBadSelection, s.slot, sub, -1);
+  } else if (selects) {
     TopkSmem tm = carve_topk_smem(stages);
     tm.bar = reinterpret_cast<uint64_t *>(smem + Sm::kTopkBar);  // never repurposed
     int *list = reinterpret_cast<int *>(stages + kTopkSmemBytes);
@@ -1090,9 +1099,10 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
 }
 
 
-template <typename T, int D, int G, bool kMass, bool kF8 = false, bool kDeep = false>
+template <typename T, int D, int G, bool kMass, bool kF8 = false, bool kDeep = false,
+          bool kReuse = false>
 cudaError_t set_smem_attrs() {
-  auto k = decode_tiles_kernel<T, D, G, kMass, kF8, kDeep>;
+  auto k = decode_tiles_kernel<T, D, G, kMass, kF8, kDeep, kReuse>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        Smem<D, G, kF8, kDeep>::kAlloc);
   if (e != cudaSuccess) return e;
@@ -1119,32 +1129,33 @@ cudaError_t set_smem_attrs_all() {
   return set_smem_attrs_g<__nv_bfloat16, 128, kMass>();
 }
 
-template <typename T, int D, int G, bool kMass, bool kF8 = false, bool kDeep = false>
+template <typename T, int D, int G, bool kMass, bool kF8 = false, bool kDeep = false,
+          bool kReuse = false>
 cudaError_t launch_one(const TileDecodeParams &p, cudaStream_t st) {
-  cudaError_t e = launch_pdl_cluster(decode_tiles_kernel<T, D, G, kMass, kF8, kDeep>,
+  cudaError_t e = launch_pdl_cluster(decode_tiles_kernel<T, D, G, kMass, kF8, kDeep, kReuse>,
                                      p.total_items, kThreads,
                                      (size_t)Smem<D, G, kF8, kDeep>::kAlloc, p.cluster, st, p);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-template <typename T, int D, bool kMass, bool kDeep = false>
+template <typename T, int D, bool kMass, bool kDeep = false, bool kReuse = false>
 cudaError_t launch_g(const TileDecodeParams &p, int G, cudaStream_t st) {
   switch (G) {
-    case 1: return launch_one<T, D, 1, kMass, false, kDeep>(p, st);
-    case 2: return launch_one<T, D, 2, kMass, false, kDeep>(p, st);
-    case 4: return launch_one<T, D, 4, kMass, false, kDeep>(p, st);
-    case 8: return launch_one<T, D, 8, kMass, false, kDeep>(p, st);
+    case 1: return launch_one<T, D, 1, kMass, false, kDeep, kReuse>(p, st);
+    case 2: return launch_one<T, D, 2, kMass, false, kDeep, kReuse>(p, st);
+    case 4: return launch_one<T, D, 4, kMass, false, kDeep, kReuse>(p, st);
+    case 8: return launch_one<T, D, 8, kMass, false, kDeep, kReuse>(p, st);
     default: return cudaErrorInvalidValue;
   }
 }
 
-template <bool kMass, bool kDeep = false>
+template <bool kMass, bool kDeep = false, bool kReuse = false>
 cudaError_t launch_variant(const TileDecodeParams &p, int dtype, int d, int G, cudaStream_t s) {
   if (dtype == 0)
-    return d == 64 ? launch_g<__half, 64, kMass, kDeep>(p, G, s)
-                   : launch_g<__half, 128, kMass, kDeep>(p, G, s);
-  return d == 64 ? launch_g<__nv_bfloat16, 64, kMass, kDeep>(p, G, s)
-                 : launch_g<__nv_bfloat16, 128, kMass, kDeep>(p, G, s);
+    return d == 64 ? launch_g<__half, 64, kMass, kDeep, kReuse>(p, G, s)
+                   : launch_g<__half, 128, kMass, kDeep, kReuse>(p, G, s);
+  return d == 64 ? launch_g<__nv_bfloat16, 64, kMass, kDeep, kReuse>(p, G, s)
+                 : launch_g<__nv_bfloat16, 128, kMass, kDeep, kReuse>(p, G, s);
 }
 
 }  // namespace

@@ -179,6 +179,10 @@ cudaError_t prepare_decode_kernels();
 cudaError_t prepare_decode_mass_kernels();  // called by prepare_decode_kernels()
 cudaError_t launch_decode_tiles_mass(const TileDecodeParams &p, int dtype, int d, int G,
                                      cudaStream_t s);
+cudaError_t prepare_decode_reuse_kernels();  // called by prepare_decode_kernels()
+// the plain 16-bit decode for launches in which no unit selects its pages
+cudaError_t launch_decode_tiles_reuse(const TileDecodeParams &p, int dtype, int d, int G,
+                                      cudaStream_t s);
 cudaError_t prepare_decode_fp8_kernels();  // called by prepare_decode_kernels()
 cudaError_t launch_decode_tiles_fp8(const TileDecodeParams &p, int dtype, int G,
                                     cudaStream_t s);
