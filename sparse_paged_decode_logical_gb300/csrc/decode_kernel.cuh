@@ -923,49 +923,41 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
   const int unit = i * p.Hkv + h;
   float *out = p.out + ((size_t)i * p.Hq + h * G) * D;
   const size_t cpart = (size_t)unit_item0 + (size_t)ci * CS;  // global slot of this cluster
-  // TPE adjacent lanes share one output element and split the CS ranks
-  // between them (fewer serial steps than one lane walking all ranks)
+  // one thread per output element of the slice, all ranks' values loaded at
+  // once (independent loads, then short max and sum chains: shorter than
+  // splitting the ranks over lanes and reducing with shuffles)
   const int E = G * slice;
-  int TPE = 1;
-  while (TPE * 2 <= CS && E * TPE * 2 <= kThreads) TPE *= 2;
-  const int ltpe = __ffs(TPE) - 1;
-  for (int base = 0; base < E * TPE; base += kThreads) {
-    const int xt = base + tid, x = xt >> ltpe, r0 = xt & (TPE - 1);
-    const bool valid = x < E;
-    const int g = valid ? x >> lsl : 0, cl = valid ? x & (slice - 1) : 0, c = rank * slice + cl;
-    float M = -CUDART_INF_F;
-    if (valid)
-      for (int r = r0; r < CS; r += TPE) M = fmaxf(M, in_M[r * G + g]);
-    for (int o = 1; o < TPE; o <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  for (int x = tid; x < E; x += kThreads) {
+    const int g = x >> lsl, cl = x & (slice - 1), c = rank * slice + cl;
+    float mr[16];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) mr[r] = r < CS ? in_M[r * G + g] : -CUDART_INF_F;
+    float M = mr[0];
+#pragma unroll
+    for (int r = 1; r < 16; ++r) M = fmaxf(M, mr[r]);
     float O = 0.f, Ls = 0.f;
-    if (valid && M != -CUDART_INF_F)
-      for (int r = r0; r < CS; r += TPE) {
-        const float mr = in_M[r * G + g];
-        if (mr != -CUDART_INF_F) {
-          const float f = exp2f(mr - M);
+    if (M != -CUDART_INF_F) {
+#pragma unroll
+      for (int r = 0; r < 16; ++r)
+        if (mr[r] != -CUDART_INF_F) {  // (ranks >= CS hold -inf)
+          const float f = exp2f(mr[r] - M);
           Ls = fmaf(f, in_L[r * G + g], Ls);
           O = fmaf(f, in_O[r * (E + 4) + g * slice + cl], O);
         }
-      }
-    for (int o = 1; o < TPE; o <<= 1) {
-      O += __shfl_xor_sync(0xffffffffu, O, o);
-      Ls += __shfl_xor_sync(0xffffffffu, Ls, o);
     }
-    if (valid && r0 == 0) {
-      if (nc == 1) {
-        // (fp8: the stored values are code * v_scale)
-        out[g * D + c] = kF8 ? O / Ls * p.v_scale[h] : O / Ls;
-        if (p.row_max && rank == 0 && cl == 0) {
-          // the logits' max in natural units (M is base 2, scale folded in)
-          // and the sum of exp(z - max) over the attended tokens
-          const size_t hq = (size_t)i * p.Hq + h * G + g;
-          p.row_max[hq] = M * 0.6931471805599453f;
-          p.row_sum[hq] = Ls;
-        }
-      } else {
-        p.part_o[(cpart * G + g) * D + c] = O;
-        if (rank == 0 && cl == 0) p.part_ml[cpart * G + g] = make_float2(M, Ls);
+    if (nc == 1) {
+      // (fp8: the stored values are code * v_scale)
+      out[g * D + c] = kF8 ? O / Ls * p.v_scale[h] : O / Ls;
+      if (p.row_max && rank == 0 && cl == 0) {
+        // the logits' max in natural units (M is base 2, scale folded in)
+        // and the sum of exp(z - max) over the attended tokens
+        const size_t hq = (size_t)i * p.Hq + h * G + g;
+        p.row_max[hq] = M * 0.6931471805599453f;
+        p.row_sum[hq] = Ls;
       }
+    } else {
+      p.part_o[(cpart * G + g) * D + c] = O;
+      if (rank == 0 && cl == 0) p.part_ml[cpart * G + g] = make_float2(M, Ls);
     }
   }
   if (nc == 1) {

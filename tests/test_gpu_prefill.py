@@ -180,3 +180,12 @@ def test_prefill_full_size_one_token_below_the_threshold_is_dense():
     # 32767 tokens: one below the threshold, every causal block attended
     _check_full(32767, 4, 1, 128, 16, "f16", budget=4096, dense_below=32768, seed=12,
                 sample=[0, 255, 511])
+
+
+@needs_gpu
+def test_prefill_full_size_eight_heads_per_kv_head_fp16():
+    # 40,000 tokens (625 blocks, the last partial), 8 query heads per kv head
+    # (two CTAs per query block and kv head on the tensor-core path), fp16
+    # (the rounded 16-bit high part of P), budget 2048 = 32 kept blocks
+    _check_full(40000, 16, 2, 128, 16, "f16", budget=2048, dense_below=32768, seed=13,
+                sample=[0, 31, 32, 400, 624])
