@@ -62,9 +62,10 @@
 // (separate translation units, built in parallel).
 #pragma once
 #include <cuda_bf16.h>
-#include <type_traits>
 #include <cuda_fp16.h>
 #include <math_constants.h>
+
+#include <type_traits>
 
 #include "ptx.cuh"
 #include "spd_internal.h"
@@ -238,9 +239,12 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
   static_assert(!kF8 || D == 128, "fp8 storage: one 128-byte row per token");
   // tensor-core element types.  q.K: T, or fp16 with fp8 storage (an E4M3
   // value widens to fp16 in one instruction; q is narrowed to fp16 once).
-  // P.V: T, so that the softmax weights keep T's exponent range.
+  // P.V: T; with fp8 storage fp16 (an E4M3 value widens to fp16 in one
+  // instruction; the weights are at most 1, and their fp16 high and low parts
+  // carry ~2^-22 of each, flushing only weights below 2^-24).
   constexpr bool kQkBf = kF8 ? false : IsBF16<T>::v;
-  constexpr bool kPvBf = IsBF16<T>::v;
+  constexpr bool kPvBf = kF8 ? false : IsBF16<T>::v;
+  using TP = typename std::conditional<kF8, __half, T>::type;  // P.V element type
   using Gm = Geo<D, kF8>;
   using Sm = Smem<D, G, kF8, kDeep>;
   constexpr int kStages = Sm::kStages;
@@ -768,9 +772,9 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
         uint16_t hi[4], lo[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const T th = Cvt<T>::from(pv[e]);
+          const TP th = Cvt<TP>::from(pv[e]);
           hi[e] = *reinterpret_cast<const uint16_t *>(&th);
-          const T tl = Cvt<T>::from(pv[e] - tof(th));
+          const TP tl = Cvt<TP>::from(pv[e] - tof(th));
           lo[e] = *reinterpret_cast<const uint16_t *>(&tl);
         }
         bh0 = (uint32_t)hi[0] | ((uint32_t)hi[1] << 16);
@@ -792,12 +796,12 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
           ldmatrix_x4_trans(vbase + swz128(row, 2 * m2 + chalf), r0, r1, r2, r3);
           const uint32_t e0 = __byte_perm(r0, 0u, 0x3120), e1 = __byte_perm(r1, 0u, 0x3120);
           const uint32_t e2 = __byte_perm(r2, 0u, 0x3120), e3 = __byte_perm(r3, 0u, 0x3120);
-          const uint32_t a0[4] = {e4m3x2_to<T>(e0), e4m3x2_to<T>(e0 >> 16), e4m3x2_to<T>(e1),
-                                  e4m3x2_to<T>(e1 >> 16)};
+          const uint32_t a0[4] = {e4m3x2_to<TP>(e0), e4m3x2_to<TP>(e0 >> 16), e4m3x2_to<TP>(e1),
+                                  e4m3x2_to<TP>(e1 >> 16)};
           mma_16816<kPvBf>(oacc[2 * m2], a0, bh0, bh1);
           mma_16816<kPvBf>(oacc[2 * m2], a0, bl0, bl1);
-          const uint32_t a1[4] = {e4m3x2_to<T>(e2), e4m3x2_to<T>(e2 >> 16), e4m3x2_to<T>(e3),
-                                  e4m3x2_to<T>(e3 >> 16)};
+          const uint32_t a1[4] = {e4m3x2_to<TP>(e2), e4m3x2_to<TP>(e2 >> 16), e4m3x2_to<TP>(e3),
+                                  e4m3x2_to<TP>(e3 >> 16)};
           mma_16816<kPvBf>(oacc[2 * m2 + 1], a1, bh0, bh1);
           mma_16816<kPvBf>(oacc[2 * m2 + 1], a1, bl0, bl1);
         }
