@@ -324,6 +324,12 @@ class SparsePagedKVCache:
         self.ctx = spd_create(self.cfg, addrs)
         self.Hq, self.Hkv, self.d = cfg["num_q_heads"], cfg["num_kv_heads"], cfg["head_dim"]
         self.dtype = torch.bfloat16 if DTYPES[cfg["dtype"]] == 1 else torch.float16
+        # per-call marshalling state: the device index as an int, the raw
+        # current-stream query, ctypes id arrays by id tuple, the entry point
+        self._dev_index = self.device.index
+        self._raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+        self._ids_cache = {}
+        self._step_fn = lib().spd_decode_step
 
     def __del__(self):
         ctx = getattr(self, "ctx", None)
@@ -333,12 +339,14 @@ class SparsePagedKVCache:
 
     def _stream(self, stream):
         if stream is None:
+            if self._raw_stream is not None:
+                return self._raw_stream(self._dev_index)
             stream = self.torch.cuda.current_stream(self.device)
         return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
     def _ptr(self, t, shape, dtype):
-        if tuple(t.shape) != tuple(shape) or t.dtype != dtype or not t.is_contiguous() \
-                or t.device != self.device:
+        if t.shape != shape or t.dtype != dtype or not t.is_contiguous() \
+                or t.get_device() != self._dev_index:
             raise ValueError("expected contiguous %s tensor %s on %s, got %s %s on %s"
                              % (dtype, tuple(shape), self.device, t.dtype, tuple(t.shape),
                                 t.device))
@@ -432,7 +440,13 @@ class SparsePagedKVCache:
         return out, rm, rs, pages, mass
 
     def decode_step(self, q, k, v, seq_ids, out=None, stream=None):
-        n = len(seq_ids)
+        key = tuple(seq_ids)
+        ids = self._ids_cache.get(key)
+        if ids is None:
+            ids = _ids(key)
+            if len(self._ids_cache) < 1024:
+                self._ids_cache[key] = ids
+        n = ids[1]
         qp = self._ptr(q, (n, self.Hq, self.d), self.dtype)
         kp = self._ptr(k, (n, self.Hkv, self.d), self.dtype)
         vp = self._ptr(v, (n, self.Hkv, self.d), self.dtype)
@@ -440,7 +454,9 @@ class SparsePagedKVCache:
             out = self.torch.empty((n, self.Hq, self.d), dtype=self.torch.float32,
                                    device=self.device)
         op = self._ptr(out, (n, self.Hq, self.d), self.torch.float32)
-        spd_decode_step(self.ctx, qp, kp, vp, seq_ids, op, self._stream(stream))
+        st = self._step_fn(self.ctx, qp, kp, vp, ids[0], n, op, self._stream(stream) or None)
+        if st != SPD_OK:
+            _check(st, "spd_decode_step", self.ctx)
         return out
 
     def selection(self, seq_id, kv_head, stream=None):
