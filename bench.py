@@ -600,7 +600,7 @@ def roofline(layers, stream, iters):
             if ":" in ln and not ln.startswith("#"):
                 k, v = ln.split(":", 1)
                 kv[k.strip()] = v.strip()
-        if kv.get("kernel_source_hash") == kernel_hash() and \
+        if kv.get("kernel_source_hash") == kernel_hash() and layers.elem == 2 and \
                 kv.get("workload", "llama3_8b_b1_128k") == layers.wl.name:
             try:
                 traffic = float(kv["traffic_bytes_per_launch"])
