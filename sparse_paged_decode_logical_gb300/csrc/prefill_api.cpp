@@ -57,6 +57,10 @@ spd_status layout(const spd_prefill_config *c, int L, PrefillLayout *z) {
 
 bool aligned(const void *p, uintptr_t a) { return p && reinterpret_cast<uintptr_t>(p) % a == 0; }
 
+spd_status enqueue(const spd_prefill_config *cfg, int seq_len, const PrefillLayout &z,
+                   const void *q, const void *k, const void *v, const float *w_q,
+                   const float *w_k, float *out, int *blocks, void *workspace, spd_stream stream);
+
 // TMA map over Q, K or V ([L][heads][d], 16-bit) for the tensor-core
 // attention: {64 channels, d / 64, heads, L}; one box is 64 tokens x 64
 // channels of one head, stored in shared memory as 64 rows of 128 bytes with
@@ -118,7 +122,22 @@ spd_status spd_prefill_block_sparse_attention(const spd_prefill_config *cfg, int
     (void)cudaGetLastError();
     return SPD_ERR_INVALID_ARG;
   }
-  if (cudaSetDevice(a.device) != cudaSuccess) return SPD_ERR_CUDA;
+  // the workspace's device for the launches, the caller's again afterwards
+  int prev = -1;
+  if (cudaGetDevice(&prev) != cudaSuccess) return SPD_ERR_CUDA;
+  if (prev != a.device && cudaSetDevice(a.device) != cudaSuccess) return SPD_ERR_CUDA;
+  const spd_status r = enqueue(cfg, seq_len, z, q, k, v, w_q, w_k, out, blocks, workspace, stream);
+  if (prev != a.device) (void)cudaSetDevice(prev);
+  return r;
+}
+
+}  // extern "C"
+
+namespace {
+
+spd_status enqueue(const spd_prefill_config *cfg, int seq_len, const PrefillLayout &z,
+                   const void *q, const void *k, const void *v, const float *w_q,
+                   const float *w_k, float *out, int *blocks, void *workspace, spd_stream stream) {
   cudaStream_t st = (cudaStream_t)stream;
   char *ws = static_cast<char *>(workspace);
   if (cudaMemsetAsync(ws, 0, 16, st) != cudaSuccess) return SPD_ERR_CUDA;
@@ -152,6 +171,10 @@ spd_status spd_prefill_block_sparse_attention(const spd_prefill_config *cfg, int
   return spd::launch_prefill(p, cfg->dtype, cfg->head_dim, st) == cudaSuccess ? SPD_OK
                                                                               : SPD_ERR_CUDA;
 }
+
+}  // namespace
+
+extern "C" {
 
 spd_status spd_prefill_check(const void *workspace, spd_stream stream) {
   if (!aligned(workspace, 256)) return SPD_ERR_INVALID_ARG;
