@@ -838,6 +838,8 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
   }
 
   // ---- merge the warps into this CTA's (M, L, O) ----
+  // (fp8: the output scale is read now, its latency hidden by the merges)
+  const float vsc = kF8 ? p.v_scale[h] : 1.f;
 #pragma unroll
   for (int off = 4; off < 32; off <<= 1) {
     l0 += __shfl_xor_sync(0xffffffffu, l0, off);
@@ -927,31 +929,44 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
   const int unit = i * p.Hkv + h;
   float *out = p.out + ((size_t)i * p.Hq + h * G) * D;
   const size_t cpart = (size_t)unit_item0 + (size_t)ci * CS;  // global slot of this cluster
-  // one thread per output element of the slice, all ranks' values loaded at
-  // once (independent loads, then short max and sum chains: shorter than
-  // splitting the ranks over lanes and reducing with shuffles)
+  // one thread per output element of the slice.  Every rank's (m, l, o) is
+  // loaded up front with no branch between the loads (independent loads,
+  // then short max and sum chains: shorter than splitting the ranks over
+  // lanes and reducing with shuffles).  A rank that attended nothing pushed
+  // m = -inf, l = 0, o = 0 and ranks >= CS read as the same, so its weight
+  // exp2(-inf - M) is 0 and adds exactly nothing.
   const int E = G * slice;
   for (int x = tid; x < E; x += kThreads) {
     const int g = x >> lsl, cl = x & (slice - 1), c = rank * slice + cl;
-    float mr[16];
+    float mr[16], lr[16], orr[16];
 #pragma unroll
-    for (int r = 0; r < 16; ++r) mr[r] = r < CS ? in_M[r * G + g] : -CUDART_INF_F;
+    for (int r = 0; r < 16; ++r) {
+      const bool in = r < CS;
+      mr[r] = in ? in_M[r * G + g] : -CUDART_INF_F;
+      lr[r] = in ? in_L[r * G + g] : 0.f;
+      orr[r] = in ? in_O[r * (E + 4) + g * slice + cl] : 0.f;
+    }
     float M = mr[0];
 #pragma unroll
     for (int r = 1; r < 16; ++r) M = fmaxf(M, mr[r]);
     float O = 0.f, Ls = 0.f;
     if (M != -CUDART_INF_F) {
+      // two chains each for the sums (even and odd ranks)
+      float O1 = 0.f, L1 = 0.f;
 #pragma unroll
-      for (int r = 0; r < 16; ++r)
-        if (mr[r] != -CUDART_INF_F) {  // (ranks >= CS hold -inf)
-          const float f = exp2f(mr[r] - M);
-          Ls = fmaf(f, in_L[r * G + g], Ls);
-          O = fmaf(f, in_O[r * (E + 4) + g * slice + cl], O);
-        }
+      for (int r = 0; r < 16; r += 2) {
+        const float f0 = exp2f(mr[r] - M), f1 = exp2f(mr[r + 1] - M);
+        Ls = fmaf(f0, lr[r], Ls);
+        O = fmaf(f0, orr[r], O);
+        L1 = fmaf(f1, lr[r + 1], L1);
+        O1 = fmaf(f1, orr[r + 1], O1);
+      }
+      O += O1;
+      Ls += L1;
     }
     if (nc == 1) {
       // (fp8: the stored values are code * v_scale)
-      out[g * D + c] = kF8 ? O / Ls * p.v_scale[h] : O / Ls;
+      out[g * D + c] = kF8 ? O / Ls * vsc : O / Ls;
       if (p.row_max && rank == 0 && cl == 0) {
         // the logits' max in natural units (M is base 2, scale folded in)
         // and the sum of exp(z - max) over the attended tokens
@@ -1077,7 +1092,7 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
   for (int j = 0; j < OPT4; ++j) {
     const int x4 = tid + kThreads * j;
     if (x4 < G * D / 4) {
-      const float inv = (kF8 ? p.v_scale[h] : 1.f) / Lh[(4 * x4) / D];
+      const float inv = vsc / Lh[(4 * x4) / D];
       reinterpret_cast<float4 *>(out)[x4] =
           make_float4(acc_o[j].x * inv, acc_o[j].y * inv, acc_o[j].z * inv, acc_o[j].w * inv);
     }
