@@ -4,9 +4,12 @@
 //
 // One CTA per (query block b, kv head, group of HC query heads), HC = 2 or 4:
 // its HC x 64 query rows are MT = HC / 2 matrices of 128 rows (two heads x
-// the block's 64 tokens each).  Per chosen key block j (ascending):
-//   S_m  = Q_m . K_j^T          tcgen05.mma, M 128 x N 64 x K d, fp32 in
-//                               tensor memory (two buffers per matrix)
+// the block's 64 tokens each).  The chosen key blocks (ascending) go in
+// pairs; per pair:
+//   S_m  = Q_m . K^T            one tcgen05.mma chain over both blocks, M 128 x
+//                               N 128 x K d (N 64 for a lone last block),
+//                               fp32 in tensor memory, block u in columns
+//                               64 u ..; per block j of the pair:
 //   softmax, one row per thread: its 64 logits from tensor memory, the
 //        causal mask on the diagonal block (and keys past the prompt), an
 //        online max and sum in fp32 (base 2), and P written back over S in
@@ -23,12 +26,15 @@
 // memory lanes 32 (warp % 4) ..), warps 4 MT + m issue matrix m's MMAs (the
 // whole warp runs the issue loop with warp-uniform operands, one elected lane
 // issues; the tensor pipe interleaves the matrices' two independent chains),
-// warp 5 MT loads Q once and K / V into a ring of stages by TMA (4-D maps
-// over [L][heads][d], 64 x 64 boxes, 128-byte swizzle).  S_m(j + 1) runs on
-// the tensor cores while the softmax of block j runs, and the two matrices'
-// work interleaves.  Every wait is bounded: a CTA that gives up records the
-// error, lets the other roles leave, waits (bounded) for its copies and MMAs
-// in flight and frees its tensor memory.
+// warp 5 MT loads Q once and K / V into a two-stage ring, a pair of blocks
+// per stage, by TMA (4-D maps over [L][heads][d], 64 x 64 boxes, 128-byte
+// swizzle).  One N 128 chain for S reads Q once per two blocks (an N 64 MMA
+// with both operands in shared memory is bound by shared-memory bandwidth);
+// P . V of a pair's first block runs while the softmax of its second runs;
+// matrix 1 starts once matrix 0's first softmax is done, so the matrices'
+// softmax phases and tensor work alternate.  Every wait is bounded: a CTA
+// that gives up records the error, lets the other roles leave, waits
+// (bounded) for its copies and MMAs in flight and frees its tensor memory.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <math_constants.h>
@@ -49,27 +55,33 @@ template <int D, int HC>
 struct TcSmem {
   static constexpr int MT = HC / 2;                 // 128-row matrices of the CTA
   static constexpr int KB = D / 64;                 // 64-column sub-tiles of a row
-  static constexpr int kStages = 4;                 // K / V ring
+  static constexpr int kStages = 2;                 // K / V ring, a pair of blocks per stage
+  static constexpr int kStageBytes = KB * 16384;    // K (or V) of two 64-row blocks
   static constexpr int kQ = 0;                      // [MT][KB][128 x 128 B]
-  static constexpr int kK = kQ + MT * KB * 16384;   // [stage][KB][64 x 128 B]
-  static constexpr int kV = kK + kStages * KB * 8192;
-  static constexpr int kBars = kV + kStages * KB * 8192;
-  // mbarriers: Q, K full, V full, K/V empty (per stage), S full and P full
-  // (per matrix and buffer), O done (per matrix and block), O final (per
-  // matrix, once), drain.  A parity wait only tells apart phases one apart:
-  // every waiter below is at most one completion behind the barrier, which
-  // is why the end of O has a barrier of its own (the softmax can finish its
-  // last block while O done is still two completions short).
+  static constexpr int kK = kQ + MT * KB * 16384;   // [stage][KB][block u][64 x 128 B]
+  static constexpr int kV = kK + kStages * kStageBytes;  // [stage][block u][KB][64 x 128 B]
+  static constexpr int kBars = kV + kStages * kStageBytes;
+  // mbarriers: Q, K full, V full, K/V empty (per stage), S full (per matrix,
+  // once per pair), P full (per matrix and block of the pair), O done (per
+  // matrix and block), pair done (per matrix and pair), O final (per matrix,
+  // once), drain.  A parity wait only tells apart phases one apart: every
+  // waiter below is at most one completion behind the barrier, which is why
+  // the end of O and the end of a pair have barriers of their own (O done
+  // completes once per block: a wait for the second block of a pair, or for
+  // the last block, could otherwise meet a phase two completions back).
   static constexpr int kBarQ = 0;
   static constexpr int kBarKF = 1;
   static constexpr int kBarVF = kBarKF + kStages;
   static constexpr int kBarKE = kBarVF + kStages;
   static constexpr int kBarSF = kBarKE + kStages;
-  static constexpr int kBarPF = kBarSF + 2 * MT;
+  static constexpr int kBarPF = kBarSF + MT;
   static constexpr int kBarOD = kBarPF + 2 * MT;
-  static constexpr int kBarOF = kBarOD + MT;
+  static constexpr int kBarOP = kBarOD + MT;
+  static constexpr int kBarOF = kBarOP + MT;
   static constexpr int kBarDR = kBarOF + MT;  // per MMA warp
-  static constexpr int kNumBars = kBarDR + MT;
+  // matrix 1 starts once matrix 0's first softmax is done (single use)
+  static constexpr int kBarLag = kBarDR + MT;
+  static constexpr int kNumBars = kBarLag + 1;
   static constexpr int kMisc = kBars + 8 * kNumBars;  // tmem base, fail flag
   static constexpr int kBytes = kMisc + 16 + 1024;    // + alignment slack
   // tensor-memory columns: S / P of matrix m, buffer u at 128 m + 64 u;
@@ -162,6 +174,7 @@ __global__ void __launch_bounds__(TcSmem<D, HC>::kThreads, 1)
     for (int x = 0; x < Sm::kNumBars; ++x)
       mbar_init(&bars[x], (x >= Sm::kBarPF && x < Sm::kBarOD)   ? 4    // P: one per softmax warp
                           : (x >= Sm::kBarKE && x < Sm::kBarSF) ? MT   // K/V empty: one per MMA warp
+                          : x == Sm::kBarLag                    ? 4    // matrix 0's softmax warps
                                                                 : 1);
     *fail = 0;
     fence_mbar_init();
@@ -177,9 +190,12 @@ __global__ void __launch_bounds__(TcSmem<D, HC>::kThreads, 1)
   pdl_launch_dependents();
   const int *list = p.lists + ((size_t)hk * p.nb + b) * p.KB;
   const int n = p.dense ? b + 1 : min(b + 1, p.kblocks);
+  const int np = (n + 1) / 2;  // pairs of chosen blocks (the last may hold one)
 
   if (warp == Sm::kLoadWarp) {
-    // ---- TMA: Q once, then K and V of every chosen block through the ring ----
+    // ---- TMA: Q once, then K and V of every pair of chosen blocks through
+    // the ring.  K of a pair lands as one 128-row operand per 64-column
+    // sub-tile (block u's rows at 64 u), V block after block. ----
     if (lane == 0) {
       int issued = 0;
       bool ok = true;
@@ -189,41 +205,47 @@ __global__ void __launch_bounds__(TcSmem<D, HC>::kThreads, 1)
           for (int hh = 0; hh < 2; ++hh)  // rows 0-63: head 2 mm, rows 64-127: head 2 mm + 1
             tma_load_4d(smem + Sm::kQ + (mm * KB + kb) * 16384 + hh * 8192, &p.tm_q, 0, kb,
                         h0 + 2 * mm + hh, t0, &bars[Sm::kBarQ]);
-      for (int j = 0; j < n; ++j) {
-        const int s = j % S;
-        if (j >= S && !(ok = tc_wait(&bars[Sm::kBarKE + s], ((j / S) - 1) & 1, fail))) break;
-        const int i = list[j];
-        if (i < 0 || i > b) {  // (the selection never yields one: record it and leave)
-          pf_set_err(p.err, kDevBadSelection, hk, b, i);
-          *fail = 1;
-          ok = false;
-          break;
+      for (int pp = 0; pp < np && ok; ++pp) {
+        const int s = pp % S, nbk = min(2, n - 2 * pp);
+        if (pp >= S && !(ok = tc_wait(&bars[Sm::kBarKE + s], ((pp / S) - 1) & 1, fail))) break;
+        for (int u = 0; u < nbk; ++u) {
+          const int i = list[2 * pp + u];
+          if (i < 0 || i > b) {  // (the selection never yields one: record it and leave)
+            pf_set_err(p.err, kDevBadSelection, hk, b, i);
+            *fail = 1;
+            ok = false;
+          }
         }
-        mbar_arrive_expect_tx(&bars[Sm::kBarKF + s], KB * 8192);
-        for (int kb = 0; kb < KB; ++kb)
-          tma_load_4d(smem + Sm::kK + (s * KB + kb) * 8192, &p.tm_k, 0, kb, hk,
-                      i * kPrefillBlock, &bars[Sm::kBarKF + s]);
-        mbar_arrive_expect_tx(&bars[Sm::kBarVF + s], KB * 8192);
-        for (int kb = 0; kb < KB; ++kb)
-          tma_load_4d(smem + Sm::kV + (s * KB + kb) * 8192, &p.tm_v, 0, kb, hk,
-                      i * kPrefillBlock, &bars[Sm::kBarVF + s]);
+        if (!ok) break;
+        mbar_arrive_expect_tx(&bars[Sm::kBarKF + s], nbk * KB * 8192);
+        for (int u = 0; u < nbk; ++u)
+          for (int kb = 0; kb < KB; ++kb)
+            tma_load_4d(smem + Sm::kK + s * Sm::kStageBytes + kb * 16384 + u * 8192, &p.tm_k, 0,
+                        kb, hk, list[2 * pp + u] * kPrefillBlock, &bars[Sm::kBarKF + s]);
+        mbar_arrive_expect_tx(&bars[Sm::kBarVF + s], nbk * KB * 8192);
+        for (int u = 0; u < nbk; ++u)
+          for (int kb = 0; kb < KB; ++kb)
+            tma_load_4d(smem + Sm::kV + s * Sm::kStageBytes + (u * KB + kb) * 8192, &p.tm_v, 0,
+                        kb, hk, list[2 * pp + u] * kPrefillBlock, &bars[Sm::kBarVF + s]);
         ++issued;
       }
       if (!ok) {  // the copies still in flight land before the CTA leaves
         tc_drain(&bars[Sm::kBarQ], 0);
-        for (int j = issued > S ? issued - S : 0; j < issued; ++j) {
-          tc_drain(&bars[Sm::kBarKF + j % S], (j / S) & 1);
-          tc_drain(&bars[Sm::kBarVF + j % S], (j / S) & 1);
+        for (int pp = issued > S ? issued - S : 0; pp < issued; ++pp) {
+          tc_drain(&bars[Sm::kBarKF + pp % S], (pp / S) & 1);
+          tc_drain(&bars[Sm::kBarVF + pp % S], (pp / S) & 1);
         }
       }
     }
   } else if (warp >= Sm::kMmaWarp) {
     // ---- MMA issue for matrix m (the whole warp, one elected lane issuing):
-    // S_m of block j + 1 ahead of P_m . V of block j ----
+    // S_m of a pair of blocks in one MMA (N = 128), then P_m . V block by
+    // block as the softmax releases them ----
     const int m = warp - Sm::kMmaWarp;
     const bool bf = PSplit<T>::bf16;
-    const uint32_t idesc_s = umma_idesc_f16(bf, 128, 64, 0, 0);  // Q . K^T: both K-major
-    const uint32_t idesc_o = umma_idesc_f16(bf, 128, 64, 0, 1);  // P . V: V MN-major
+    const uint32_t idesc_s2 = umma_idesc_f16(bf, 128, 128, 0, 0);  // Q . K^T, a pair
+    const uint32_t idesc_s1 = umma_idesc_f16(bf, 128, 64, 0, 0);   // Q . K^T, a lone block
+    const uint32_t idesc_o = umma_idesc_f16(bf, 128, 64, 0, 1);    // P . V: V MN-major
     // base descriptors; a byte offset o inside the region adds o / 16
     const uint64_t dq = umma_desc_sw128(smem_u32(smem + Sm::kQ + m * KB * 16384), 16, 1024);
     const uint64_t dk = umma_desc_sw128(smem_u32(smem + Sm::kK), 16, 1024);
@@ -233,49 +255,60 @@ __global__ void __launch_bounds__(TcSmem<D, HC>::kThreads, 1)
     auto wwait = [&](uint64_t *bar, uint32_t parity) {
       return __all_sync(0xffffffffu, tc_wait(bar, parity, fail));
     };
-    // S_m(j) = Q_m . K_j^T into buffer j & 1
-    auto issue_s = [&](int j) {
-      const uint64_t kt = dk + (uint64_t)(((j % S) * KB * 8192) >> 4);
+    // S_m of pair pp = Q_m . K^T over its one or two blocks: block u's logits
+    // in columns 64 u .. 64 u + 63 of the matrix's S / P region
+    auto issue_s = [&](int pp) {
+      const uint64_t kt = dk + (uint64_t)(((pp % S) * Sm::kStageBytes) >> 4);
+      const uint32_t idesc = n - 2 * pp >= 2 ? idesc_s2 : idesc_s1;
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk)
-        umma_f16_warp(tmem + 128 * m + 64 * (j & 1),
-                      dq + (uint64_t)((((kk >> 2)) * 16384 + (kk & 3) * 32) >> 4),
-                      kt + (uint64_t)(((kk >> 2) * 8192 + (kk & 3) * 32) >> 4), idesc_s, kk > 0);
-      umma_commit_warp(&bars[Sm::kBarSF + 2 * m + (j & 1)]);
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint64_t off = (uint64_t)((((kk >> 2)) * 16384 + (kk & 3) * 32) >> 4);
+        umma_f16_warp(tmem + 128 * m, dq + off, kt + off, idesc, kk > 0);
+      }
+      umma_commit_warp(&bars[Sm::kBarSF + m]);
     };
     bool ok = wwait(&bars[Sm::kBarQ], 0) && wwait(&bars[Sm::kBarKF], 0);
+    // the matrices start half a step apart: their softmax phases and their
+    // MMAs then alternate instead of meeting (both follow the same K / V
+    // stages, so in step they wait at the same time and the tensor pipe idles)
+    if (m == 1 && ok) ok = wwait(&bars[Sm::kBarLag], 0);
     const bool any = ok;
     if (ok) {
       tc_fence_after();
       issue_s(0);
     }
-    for (int j = 0; j < n && ok; ++j) {
-      const int s = j % S;
-      if (j + 1 < n) {
-        const int j1 = j + 1;
-        // buffer j1 & 1 held P_m(j - 1): its P . V has to be done
-        if (!(ok = wwait(&bars[Sm::kBarKF + j1 % S], (j1 / S) & 1))) break;
-        if (j >= 1 && !(ok = wwait(&bars[Sm::kBarOD + m], (j - 1) & 1))) break;
+    for (int pp = 0; pp < np && ok; ++pp) {
+      const int s = pp % S, nbk = min(2, n - 2 * pp);
+      if (!(ok = wwait(&bars[Sm::kBarVF + s], (pp / S) & 1))) break;
+      for (int u = 0; u < nbk; ++u) {
+        const int j = 2 * pp + u;
+        if (!(ok = wwait(&bars[Sm::kBarPF + 2 * m + u], pp & 1))) break;
         tc_fence_after();
-        issue_s(j1);
+        const uint64_t vt = dv + (uint64_t)((s * Sm::kStageBytes + u * KB * 8192) >> 4);
+        const uint32_t pa = tmem + 128 * m + 64 * u;
+#pragma unroll
+        for (int half = 0; half < KB; ++half)
+#pragma unroll
+          for (int part = 0; part < 2; ++part)  // P_hi, then P_lo
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              umma_f16_ts_warp(t_o + 64 * half, pa + 32 * part + 8 * kk,
+                               vt + (uint64_t)((half * 8192 + kk * 2048) >> 4), idesc_o,
+                               j > 0 || part > 0 || kk > 0);
+        umma_commit_warp(&bars[Sm::kBarOD + m]);
       }
-      if (!(ok = wwait(&bars[Sm::kBarVF + s], (j / S) & 1))) break;
-      if (!(ok = wwait(&bars[Sm::kBarPF + 2 * m + (j & 1)], (j >> 1) & 1))) break;
-      tc_fence_after();
-      const uint64_t vt = dv + (uint64_t)((s * KB * 8192) >> 4);
-      const uint32_t pa = tmem + 128 * m + 64 * (j & 1);
-#pragma unroll
-      for (int half = 0; half < KB; ++half)
-#pragma unroll
-        for (int part = 0; part < 2; ++part)  // P_hi, then P_lo
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            umma_f16_ts_warp(t_o + 64 * half, pa + 32 * part + 8 * kk,
-                             vt + (uint64_t)((half * 8192 + kk * 2048) >> 4), idesc_o,
-                             j > 0 || part > 0 || kk > 0);
-      umma_commit_warp(&bars[Sm::kBarOD + m]);
-      if (j == n - 1) umma_commit_warp(&bars[Sm::kBarOF + m]);
+      if (!ok) break;
+      umma_commit_warp(&bars[Sm::kBarOP + m]);
+      if (pp == np - 1) umma_commit_warp(&bars[Sm::kBarOF + m]);
       umma_commit_warp(&bars[Sm::kBarKE + s]);  // the stage is free once both warps' MMAs are done
+      if (pp + 1 < np) {
+        // the next pair's S overwrites this pair's P: both P . V done first
+        const int p1 = pp + 1;
+        if (!(ok = wwait(&bars[Sm::kBarKF + p1 % S], (p1 / S) & 1))) break;
+        if (!(ok = wwait(&bars[Sm::kBarOP + m], pp & 1))) break;
+        tc_fence_after();
+        issue_s(p1);
+      }
     }
     if (any) {  // every MMA of this warp done before the CTA frees its memory
       umma_commit_warp(&bars[Sm::kBarDR + m]);
@@ -291,10 +324,11 @@ __global__ void __launch_bounds__(TcSmem<D, HC>::kThreads, 1)
     float m_run = -CUDART_INF_F, l_run = 0.f;
     bool ok = true;
     for (int j = 0; j < n; ++j) {
-      const int u = j & 1;
+      const int u = j & 1;  // block u of pair j / 2: S / P columns 64 u ..
       const uint32_t t_s = lanes + 128 * m + 64 * u;
       const int i = list[j];
-      ok = tc_wait(&bars[Sm::kBarSF + 2 * m + u], (j >> 1) & 1, fail);
+      // (the pair's S: for its second block this phase has already completed)
+      ok = tc_wait(&bars[Sm::kBarSF + m], (j >> 1) & 1, fail);
       if (!(ok = __all_sync(0xffffffffu, ok))) break;  // the tensor-memory accesses are warp-wide
       tc_fence_after();
       uint32_t s[64];
@@ -356,6 +390,7 @@ __global__ void __launch_bounds__(TcSmem<D, HC>::kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[Sm::kBarPF + 2 * m + u]);
+      if (m == 0 && j == 0 && lane == 0) mbar_arrive(&bars[Sm::kBarLag]);
     }
     if (ok) {
       ok = tc_wait(&bars[Sm::kBarOF + m], 0, fail);
