@@ -718,9 +718,9 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
       }
       const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-      const float c0 = exp2f(m0 - mn0), c1 = exp2f(m1 - mn1);
-      const float p0 = exp2f(z0 - mn0), p1 = exp2f(z1 - mn1);
-      const float p2 = exp2f(z2 - mn0), p3 = exp2f(z3 - mn1);
+      const float c0 = ex2_approx(m0 - mn0), c1 = ex2_approx(m1 - mn1);
+      const float p0 = ex2_approx(z0 - mn0), p1 = ex2_approx(z1 - mn1);
+      const float p2 = ex2_approx(z2 - mn0), p3 = ex2_approx(z3 - mn1);
       l0 = l0 * c0 + p0 + p2;
       l1 = l1 * c1 + p1 + p3;
       m0 = mn0;
@@ -905,7 +905,7 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
     if (M != -CUDART_INF_F) {
 #pragma unroll
       for (int w = 0; w < kWarps; ++w) {
-        const float f = exp2f(m_w[w * G + g] - M);
+        const float f = ex2_approx(m_w[w * G + g] - M);
         const float4 o = *reinterpret_cast<const float4 *>(&o_w[(w * G + g) * OS + c]);
         O.x = fmaf(f, o.x, O.x);
         O.y = fmaf(f, o.y, O.y);
@@ -955,7 +955,7 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
       float O1 = 0.f, L1 = 0.f;
 #pragma unroll
       for (int r = 0; r < 16; r += 2) {
-        const float f0 = exp2f(mr[r] - M), f1 = exp2f(mr[r + 1] - M);
+        const float f0 = ex2_approx(mr[r] - M), f1 = ex2_approx(mr[r + 1] - M);
         Ls = fmaf(f0, lr[r], Ls);
         O = fmaf(f0, orr[r], O);
         L1 = fmaf(f1, lr[r + 1], L1);
