@@ -166,6 +166,34 @@ template <> struct Cvt<__nv_bfloat16> {
   static __device__ __forceinline__ __nv_bfloat16 from(float x) { return __float2bfloat16_rn(x); }
 };
 
+// Two weights (a in the low half) split into their 16-bit roundings (hi) and
+// the 16-bit roundings of what is left (lo): the rest a - hi is exact in fp32.
+template <typename T> struct Split2;
+template <> struct Split2<__half> {
+  static __device__ __forceinline__ void run(float a, float b, uint32_t &hi, uint32_t &lo) {
+    const __half2 h = __floats2half2_rn(a, b);
+    const float2 r = f2_sub(make_float2(a, b), __half22float2(h));
+    const __half2 l = __floats2half2_rn(r.x, r.y);
+    hi = *reinterpret_cast<const uint32_t *>(&h);
+    lo = *reinterpret_cast<const uint32_t *>(&l);
+  }
+};
+template <> struct Split2<__nv_bfloat16> {
+  static __device__ __forceinline__ void run(float a, float b, uint32_t &hi, uint32_t &lo) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    const float2 r = f2_sub(make_float2(a, b), __bfloat1622float2(h));
+    const __nv_bfloat162 l = __floats2bfloat162_rn(r.x, r.y);
+    hi = *reinterpret_cast<const uint32_t *>(&h);
+    lo = *reinterpret_cast<const uint32_t *>(&l);
+  }
+};
+
+// A warp's running max of a head moves only when a tile's max exceeds it by
+// more than this (log2 units), so the output accumulators are rescaled
+// rarely; weights then stay below 2^8, and every merge pairs each (m, l, o)
+// with its own m.  Launches that export the row max keep it exact (0).
+constexpr float kStaleMax = 8.f;
+
 __device__ __forceinline__ void set_err(int *err, int code, int a, int b, int c) {
   if (atomicCAS(err, 0, code) == 0) {
     err[1] = a;
@@ -530,6 +558,7 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
   float *Pw = P_all + warp * kRows * GPAD;
   // fp8: the stored keys are code * k_scale; the scale folds into the logits'
   const float sc = kF8 ? p.scale_log2 * p.k_scale[h] : p.scale_log2;
+  const float stale = p.row_max ? 0.f : kStaleMax;
 
   for (int t = warp; t < nt;) {
     const TileDesc td = tdesc[t];
@@ -717,7 +746,9 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
         mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
       }
-      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+      // (m = -inf before the first tile: any finite tile max moves it)
+      const float mn0 = mx0 > m0 + stale ? mx0 : m0, mn1 = mx1 > m1 + stale ? mx1 : m1;
+      const bool moved = __any_sync(0xffffffffu, mn0 != m0 || mn1 != m1);
       const float c0 = ex2_approx(m0 - mn0), c1 = ex2_approx(m1 - mn1);
       const float p0 = ex2_approx(z0 - mn0), p1 = ex2_approx(z1 - mn1);
       const float p2 = ex2_approx(z2 - mn0), p3 = ex2_approx(z3 - mn1);
@@ -752,13 +783,16 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
       }
       __syncwarp();
 
-      // P.V on tensor cores: rescale, then O^T += V^T (P_hi + P_lo)^T
+      // P.V on tensor cores: rescale (when a max moved), then
+      // O^T += V^T (P_hi + P_lo)^T
+      if (moved) {
 #pragma unroll
-      for (int m = 0; m < MT; ++m) {
-        oacc[m][0] *= c0;
-        oacc[m][1] *= c1;
-        oacc[m][2] *= c0;
-        oacc[m][3] *= c1;
+        for (int m = 0; m < MT; ++m) {
+          oacc[m][0] *= c0;
+          oacc[m][1] *= c1;
+          oacc[m][2] *= c0;
+          oacc[m][3] *= c1;
+        }
       }
       uint32_t bh0, bh1, bl0, bl1;  // B = P^T: k = tokens 2t4.. / 2t4+8.., n = head g8
       {
@@ -769,18 +803,8 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
           pv[2] = Pw[(2 * t4 + 8) * GPAD + g8];
           pv[3] = Pw[(2 * t4 + 9) * GPAD + g8];
         }
-        uint16_t hi[4], lo[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const TP th = Cvt<TP>::from(pv[e]);
-          hi[e] = *reinterpret_cast<const uint16_t *>(&th);
-          const TP tl = Cvt<TP>::from(pv[e] - tof(th));
-          lo[e] = *reinterpret_cast<const uint16_t *>(&tl);
-        }
-        bh0 = (uint32_t)hi[0] | ((uint32_t)hi[1] << 16);
-        bh1 = (uint32_t)hi[2] | ((uint32_t)hi[3] << 16);
-        bl0 = (uint32_t)lo[0] | ((uint32_t)lo[1] << 16);
-        bl1 = (uint32_t)lo[2] | ((uint32_t)lo[3] << 16);
+        Split2<TP>::run(pv[0], pv[1], bh0, bl0);
+        Split2<TP>::run(pv[2], pv[3], bh1, bl1);
       }
       if constexpr (kF8) {
         // A = V^T, transposed ldmatrix of byte pairs: matrices (tokens 0-7 |
