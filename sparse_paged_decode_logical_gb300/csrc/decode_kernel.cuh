@@ -39,8 +39,11 @@
 // Merge.  The 8 warps merge in shared memory into the CTA's (m, l, o).  The
 // CTAs of a cluster then merge over distributed shared memory: every CTA
 // pushes each channel slice of its (m, l, o) into the inbox of the CTA that
-// owns that slice (remote shared-memory stores), and after one cluster
-// barrier each CTA combines its slice locally -- the row max / row sum export
+// owns that slice (remote shared-memory stores that count their bytes on the
+// owner's inbox mbarrier), and once its inbox holds every rank's bytes each
+// CTA combines its slice locally (a split cluster barrier, arrived after the
+// pushes and waited for before the CTA leaves, keeps every CTA resident
+// while peers may store into it) -- the row max / row sum export
 // of the Novita KV-sparsity article's modified FlashAttention ("attention
 // mechanism modifications").  When a
 // unit has several clusters (nc > 1), their results meet in global memory:
@@ -132,7 +135,8 @@ struct Smem {
   static constexpr int kInbox = (kML + 2 * kWarps * G * 4 + 15) / 16 * 16;
   static constexpr int kFlag = kInbox + (32 * G + G * D + 64) * 4;     // int [4 + kStages]
   static constexpr int kTopkBar = (kFlag + (4 + kStages) * 4 + 7) / 8 * 8;  // uint64
-  static constexpr int kTiles = (kTopkBar + 8 + 1023) / 1024 * 1024;
+  static constexpr int kInboxBar = kTopkBar + 8;  // uint64: the inbox's bytes have landed
+  static constexpr int kTiles = (kInboxBar + 8 + 1023) / 1024 * 1024;
   static constexpr int kStageRegion = kStages * Geo<D, F8>::kTileBytes;
   static constexpr int kMergeRegion = kWarps * G * (D + 4) * 4;        // o of every warp
   static constexpr int kCombineRegion = 256 * G * 12 + 64;             // (m, l), weights
@@ -294,6 +298,19 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
   int *s_iss = s_flag + 4;                                   // loads issued per stage
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // The inbox barrier counts the bytes the cluster's CTAs push into this
+  // CTA's inbox: from each of CS ranks, its (M, L) and its O of this CTA's
+  // channel slice for every head.  Set up before the cluster's start arrive,
+  // so no rank stores into it before it exists.  (A launch of one-CTA
+  // clusters is a plain grid, where the CTA fills its own inbox with plain
+  // stores: the byte-counting remote stores need a cluster launch.)
+  uint64_t *inbox_bar = reinterpret_cast<uint64_t *>(smem + Sm::kInboxBar);
+  const bool remote = p.cluster > 1;
+  if (tid == 0 && remote) {
+    mbar_init(inbox_bar, 1);
+    fence_mbar_init();
+    mbar_arrive_expect_tx(inbox_bar, (uint32_t)(p.cluster * G * ((D / p.cluster) + 2) * 4));
+  }
   cluster_arrive_relaxed();  // paired with the wait before the first remote store
   if (tid == 0) {
     prefetch_tmap(&p.tm_k);
@@ -916,6 +933,7 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
   const int lcs = __ffs(CS) - 1;
   const int slice = D >> lcs, lsl = __ffs(slice) - 1;
   const uint32_t aM = smem_u32(in_M), aL = smem_u32(in_L), aO = smem_u32(in_O);
+  const uint32_t aB = smem_u32(inbox_bar);
   // a thread takes 4 adjacent channels of one head: the warp weights are
   // computed once for them, read and pushed 16 bytes at a time (a slice
   // holds a multiple of 4 channels, so the 4 share an owner)
@@ -941,15 +959,37 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
     const int owner = c >> lsl, cs_ = c & (slice - 1);
     // an owner's inbox row per sending rank is G * slice + 4 words: the
     // ranks of one element fall in different banks when it is read back
-    st_dsmem_v4_f32(map_rank(aO + 4 * (rank * (G * slice + 4) + g * slice + cs_), owner), O);
-    if (cs_ == 0) {
-      st_dsmem_f32(map_rank(aM + 4 * (rank * G + g), owner), M);
-      st_dsmem_f32(map_rank(aL + 4 * (rank * G + g), owner), Ls);
+    const int io = rank * (G * slice + 4) + g * slice + cs_;
+    if (remote) {
+      const uint32_t rb = map_rank(aB, owner);
+      st_async_v4_f32(map_rank(aO + 4 * io, owner), O, rb);
+      if (cs_ == 0) {
+        st_async_f32(map_rank(aM + 4 * (rank * G + g), owner), M, rb);
+        st_async_f32(map_rank(aL + 4 * (rank * G + g), owner), Ls, rb);
+      }
+    } else {  // (rank 0 of one: its own inbox)
+      *reinterpret_cast<float4 *>(&in_O[io]) = O;
+      if (cs_ == 0) {
+        in_M[g] = M;
+        in_L[g] = Ls;
+      }
     }
   }
+  // (waited for just before the CTA leaves, so no CTA of the cluster exits
+  // while a peer may still be storing into it; with the page-mass export it
+  // also releases this CTA's per-tile pairs, which the cluster's CTAs read)
+  if constexpr (kMass)
+    cluster_arrive_release();
+  else
+    cluster_arrive_relaxed();
 
   // ---- merge the cluster: this CTA combines channels [rank*slice, +slice) ----
-  cluster_sync();  // every push has landed; nothing remote is touched after this
+  // every rank's pushes into this CTA's inbox have landed
+  if (!__syncthreads_and(!remote || mbar_wait(inbox_bar, 0, kWaitLimit))) {
+    if (tid == 0) set_err(p.err, kDevTimeout, s.slot, h, -2);
+    cluster_wait();
+    return;
+  }
   const int unit = i * p.Hkv + h;
   float *out = p.out + ((size_t)i * p.Hq + h * G) * D;
   const size_t cpart = (size_t)unit_item0 + (size_t)ci * CS;  // global slot of this cluster
@@ -1004,6 +1044,7 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
     }
   }
   if (nc == 1) {
+    cluster_wait();  // (acquire: the cluster's per-tile pairs, for the page mass)
     if (kMass && dyn) {
       // every CTA of the cluster stored its tiles' pairs before the cluster
       // barrier; the unit's final max and sum per head come from the inbox
@@ -1023,6 +1064,7 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
     }
     return;
   }
+  cluster_wait();
   cluster_sync();  // every rank's slice is written before rank 0 releases it
   if (rank != 0) return;
 

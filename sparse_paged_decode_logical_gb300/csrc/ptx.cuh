@@ -191,6 +191,9 @@ __device__ __forceinline__ void cluster_sync() {
 }
 // Split cluster barrier: arrive (no ordering) and, later, wait.  Used to know
 // that every CTA of the cluster has started before touching its shared memory.
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
 __device__ __forceinline__ void cluster_arrive_relaxed() {
   asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 }
@@ -205,6 +208,20 @@ __device__ __forceinline__ uint32_t map_rank(uint32_t smem_addr, uint32_t rank) 
 }
 __device__ __forceinline__ void st_dsmem_f32(uint32_t addr, float v) {
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+// Remote shared-memory stores that count their bytes on an mbarrier of the
+// destination CTA (addresses from mapa): the receiver waits on its own
+// barrier for the bytes it expects, with no fence or cluster barrier.
+__device__ __forceinline__ void st_async_v4_f32(uint32_t addr, float4 v, uint32_t bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(addr),
+      "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void st_async_f32(uint32_t addr, float v, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];" ::"r"(addr),
+               "f"(v), "r"(bar)
+               : "memory");
 }
 __device__ __forceinline__ void st_dsmem_v4_f32(uint32_t addr, float4 v) {  // 16-byte aligned
   asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x),
