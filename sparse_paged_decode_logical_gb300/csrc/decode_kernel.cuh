@@ -537,6 +537,9 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
     if (!skip_wait) pdl_wait();
     pdl_launch_dependents();
   }
+  // every CTA of the cluster has started (its inbox barrier is set up): the
+  // CTAs of a cluster start together, so this is off the merge's path
+  cluster_wait();
 
   // ---- q^T fragments (B operand), heads padded to 8 columns ----
   const int g8 = lane >> 2, t4 = lane & 3;
@@ -925,7 +928,6 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
     }
   }
   __syncthreads();
-  cluster_wait();  // every CTA of the cluster has started: its inbox may be written
   // this CTA's (M, L, O), pushed straight into the inbox of the cluster CTA
   // that owns each channel slice (remote shared-memory stores)
   // CS, the slice and TPE below are powers of two: shifts and masks, not
@@ -975,19 +977,24 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
       }
     }
   }
-  // (waited for just before the CTA leaves, so no CTA of the cluster exits
-  // while a peer may still be storing into it; with the page-mass export it
-  // also releases this CTA's per-tile pairs, which the cluster's CTAs read)
-  if constexpr (kMass)
-    cluster_arrive_release();
-  else
-    cluster_arrive_relaxed();
+  // A CTA leaves only once its inbox holds every rank's bytes, so no peer is
+  // still storing into it.  A second cluster phase is needed only when the
+  // cluster's CTAs read one another's global writes: the per-tile pairs of
+  // the page-mass export (released here, acquired before they are read) and
+  // the slices several clusters merge in global memory.
+  const bool phase2 = kMass || nc > 1;  // (the same in every CTA of a cluster)
+  if (phase2) {
+    if constexpr (kMass)
+      cluster_arrive_release();
+    else
+      cluster_arrive_relaxed();
+  }
 
   // ---- merge the cluster: this CTA combines channels [rank*slice, +slice) ----
   // every rank's pushes into this CTA's inbox have landed
   if (!__syncthreads_and(!remote || mbar_wait(inbox_bar, 0, kWaitLimit))) {
     if (tid == 0) set_err(p.err, kDevTimeout, s.slot, h, -2);
-    cluster_wait();
+    if (phase2) cluster_wait();
     return;
   }
   const int unit = i * p.Hkv + h;
@@ -1044,7 +1051,7 @@ __global__ void __launch_bounds__(kThreads) decode_tiles_kernel(const __grid_con
     }
   }
   if (nc == 1) {
-    cluster_wait();  // (acquire: the cluster's per-tile pairs, for the page mass)
+    if (kMass) cluster_wait();  // (acquire: the cluster's per-tile pairs)
     if (kMass && dyn) {
       // every CTA of the cluster stored its tiles' pairs before the cluster
       // barrier; the unit's final max and sum per head come from the inbox
