@@ -41,9 +41,10 @@
 // pushes each channel slice of its (m, l, o) into the inbox of the CTA that
 // owns that slice (remote shared-memory stores that count their bytes on the
 // owner's inbox mbarrier), and once its inbox holds every rank's bytes each
-// CTA combines its slice locally (a split cluster barrier, arrived after the
-// pushes and waited for before the CTA leaves, keeps every CTA resident
-// while peers may store into it) -- the row max / row sum export
+// CTA combines its slice locally (a CTA leaves only after its own inbox is
+// complete, so no peer is still storing into it; a second cluster phase
+// remains only where CTAs read one another's global writes) -- the row max /
+// row sum export
 // of the Novita KV-sparsity article's modified FlashAttention ("attention
 // mechanism modifications").  When a
 // unit has several clusters (nc > 1), their results meet in global memory:
